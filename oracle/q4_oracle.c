@@ -1,0 +1,364 @@
+/*
+ * Q4_0 oracle: a plain, slow, obviously correct CPU reference of the
+ * weight-only Q4_0 dequant-matmul, in fp64.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the CPU-baseline
+ * leg of the benchmark load this library.  The CUDA product path never links,
+ * imports or calls it, and it shares no code, header, table or constant with
+ * the CUDA sources.
+ *
+ * Sources (pages of the reference material, cited by title and section):
+ *   [Eng]  "用两千行 C++ 重写一个 DeepSeek 推理引擎" (C++ DeepSeek engine page)
+ *          §2.2 block_q4_0 and dequantize; §2.3 row-major layout and column
+ *          padding to a multiple of 32; §3.1 textbook triple loop; §3.2
+ *          reordered i-k-j loop that zeroes C first; §3.4 fused dequant
+ *          matmul; §7.1 little-endian files.
+ *   [KT]   "KTransformers DeepSeek-V2 异构 MoE 推理…" page, «优化三» (160
+ *          routed experts, 6 active per token, run as batched GEMVs) and
+ *          «规则二» (gate -> top-k indices and weights -> experts).
+ *
+ * Everything is computed in fp64.  Each product a*w is exact in fp64 (a has
+ * at most 24 significant bits, w = (q-8)*d at most 15), so the only error of
+ * the oracle is the fp64 summation, at most about K*2^-53*sum|a*w|.
+ *
+ * Pins: every function here is pinned by a CPU test against something other
+ * than itself (library conversions over all 65536 codes, hand-built blocks,
+ * exact rational sums, one-hot and zero cases, linearity, padding invariance,
+ * closed forms of SiLU).  No function is parity-unpinned.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define QO_BLOCK 32
+#define QO_BLOCK_BYTES 18
+
+/* ------------------------------------------------------------------ */
+/* Number formats                                                      */
+/* ------------------------------------------------------------------ */
+
+/* IEEE 754 binary16 -> fp64, from the format's definition: 1 sign bit,
+ * 5 exponent bits with bias 15, 10 fraction bits; exponent 0 is zero or
+ * subnormal (f * 2^-24), exponent 31 is Inf (f == 0) or NaN.
+ * [Eng §2.2: the block scale d is fp16, widened by fp16_to_fp32.] */
+double q4o_fp16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 31;
+    int f = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25);   /* (1 + f/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16 -> fp64: 1 sign bit, 8 exponent bits with bias 127, 7 fraction
+ * bits; exponent 0 is zero or subnormal (f * 2^-133), 255 is Inf or NaN. */
+double q4o_bf16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 7) & 255;
+    int f = h & 127;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -133);
+    else if (e == 255)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(128 + f), e - 134);   /* (1 + f/128) * 2^(e-127) */
+    return sign ? -v : v;
+}
+
+/* fp64 -> bfloat16 bits, round to nearest with ties to even, from the
+ * definition: keep 8 significant bits (normal range) or quantum 2^-133
+ * (subnormal range); values that round to >= 2^128 become Inf. */
+uint16_t q4o_f64_to_bf16(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (isnan(x))
+        return (uint16_t)(sign | 0x7FC0);
+    if (isinf(x))
+        return (uint16_t)(sign | 0x7F80);
+    if (a == 0.0)
+        return sign;
+    int e;
+    double m = frexp(a, &e);              /* a = m * 2^e, m in [0.5, 1) */
+    int expo = e - 1;                     /* a = 1.xxx * 2^expo */
+    double quantum_exp = (expo < -126) ? -133 : (double)(expo - 7);
+    double y = ldexp(a, -(int)quantum_exp);   /* a in units of the quantum */
+    double fl = floor(y);
+    double r = fl;
+    double diff = y - fl;
+    if (diff > 0.5 || (diff == 0.5 && fmod(fl, 2.0) != 0.0))
+        r = fl + 1.0;
+    double v = ldexp(r, (int)quantum_exp);
+    if (v >= ldexp(1.0, 128))
+        return (uint16_t)(sign | 0x7F80);
+    /* encode v (exact in bf16 now) */
+    if (v < ldexp(1.0, -126)) {
+        return (uint16_t)(sign | (uint16_t)ldexp(v, 133));   /* subnormal */
+    }
+    m = frexp(v, &e);
+    expo = e - 1;
+    int frac = (int)(ldexp(m, 8)) - 128;     /* m*256 in [128, 256) */
+    return (uint16_t)(sign | (uint16_t)((expo + 127) << 7) | (uint16_t)frac);
+}
+
+/* Activation element i of a buffer of dtype 0 = fp32, 1 = bf16 bits. */
+static double act_at(const void *A, int dtype, int64_t i)
+{
+    if (dtype == 0) {
+        float f;
+        memcpy(&f, (const char *)A + 4 * i, 4);
+        return (double)f;
+    }
+    uint16_t h;
+    memcpy(&h, (const char *)A + 2 * i, 2);
+    return q4o_bf16_to_f64(h);
+}
+
+/* ------------------------------------------------------------------ */
+/* Q4_0 block access                                                   */
+/* ------------------------------------------------------------------ */
+
+/* Scale of block (k, b): bytes 0-1 of the block, little-endian fp16
+ * [Eng §2.2 struct block_q4_0; §7.1 the files are little-endian]. */
+static double block_scale(const uint8_t *blk)
+{
+    uint16_t h = (uint16_t)(blk[0] | (blk[1] << 8));
+    return q4o_fp16_to_f64(h);
+}
+
+/* Nibble l of a block: byte l/2 of qs; low nibble for even l, high nibble
+ * for odd l [Eng §2.2 dequantize]. */
+static int block_nibble(const uint8_t *blk, int l)
+{
+    uint8_t packed = blk[2 + l / 2];
+    return (l % 2 == 0) ? (packed & 0x0F) : (packed >> 4);
+}
+
+/* Weight W[k, j] = (q - 8) * fp16_to_fp32(d) [Eng §2.2], where block
+ * (k, j/32) sits at byte (k*nb + j/32)*18 of B: K rows, each of nb blocks
+ * running along the output columns [Eng §2.3, §3.4 block = &B[k*(N/32)]]. */
+static double weight_at(const uint8_t *B, int64_t nb, int64_t k, int64_t j)
+{
+    const uint8_t *blk = B + (k * nb + j / QO_BLOCK) * QO_BLOCK_BYTES;
+    int q = block_nibble(blk, (int)(j % QO_BLOCK));
+    return (double)(q - 8) * block_scale(blk);
+}
+
+/* ------------------------------------------------------------------ */
+/* Dequantisation                                                      */
+/* ------------------------------------------------------------------ */
+
+/* W [K, N] fp32 = (q - 8) * d for every real column j < N [Eng §2.2].
+ * (q-8)*d has at most 15 significant bits, so the fp32 value is exact. */
+void q4o_dequant_f32(const uint8_t *B, int64_t K, int64_t N, float *W)
+{
+    int64_t nb = (N + QO_BLOCK - 1) / QO_BLOCK;
+    for (int64_t k = 0; k < K; k++)
+        for (int64_t j = 0; j < N; j++)
+            W[k * N + j] = (float)weight_at(B, nb, k, j);
+}
+
+/* W [K, N] as bf16 bits: bf16_rn((q - 8) * d), the 16-bit tile value the
+ * tensor-core path multiplies. */
+void q4o_dequant_bf16(const uint8_t *B, int64_t K, int64_t N, uint16_t *W)
+{
+    int64_t nb = (N + QO_BLOCK - 1) / QO_BLOCK;
+    for (int64_t k = 0; k < K; k++)
+        for (int64_t j = 0; j < N; j++)
+            W[k * N + j] = q4o_f64_to_bf16(weight_at(B, nb, k, j));
+}
+
+/* ------------------------------------------------------------------ */
+/* Matmul                                                              */
+/* ------------------------------------------------------------------ */
+
+/* One output row: c[j] = sum_k a[k] * W[k, j], s[j] = sum_k |a[k] * W[k, j]|.
+ * Loop order k -> block -> l, c zeroed first and overwritten: the fused
+ * dequant loop of [Eng §3.4] with the zeroing of [Eng §3.2], in fp64. */
+static void row_matmul(const double *a, const uint8_t *B, int64_t N, int64_t K,
+                       double *c, double *s)
+{
+    int64_t nb = (N + QO_BLOCK - 1) / QO_BLOCK;
+    for (int64_t j = 0; j < N; j++) {
+        c[j] = 0.0;
+        if (s)
+            s[j] = 0.0;
+    }
+    for (int64_t k = 0; k < K; k++) {
+        double av = a[k];
+        const uint8_t *row = B + k * nb * QO_BLOCK_BYTES;
+        for (int64_t b = 0; b < nb; b++) {
+            const uint8_t *blk = row + b * QO_BLOCK_BYTES;
+            double d = block_scale(blk);
+            for (int l = 0; l < QO_BLOCK; l++) {
+                int64_t j = b * QO_BLOCK + l;
+                if (j >= N)
+                    break;          /* padding column: never stored */
+                int q = block_nibble(blk, l);
+                double p = av * (double)(q - 8) * d;
+                c[j] += p;
+                if (s)
+                    s[j] += fabs(p);
+            }
+        }
+    }
+}
+
+/* c[j] = sum_k a[k] * |W[k, j]|: the first-order carry of per-row errors a[k]
+ * through one matrix (used by the tolerance of the expert chain). */
+static void row_matmul_abs(const double *a, const uint8_t *B, int64_t N, int64_t K,
+                           double *c)
+{
+    int64_t nb = (N + QO_BLOCK - 1) / QO_BLOCK;
+    for (int64_t j = 0; j < N; j++)
+        c[j] = 0.0;
+    for (int64_t k = 0; k < K; k++) {
+        const uint8_t *row = B + k * nb * QO_BLOCK_BYTES;
+        for (int64_t b = 0; b < nb; b++) {
+            const uint8_t *blk = row + b * QO_BLOCK_BYTES;
+            double d = fabs(block_scale(blk));
+            for (int l = 0; l < QO_BLOCK; l++) {
+                int64_t j = b * QO_BLOCK + l;
+                if (j >= N)
+                    break;
+                c[j] += a[k] * fabs((double)(block_nibble(blk, l) - 8)) * d;
+            }
+        }
+    }
+}
+
+/* C [M, N] = A [M, K] . W, with S [M, N] = sum_k |A[i,k] * W[k,j]| (may be
+ * NULL).  A is fp32 (a_dtype 0) or bf16 bits (a_dtype 1), row-major.
+ * [Eng §3.4 matmul_q4_0; C is overwritten as in §3.2.] */
+void q4o_matmul(const void *A, int a_dtype, const uint8_t *B,
+                int64_t M, int64_t N, int64_t K, double *C, double *S)
+{
+    double *a = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+    for (int64_t i = 0; i < M; i++) {
+        for (int64_t k = 0; k < K; k++)
+            a[k] = act_at(A, a_dtype, i * K + k);
+        row_matmul(a, B, N, K, C + i * N, S ? S + i * N : NULL);
+    }
+    free(a);
+}
+
+/* Same product by the textbook route: dequantise W first, then the i-j-k
+ * triple loop of [Eng §3.1], in fp64.  A cross-check of q4o_matmul. */
+void q4o_matmul_naive(const void *A, int a_dtype, const uint8_t *B,
+                      int64_t M, int64_t N, int64_t K, double *C)
+{
+    int64_t nb = (N + QO_BLOCK - 1) / QO_BLOCK;
+    double *W = (double *)malloc(sizeof(double) * (size_t)(K * N > 0 ? K * N : 1));
+    for (int64_t k = 0; k < K; k++)
+        for (int64_t j = 0; j < N; j++)
+            W[k * N + j] = weight_at(B, nb, k, j);
+    for (int64_t i = 0; i < M; i++)
+        for (int64_t j = 0; j < N; j++) {
+            double sum = 0.0;
+            for (int64_t k = 0; k < K; k++)
+                sum += act_at(A, a_dtype, i * K + k) * W[k * N + j];
+            C[i * N + j] = sum;
+        }
+    free(W);
+}
+
+/* ------------------------------------------------------------------ */
+/* Routed experts                                                      */
+/* ------------------------------------------------------------------ */
+
+static double sigmoid(double g) { return 1.0 / (1.0 + exp(-g)); }
+
+/* out[t, :] = sum_{k=0..topk-1} w[t,k] * down_e( SiLU(gate_e(x_t)) * up_e(x_t) )
+ * with e = idx[t,k], summed in slot order k.  SiLU(g) = g * sigmoid(g).
+ * Weights per expert e: W_gate[e], W_up[e] are H x I (K = H, N = I) and
+ * W_down[e] is I x H, each in the Q4_0 block layout above.  Slots whose index
+ * lies outside [0, E) contribute nothing.  [KT «优化三»: routed experts as
+ * batched GEMVs, 6 of 160 per token; «规则二»: gate -> top-k -> experts.]
+ *
+ * tol[t, j] (may be NULL) is the per-element tolerance obtained by carrying
+ * the single-matmul tolerance 1e-3*sum|a*w| + 1e-6 through the chain to first
+ * order: the gate and up errors through SiLU(g)*u, then through down, then
+ * through the weighted sum.
+ * g, u, h (may be NULL) receive the per-slot stage values [T*topk, I]. */
+void q4o_moe(const void *x, int x_dtype,
+             const uint8_t *Wg, const uint8_t *Wu, const uint8_t *Wd,
+             const int32_t *idx, const float *w,
+             int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I,
+             double *out, double *tol, double *g_out, double *u_out, double *h_out)
+{
+    int64_t nbI = (I + QO_BLOCK - 1) / QO_BLOCK;
+    int64_t nbH = (H + QO_BLOCK - 1) / QO_BLOCK;
+    size_t up_bytes = (size_t)(H * nbI * QO_BLOCK_BYTES);
+    size_t down_bytes = (size_t)(I * nbH * QO_BLOCK_BYTES);
+
+    double *xt = (double *)malloc(sizeof(double) * (size_t)H);
+    double *g = (double *)malloc(sizeof(double) * (size_t)I);
+    double *sg = (double *)malloc(sizeof(double) * (size_t)I);
+    double *u = (double *)malloc(sizeof(double) * (size_t)I);
+    double *su = (double *)malloc(sizeof(double) * (size_t)I);
+    double *h = (double *)malloc(sizeof(double) * (size_t)I);
+    double *dh = (double *)malloc(sizeof(double) * (size_t)I);
+    double *y = (double *)malloc(sizeof(double) * (size_t)H);
+    double *sy = (double *)malloc(sizeof(double) * (size_t)H);
+
+    for (int64_t t = 0; t < T; t++) {
+        for (int64_t i = 0; i < H; i++)
+            xt[i] = act_at(x, x_dtype, t * H + i);
+        for (int64_t j = 0; j < H; j++) {
+            out[t * H + j] = 0.0;
+            if (tol)
+                tol[t * H + j] = 1e-6;
+        }
+        for (int64_t k = 0; k < topk; k++) {
+            int64_t slot = t * topk + k;
+            int32_t e = idx[slot];
+            double wk = (double)w[slot];
+            if (e < 0 || e >= E) {
+                if (g_out) for (int64_t i = 0; i < I; i++) g_out[slot * I + i] = 0.0;
+                if (u_out) for (int64_t i = 0; i < I; i++) u_out[slot * I + i] = 0.0;
+                if (h_out) for (int64_t i = 0; i < I; i++) h_out[slot * I + i] = 0.0;
+                continue;
+            }
+            const uint8_t *wg = Wg + (size_t)e * up_bytes;
+            const uint8_t *wu = Wu + (size_t)e * up_bytes;
+            const uint8_t *wd = Wd + (size_t)e * down_bytes;
+            row_matmul(xt, wg, I, H, g, sg);
+            row_matmul(xt, wu, I, H, u, su);
+            for (int64_t i = 0; i < I; i++) {
+                double sgm = sigmoid(g[i]);
+                double silu = g[i] * sgm;
+                double dsilu = sgm * (1.0 + g[i] * (1.0 - sgm));
+                h[i] = silu * u[i];
+                dh[i] = fabs(dsilu * u[i]) * (1e-3 * sg[i] + 1e-6)
+                      + fabs(silu) * (1e-3 * su[i] + 1e-6);
+                if (g_out) g_out[slot * I + i] = g[i];
+                if (u_out) u_out[slot * I + i] = u[i];
+                if (h_out) h_out[slot * I + i] = h[i];
+            }
+            row_matmul(h, wd, H, I, y, sy);
+            for (int64_t j = 0; j < H; j++)
+                out[t * H + j] += wk * y[j];
+            if (tol) {
+                /* prop[j] = sum_i dh[i] * |Wd[i, j]| */
+                double *prop = (double *)malloc(sizeof(double) * (size_t)H);
+                row_matmul_abs(dh, wd, H, I, prop);
+                for (int64_t j = 0; j < H; j++)
+                    tol[t * H + j] += fabs(wk) * (1e-3 * sy[j] + 1e-6 + prop[j]);
+                free(prop);
+            }
+        }
+    }
+    free(xt); free(g); free(sg); free(u); free(su); free(h); free(dh); free(y); free(sy);
+}
+
+/* SiLU(g) = g * sigmoid(g) in fp64, exposed for its closed-form pins. */
+double q4o_silu(double g) { return g * sigmoid(g); }

@@ -1,0 +1,73 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one mistake in a copy of the oracle's C source (on the CPU),
+builds it, routes the oracle module to the mutant and runs the pin battery:
+at least one pin must fail.  The real oracle is restored afterwards.
+"""
+
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+MUTANTS = {
+    "nibble order swapped": ("(packed & 0x0F) : (packed >> 4)", "(packed >> 4) : (packed & 0x0F)"),
+    "scale bytes big-endian": ("blk[0] | (blk[1] << 8)", "blk[1] | (blk[0] << 8)"),
+    "offset 8 dropped in matmul": ("double p = av * (double)(q - 8) * d;", "double p = av * (double)(q) * d;"),
+    "offset 8 dropped in dequant": ("return (double)(q - 8) * block_scale(blk);", "return (double)(q - 7) * block_scale(blk);"),
+    "fp16 exponent bias off by one": ("e - 25);   /* (1 + f/1024)", "e - 24);   /* (1 + f/1024)"),
+    "fp16 subnormal scale": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
+    "row stride wrong": ("const uint8_t *row = B + k * nb * QO_BLOCK_BYTES;\n        for (int64_t b = 0; b < nb; b++) {\n            const uint8_t *blk = row + b * QO_BLOCK_BYTES;\n            double d = block_scale(blk);\n            for (int l = 0; l < QO_BLOCK; l++) {\n                int64_t j = b * QO_BLOCK + l;\n                if (j >= N)\n                    break;          /* padding column: never stored */",
+                         "const uint8_t *row = B + k * nb * QO_BLOCK_BYTES;\n        for (int64_t b = 0; b < nb; b++) {\n            const uint8_t *blk = row + ((b + 1) % nb) * QO_BLOCK_BYTES;\n            double d = block_scale(blk);\n            for (int l = 0; l < QO_BLOCK; l++) {\n                int64_t j = b * QO_BLOCK + l;\n                if (j >= N)\n                    break;          /* padding column: never stored */"),
+    "operand transposed": ("a[k] = act_at(A, a_dtype, i * K + k);", "a[k] = act_at(A, a_dtype, k * M + i);"),
+    "C accumulated, not zeroed": ("        c[j] = 0.0;\n        if (s)\n            s[j] = 0.0;", "        if (s)\n            s[j] = 0.0;"),
+    "sigmoid sign": ("return 1.0 / (1.0 + exp(-g));", "return 1.0 / (1.0 + exp(g));"),
+    "routing weight dropped": ("out[t * H + j] += wk * y[j];", "out[t * H + j] += y[j];"),
+    "up projection dropped": ("h[i] = silu * u[i];", "h[i] = silu;"),
+    "bf16 ties away from zero": ("(diff == 0.5 && fmod(fl, 2.0) != 0.0)", "(diff == 0.5)"),
+}
+
+BATTERY = [
+    lambda: pins.test_dequant_hand_built_blocks(oracle),
+    lambda: pins.test_dequant_all_nibbles_both_positions(oracle),
+    lambda: pins.test_fp16_decode_all_codes(oracle),
+    lambda: pins.test_bf16_encode_matches_torch(oracle),
+    pins.test_layout_one_hot,
+    pins.test_zero_cases,
+    lambda: pins.test_matmul_exact_rational(2, 3, 64),
+    lambda: pins.test_matmul_exact_rational(3, 17, 40),
+    pins.test_fused_equals_textbook,
+    pins.test_moe_closed_form,
+    lambda: pins.test_silu_closed_forms(oracle),
+]
+
+
+def _build_mutant(tmp_path, name, old, new):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "q4_oracle.c")).read()
+    assert src.count(old) == 1, f"mutation site for '{name}' not unique"
+    path = tmp_path / "mut.c"
+    path.write_text(src.replace(old, new))
+    so = tmp_path / "libmut.so"
+    subprocess.run(["gcc", "-std=c99", "-O1", "-fPIC", "-shared", str(path), "-o", str(so), "-lm"],
+                   check=True)
+    return str(so)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    lib = oracle.bind(_build_mutant(tmp_path, name, old, new))
+    oracle.use(lib)
+    try:
+        failed = []
+        for check in BATTERY:
+            try:
+                check()
+            except (AssertionError, ValueError, ZeroDivisionError, OverflowError):
+                failed.append(check)
+        assert failed, f"no pin caught the mutant '{name}'"
+    finally:
+        oracle.use(None)

@@ -1,0 +1,404 @@
+"""Pins of the fp64 CPU oracle against what the pages and mathematics fix.
+
+Nothing here calls the CUDA path.  Each test ties an oracle function to
+something other than itself: a library conversion over every code, blocks
+whose values were worked out by hand from the block definition (C++ DeepSeek
+engine page, §2.2), exact rational sums, one-hot / zero / scaling / padding
+invariants, and closed forms of SiLU for the routed-expert chain
+(KTransformers DeepSeek-V2 page, «优化三»).
+"""
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import seeded_inputs as si
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "q4_0_blocks.txt")
+
+
+def _golden_blocks():
+    recs = []
+    with open(GOLDEN) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, d, qs, vals = [p.strip() for p in line.split("|")]
+            dbits = int(d, 16)
+            qsb = bytes(int(x, 16) for x in qs.split())
+            assert len(qsb) == 16
+            blk = bytes([dbits & 0xFF, dbits >> 8]) + qsb
+            special = {"inf": math.inf, "-inf": -math.inf, "nan": math.nan,
+                       "-0": -0.0, "0": 0.0}
+            v = [special[t] if t in special else float(t) for t in vals.split()]
+            assert len(v) == 32
+            recs.append((name, blk, v))
+    return recs
+
+
+def _same(a: float, b: float) -> bool:
+    """Equal including the sign of zero; NaN matches NaN."""
+    if math.isnan(a) or math.isnan(b):
+        return math.isnan(a) and math.isnan(b)
+    return a == b and math.copysign(1.0, a) == math.copysign(1.0, b)
+
+
+# ---------------------------------------------------------------- formats
+
+def test_fp16_decode_all_codes(oracle_lib):
+    """The oracle's binary16 decode equals numpy's for all 65536 codes."""
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = codes.view(np.float16).astype(np.float64)
+    for c in range(65536):
+        got = oracle_lib.fp16_to_f64(c)
+        assert _same(got, float(ref[c])), hex(c)
+
+
+def test_bf16_decode_all_codes(oracle_lib):
+    """bf16 decode equals the fp32 whose upper half is the code, for all codes."""
+    codes = np.arange(65536, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):
+        ref = (codes << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+    for c in range(65536):
+        assert _same(oracle_lib.bf16_to_f64(c), float(ref[c])), hex(c)
+
+
+def test_bf16_encode_matches_torch(oracle_lib):
+    """fp64 -> bf16 round-to-nearest-even equals torch's fp32 -> bf16 cast,
+    on random values and on exact ties (inputs exactly representable in fp32)."""
+    torch = pytest.importorskip("torch")
+    g = si.rng(7, 0)
+    with np.errstate(over="ignore"):
+        x = np.concatenate([
+            g.standard_normal(20000).astype(np.float32),
+            (g.standard_normal(2000) * 1e-38).astype(np.float32),   # bf16 subnormals
+            (g.standard_normal(2000) * 3e38).astype(np.float32),    # overflow to inf
+        ])
+    # ties: bf16 value + half an ulp, both parities
+    base = (g.integers(0, 0x7F00, 4000).astype(np.uint32) << 16)
+    ties = (base | 0x8000).view(np.float32)
+    x = np.concatenate([x, ties, -ties, np.array([0.0, -0.0, np.inf, -np.inf], np.float32)])
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    for xi, r in zip(x, ref):
+        assert oracle_lib.f64_to_bf16(float(xi)) == int(r), (float(xi), hex(int(r)))
+
+
+# ---------------------------------------------------------------- dequant
+
+def test_dequant_hand_built_blocks(oracle_lib):
+    """Every hand-built block dequantises to the hand-derived values."""
+    for name, blk, vals in _golden_blocks():
+        W = oracle_lib.dequant_f32(np.frombuffer(blk, np.uint8), 1, 32)
+        for l in range(32):
+            assert _same(float(W[0, l]), vals[l]), (name, l, W[0, l], vals[l])
+
+
+def test_dequant_all_nibbles_both_positions(oracle_lib):
+    """All 16 codes in both nibble positions, for several scales: value = (q-8)*d."""
+    for dbits in (0x3C00, 0xBC00, 0x3800, 0x0400, 0x03FF, 0x5640):
+        d = float(np.array([dbits], np.uint16).view(np.float16)[0])
+        for q in range(16):
+            lo = bytes([dbits & 0xFF, dbits >> 8]) + bytes([0x80 | q] * 16)       # lo = q, hi = 8
+            hi = bytes([dbits & 0xFF, dbits >> 8]) + bytes([(q << 4) | 8] * 16)   # lo = 8, hi = q
+            Wlo = oracle_lib.dequant_f32(np.frombuffer(lo, np.uint8), 1, 32)[0]
+            Whi = oracle_lib.dequant_f32(np.frombuffer(hi, np.uint8), 1, 32)[0]
+            for l in range(32):
+                even = (l % 2 == 0)
+                exp_lo = (q - 8) * d if even else 0.0 * d
+                exp_hi = 0.0 * d if even else (q - 8) * d
+                assert _same(float(Wlo[l]), float(np.float32(exp_lo))), (dbits, q, l)
+                assert _same(float(Whi[l]), float(np.float32(exp_hi))), (dbits, q, l)
+
+
+def test_dequant_bf16_is_rounded_f32(oracle_lib):
+    """The bf16 tile value is the fp32 value rounded by torch's cast."""
+    torch = pytest.importorskip("torch")
+    K, N = 16, 96
+    B = si.q4_weights(K, N, seed=3, d_lo=0.001, d_hi=40.0)
+    W32 = oracle_lib.dequant_f32(B, K, N)
+    W16 = oracle_lib.dequant_bf16(B, K, N)
+    ref = torch.from_numpy(W32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(W16, ref)
+
+
+# ---------------------------------------------------------------- matmul
+
+def _hand_matrix(K, N, k0, b0, qs_pattern, dbits=0x3C00):
+    """K x N blocks with every code 8 (value 0) except block (k0, b0)."""
+    nb = si.nblocks(N)
+    B = np.zeros((K, nb, 18), np.uint8)
+    B[:, :, 2:] = 0x88
+    B[:, :, 0] = dbits & 0xFF
+    B[:, :, 1] = dbits >> 8
+    B[k0, b0, 2:] = np.frombuffer(bytes(qs_pattern), np.uint8)
+    return B.reshape(K, nb * 18)
+
+
+def test_layout_one_hot():
+    """Only block (k0, b0) is non-zero: a one-hot A on row k0 reads the ramp
+    into columns 32*b0 .. 32*b0+31 and nowhere else; other rows give zero."""
+    import oracle
+    K, N, k0, b0 = 5, 96, 3, 1
+    ramp = [0x10, 0x32, 0x54, 0x76, 0x98, 0xBA, 0xDC, 0xFE] * 2
+    B = _hand_matrix(K, N, k0, b0, ramp)
+    for k in range(K):
+        A = np.zeros((1, K), np.float32)
+        A[0, k] = 1.0
+        C, _ = oracle.matmul(A, B, 1, N, K)
+        exp = np.zeros(N)
+        if k == k0:
+            exp[32 * b0:32 * b0 + 32] = [(l % 16) - 8 for l in range(32)]
+        assert np.array_equal(C[0], exp), k
+
+
+def test_zero_cases():
+    import oracle
+    K, N = 7, 64
+    A = si.activations_f32(2, K, seed=1)
+    B = si.q4_weights(K, N, seed=1)
+    # all codes 8
+    Z = B.reshape(K, -1, 18).copy()
+    Z[:, :, 2:] = 0x88
+    C, S = oracle.matmul(A, Z.reshape(K, -1), 2, N, K)
+    assert np.all(C == 0) and np.all(S == 0)
+    # d = +0 and d = -0
+    for lo, hi in ((0, 0), (0, 0x80)):
+        Z = B.reshape(K, -1, 18).copy()
+        Z[:, :, 0], Z[:, :, 1] = lo, hi
+        C, _ = oracle.matmul(A, Z.reshape(K, -1), 2, N, K)
+        assert np.all(C == 0)
+    # A = 0
+    C, _ = oracle.matmul(np.zeros((2, K), np.float32), B, 2, N, K)
+    assert np.all(C == 0)
+
+
+def _exact_product(A, W):
+    """Exact rational A . W from the fp32 values (no rounding anywhere)."""
+    M, K = A.shape
+    N = W.shape[1]
+    out = [[Fraction(0)] * N for _ in range(M)]
+    for i in range(M):
+        for k in range(K):
+            a = Fraction(float(A[i, k]))
+            if a == 0:
+                continue
+            for j in range(N):
+                out[i][j] += a * Fraction(float(W[k, j]))
+    return out
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 1, 32), (2, 3, 64), (3, 17, 40), (1, 64, 96)])
+def test_matmul_exact_rational(M, K, N):
+    """C64 is within the fp64 summation bound of the exact rational sum, and
+    S bounds |C|; on small-integer data every sum is exact."""
+    import oracle
+    A = si.activations_f32(M, K, seed=K)
+    B = si.q4_weights(K, N, seed=K)
+    W = oracle.dequant_f32(B, K, N)
+    C, S = oracle.matmul(A, B, M, N, K)
+    ex = _exact_product(A, W)
+    for i in range(M):
+        for j in range(N):
+            err = abs(Fraction(C[i, j]) - ex[i][j])
+            assert err <= Fraction(K * 2.0 ** -52) * Fraction(S[i, j]) + Fraction(1, 2 ** 1070)
+            assert abs(C[i, j]) <= S[i, j]
+    # integer activations and unit scales: everything is exact
+    Ai = np.asarray(si.rng(K, 9).integers(-3, 4, size=(M, K)), np.float32)
+    Bi = B.reshape(K, -1, 18).copy()
+    Bi[:, :, 0], Bi[:, :, 1] = 0x00, 0x3C
+    Bi = Bi.reshape(K, -1)
+    Ci, _ = oracle.matmul(Ai, Bi, M, N, K)
+    exi = _exact_product(Ai, oracle.dequant_f32(Bi, K, N))
+    for i in range(M):
+        for j in range(N):
+            assert Fraction(Ci[i, j]) == exi[i][j]
+
+
+def test_fused_equals_textbook():
+    """The fused loop (engine page §3.4) and dequantise-then-triple-loop
+    (§3.1) agree within the fp64 summation bound, for fp32 and bf16 A."""
+    import oracle
+    for dt in ("f32", "bf16"):
+        M, K, N = 3, 200, 160
+        A = si.activations_f32(M, K, 4) if dt == "f32" else si.activations_bf16(M, K, 4)
+        B = si.q4_weights(K, N, seed=4)
+        C, S = oracle.matmul(A, B, M, N, K)
+        Cn = oracle.matmul_naive(A, B, M, N, K)
+        assert np.all(np.abs(C - Cn) <= 2 * K * 2.0 ** -53 * S)
+
+
+def test_scaling_is_exact():
+    """Doubling every scale d (exact in fp16) or every activation doubles C exactly."""
+    import oracle
+    M, K, N = 2, 50, 96
+    A = si.activations_f32(M, K, 5)
+    B = si.q4_weights(K, N, seed=5)
+    C, _ = oracle.matmul(A, B, M, N, K)
+    d = B.reshape(K, -1, 18)[:, :, 0:2].copy().view(np.float16)
+    B2 = B.reshape(K, -1, 18).copy()
+    B2[:, :, 0:2] = (d * np.float16(2)).view(np.uint8)
+    C2, _ = oracle.matmul(A, B2.reshape(K, -1), M, N, K)
+    assert np.array_equal(C2, 2 * C)
+    C3, _ = oracle.matmul(2 * A, B, M, N, K)
+    assert np.array_equal(C3, 2 * C)
+
+
+def test_padding_never_contributes():
+    """Random codes in padding nibbles leave every real output bit-identical
+    (engine page §2.3: columns padded to a multiple of 32)."""
+    import oracle
+    for N in (1, 33, 40, 95):
+        K = 9
+        A = si.activations_f32(2, K, 6)
+        B = si.q4_weights(K, N, seed=6)
+        Br = si.randomise_padding(B, K, N, seed=6, stream=77)
+        assert not np.array_equal(B, Br) or N % 32 == 0
+        C, S = oracle.matmul(A, B, 2, N, K)
+        Cr, Sr = oracle.matmul(A, Br, 2, N, K)
+        assert np.array_equal(C, Cr) and np.array_equal(S, Sr)
+
+
+def test_generator_padding_is_zero_code():
+    """Padding columns hold the zero code q = 8 (reading of 'padding set to zero')."""
+    K, N = 3, 40
+    B = si.q4_weights(K, N, seed=1).reshape(K, 2, 18)
+    last = B[:, 1, 2:]
+    for l in range(N - 32, 32):
+        q = (last[:, l // 2] >> (4 * (l % 2))) & 15
+        assert np.all(q == 8)
+
+
+# ---------------------------------------------------------------- experts
+
+def _expert_closed_form(E, gcodes, ucodes):
+    """H = I = 32 experts whose chain is computable by hand.
+
+    W_gate[e] row 0 holds codes gcodes[e] with d = 1 (other rows zero code),
+    W_up[e] row 0 holds codes ucodes[e], W_down[e] is the identity (row i has
+    code 9 in column i, code 8 elsewhere, d = 1).  With x = e_0 this gives
+    g = q_gate - 8, u = q_up - 8, y = h.
+    """
+    H = I = 32
+
+    def mat(codes_row0):
+        B = np.zeros((H, 1, 18), np.uint8)
+        B[:, :, 0], B[:, :, 1] = 0x00, 0x3C
+        B[:, :, 2:] = 0x88
+        for l, q in enumerate(codes_row0):
+            b = 2 + l // 2
+            if l % 2 == 0:
+                B[0, 0, b] = (B[0, 0, b] & 0xF0) | q
+            else:
+                B[0, 0, b] = (B[0, 0, b] & 0x0F) | (q << 4)
+        return B.reshape(H, 18)
+
+    ident = np.zeros((I, 1, 18), np.uint8)
+    ident[:, :, 0], ident[:, :, 1] = 0x00, 0x3C
+    ident[:, :, 2:] = 0x88
+    for i in range(I):
+        b = 2 + i // 2
+        ident[i, 0, b] = (ident[i, 0, b] & (0x0F if i % 2 else 0xF0)) | (9 << (4 * (i % 2)))
+    Wg = np.stack([mat(gcodes[e]) for e in range(E)])
+    Wu = np.stack([mat(ucodes[e]) for e in range(E)])
+    Wd = np.stack([ident.reshape(I, 18)] * E)
+    return Wg, Wu, Wd
+
+
+def test_moe_closed_form():
+    """out = sum_k w_k * SiLU(g_k) * u_k with g, u known integers; SiLU from
+    its definition g / (1 + e^-g), evaluated with Python's math module."""
+    import oracle
+    E, H, I, T, topk = 3, 32, 32, 1, 2
+    gcodes = [[(l % 16) for l in range(32)], [8] * 32, [(15 - l % 16) for l in range(32)]]
+    ucodes = [[9 + (l % 3) for l in range(32)], [(l % 16) for l in range(32)], [10] * 32]
+    Wg, Wu, Wd = _expert_closed_form(E, gcodes, ucodes)
+    x = np.zeros((T, H), np.float32)
+    x[0, 0] = 1.0
+    idx = np.array([[2, 0]], np.int32)
+    w = np.array([[0.25, 0.75]], np.float32)
+    out, tol, (g, u, h) = oracle.moe(x, Wg, Wu, Wd, idx, w, T, topk, E, H, I, stages=True)
+    for j in range(H):
+        exp = 0.0
+        for k, e in enumerate(idx[0]):
+            gv = gcodes[e][j] - 8
+            uv = ucodes[e][j] - 8
+            exp += float(w[0, k]) * (gv / (1.0 + math.exp(-gv))) * uv
+        assert abs(out[0, j] - exp) <= 1e-15 * (1 + abs(exp)), j
+        assert tol[0, j] >= 1e-6
+    # expert 1 has g = 0 everywhere: SiLU(0) = 0, so routing only to it gives 0
+    out1, _, _ = oracle.moe(x, Wg, Wu, Wd, np.array([[1, 1]], np.int32), w, T, topk, E, H, I)
+    assert np.all(out1 == 0)
+
+
+def test_silu_closed_forms(oracle_lib):
+    assert oracle_lib.silu(0.0) == 0.0
+    assert abs(oracle_lib.silu(1.0) - 1.0 / (1.0 + math.exp(-1.0))) < 1e-16
+    assert oracle_lib.silu(50.0) == pytest.approx(50.0, rel=1e-20)
+    assert abs(oracle_lib.silu(-50.0)) < 1e-19
+    # odd-part identity SiLU(x) - SiLU(-x) = x
+    for xv in (0.3, 1.7, 4.2):
+        assert abs(oracle_lib.silu(xv) - oracle_lib.silu(-xv) - xv) < 1e-15
+
+
+def _small_moe(T=3, E=5, H=64, I=96, topk=2, seed=11):
+    Wg = np.stack([si.q4_weights(H, I, seed, 10 + e) for e in range(E)])
+    Wu = np.stack([si.q4_weights(H, I, seed, 20 + e) for e in range(E)])
+    Wd = np.stack([si.q4_weights(I, H, seed, 30 + e) for e in range(E)])
+    x = si.activations_bf16(T, H, seed)
+    idx, w = si.routing(T, E, topk, seed)
+    return x, Wg, Wu, Wd, idx, w, T, topk, E, H, I
+
+
+def test_moe_invalid_slots_and_linearity():
+    import oracle
+    x, Wg, Wu, Wd, idx, w, T, topk, E, H, I = _small_moe()
+    out, _, _ = oracle.moe(x, Wg, Wu, Wd, idx, w, T, topk, E, H, I)
+    # an out-of-range index contributes nothing
+    bad = idx.copy()
+    bad[:, 1] = E
+    wb = w.copy()
+    out_bad, _, _ = oracle.moe(x, Wg, Wu, Wd, bad, wb, T, topk, E, H, I)
+    only0 = w.copy()
+    only0[:, 1] = 0.0
+    out0, _, _ = oracle.moe(x, Wg, Wu, Wd, idx, only0, T, topk, E, H, I)
+    assert np.array_equal(out_bad, out0)
+    bad[:, 1] = -1
+    out_neg, _, _ = oracle.moe(x, Wg, Wu, Wd, bad, wb, T, topk, E, H, I)
+    assert np.array_equal(out_neg, out0)
+    # linear in the routing weights
+    only1 = w.copy()
+    only1[:, 0] = 0.0
+    out1, _, _ = oracle.moe(x, Wg, Wu, Wd, idx, only1, T, topk, E, H, I)
+    assert np.allclose(out0 + out1, out, rtol=0, atol=1e-12 * (1 + np.abs(out).max()))
+
+
+def test_moe_expert_relabel_invariance():
+    """Renaming experts (permuting the weight stacks and the indices together)
+    leaves the output bit-identical."""
+    import oracle
+    x, Wg, Wu, Wd, idx, w, T, topk, E, H, I = _small_moe()
+    out, tol, _ = oracle.moe(x, Wg, Wu, Wd, idx, w, T, topk, E, H, I)
+    perm = np.array([3, 0, 4, 1, 2])           # new id of old expert e is perm[e]
+    inv = np.argsort(perm)
+    out2, tol2, _ = oracle.moe(x, Wg[inv], Wu[inv], Wd[inv], perm[idx].astype(np.int32), w,
+                               T, topk, E, H, I)
+    assert np.array_equal(out, out2) and np.array_equal(tol, tol2)
+
+
+def test_moe_single_expert_is_matmul_chain():
+    """With one slot of weight 1, out equals down(SiLU(gate x) * up x) built
+    from the oracle's single-matmul pieces (stage values agree too)."""
+    import oracle
+    x, Wg, Wu, Wd, idx, w, T, topk, E, H, I = _small_moe(T=1, topk=1)
+    w = np.ones_like(w)
+    out, _, (g, u, h) = oracle.moe(x, Wg, Wu, Wd, idx, w, T, topk, E, H, I, stages=True)
+    e = int(idx[0, 0])
+    g2, _ = oracle.matmul(x, Wg[e], 1, I, H)
+    u2, _ = oracle.matmul(x, Wu[e], 1, I, H)
+    assert np.array_equal(g[0], g2[0]) and np.array_equal(u[0], u2[0])
+    hv = np.array([oracle.silu(float(v)) for v in g2[0]]) * u2[0]
+    assert np.allclose(h[0], hv, rtol=1e-15, atol=0)
