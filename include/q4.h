@@ -1,0 +1,172 @@
+/*
+ * q4.h -- C ABI of the GB300 (sm_103a) Q4_0 weight-only dequant-matmul library.
+ *
+ * The operation (C++ DeepSeek engine page, "用两千行 C++ 重写一个 DeepSeek 推理引擎",
+ * §2.2 block_q4_0 / dequantize, §2.3 layout and padding, §3.4 matmul_q4_0):
+ *
+ *   B holds a K x N weight matrix W as K rows of nb = ceil(N/32) blocks
+ *   block_q4_0 { uint16 d (IEEE fp16, little-endian); uint8 qs[16]; }  (18 bytes).
+ *   Block (k, b) sits at byte offset (k*nb + b)*18 and covers columns 32b..32b+31
+ *   of row k.  Element l of a block is the low nibble of qs[l/2] for even l and
+ *   the high nibble for odd l; its value is W[k, 32b + l] = (q - 8) * d.
+ *   Columns >= N in the last block of a row are padding: they are never read
+ *   into any output.
+ *
+ *   C[i, j] = sum_k A[i, k] * W[k, j]   (A: M x K row-major, C: M x N row-major)
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers (cudaMalloc / torch CUDA tensors)
+ *     on the current CUDA device.  The caller owns every buffer; the library
+ *     never frees caller memory.
+ *   - Calls are asynchronous on the given stream (NULL = legacy default
+ *     stream); none synchronises the host.  Outputs are overwritten.
+ *   - B, A, C, x, out and workspace must be 16-byte aligned, else Q4_ERR_ALIGN.
+ *   - Integer sizes must be > 0 (K, N, M, T, E, H, I), else Q4_ERR_ARG.
+ *   - Return value: Q4_OK (0) or a negative Q4_ERR_* code; no call traps or
+ *     aborts.  Errors found on the device (a routing index outside [0, E) or
+ *     a wait that timed out) are recorded in a per-device status word that
+ *     q4_get_device_status() reads.
+ *   - There is no CPU fallback: every call runs on the GPU or returns an error.
+ */
+#ifndef Q4_GB300_H
+#define Q4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define Q4_API __attribute__((visibility("default")))
+#else
+#define Q4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---- */
+#define Q4_OK              0
+#define Q4_ERR_ARG        (-1)   /* null pointer, size <= 0, bad enum value      */
+#define Q4_ERR_DTYPE      (-2)   /* unsupported dtype combination                */
+#define Q4_ERR_ALIGN      (-3)   /* a pointer is not 16-byte aligned             */
+#define Q4_ERR_CUDA       (-4)   /* a CUDA runtime call or launch failed         */
+#define Q4_ERR_WORKSPACE  (-5)   /* workspace smaller than the *_workspace_size  */
+#define Q4_ERR_SHAPE      (-6)   /* shape outside what this entry point supports */
+#define Q4_ERR_DEVICE     (-7)   /* q4_get_device_status: device-side error seen */
+
+/* device status bits (q4_get_device_status() returns Q4_ERR_DEVICE and
+ * q4_last_device_flags() the bits) */
+#define Q4_DEVERR_INDEX    0x1u  /* a topk_idx entry outside [0, E) was skipped  */
+#define Q4_DEVERR_TIMEOUT  0x2u  /* a bounded wait gave up; outputs are invalid  */
+
+/* ---- element types ---- */
+#define Q4_F32   0   /* IEEE fp32                        */
+#define Q4_BF16  1   /* bfloat16, passed as raw uint16   */
+
+/* ---- weight layouts ---- */
+#define Q4_LAYOUT_BLOCKS 0   /* the 18-byte block_q4_0 array described above */
+#define Q4_LAYOUT_PLANAR 1   /* q4_repack output: scales plane then nibble plane */
+
+/*
+ * q4_matmul -- C = A . W, fp32 A [M, K], fp32 C [M, N], B in Q4_LAYOUT_BLOCKS,
+ * on the legacy default stream, using a library-owned workspace.
+ * [engine page §3.4: matmul_q4_0(A, B, C, M, N, K), C overwritten as in §3.2]
+ * The library-owned workspace of each device is allocated (cudaMalloc) by the
+ * first call that needs more than it has; make one call of the largest shape
+ * before capturing a stream into a CUDA graph.
+ */
+Q4_API int q4_matmul(float *C, const float *A, const void *B, int64_t M, int64_t N, int64_t K);
+
+/*
+ * q4_matmul_ex -- C = A . W with explicit types, layout, workspace and stream.
+ *   C          [M, N] row-major, c_dtype Q4_F32 or Q4_BF16 (bf16 = RN of fp32)
+ *   A          [M, K] row-major, a_dtype Q4_F32 or Q4_BF16
+ *   B          weights in b_layout (Q4_LAYOUT_BLOCKS or Q4_LAYOUT_PLANAR)
+ *   workspace  device scratch of >= q4_matmul_workspace_size(M, N, K) bytes,
+ *              or NULL to use the library-owned workspace (see q4_matmul).
+ *              A caller-owned workspace must be zero-filled once before its
+ *              first use; the library leaves it zero-filled where it must be.
+ *              Calls that share a workspace must not overlap in time (issue
+ *              them on one stream, or order them with events).
+ *   stream     cudaStream_t (NULL = legacy default stream)
+ * Kernel choice: M <= 64 split-K GEMV on the CUDA cores; larger M with
+ * bf16 A and C uses the tcgen05 tensor-core GEMM when the shape allows it
+ * (N a multiple of 256, K a multiple of 64), otherwise the GEMV in chunks of
+ * rows.
+ * Launches use programmatic dependent launch: a kernel may start streaming
+ * its weights while the previous kernel on the stream finishes, and reads A
+ * only after that kernel has completed.
+ */
+Q4_API int q4_matmul_ex(void *C, int c_dtype, const void *A, int a_dtype,
+                 const void *B, int b_layout, int64_t M, int64_t N, int64_t K,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace q4_matmul_ex needs for this shape (0 if none). */
+Q4_API size_t q4_matmul_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/*
+ * q4_moe_experts -- DeepSeek-V2-style routed experts on the legacy default
+ * stream with the library-owned workspace and top-k = 6
+ * [KTransformers DeepSeek-V2 page, «优化三»: 160 experts, 6 active per token,
+ *  run as batched GEMVs; «规则二»: gate -> top-k indices and weights].
+ *   out       fp32 [T, H]
+ *   x         bf16 [T, H] (raw uint16)
+ *   W_gate    [E] experts x (H rows x ceil(I/32) blocks), Q4_LAYOUT_BLOCKS
+ *   W_up      same shape as W_gate
+ *   W_down    [E] experts x (I rows x ceil(H/32) blocks)
+ *   topk_idx  int32 [T, 6]; entries outside [0, E) are skipped and flagged
+ *   topk_w    fp32 [T, 6]
+ * out[t] = sum_{k=0..5} topk_w[t,k] * ( SiLU(x_t.Wg[e]) * (x_t.Wu[e]) ) . Wd[e],
+ * e = topk_idx[t,k], SiLU(g) = g * sigmoid(g), summed in slot order k.
+ */
+Q4_API int q4_moe_experts(float *out, const void *x, const void *W_gate, const void *W_up,
+                   const void *W_down, const int32_t *topk_idx, const float *topk_w,
+                   int64_t T, int64_t E, int64_t H, int64_t I);
+
+/* q4_moe_experts with x_dtype (Q4_F32 / Q4_BF16), any topk in [1, 16],
+ * an explicit workspace (>= q4_moe_workspace_size, NULL = library-owned) and
+ * a stream. */
+Q4_API int q4_moe_experts_ex(float *out, const void *x, int x_dtype, const void *W_gate,
+                      const void *W_up, const void *W_down, const int32_t *topk_idx,
+                      const float *topk_w, int64_t T, int64_t topk, int64_t E,
+                      int64_t H, int64_t I, void *workspace, size_t workspace_bytes,
+                      void *stream);
+
+Q4_API size_t q4_moe_workspace_size(int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I);
+
+/*
+ * q4_repack / q4_unpack -- lossless change of layout, bit-exact both ways.
+ * Q4_LAYOUT_PLANAR for K x N: the fp16 scales d[K][nb] (little-endian), then,
+ * from byte offset q4_planar_qs_offset(K, N) (a multiple of 16), the nibble
+ * bytes qs[K][nb][16]; q4_planar_bytes(K, N) bytes in all.
+ * dst and src must not overlap.
+ */
+Q4_API int q4_repack(void *dst, const void *src, int64_t K, int64_t N, void *stream);
+Q4_API int q4_unpack(void *dst, const void *src, int64_t K, int64_t N, void *stream);
+Q4_API size_t q4_planar_qs_offset(int64_t K, int64_t N);
+Q4_API size_t q4_planar_bytes(int64_t K, int64_t N);
+
+/*
+ * q4_dequant -- W [K, N] fp32 = (q - 8) * d, exact  [engine page §2.2].
+ * q4_dequant_bf16 -- W [K, N] bf16 bits = bf16 round-to-nearest-even of the
+ * same value: the 16-bit operand the tensor-core path multiplies.
+ */
+Q4_API int q4_dequant(float *W, const void *B, int64_t K, int64_t N, void *stream);
+Q4_API int q4_dequant_bf16(uint16_t *W, const void *B, int64_t K, int64_t N, void *stream);
+
+/* Synchronises `stream`, then reads and clears the device status word of the
+ * current device: Q4_OK, Q4_ERR_DEVICE (bits in q4_last_device_flags()) or
+ * Q4_ERR_CUDA. */
+Q4_API int q4_get_device_status(void *stream);
+Q4_API unsigned int q4_last_device_flags(void);
+
+/* Human-readable text of a status code (static storage). */
+Q4_API const char *q4_status_str(int status);
+
+/* Library ABI version (major*100 + minor). */
+Q4_API int q4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* Q4_GB300_H */

@@ -1,0 +1,214 @@
+"""GB300 (sm_103a) Q4_0 weight-only dequant-matmul: the Python binding.
+
+A thin ctypes layer over the C ABI declared in ``include/q4.h``.  Every
+function marshals arguments only (device pointers, sizes, the current torch
+stream) and calls the library; all arithmetic runs in the CUDA kernels.
+PyTorch provides device memory and streams.
+
+If the compiled library is missing, importing this package raises: there is
+no CPU fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+Q4_OK = 0
+Q4_ERR_ARG = -1
+Q4_ERR_DTYPE = -2
+Q4_ERR_ALIGN = -3
+Q4_ERR_CUDA = -4
+Q4_ERR_WORKSPACE = -5
+Q4_ERR_SHAPE = -6
+Q4_ERR_DEVICE = -7
+Q4_DEVERR_INDEX = 0x1
+Q4_DEVERR_TIMEOUT = 0x2
+Q4_F32 = 0
+Q4_BF16 = 1
+Q4_LAYOUT_BLOCKS = 0
+Q4_LAYOUT_PLANAR = 1
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_sz = ctypes.c_size_t
+_int = ctypes.c_int
+
+# name -> (restype, argtypes), as declared in include/q4.h
+SIGNATURES = {
+    "q4_matmul": (_int, [_vp, _vp, _vp, _i64, _i64, _i64]),
+    "q4_matmul_ex": (_int, [_vp, _int, _vp, _int, _vp, _int, _i64, _i64, _i64, _vp, _sz, _vp]),
+    "q4_matmul_workspace_size": (_sz, [_i64, _i64, _i64]),
+    "q4_moe_experts": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64]),
+    "q4_moe_experts_ex": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _vp, _vp,
+                                 _i64, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
+    "q4_moe_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _i64]),
+    "q4_repack": (_int, [_vp, _vp, _i64, _i64, _vp]),
+    "q4_unpack": (_int, [_vp, _vp, _i64, _i64, _vp]),
+    "q4_planar_qs_offset": (_sz, [_i64, _i64]),
+    "q4_planar_bytes": (_sz, [_i64, _i64]),
+    "q4_dequant": (_int, [_vp, _vp, _i64, _i64, _vp]),
+    "q4_dequant_bf16": (_int, [_vp, _vp, _i64, _i64, _vp]),
+    "q4_get_device_status": (_int, [_vp]),
+    "q4_last_device_flags": (ctypes.c_uint, []),
+    "q4_status_str": (ctypes.c_char_p, [_int]),
+    "q4_version": (_int, []),
+}
+
+
+class Q4Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status} ({status_str(status)})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                raise ImportError(
+                    f"{path} is missing: build it with quantized_weight_q4_gb300._build.build() "
+                    "(or __graft_entry__.build()); there is no CPU fallback")
+            L = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = L
+        return _lib
+
+
+def status_str(status: int) -> str:
+    return lib().q4_status_str(int(status)).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != Q4_OK:
+        raise Q4Error(fn, status)
+
+
+# ------------------------------------------------------------------ helpers
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    """cudaStream_t of a torch stream (default: torch's current stream)."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream or None
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return Q4_F32
+    if t.dtype in (torch.bfloat16, torch.int16, torch.uint16):
+        return Q4_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors (there is no CPU path)")
+        if t is not None and not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+
+
+# ------------------------------------------------------------------ entry points
+def q4_matmul(C, A, B, M: int, N: int, K: int) -> None:
+    """C = A . W (fp32 A and C, legacy default stream), as the C entry point."""
+    _require_cuda(C, A, B)
+    _check("q4_matmul", lib().q4_matmul(_ptr(C), _ptr(A), _ptr(B), M, N, K))
+
+
+def q4_matmul_ex(C, A, B, M: int, N: int, K: int, workspace=None, stream=None,
+                 b_layout: int = Q4_LAYOUT_BLOCKS) -> None:
+    _require_cuda(C, A, B, workspace)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("q4_matmul_ex", lib().q4_matmul_ex(
+        _ptr(C), _dtype_code(C), _ptr(A), _dtype_code(A), _ptr(B), b_layout,
+        M, N, K, _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def q4_matmul_workspace_size(M: int, N: int, K: int) -> int:
+    return lib().q4_matmul_workspace_size(M, N, K)
+
+
+def q4_moe_experts(out, x, W_gate, W_up, W_down, topk_idx, topk_w, T: int, E: int, H: int,
+                   I: int) -> None:
+    _require_cuda(out, x, W_gate, W_up, W_down, topk_idx, topk_w)
+    _check("q4_moe_experts", lib().q4_moe_experts(
+        _ptr(out), _ptr(x), _ptr(W_gate), _ptr(W_up), _ptr(W_down), _ptr(topk_idx),
+        _ptr(topk_w), T, E, H, I))
+
+
+def q4_moe_experts_ex(out, x, W_gate, W_up, W_down, topk_idx, topk_w, T: int, topk: int, E: int,
+                      H: int, I: int, workspace=None, stream=None) -> None:
+    _require_cuda(out, x, W_gate, W_up, W_down, topk_idx, topk_w, workspace)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("q4_moe_experts_ex", lib().q4_moe_experts_ex(
+        _ptr(out), _ptr(x), _dtype_code(x), _ptr(W_gate), _ptr(W_up), _ptr(W_down),
+        _ptr(topk_idx), _ptr(topk_w), T, topk, E, H, I, _ptr(workspace), ws_bytes,
+        _stream(stream)))
+
+
+def q4_moe_workspace_size(T: int, topk: int, E: int, H: int, I: int) -> int:
+    return lib().q4_moe_workspace_size(T, topk, E, H, I)
+
+
+def q4_repack(dst, src, K: int, N: int, stream=None) -> None:
+    _require_cuda(dst, src)
+    _check("q4_repack", lib().q4_repack(_ptr(dst), _ptr(src), K, N, _stream(stream)))
+
+
+def q4_unpack(dst, src, K: int, N: int, stream=None) -> None:
+    _require_cuda(dst, src)
+    _check("q4_unpack", lib().q4_unpack(_ptr(dst), _ptr(src), K, N, _stream(stream)))
+
+
+def q4_planar_qs_offset(K: int, N: int) -> int:
+    return lib().q4_planar_qs_offset(K, N)
+
+
+def q4_planar_bytes(K: int, N: int) -> int:
+    return lib().q4_planar_bytes(K, N)
+
+
+def q4_dequant(W, B, K: int, N: int, stream=None) -> None:
+    _require_cuda(W, B)
+    _check("q4_dequant", lib().q4_dequant(_ptr(W), _ptr(B), K, N, _stream(stream)))
+
+
+def q4_dequant_bf16(W, B, K: int, N: int, stream=None) -> None:
+    _require_cuda(W, B)
+    _check("q4_dequant_bf16", lib().q4_dequant_bf16(_ptr(W), _ptr(B), K, N, _stream(stream)))
+
+
+def q4_get_device_status(stream=None) -> int:
+    return lib().q4_get_device_status(_stream(stream))
+
+
+def q4_last_device_flags() -> int:
+    return lib().q4_last_device_flags()
+
+
+def q4_version() -> int:
+    return lib().q4_version()

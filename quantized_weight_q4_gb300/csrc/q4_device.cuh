@@ -1,0 +1,166 @@
+// Device-side helpers shared by the sm_103a kernels: inline PTX for mbarriers,
+// TMA bulk copies, programmatic dependent launch and packed fp32x2 arithmetic.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+namespace q4 {
+
+constexpr int kBlockBytes = 18;   // sizeof(block_q4_0)
+constexpr int kBlockCols = 32;    // weights per block
+
+// Device status bits (mirrors Q4_DEVERR_* of the public header).
+constexpr unsigned kDevErrIndex = 0x1u;
+constexpr unsigned kDevErrTimeout = 0x2u;
+
+// Upper bound of any spin-wait, in nanoseconds of %globaltimer.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- mbarrier -------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+// Makes initialised barriers visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for phase `parity` of `bar` to complete, giving up after kWaitLimitNs.
+// Returns false on timeout; the caller records the error and stops.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// ---- TMA bulk copy (non-tensor): global -> shared, completes on an mbarrier --
+// Requirements: dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---- programmatic dependent launch ------------------------------------------
+// pdl_wait: blocks until every grid this grid depends on has completed and its
+// memory operations are visible (a no-op when launched without the attribute).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// pdl_launch_dependents: lets the next kernel on the stream begin launching.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---- packed fp32x2 arithmetic (sm_100+) -------------------------------------
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(f32x2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// ---- Q4_0 nibble decoding ---------------------------------------------------
+// A nibble q placed at bit 4p (p = 0..4) of a word ORed with the bit pattern of
+// 2^23 reads as the float 2^23 + q*16^p exactly (it lies in [2^23, 2^24), where
+// floats are the integers).  Subtracting 2^23 + 8*16^p, also exact, leaves
+// 16^p * (q - 8): the signed weight code, scaled by a power of two that the
+// per-block scale factor absorbs.
+constexpr uint32_t kMagic = 0x4B000000u;   // bit pattern of 2^23
+
+__device__ __forceinline__ float nib_f(uint32_t w, uint32_t mask) {
+  return __uint_as_float((w & mask) | kMagic);
+}
+
+// -(2^23 + 8 * 16^p) for p = 0..4
+__device__ __forceinline__ float neg_bias(int p) {
+  return -(8388608.0f + 8.0f * static_cast<float>(1u << (4 * p)));
+}
+
+// Reads the 18-byte block at byte offset `off` of a 4-byte-aligned shared
+// row: returns the fp16 scale bits and the four 32-bit words of qs.
+__device__ __forceinline__ void load_block_smem(const uint8_t* row, uint32_t off, uint32_t& dbits,
+                                                uint32_t (&qs)[4]) {
+  const uint32_t* wp = reinterpret_cast<const uint32_t*>(row + (off & ~3u));
+  const uint32_t w0 = wp[0], w1 = wp[1], w2 = wp[2], w3 = wp[3], w4 = wp[4];
+  const uint32_t odd = off & 2u;   // block starts at 2 mod 4
+  dbits = odd ? (w0 >> 16) : (w0 & 0xFFFFu);
+  const uint32_t sh = odd ? 32u : 16u;
+  qs[0] = __funnelshift_rc(w0, w1, sh);
+  qs[1] = __funnelshift_rc(w1, w2, sh);
+  qs[2] = __funnelshift_rc(w2, w3, sh);
+  qs[3] = __funnelshift_rc(w3, w4, sh);
+}
+
+__device__ __forceinline__ float fp16_bits_to_f32(uint32_t bits) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits) {
+  return __uint_as_float(bits << 16);
+}
+
+}  // namespace q4

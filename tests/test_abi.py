@@ -1,0 +1,84 @@
+"""The C ABI library loads, exports every function include/q4.h declares, and
+rejects bad arguments on the host (no GPU needed: none of these calls reaches
+a CUDA API)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_weight_q4_gb300 as q4
+from quantized_weight_q4_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "q4.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return q4.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"Q4_API\s+[\w\s\*]+?\b(q4_\w+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for must in ("q4_matmul", "q4_moe_experts", "q4_repack", "q4_unpack", "q4_dequant"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert names
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in q4.SIGNATURES, f"binding lacks {n}"
+
+
+def test_binding_has_no_extra_symbols():
+    assert set(q4.SIGNATURES) == set(declared_functions())
+
+
+def test_status_strings(L):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
+        assert q4.status_str(code)
+    assert q4.status_str(-99) == "unknown status"
+    assert L.q4_version() >= 100
+
+
+def test_planar_sizes(L):
+    # K = 3, N = 40: nb = 2, 6 blocks: scales 12 bytes -> qs from 16, 96 qs bytes
+    assert L.q4_planar_qs_offset(3, 40) == 16
+    assert L.q4_planar_bytes(3, 40) == 16 + 6 * 16
+    assert L.q4_planar_bytes(0, 40) == 0
+
+
+def test_argument_errors_on_host(L):
+    vp = ctypes.c_void_p
+    good = vp(0x10000)
+    # null pointers and non-positive sizes
+    assert L.q4_matmul(None, good, good, 1, 32, 32) == q4.Q4_ERR_ARG
+    assert L.q4_matmul(good, good, good, 0, 32, 32) == q4.Q4_ERR_ARG
+    assert L.q4_matmul(good, good, good, 1, -5, 32) == q4.Q4_ERR_ARG
+    # bad dtype and layout codes
+    assert L.q4_matmul_ex(good, 7, good, 0, good, 0, 1, 32, 32, None, 0, None) == q4.Q4_ERR_DTYPE
+    assert L.q4_matmul_ex(good, 0, good, 0, good, 9, 1, 32, 32, None, 0, None) == q4.Q4_ERR_ARG
+    # misaligned pointers
+    bad = vp(0x10004)
+    assert L.q4_matmul(bad, good, good, 1, 32, 32) == q4.Q4_ERR_ALIGN
+    assert L.q4_matmul(good, good, bad, 1, 32, 32) == q4.Q4_ERR_ALIGN
+    # experts
+    args = [good] * 7
+    assert L.q4_moe_experts(None, *args[1:], 1, 160, 5120, 1536) == q4.Q4_ERR_ARG
+    assert L.q4_moe_experts(*args, 0, 160, 5120, 1536) == q4.Q4_ERR_ARG
+    assert L.q4_moe_experts_ex(*args[:2], 0, *args[2:], 1, 17, 160, 5120, 1536, None, 0,
+                               None) == q4.Q4_ERR_SHAPE
+    assert L.q4_moe_experts_ex(*args[:2], 5, *args[2:], 1, 6, 160, 5120, 1536, None, 0,
+                               None) == q4.Q4_ERR_DTYPE
+    assert L.q4_repack(bad, good, 4, 64, None) == q4.Q4_ERR_ALIGN
+    assert L.q4_dequant(good, good, 0, 64, None) == q4.Q4_ERR_ARG
