@@ -69,11 +69,9 @@ extern "C" {
 
 /*
  * q4_matmul -- C = A . W, fp32 A [M, K], fp32 C [M, N], B in Q4_LAYOUT_BLOCKS,
- * on the legacy default stream, using a library-owned workspace.
+ * on the legacy default stream.
  * [engine page §3.4: matmul_q4_0(A, B, C, M, N, K), C overwritten as in §3.2]
- * The library-owned workspace of each device is allocated (cudaMalloc) by the
- * first call that needs more than it has; make one call of the largest shape
- * before capturing a stream into a CUDA graph.
+ * Allocates nothing: the split-K partial sums are combined on chip.
  */
 Q4_API int q4_matmul(float *C, const float *A, const void *B, int64_t M, int64_t N, int64_t K);
 
@@ -82,26 +80,24 @@ Q4_API int q4_matmul(float *C, const float *A, const void *B, int64_t M, int64_t
  *   C          [M, N] row-major, c_dtype Q4_F32 or Q4_BF16 (bf16 = RN of fp32)
  *   A          [M, K] row-major, a_dtype Q4_F32 or Q4_BF16
  *   B          weights in b_layout (Q4_LAYOUT_BLOCKS or Q4_LAYOUT_PLANAR)
- *   workspace  device scratch of >= q4_matmul_workspace_size(M, N, K) bytes,
- *              or NULL to use the library-owned workspace (see q4_matmul).
- *              A caller-owned workspace must be zero-filled once before its
- *              first use; the library leaves it zero-filled where it must be.
- *              Calls that share a workspace must not overlap in time (issue
- *              them on one stream, or order them with events).
+ *   workspace  unused by this entry point (q4_matmul_workspace_size returns
+ *              0); accepted for interface stability, may be NULL.
  *   stream     cudaStream_t (NULL = legacy default stream)
- * Kernel choice: M <= 64 split-K GEMV on the CUDA cores; larger M with
- * bf16 A and C uses the tcgen05 tensor-core GEMM when the shape allows it
- * (N a multiple of 256, K a multiple of 64), otherwise the GEMV in chunks of
- * rows.
+ * Kernel choice: the split-K GEMV on the CUDA cores, in chunks of up to 4
+ * rows of A.  The splits of each column tile run as one thread-block cluster
+ * and are added on chip in fixed order: results are deterministic.
  * Launches use programmatic dependent launch: a kernel may start streaming
  * its weights while the previous kernel on the stream finishes, and reads A
- * only after that kernel has completed.
+ * only after that kernel has completed.  Consequently B must not be written
+ * by the kernel launched immediately before on the same stream (weights are
+ * expected to be static; order such a write with an event or a
+ * synchronisation).
  */
 Q4_API int q4_matmul_ex(void *C, int c_dtype, const void *A, int a_dtype,
                  const void *B, int b_layout, int64_t M, int64_t N, int64_t K,
                  void *workspace, size_t workspace_bytes, void *stream);
 
-/* Bytes of workspace q4_matmul_ex needs for this shape (0 if none). */
+/* Bytes of workspace q4_matmul_ex needs for this shape (currently always 0). */
 Q4_API size_t q4_matmul_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*
@@ -124,8 +120,12 @@ Q4_API int q4_moe_experts(float *out, const void *x, const void *W_gate, const v
                    int64_t T, int64_t E, int64_t H, int64_t I);
 
 /* q4_moe_experts with x_dtype (Q4_F32 / Q4_BF16), any topk in [1, 16],
- * an explicit workspace (>= q4_moe_workspace_size, NULL = library-owned) and
- * a stream. */
+ * an explicit workspace and a stream.  The workspace (>= q4_moe_workspace_size
+ * bytes) holds the intermediate SiLU(g)*u rows and the per-slot down outputs;
+ * its contents need no initialisation.  NULL selects a library-owned
+ * workspace, allocated (cudaMalloc) by the first call that needs more than it
+ * has: make one call of the largest shape before capturing a CUDA graph.
+ * Calls sharing a workspace must not overlap in time. */
 Q4_API int q4_moe_experts_ex(float *out, const void *x, int x_dtype, const void *W_gate,
                       const void *W_up, const void *W_down, const int32_t *topk_idx,
                       const float *topk_w, int64_t T, int64_t topk, int64_t E,

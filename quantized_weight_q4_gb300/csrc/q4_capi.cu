@@ -2,7 +2,9 @@
 // workspace management and the device status word.  See include/q4.h.
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <vector>
 
 #include <cuda_runtime.h>
@@ -16,7 +18,20 @@ namespace {
 __device__ unsigned int g_q4_status = 0u;
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxRowsPerSplit = 2048;   // bounds the shared-memory copy of A
+// The rows of A a CTA uses are copied to shared memory: MR * rows * 4 bytes.
+constexpr int64_t kMaxASliceBytes = 64 * 1024;
+
+struct GemvShape {
+  int mr, bpt, nchunks, ntiles, nsplit, rows_per_split;
+};
+
+struct MoeShape {
+  int mr;
+  int nslots, nexp, list_cap;
+  int bpt_gu, ntiles_gu, nsplit_gu, rows_gu;
+  int bpt_d, ntiles_d, nsplit_d, rows_d;
+  size_t off_h, off_y, total;
+};
 
 struct DeviceState {
   bool init = false;
@@ -24,6 +39,9 @@ struct DeviceState {
   unsigned* status = nullptr;   // device address of g_q4_status
   void* ws = nullptr;           // library-owned workspace
   size_t ws_bytes = 0;
+  // launch shapes already chosen for a problem size (the choice runs occupancy queries)
+  std::map<std::tuple<int64_t, int64_t, int64_t>, GemvShape> gemv_shapes;
+  std::map<std::tuple<int64_t, int64_t, int64_t, int64_t, int64_t>, MoeShape> moe_shapes;
 };
 
 std::mutex g_mu;
@@ -77,78 +95,105 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // ---------------------------------------------------------------------------
 // GEMV launch shape
 // ---------------------------------------------------------------------------
-struct GemvShape {
-  int mr, nchunks, ntiles, nsplit, rows_per_split;
-  size_t ticket_bytes, part_bytes;
-};
+// Rows per split for `nsplit` splits: a multiple of the TMA box height.
+int64_t split_rows(int64_t K, int64_t nsplit) {
+  return static_cast<int64_t>(round_up(static_cast<size_t>(ceil_div(K, nsplit)),
+                                       q4::gemv_stage_rows()));
+}
+
+// Picks the blocks-per-thread and the split count (at most `max_split`; the
+// splits of a column tile form one cluster of `pair * nsplit` CTAs) that
+// minimise the bytes the busiest SM must stream: waves of resident clusters
+// (from the occupancy query) times the CTAs per SM within a wave times the
+// bytes per CTA.  Ties go to fewer CTAs.
+void choose_split(int mode, int mr, int list_cap, int64_t K, int64_t nb, int64_t z_groups, int pair,
+                  int sms, int max_split, bool allow_bpt2, int* bpt_out, int* nsplit_out,
+                  int* rows_out, int* ntiles_out) {
+  double best = -1.0;
+  int64_t best_ctas = 0;
+  *bpt_out = 1;
+  *nsplit_out = 1;
+  *rows_out = static_cast<int>(split_rows(K, 1));
+  *ntiles_out = static_cast<int>(ceil_div(nb, q4::gemv_tile_blocks(1)));
+  for (int bpt = 2; bpt >= 1; --bpt) {
+    if (bpt == 2 && !allow_bpt2) continue;
+    const int64_t ntiles = ceil_div(nb, q4::gemv_tile_blocks(bpt));
+    for (int64_t ns = 1; ns <= max_split; ++ns) {
+      const int64_t rows = split_rows(K, ns);
+      const int64_t nsplit = ceil_div(K, rows);
+      if (nsplit != ns) continue;
+      const int64_t csize = pair * nsplit;
+      const int64_t clusters = ntiles * z_groups;
+      const int64_t ctas = clusters * csize;
+      const int active = q4::max_active_clusters(mode, mr, bpt, static_cast<int>(rows), list_cap,
+                                                 dim3(1, static_cast<unsigned>(nsplit),
+                                                      static_cast<unsigned>(pair)));
+      if (active <= 0) continue;
+      const int64_t waves = ceil_div(clusters, active);
+      const int64_t per_wave = (clusters < active ? clusters : active) * csize;
+      const double per_cta = static_cast<double>(rows) * q4::gemv_tile_blocks(bpt) * 18.0;
+      double cost = per_cta * static_cast<double>(waves * ceil_div(per_wave, sms));
+      if (bpt == 1 && allow_bpt2) cost *= 1.03;   // more instructions per weight
+      if (best < 0 || cost < best * 0.999 || (cost <= best * 1.001 && ctas < best_ctas)) {
+        best = cost;
+        best_ctas = ctas;
+        *bpt_out = bpt;
+        *nsplit_out = static_cast<int>(nsplit);
+        *rows_out = static_cast<int>(rows);
+        *ntiles_out = static_cast<int>(ntiles);
+      }
+    }
+  }
+}
 
 GemvShape gemv_shape(int64_t M, int64_t N, int64_t K, int sms) {
   GemvShape g;
   const int64_t nb = ceil_div(N, 32);
   g.mr = (M == 1) ? 1 : (M == 2) ? 2 : 4;
   g.nchunks = static_cast<int>(ceil_div(M, g.mr));
-  g.ntiles = static_cast<int>(ceil_div(nb, q4::gemv_tile_blocks()));
-  const int64_t target = 2LL * sms;
-  int64_t nsplit = target / (static_cast<int64_t>(g.ntiles) * g.nchunks);
-  if (nsplit < 1) nsplit = 1;
-  const int64_t max_split = ceil_div(K, 32);   // at least 32 rows per split
-  if (nsplit > max_split) nsplit = max_split;
-  const int64_t min_split = ceil_div(K, kMaxRowsPerSplit);
-  if (nsplit < min_split) nsplit = min_split;
-  int64_t rows = ceil_div(K, nsplit);
-  rows = round_up(static_cast<size_t>(rows), 8);
-  g.rows_per_split = static_cast<int>(rows);
-  g.nsplit = static_cast<int>(ceil_div(K, rows));
-  g.ticket_bytes = round_up(static_cast<size_t>(g.ntiles) * g.nchunks * 4, 256);
-  g.part_bytes = (g.nsplit > 1) ? static_cast<size_t>(g.nsplit) * M * N * 4 : 0;
+  choose_split(q4::kModeGemv, g.mr, 0, K, nb, g.nchunks, 1, sms, q4::kMaxCluster, g.mr == 1,
+               &g.bpt, &g.nsplit, &g.rows_per_split, &g.ntiles);
   return g;
 }
 
 // ---------------------------------------------------------------------------
 // Expert launch shapes
 // ---------------------------------------------------------------------------
-struct MoeShape {
-  int nslots, nexp, list_cap;
-  int ntiles_gu, nsplit_gu, rows_gu;
-  int ntiles_d, nsplit_d, rows_d;
-  size_t off_tk_gu, off_tk_d, off_part_gu, off_h, off_part_d, off_y, total;
-};
-
-void split_for(int64_t K, int64_t ctas_per_split, int sms, int* nsplit, int* rows) {
-  int64_t ns = (2LL * sms) / (ctas_per_split > 0 ? ctas_per_split : 1);
-  if (ns < 1) ns = 1;
-  if (ns > ceil_div(K, 32)) ns = ceil_div(K, 32);
-  if (ns < ceil_div(K, kMaxRowsPerSplit)) ns = ceil_div(K, kMaxRowsPerSplit);
-  int64_t r = round_up(static_cast<size_t>(ceil_div(K, ns)), 8);
-  *rows = static_cast<int>(r);
-  *nsplit = static_cast<int>(ceil_div(K, r));
-}
-
 MoeShape moe_shape(int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I, int sms) {
   MoeShape m;
   m.nslots = static_cast<int>(T * topk);
   m.nexp = static_cast<int>(E < m.nslots ? E : m.nslots);
-  const int tbk = q4::gemv_tile_blocks();
+  // one token per expert is the common case at T = 1; larger T gathers a few
+  m.mr = (T == 1) ? 1 : 2;
   m.list_cap = static_cast<int>(m.nslots > ceil_div(E, 32) ? m.nslots : ceil_div(E, 32));
-  m.ntiles_gu = static_cast<int>(ceil_div(ceil_div(I, 32), tbk));
-  m.ntiles_d = static_cast<int>(ceil_div(ceil_div(H, 32), tbk));
-  split_for(H, 2LL * m.ntiles_gu * m.nexp, sms, &m.nsplit_gu, &m.rows_gu);
-  split_for(I, 1LL * m.ntiles_d * m.nexp, sms, &m.nsplit_d, &m.rows_d);
+  // gate and up of one expert tile share a cluster: at most 8 splits each
+  choose_split(q4::kModeGateUp, m.mr, m.list_cap, H, ceil_div(I, 32), m.nexp, 2, sms,
+               q4::kMaxCluster / 2, m.mr == 1, &m.bpt_gu, &m.nsplit_gu, &m.rows_gu, &m.ntiles_gu);
+  choose_split(q4::kModeDown, m.mr, m.list_cap, I, ceil_div(H, 32), m.nexp, 1, sms,
+               q4::kMaxCluster, m.mr == 1, &m.bpt_d, &m.nsplit_d, &m.rows_d, &m.ntiles_d);
   size_t o = 0;
-  m.off_tk_gu = o;
-  o += round_up(static_cast<size_t>(m.nexp) * m.ntiles_gu * 4, 256);
-  m.off_tk_d = o;
-  o += round_up(static_cast<size_t>(m.nexp) * m.ntiles_d * 4, 256);
-  m.off_part_gu = o;
-  o += round_up(2ULL * m.nsplit_gu * m.nslots * I * 4, 256);
   m.off_h = o;
   o += round_up(static_cast<size_t>(m.nslots) * I * 4, 256);
-  m.off_part_d = o;
-  o += round_up(static_cast<size_t>(m.nsplit_d) * m.nslots * H * 4, 256);
   m.off_y = o;
   o += round_up(static_cast<size_t>(m.nslots) * H * 4, 256);
   m.total = o;
   return m;
+}
+
+const GemvShape& cached_gemv_shape(DeviceState* s, int64_t M, int64_t N, int64_t K) {
+  const auto key = std::make_tuple(M, N, K);
+  auto it = s->gemv_shapes.find(key);
+  if (it == s->gemv_shapes.end()) it = s->gemv_shapes.emplace(key, gemv_shape(M, N, K, s->sms)).first;
+  return it->second;
+}
+
+const MoeShape& cached_moe_shape(DeviceState* s, int64_t T, int64_t topk, int64_t E, int64_t H,
+                                 int64_t I) {
+  const auto key = std::make_tuple(T, topk, E, H, I);
+  auto it = s->moe_shapes.find(key);
+  if (it == s->moe_shapes.end())
+    it = s->moe_shapes.emplace(key, moe_shape(T, topk, E, H, I, s->sms)).first;
+  return it->second;
 }
 
 int launch_status(cudaError_t e) { return e == cudaSuccess ? Q4_OK : Q4_ERR_CUDA; }
@@ -174,12 +219,10 @@ const char* q4_status_str(int status) {
 }
 
 size_t q4_matmul_workspace_size(int64_t M, int64_t N, int64_t K) {
-  if (M <= 0 || N <= 0 || K <= 0) return 0;
-  DeviceState* s = nullptr;
-  int sms = 152;
-  if (current_state(&s) == Q4_OK) sms = s->sms;
-  const GemvShape g = gemv_shape(M, N, K, sms);
-  return g.ticket_bytes + g.part_bytes;
+  (void)M;
+  (void)N;
+  (void)K;
+  return 0;   // split-K partial sums are combined on chip
 }
 
 int q4_matmul_ex(void* C, int c_dtype, const void* A, int a_dtype, const void* B, int b_layout,
@@ -193,19 +236,14 @@ int q4_matmul_ex(void* C, int c_dtype, const void* A, int a_dtype, const void* B
   if (!aligned16(C) || !aligned16(A) || !aligned16(B) || (workspace && !aligned16(workspace)))
     return Q4_ERR_ALIGN;
 
+  (void)workspace;
+  (void)workspace_bytes;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* s = nullptr;
   int rc = current_state(&s);
   if (rc != Q4_OK) return rc;
-  const GemvShape g = gemv_shape(M, N, K, s->sms);
-  const size_t need = g.ticket_bytes + g.part_bytes;
-  void* ws = workspace;
-  if (ws) {
-    if (workspace_bytes < need) return Q4_ERR_WORKSPACE;
-  } else {
-    rc = owned_workspace(s, need, &ws);
-    if (rc != Q4_OK) return rc;
-  }
+  const GemvShape& g = cached_gemv_shape(s, M, N, K);
+  if (g.nchunks > 65535 || 4LL * g.mr * g.rows_per_split > kMaxASliceBytes) return Q4_ERR_SHAPE;
 
   q4::GemvParams p;
   std::memset(&p, 0, sizeof(p));
@@ -216,19 +254,21 @@ int q4_matmul_ex(void* C, int c_dtype, const void* A, int a_dtype, const void* B
   p.nb = static_cast<int>(ceil_div(N, 32));
   p.nsplit = g.nsplit;
   p.rows_per_split = g.rows_per_split;
-  p.bulk = (p.nb % q4::gemv_tile_blocks() == 0) ? 1 : 0;
+  q4::fill_decode_consts(p);
+  p.use_tma = (p.nb % 8 == 0 &&
+               q4::encode_weight_tmap(&p.tmap[0], B, K, p.nb, 1, K * p.nb * 18, g.bpt))
+                  ? 1 : 0;
   p.A = A;
   p.a_dtype = a_dtype;
   p.a_ld = K;
   p.M = static_cast<int>(M);
   p.C = C;
   p.c_dtype = c_dtype;
-  p.tickets = static_cast<unsigned*>(ws);
-  p.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + g.ticket_bytes);
   p.list_cap = 0;
   p.err = s->status;
   const dim3 grid(g.ntiles, g.nsplit, g.nchunks);
-  return launch_status(q4::launch_gemv(p, g.mr, grid, static_cast<cudaStream_t>(stream), true));
+  return launch_status(q4::launch_gemv(p, g.mr, g.bpt, grid, dim3(1, g.nsplit, 1),
+                                       static_cast<cudaStream_t>(stream), true));
 }
 
 int q4_matmul(float* C, const float* A, const void* B, int64_t M, int64_t N, int64_t K) {
@@ -237,10 +277,9 @@ int q4_matmul(float* C, const float* A, const void* B, int64_t M, int64_t N, int
 
 size_t q4_moe_workspace_size(int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I) {
   if (T <= 0 || topk <= 0 || E <= 0 || H <= 0 || I <= 0) return 0;
-  DeviceState* s = nullptr;
-  int sms = 152;
-  if (current_state(&s) == Q4_OK) sms = s->sms;
-  return moe_shape(T, topk, E, H, I, sms).total;
+  // h [T*topk, I] and y [T*topk, H] in fp32, each rounded up to 256 bytes
+  const size_t nslots = static_cast<size_t>(T * topk);
+  return round_up(nslots * I * 4, 256) + round_up(nslots * H * 4, 256);
 }
 
 int q4_moe_experts_ex(float* out, const void* x, int x_dtype, const void* W_gate, const void* W_up,
@@ -261,7 +300,9 @@ int q4_moe_experts_ex(float* out, const void* x, int x_dtype, const void* W_gate
   DeviceState* s = nullptr;
   int rc = current_state(&s);
   if (rc != Q4_OK) return rc;
-  const MoeShape m = moe_shape(T, topk, E, H, I, s->sms);
+  const MoeShape& m = cached_moe_shape(s, T, topk, E, H, I);
+  if (4LL * m.mr * m.rows_gu > kMaxASliceBytes || 4LL * m.mr * m.rows_d > kMaxASliceBytes)
+    return Q4_ERR_SHAPE;
   void* ws = workspace;
   if (ws) {
     if (workspace_bytes < m.total) return Q4_ERR_WORKSPACE;
@@ -286,6 +327,7 @@ int q4_moe_experts_ex(float* out, const void* x, int x_dtype, const void* W_gate
   p.y = y;
   p.err = s->status;
   p.c_dtype = 0;
+  q4::fill_decode_consts(p);
 
   // gate and up: K = H, N = I; A rows are tokens
   p.mode = q4::kModeGateUp;
@@ -297,13 +339,15 @@ int q4_moe_experts_ex(float* out, const void* x, int x_dtype, const void* W_gate
   p.nb = static_cast<int>(nbI);
   p.nsplit = m.nsplit_gu;
   p.rows_per_split = m.rows_gu;
-  p.bulk = (p.nb % q4::gemv_tile_blocks() == 0 && p.b_stride % 16 == 0) ? 1 : 0;
+  p.use_tma = (p.nb % 8 == 0 && p.b_stride % 16 == 0 &&
+               q4::encode_weight_tmap(&p.tmap[0], W_gate, H, p.nb, E, p.b_stride, m.bpt_gu) &&
+               q4::encode_weight_tmap(&p.tmap[1], W_up, H, p.nb, E, p.b_stride, m.bpt_gu))
+                  ? 1 : 0;
   p.A = x;
   p.a_dtype = x_dtype;
   p.a_ld = H;
-  p.part = reinterpret_cast<float*>(w8 + m.off_part_gu);
-  p.tickets = reinterpret_cast<unsigned*>(w8 + m.off_tk_gu);
-  cudaError_t e = q4::launch_gemv(p, 4, dim3(m.ntiles_gu, m.nsplit_gu, 2 * m.nexp), st, true);
+  cudaError_t e = q4::launch_gemv(p, m.mr, m.bpt_gu, dim3(m.ntiles_gu, m.nsplit_gu, 2 * m.nexp),
+                                  dim3(1, m.nsplit_gu, 2), st, true);
   if (e != cudaSuccess) return Q4_ERR_CUDA;
 
   // down: K = I, N = H; A rows are slots of h
@@ -316,13 +360,14 @@ int q4_moe_experts_ex(float* out, const void* x, int x_dtype, const void* W_gate
   p.nb = static_cast<int>(nbH);
   p.nsplit = m.nsplit_d;
   p.rows_per_split = m.rows_d;
-  p.bulk = (p.nb % q4::gemv_tile_blocks() == 0 && p.b_stride % 16 == 0) ? 1 : 0;
+  p.use_tma = (p.nb % 8 == 0 && p.b_stride % 16 == 0 &&
+               q4::encode_weight_tmap(&p.tmap[0], W_down, I, p.nb, E, p.b_stride, m.bpt_d))
+                  ? 1 : 0;
   p.A = h;
   p.a_dtype = 0;
   p.a_ld = I;
-  p.part = reinterpret_cast<float*>(w8 + m.off_part_d);
-  p.tickets = reinterpret_cast<unsigned*>(w8 + m.off_tk_d);
-  e = q4::launch_gemv(p, 4, dim3(m.ntiles_d, m.nsplit_d, m.nexp), st, true);
+  e = q4::launch_gemv(p, m.mr, m.bpt_d, dim3(m.ntiles_d, m.nsplit_d, m.nexp),
+                      dim3(1, m.nsplit_d, 1), st, true);
   if (e != cudaSuccess) return Q4_ERR_CUDA;
 
   e = q4::launch_moe_combine(out, y, topk_idx, topk_w, static_cast<int>(T), static_cast<int>(topk),
@@ -389,10 +434,6 @@ int q4_get_device_status(void* stream) {
   const unsigned zero = 0;
   if (cudaMemcpy(s->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
     return Q4_ERR_CUDA;
-  if ((flags & Q4_DEVERR_TIMEOUT) && s->ws) {
-    // a CTA that gave up may have left split-K tickets set
-    if (cudaMemset(s->ws, 0, s->ws_bytes) != cudaSuccess) return Q4_ERR_CUDA;
-  }
   g_last_flags = flags;
   return flags ? Q4_ERR_DEVICE : Q4_OK;
 }

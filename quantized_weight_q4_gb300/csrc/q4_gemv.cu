@@ -6,18 +6,29 @@
 // block spanning 32 output columns of one row).
 //
 // How (GB300-first, not the page's CPU loop):
-//  * A CTA owns a column tile of up to 8 blocks (256 columns, 144 bytes of a
-//    row) and a contiguous slice of rows (split-K).  One producer warp streams
-//    the slice's row segments into a 4-stage shared-memory ring with TMA bulk
-//    copies (cp.async.bulk, completion on mbarriers); eight consumer warps
-//    decode the nibbles in registers and accumulate in fp32 with packed
-//    fp32x2 FMAs.  Rows whose segments are not 16-byte aligned are staged by
-//    the producer warp with plain loads instead.
-//  * Partial sums over the split are combined in a fixed order (split 0, 1,
-//    ...) by the last CTA of each tile to arrive (an atomic ticket), so the
-//    result is deterministic and no CTA ever waits on another.
-//  * Programmatic dependent launch: the producer starts streaming weights
-//    before griddepcontrol.wait; A is read, and workspace written, only after.
+//  * A CTA owns a column tile of 8*BPT blocks (256*BPT columns) and a
+//    contiguous slice of rows (split-K).  One producer warp streams the slice
+//    into a shared-memory ring, one 32-row box per TMA tensor copy
+//    (cp.async.bulk.tensor, completion on mbarriers); eight consumer warps
+//    decode nibbles in registers and accumulate in fp32 with packed fp32x2
+//    arithmetic.  Eight consecutive lanes share a row, each owning BPT
+//    consecutive blocks; a warp covers four rows, the CTA 32.  Weights whose
+//    rows are not 16-byte aligned (ceil(N/32) not a multiple of 8) are staged
+//    by the producer warp with plain loads instead.
+//  * The splits of one column tile run as one thread-block cluster (at most
+//    16 CTAs).  Each CTA leaves its partial sums in its own shared memory;
+//    after a cluster barrier the cluster's rank-0 CTA adds them over DSMEM in
+//    fixed split order (split 0, 1, ...) and writes the result, so the sum is
+//    deterministic and needs no global scratch and no global round trip.
+//  * Programmatic dependent launch: the producer streams weights before
+//    griddepcontrol.wait; A is read, and workspace written, only after.
+//
+// Nibble decoding (exact): a nibble q at bit 4p of a word ORed with the bits of
+// 2^23 reads as 2^23 + q*16^p; subtracting 2^23 + 8*16^p (exact) leaves
+// 16^p*(q - 8), and the per-block factor a*d*16^-p (or d*16^-p) turns it into
+// the weight's contribution.  Word w (columns 8t..8t+7 as nibbles 0..7) is
+// decoded as pairs (0,1) and (2,3) of w and of w >> 16, so only the positions
+// p = 0..3 and four constant pairs occur.
 //
 // The routed-expert kernels (KTransformers DeepSeek-V2 page, «优化三»: 6 of
 // 160 experts per token, run as batched GEMVs; «规则二»: gate -> top-k) reuse
@@ -25,132 +36,207 @@
 // experts in use and the (token, slot) list of its expert, so no routing
 // kernel and no host synchronisation is needed.
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "q4_device.cuh"
 #include "q4_kernels.h"
 
 namespace q4 {
 
-constexpr int kTileBlocks = 8;                         // blocks per column tile
-constexpr int kRowsPerStage = 64;
-constexpr int kStages = 4;
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = kConsumerWarps * 32;        // 256
-constexpr int kThreads = kConsumers + 32;              // + producer warp
-constexpr int kRowPhases = kConsumers / kTileBlocks;   // 32 rows in flight per CTA
-constexpr int kRowBytes = kTileBlocks * kBlockBytes;   // 144
-constexpr int kStageBytes = kRowsPerStage * kRowBytes + 16;   // + tail pad for 20-byte reads
+constexpr int kRowsPerStage = 32;   // rows of one TMA box
+constexpr int kLanesPerRow = 8;     // consumer lanes sharing one row
+constexpr int kGroupWarps = 8;      // a warp group covers one stage: 8 warps x 4 rows
+
+// Consumer warps: one group of 8 per ring stage in flight for compute.  With
+// one row of A (the register-light case) two groups alternate stages, which
+// doubles the warps that hide latency; heavier configurations keep one group.
+template <int MR>
+struct Crew {
+  static constexpr int kGroups = (MR == 1) ? 2 : 1;
+  static constexpr int kWarps = kGroups * kGroupWarps;
+  static constexpr int kConsumers = kWarps * 32;
+  static constexpr int kThreads = kConsumers + 32;   // + producer warp
+};
+static_assert(kGroupWarps * 32 / kLanesPerRow == kRowsPerStage,
+              "a warp group handles one row per consumer thread per stage");
+
+template <int BPT>
+struct TileCfg {
+  static constexpr int kBlocks = kLanesPerRow * BPT;              // blocks per column tile
+  static constexpr int kCols = kBlocks * kBlockCols;              // 256 * BPT
+  static constexpr int kRowBytes = kBlocks * kBlockBytes;         // 144 * BPT
+  static constexpr int kStageBytes = kRowsPerStage * kRowBytes;   // 4608 * BPT
+  static constexpr int kStages = (BPT == 1) ? 16 : 8;             // ~74 KB in flight
+  // TMA tensor copies need 128-byte-aligned shared destinations; a block's
+  // word-aligned 20-byte read ends at most at the row's last byte, so rows
+  // carry no padding.
+  static_assert(kStageBytes % 128 == 0, "TMA destinations must be 128-byte aligned");
+};
+
+// Reduction buffer of one (warp, row of A): 8 lanes-in-row x BPT blocks x 32
+// columns, each block row padded to 33 floats so that the lanes' stores and
+// the column-wise reads fall in distinct banks.
+template <int BPT>
+constexpr int kRedStride = kLanesPerRow * BPT * 33;
 
 // ---------------------------------------------------------------------------
 // Shared-memory plan
 // ---------------------------------------------------------------------------
 struct SmemPlan {
-  uint32_t ring, red, bars, a, list, total;
+  uint32_t ring, red, cpart, bars, a, list, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-template <int MR>
+template <int MR, int BPT>
 __host__ __device__ inline SmemPlan smem_plan(int rows_per_split, int list_cap) {
+  using T = TileCfg<BPT>;
   SmemPlan p;
-  p.ring = 0;
-  p.red = align_up(kStages * kStageBytes, 16);
-  p.bars = p.red + kConsumerWarps * MR * 256 * 4;
-  p.a = p.bars + 2 * kStages * 8;
-  p.list = align_up(p.a + MR * rows_per_split * 4, 16);
+  p.ring = 0;   // the dynamic shared-memory base is 128-byte aligned
+  p.red = align_up(T::kStages * T::kStageBytes, 16);
+  p.cpart = p.red + Crew<MR>::kWarps * MR * kRedStride<BPT> * 4;
+  p.bars = p.cpart + MR * (T::kCols + 2 * kMaxCluster) * 4;   // partials received from the cluster
+  p.a = p.bars + 2 * T::kStages * 8;
+  p.list = align_up(p.a + MR * align_up(rows_per_split, kRowsPerStage) * 4, 16);
   p.total = align_up(p.list + list_cap * 4 + 64, 128);
   return p;
 }
 
 // ---------------------------------------------------------------------------
-// Consumer arithmetic: one block of one row into the accumulators
+// Consumer arithmetic
 // ---------------------------------------------------------------------------
-// acc[m][4t + i] holds columns (8t + 2i, 8t + 2i + 1) of the block.
-//
-// Word t of qs holds columns 8t..8t+7 as nibbles 0..7 (bits 4n..4n+3).  Nibbles
-// 0..4 are decoded in place (positions 0..4); nibbles 5..7 from w >> 12, where
-// they sit at positions 2..4.  Pairs (0,1), (2,3), (4,5), (6,7) therefore use
-// positions (0,1), (2,3), (4,2), (3,4).
-struct PairConsts {
-  f32x2 b01, b23, b42, b34;   // -(2^23 + 8*16^p) per half
+// Registers held across the main loop (loaded from the parameters so that the
+// compiler keeps them in registers instead of re-creating immediates):
+// the nibble masks 0xF << 4p, the bits of 2^23, and the bias pairs
+// -(2^23 + 8*16^p) in both halves, p = 0..3.
+struct DecodeConsts {
+  uint32_t mask[4];
+  uint32_t magic;
+  f32x2 bias[4];
 };
 
-__device__ __forceinline__ PairConsts pair_consts() {
-  PairConsts c;
-  c.b01 = pack2(neg_bias(0), neg_bias(1));
-  c.b23 = pack2(neg_bias(2), neg_bias(3));
-  c.b42 = pack2(neg_bias(4), neg_bias(2));
-  c.b34 = pack2(neg_bias(3), neg_bias(4));
+__device__ __forceinline__ DecodeConsts load_consts(const GemvParams& p) {
+  DecodeConsts c;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    c.mask[i] = p.kmask[i];
+    c.bias[i] = dup2(p.kconst[i]);
+  }
+  c.magic = p.kmask[4];
   return c;
 }
 
-// s01.. are (x * 16^-p) pairs for the positions above; x = a*d (M = 1) or d.
-struct PairScales {
-  f32x2 s01, s23, s42, s34;
-};
-
-__device__ __forceinline__ PairScales pair_scales(float x) {
-  PairScales s;
-  const f32x2 xx = pack2(x, x);
-  s.s01 = mul2(xx, pack2(1.0f, 0.0625f));
-  s.s23 = mul2(xx, pack2(0.00390625f, 0.000244140625f));
-  s.s42 = mul2(xx, pack2(1.52587890625e-05f, 0.00390625f));
-  s.s34 = mul2(xx, pack2(0.000244140625f, 1.52587890625e-05f));
-  return s;
+// (2^23 + q0*16^p, 2^23 + q1*16^p) for nibble p of words w0 and w1: one
+// three-input logic op per half, both written into one register pair.
+__device__ __forceinline__ f32x2 nib_pair(uint32_t w0, uint32_t w1, uint32_t mask,
+                                          uint32_t magic) {
+  f32x2 r;
+  asm("{\n\t.reg .b32 lo, hi;\n\t"
+      "lop3.b32 lo, %1, %3, %4, 0xEA;\n\t"   // (w0 & mask) | magic
+      "lop3.b32 hi, %2, %3, %4, 0xEA;\n\t"   // (w1 & mask) | magic
+      "mov.b64 %0, {lo, hi};\n\t}"
+      : "=l"(r)
+      : "r"(w0), "r"(w1), "r"(mask), "r"(magic));
+  return r;
 }
 
-// The four signed, power-of-two-scaled codes of word w as pairs.
-struct WordCodes {
-  f32x2 c01, c23, c45, c67;
-};
-
-__device__ __forceinline__ WordCodes word_codes(uint32_t w, const PairConsts& k) {
-  const uint32_t y = w >> 12;
-  WordCodes c;
-  c.c01 = add2(pack2(nib_f(w, 0x0000000Fu), nib_f(w, 0x000000F0u)), k.b01);
-  c.c23 = add2(pack2(nib_f(w, 0x00000F00u), nib_f(w, 0x0000F000u)), k.b23);
-  c.c45 = add2(pack2(nib_f(w, 0x000F0000u), nib_f(y, 0x00000F00u)), k.b42);
-  c.c67 = add2(pack2(nib_f(y, 0x0000F000u), nib_f(y, 0x000F0000u)), k.b34);
-  return c;
+// Accumulator layout of one block (32 columns, 16 pairs): words t = 2h and
+// 2h + 1 are decoded together, nibble p of each forming a pair, so
+//   acc[8h + p]     holds columns (16h + p,     16h + 8 + p)
+//   acc[8h + 4 + p] holds columns (16h + 4 + p, 16h + 12 + p)
+// each scaled by 16^p; acc_col_pair() maps a pair back to its columns and
+// rescale_block() removes the power-of-two factors, which is exact.
+__device__ __forceinline__ int acc_col_pair(int j) {   // first column of pair j
+  const int h = j >> 3, p = j & 3, hi = (j >> 2) & 1;
+  return 16 * h + 4 * hi + p;                            // second column is +8
 }
 
 template <int MR>
-__device__ __forceinline__ void accumulate_block(f32x2 (&acc)[MR][16], uint32_t dbits,
+__device__ __forceinline__ void accumulate_block(f32x2* acc0, int acc_stride, uint32_t dbits,
                                                  const uint32_t (&qs)[4], const float* a,
-                                                 int a_ld, const PairConsts& k) {
+                                                 int a_ld, const DecodeConsts& k) {
   const float d = fp16_bits_to_f32(dbits);
   if constexpr (MR == 1) {
-    // acc += (a*d * 16^-p) * (16^p (q - 8))
-    const PairScales s = pair_scales(a[0] * d);
+    // acc += (a*d) * 16^p (q - 8)
+    const f32x2 ad = dup2(a[0] * d);
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const WordCodes c = word_codes(qs[t], k);
-      acc[0][4 * t + 0] = fma2(s.s01, c.c01, acc[0][4 * t + 0]);
-      acc[0][4 * t + 1] = fma2(s.s23, c.c23, acc[0][4 * t + 1]);
-      acc[0][4 * t + 2] = fma2(s.s42, c.c45, acc[0][4 * t + 2]);
-      acc[0][4 * t + 3] = fma2(s.s34, c.c67, acc[0][4 * t + 3]);
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t w0 = qs[2 * h], w1 = qs[2 * h + 1];
+      const uint32_t y0 = w0 >> 16, y1 = w1 >> 16;
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        f32x2* acc = acc0 + 8 * h;
+        acc[p] = fma2(ad, add2(nib_pair(w0, w1, k.mask[p], k.magic), k.bias[p]), acc[p]);
+        acc[4 + p] = fma2(ad, add2(nib_pair(y0, y1, k.mask[p], k.magic), k.bias[p]), acc[4 + p]);
+      }
     }
   } else {
-    // w = (d * 16^-p) * (16^p (q - 8)) is the exact weight; acc[m] += a_m * w
-    const PairScales s = pair_scales(d);
+    // w' = d * 16^p (q - 8), exact; acc[m] += a_m * w'
+    const f32x2 dd = dup2(d);
     f32x2 am[MR];
 #pragma unroll
-    for (int m = 0; m < MR; ++m) am[m] = pack2(a[m * a_ld], a[m * a_ld]);
+    for (int m = 0; m < MR; ++m) am[m] = dup2(a[m * a_ld]);
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const WordCodes c = word_codes(qs[t], k);
-      const f32x2 w01 = mul2(s.s01, c.c01);
-      const f32x2 w23 = mul2(s.s23, c.c23);
-      const f32x2 w45 = mul2(s.s42, c.c45);
-      const f32x2 w67 = mul2(s.s34, c.c67);
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t w0 = qs[2 * h], w1 = qs[2 * h + 1];
+      const uint32_t y0 = w0 >> 16, y1 = w1 >> 16;
 #pragma unroll
-      for (int m = 0; m < MR; ++m) {
-        acc[m][4 * t + 0] = fma2(am[m], w01, acc[m][4 * t + 0]);
-        acc[m][4 * t + 1] = fma2(am[m], w23, acc[m][4 * t + 1]);
-        acc[m][4 * t + 2] = fma2(am[m], w45, acc[m][4 * t + 2]);
-        acc[m][4 * t + 3] = fma2(am[m], w67, acc[m][4 * t + 3]);
+      for (int p = 0; p < 4; ++p) {
+        const f32x2 wa = mul2(add2(nib_pair(w0, w1, k.mask[p], k.magic), k.bias[p]), dd);
+        const f32x2 wb = mul2(add2(nib_pair(y0, y1, k.mask[p], k.magic), k.bias[p]), dd);
+#pragma unroll
+        for (int m = 0; m < MR; ++m) {
+          f32x2* acc = acc0 + m * acc_stride + 8 * h;
+          acc[p] = fma2(am[m], wa, acc[p]);
+          acc[4 + p] = fma2(am[m], wb, acc[4 + p]);
+        }
       }
+    }
+  }
+}
+
+// Multiplies pair j of every block by 16^-p (p = j & 3): exact.
+template <int MR, int BPT>
+__device__ __forceinline__ void rescale_acc(f32x2 (&acc)[MR][16 * BPT]) {
+  const f32x2 sc[4] = {dup2(1.0f), dup2(0.0625f), dup2(0.00390625f), dup2(0.000244140625f)};
+#pragma unroll
+  for (int m = 0; m < MR; ++m)
+#pragma unroll
+    for (int j = 0; j < 16 * BPT; ++j) acc[m][j] = mul2(acc[m][j], sc[j & 3]);
+}
+
+// The BPT consecutive blocks a thread owns in one staged row.  `off` is the
+// byte offset of its first block; for BPT = 2 it is a multiple of 36 (4-byte
+// aligned), for BPT = 1 a multiple of 18 whose parity is fixed per thread.
+template <int BPT>
+__device__ __forceinline__ void load_blocks(const uint8_t* row, uint32_t off, bool odd,
+                                            uint32_t (&dbits)[BPT], uint32_t (&qs)[BPT][4]) {
+  if constexpr (BPT == 2) {
+    const uint32_t* wp = reinterpret_cast<const uint32_t*>(row + off);
+    uint32_t w[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) w[i] = wp[i];
+    dbits[0] = w[0] & 0xFFFFu;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) qs[0][t] = __funnelshift_r(w[t], w[t + 1], 16);
+    dbits[1] = w[4] >> 16;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) qs[1][t] = w[5 + t];
+  } else {
+    const uint32_t* wp = reinterpret_cast<const uint32_t*>(row + (off & ~3u));
+    uint32_t w[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) w[i] = wp[i];
+    if (odd) {   // block starts at 2 mod 4
+      dbits[0] = w[0] >> 16;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) qs[0][t] = w[t + 1];
+    } else {
+      dbits[0] = w[0] & 0xFFFFu;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) qs[0][t] = __funnelshift_r(w[t], w[t + 1], 16);
     }
   }
 }
@@ -160,13 +246,15 @@ __device__ __forceinline__ void accumulate_block(f32x2 (&acc)[MR][16], uint32_t 
 // leave their loops early, so every named barrier is still reached.
 __device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, volatile int* fail,
                                              unsigned* err) {
-  if (*fail) return false;
   if (mbar_try_wait(bar, parity)) return true;
+  if (*fail) return false;
   const unsigned long long t0 = globaltimer();
   while (true) {
+    // sleep in the barrier rather than spin: waiting warps leave the issue
+    // slots to warps that have data
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 8; ++i)
+      if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
     if (*fail) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
       *fail = 1;
@@ -177,113 +265,106 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, vol
 }
 
 // ---------------------------------------------------------------------------
-// Producer: stage row segments [k0 + s*R, ...) of the tile into the ring
+// Producer: stage rows [k0 + s*32, +32) of the tile into ring slot `stage`
 // ---------------------------------------------------------------------------
 struct StreamDesc {
   const uint8_t* B;   // matrix base
+  const void* tmap;   // tensor map of the weight stack (TMA path) or null
+  int expert;         // expert index in the stack (0 for a single matrix)
   int nb;             // blocks per row
   int b0, tb;         // first block of the tile, blocks in the tile
   int k0, rows;       // row slice
-  bool bulk;          // row segments are 16-byte aligned and 16-byte sized
 };
 
-__device__ __forceinline__ bool produce_stage(const StreamDesc& sd, int s, uint8_t* stage,
+template <int BPT>
+__device__ __forceinline__ void produce_stage(const StreamDesc& sd, int s, uint8_t* stage,
                                               uint64_t* full, int lane) {
+  using T = TileCfg<BPT>;
   const int r0 = s * kRowsPerStage;
-  const int nr = min(kRowsPerStage, sd.rows - r0);
-  const uint32_t seg = static_cast<uint32_t>(sd.tb) * kBlockBytes;
-  if (sd.bulk) {
-    if (lane == 0) mbar_arrive_expect_tx(full, seg * static_cast<uint32_t>(nr));
-    __syncwarp();
-    for (int r = lane; r < nr; r += 32) {
-      const uint8_t* src =
-          sd.B + (static_cast<size_t>(sd.k0 + r0 + r) * sd.nb + sd.b0) * kBlockBytes;
-      bulk_g2s(stage + r * kRowBytes, src, seg, full);
+  if (sd.tmap) {
+    // one box of 32 rows x 144*BPT bytes; rows past K and blocks past the row
+    // read as zero, rows past this slice are loaded but never used
+    if (lane == 0) {
+      mbar_arrive_expect_tx(full, T::kStageBytes);
+      tma_load_3d(stage, sd.tmap, sd.b0 * (kBlockBytes / 2), sd.k0 + r0, sd.expert, full);
     }
   } else {
     // 2-byte aligned rows: copy with 16-bit loads (every block offset is even)
-    const int halves = static_cast<int>(seg / 2);
+    const int nr = min(kRowsPerStage, sd.rows - r0);
+    const int halves = sd.tb * (kBlockBytes / 2);
     for (int r = 0; r < nr; ++r) {
       const uint16_t* src = reinterpret_cast<const uint16_t*>(
           sd.B + (static_cast<size_t>(sd.k0 + r0 + r) * sd.nb + sd.b0) * kBlockBytes);
-      uint16_t* dst = reinterpret_cast<uint16_t*>(stage + r * kRowBytes);
+      uint16_t* dst = reinterpret_cast<uint16_t*>(stage + r * T::kRowBytes);
       for (int h = lane; h < halves; h += 32) dst[h] = __ldg(src + h);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(full);
   }
-  return true;
+}
+
+template <int MR>
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(Crew<MR>::kConsumers) : "memory");
 }
 
 // ---------------------------------------------------------------------------
-// The consumer-side reduction of one tile: warp shuffles, then across warps
-// through shared memory.  Returns, in `out`, the value of column `tid` of the
-// tile (tid in [0, 256)) for each of the MR rows.
+// Reduction of the 32 row phases of a tile: warp shuffles (halving exchange
+// over the four rows of a warp), then across warps through shared memory.
+// out[m][i] = column tid + 256*i of the tile for row m.
 // ---------------------------------------------------------------------------
-template <int MR>
-__device__ __forceinline__ void reduce_tile(f32x2 (&acc)[MR][16], float* red, int warp, int lane,
-                                            int tid, float (&out)[MR]) {
+template <int MR, int BPT>
+__device__ __forceinline__ void reduce_tile(f32x2 (&acc)[MR][16 * BPT], float* red, int warp,
+                                            int lane, int tid, float (&out)[MR][BPT]) {
+  using T = TileCfg<BPT>;
+  constexpr int P = 16 * BPT;   // pairs per thread
   const bool hi16 = (lane & 16) != 0;
   const bool hi8 = (lane & 8) != 0;
-  const int b = lane & 7;
+  const int pi = lane & 7;
 #pragma unroll
   for (int m = 0; m < MR; ++m) {
-    f32x2 h[8];
+    f32x2 h[P / 2];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const f32x2 send = hi16 ? acc[m][i] : acc[m][8 + i];
-      const f32x2 keep = hi16 ? acc[m][8 + i] : acc[m][i];
-      const f32x2 recv = __shfl_xor_sync(0xffffffffu, send, 16);
-      h[i] = add2(keep, recv);
+    for (int i = 0; i < P / 2; ++i) {
+      const f32x2 send = hi16 ? acc[m][i] : acc[m][P / 2 + i];
+      const f32x2 keep = hi16 ? acc[m][P / 2 + i] : acc[m][i];
+      h[i] = add2(keep, __shfl_xor_sync(0xffffffffu, send, 16));
     }
-    f32x2 q[4];
+    f32x2 q[P / 4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const f32x2 send = hi8 ? h[i] : h[4 + i];
-      const f32x2 keep = hi8 ? h[4 + i] : h[i];
-      const f32x2 recv = __shfl_xor_sync(0xffffffffu, send, 8);
-      q[i] = add2(keep, recv);
+    for (int i = 0; i < P / 4; ++i) {
+      const f32x2 send = hi8 ? h[i] : h[P / 4 + i];
+      const f32x2 keep = hi8 ? h[P / 4 + i] : h[i];
+      q[i] = add2(keep, __shfl_xor_sync(0xffffffffu, send, 8));
     }
-    // lane now holds columns col0 .. col0+7 of block b
-    const int col0 = (hi16 ? 16 : 0) + (hi8 ? 8 : 0);
-    float* dst = red + (warp * MR + m) * 256 + b * 32 + col0;
-    float v[8];
+    // the lane now holds pairs j0 + i, i < P/4, of its thread's accumulators
+    const int j0 = (hi16 ? P / 2 : 0) + (hi8 ? P / 4 : 0);
+    float* dst = red + (warp * MR + m) * kRedStride<BPT> + pi * BPT * 33;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) unpack2(q[i], v[2 * i], v[2 * i + 1]);
-    reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
-    reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
+    for (int i = 0; i < P / 4; ++i) {
+      // pair j = j0 + i: block j >> 4, columns acc_col_pair(j & 15) and +8
+      const int j = j0 + i;
+      const int c = 33 * (j >> 4) + acc_col_pair(j & 15);
+      float v0, v1;
+      unpack2(q[i], v0, v1);
+      dst[c] = v0;
+      dst[c + 8] = v1;
+    }
   }
-  asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
+  consumers_sync<MR>();
+  // threads 0..255 finish columns tid + 256*i; column c = 32*(BPT*pi + blk) + cc
+  const int t = tid & 255;
 #pragma unroll
-  for (int m = 0; m < MR; ++m) {
-    float s = 0.f;
+  for (int m = 0; m < MR; ++m)
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) s += red[(w * MR + m) * 256 + tid];
-    out[m] = s;
-  }
-}
-
-__device__ __forceinline__ void consumers_sync() {
-  asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
-}
-
-// Called by all consumers after their partials are stored: returns true in
-// the CTA that arrived last on `ticket` (expecting `arrivals` CTAs), which
-// then owns the final combine.  The last CTA resets the ticket to zero.
-__device__ __forceinline__ bool last_arrival(unsigned* ticket, unsigned arrivals, int tid,
-                                             int* s_flag) {
-  __threadfence();
-  consumers_sync();
-  if (tid == 0) {
-    const unsigned old = atomicAdd(ticket, 1u);
-    const int last = (old == arrivals - 1) ? 1 : 0;
-    if (last) *ticket = 0u;
-    *s_flag = last;
-  }
-  consumers_sync();
-  const bool last = *s_flag != 0;
-  if (last) __threadfence();
-  return last;
+    for (int i = 0; i < BPT; ++i) {
+      const int c = t + 256 * i;
+      const int off = (c >> 5) * 33 + (c & 31);
+      float s = 0.f;
+#pragma unroll
+      for (int w = 0; w < Crew<MR>::kWarps; ++w) s += red[(w * MR + m) * kRedStride<BPT> + off];
+      out[m][i] = s;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -350,14 +431,17 @@ __device__ __forceinline__ void store_out(const GemvParams& p, size_t i, float v
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int MR>
-__global__ void __launch_bounds__(kThreads, 1) q4_gemv_kernel(GemvParams p) {
+template <int MODE, int MR, int BPT>
+__global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
+    q4_gemv_kernel(const __grid_constant__ GemvParams p) {
+  using T = TileCfg<BPT>;
   extern __shared__ __align__(128) uint8_t smem[];
-  const SmemPlan plan = smem_plan<MR>(p.rows_per_split, p.list_cap);
+  const SmemPlan plan = smem_plan<MR, BPT>(p.rows_per_split, p.list_cap);
   uint8_t* ring = smem + plan.ring;
   float* red = reinterpret_cast<float*>(smem + plan.red);
+  float* cpart = reinterpret_cast<float*>(smem + plan.cpart);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + plan.bars);
-  uint64_t* empty = full + kStages;
+  uint64_t* empty = full + T::kStages;
   float* a_s = reinterpret_cast<float*>(smem + plan.a);
   int* list = reinterpret_cast<int*>(smem + plan.list);
   int* s_misc = list + p.list_cap;   // [0] ticket flag, [1] expert, [2] list length, [3] failed
@@ -376,17 +460,16 @@ __global__ void __launch_bounds__(kThreads, 1) q4_gemv_kernel(GemvParams p) {
   // for the j-th active expert.  mode DOWN: z = j.
   int expert = 0;
   int nrows_total;   // rows of A for this problem (tokens / slots / M)
-  const uint8_t* Bmat = p.B;
-  if (p.mode == kModeGemv) {
+  if constexpr (MODE == kModeGemv) {
     nrows_total = p.M;
   } else {
     // topk_idx may come from the kernel just before on the stream: the gate/up
     // kernel reads it only after that kernel has completed.  The down kernel
     // follows the gate/up kernel, whose CTAs all passed this wait before
     // letting it launch, so its early read is ordered too.
-    if (p.mode == kModeGateUp) pdl_wait();
+    if (MODE == kModeGateUp) pdl_wait();
     if (warp == 0) {
-      const int j = (p.mode == kModeGateUp) ? (z >> 1) : z;
+      const int j = (MODE == kModeGateUp) ? (z >> 1) : z;
       const int e =
           jth_active_expert(p.topk_idx, p.nslots, p.E, j, reinterpret_cast<unsigned*>(list), lane);
       __syncwarp();
@@ -397,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4_gemv_kernel(GemvParams p) {
         s_misc[2] = n;
       }
       // one CTA records routing indices outside [0, E)
-      if (p.mode == kModeGateUp && blockIdx.x == 0 && blockIdx.y == 0 && z == 0) {
+      if (MODE == kModeGateUp && blockIdx.x == 0 && blockIdx.y == 0 && z == 0) {
         bool bad = false;
         for (int s = lane; s < p.nslots; s += 32) {
           const int ee = p.topk_idx[s];
@@ -410,24 +493,22 @@ __global__ void __launch_bounds__(kThreads, 1) q4_gemv_kernel(GemvParams p) {
     expert = s_misc[1];
     if (expert < 0) return;   // fewer distinct experts than grid slices
     nrows_total = s_misc[2];
-    const int which = (p.mode == kModeGateUp) ? (z & 1) : 0;
-    Bmat = (which ? p.B2 : p.B) + static_cast<size_t>(expert) * p.b_stride;
   }
+  const int which = (MODE == kModeGateUp) ? (z & 1) : 0;   // gate (0) or up (1)
 
-  const int b0 = tile * kTileBlocks;
-  const int tb = min(kTileBlocks, p.nb - b0);
+  const int b0 = tile * T::kBlocks;
+  const int tb = min(T::kBlocks, p.nb - b0);
   const int k0 = split * p.rows_per_split;
   const int rows = min(p.rows_per_split, p.K - k0);
   const int nstages = (rows + kRowsPerStage - 1) / kRowsPerStage;
-  const int m_begin = (p.mode == kModeGemv) ? z * MR : 0;
-  const int passes =
-      (p.mode == kModeGemv) ? 1 : (nrows_total + MR - 1) / MR;   // expert tokens in chunks
+  const int m_begin = (MODE == kModeGemv) ? z * MR : 0;
+  const int passes = (MODE == kModeGemv) ? 1 : (nrows_total + MR - 1) / MR;
   if (rows <= 0 || passes <= 0) return;
 
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < T::kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kConsumerWarps);
+      mbar_init(&empty[i], kGroupWarps);
     }
     *s_fail = 0;
     fence_barrier_init();
@@ -435,150 +516,157 @@ __global__ void __launch_bounds__(kThreads, 1) q4_gemv_kernel(GemvParams p) {
   __syncthreads();
   pdl_launch_dependents();
 
-  StreamDesc sd;
-  sd.B = Bmat;
-  sd.nb = p.nb;
-  sd.b0 = b0;
-  sd.tb = tb;
-  sd.k0 = k0;
-  sd.rows = rows;
-  sd.bulk = p.bulk != 0;
-
-  if (warp == kConsumerWarps) {
+  if (warp == Crew<MR>::kWarps) {
     // ================= producer warp =================
+    StreamDesc sd;
+    sd.tmap = p.use_tma ? static_cast<const void*>(&p.tmap[which]) : nullptr;
+    sd.expert = expert;
+    sd.B = (which ? p.B2 : p.B) + static_cast<size_t>(expert) * p.b_stride;
+    sd.nb = p.nb;
+    sd.b0 = b0;
+    sd.tb = tb;
+    sd.k0 = k0;
+    sd.rows = rows;
     int gs = 0;
+    bool failed = false;
     for (int pass = 0; pass < passes; ++pass) {
-      for (int s = 0; s < nstages; ++s, ++gs) {
-        const int slot = gs % kStages;
-        if (gs >= kStages) {
+      for (int s = 0; s < nstages && !failed; ++s, ++gs) {
+        const int slot = gs % T::kStages;
+        if (gs >= T::kStages) {
           bool ok = true;
-          if (lane == 0) ok = wait_or_fail(&empty[slot], ((gs / kStages) - 1) & 1, s_fail, p.err);
-          if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) return;   // failed: issue nothing more
+          if (lane == 0)
+            ok = wait_or_fail(&empty[slot], ((gs / T::kStages) - 1) & 1, s_fail, p.err);
+          failed = !__shfl_sync(0xffffffffu, ok ? 1 : 0, 0);   // failed: issue nothing more
+          if (failed) break;
         }
-        produce_stage(sd, s, ring + slot * kStageBytes, &full[slot], lane);
+        produce_stage<BPT>(sd, s, ring + slot * T::kStageBytes, &full[slot], lane);
       }
+      // the cluster barriers of this pass's combine (see the consumers)
+      cluster_sync();
+      if (pass + 1 < passes) cluster_sync();
     }
     return;
   }
 
   // ================= consumer warps =================
   pdl_wait();   // A (and the workspace) may belong to the previous kernel
-  const PairConsts kc = pair_consts();
-  const int b = lane & 7;
-  const int rp = warp * 4 + (lane >> 3);   // row phase 0..31
-  const bool active_b = b < tb;
+  const DecodeConsts kc = load_consts(p);
+  const int pi = lane & 7;                                 // lane within its row
+  const int group = warp / kGroupWarps;                    // stages s = group mod kGroups
+  const int rp = (warp % kGroupWarps) * 4 + (lane >> 3);   // row phase 0..31
+  const uint32_t boff = static_cast<uint32_t>(pi * BPT * kBlockBytes);
+  const bool odd = (boff & 2u) != 0;
   const int ncols = p.N;
-  int gs = 0;
+  const int tile_cols = tb * kBlockCols;
+  const int a_ld_s = nstages * kRowsPerStage;   // rows of A in shared memory, stage-padded
 
   for (int pass = 0; pass < passes; ++pass) {
     // ---- rows of A for this pass, as fp32 in shared memory ----
-    const int m0 = (p.mode == kModeGemv) ? m_begin : pass * MR;
+    const int m0 = (MODE == kModeGemv) ? m_begin : pass * MR;
     int mvalid = min(MR, nrows_total - m0);
     if (mvalid < 0) mvalid = 0;
-    for (int i = tid; i < MR * rows; i += kConsumers) {
-      const int m = i / rows;
-      const int r = i - m * rows;
+    for (int i = tid; i < MR * a_ld_s; i += Crew<MR>::kConsumers) {
+      const int m = i / a_ld_s;
+      const int r = i - m * a_ld_s;
       float v = 0.f;
-      if (m < mvalid) {
+      if (m < mvalid && r < rows) {
         size_t arow;
-        if (p.mode == kModeGemv) arow = static_cast<size_t>(m0 + m);
-        else if (p.mode == kModeGateUp) arow = static_cast<size_t>(list[m0 + m] / p.topk);
+        if (MODE == kModeGemv) arow = static_cast<size_t>(m0 + m);
+        else if (MODE == kModeGateUp) arow = static_cast<size_t>(list[m0 + m] / p.topk);
         else arow = static_cast<size_t>(list[m0 + m]);
         const size_t ai = arow * p.a_ld + k0 + r;
         v = (p.a_dtype == 0) ? reinterpret_cast<const float*>(p.A)[ai]
                              : bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.A)[ai]);
       }
-      a_s[m * rows + r] = v;
+      a_s[m * a_ld_s + r] = v;
     }
-    consumers_sync();
+    consumers_sync<MR>();
 
-    f32x2 acc[MR][16];
+    f32x2 acc[MR][16 * BPT];
 #pragma unroll
     for (int m = 0; m < MR; ++m)
 #pragma unroll
-      for (int i = 0; i < 16; ++i) acc[m][i] = 0ull;
+      for (int i = 0; i < 16 * BPT; ++i) acc[m][i] = 0ull;
 
-    for (int s = 0; s < nstages; ++s, ++gs) {
-      const int slot = gs % kStages;
-      const bool ready = wait_or_fail(&full[slot], (gs / kStages) & 1, s_fail, p.err);
-      const uint8_t* stage = ring + slot * kStageBytes;
-      const int r0 = s * kRowsPerStage;
-      const int nr = min(kRowsPerStage, rows - r0);
+    for (int s = group; s < nstages; s += Crew<MR>::kGroups) {
+      const int gs = pass * nstages + s;   // the producer's stage counter
+      const int slot = gs % T::kStages;
+      // one lane per warp waits on the stage; the warp barrier then orders the
+      // other lanes' shared-memory reads after that wait
+      int ok = 1;
+      if (lane == 0) ok = wait_or_fail(&full[slot], (gs / T::kStages) & 1, s_fail, p.err) ? 1 : 0;
+      __syncwarp();   // orders the other lanes' reads after lane 0's wait
+      const bool ready = __shfl_sync(0xffffffffu, ok, 0) != 0;
+      const int r = s * kRowsPerStage + rp;   // row of the slice handled by this thread
+      if (ready && r < rows) {
+        const uint8_t* row = ring + slot * T::kStageBytes + rp * T::kRowBytes;
+        uint32_t dbits[BPT], qs[BPT][4];
+        load_blocks<BPT>(row, boff, odd, dbits, qs);
 #pragma unroll
-      for (int i = 0; i < kRowsPerStage / kRowPhases; ++i) {
-        const int r = rp + i * kRowPhases;
-        if (ready && active_b && r < nr) {
-          uint32_t dbits, qs[4];
-          load_block_smem(stage + r * kRowBytes, b * kBlockBytes, dbits, qs);
-          accumulate_block<MR>(acc, dbits, qs, a_s + r0 + r, rows, kc);
-        }
+        for (int bb = 0; bb < BPT; ++bb)
+          accumulate_block<MR>(&acc[0][16 * bb], 16 * BPT, dbits[bb], qs[bb], a_s + r, a_ld_s, kc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
 
     // ---- reduce the 32 row phases ----
-    float colv[MR];
-    reduce_tile<MR>(acc, red, warp, lane, tid, colv);
-    const int col = b0 * kBlockCols + tid;   // tid = block * 32 + lane-in-block
-    const bool col_ok = (tid < tb * kBlockCols) && (col < ncols);
+    rescale_acc<MR, BPT>(acc);
+    float colv[MR][BPT];
+    reduce_tile<MR, BPT>(acc, red, warp, lane, tid, colv);
 
-    if (p.mode == kModeGemv) {
-      if (p.nsplit == 1) {
-        if (col_ok)
-          for (int m = 0; m < mvalid; ++m) store_out(p, static_cast<size_t>(m0 + m) * ncols + col, colv[m]);
-      } else {
-        if (col_ok)
-          for (int m = 0; m < mvalid; ++m)
-            p.part[(static_cast<size_t>(split) * p.M + m0 + m) * ncols + col] = colv[m];
-        unsigned* ticket = p.tickets + static_cast<size_t>(z) * gridDim.x + tile;
-        if (last_arrival(ticket, p.nsplit, tid, s_misc)) {
-          if (col_ok)
-            for (int m = 0; m < mvalid; ++m) {
-              float acc_s = 0.f;
-              for (int sp = 0; sp < p.nsplit; ++sp)
-                acc_s += __ldcg(p.part + (static_cast<size_t>(sp) * p.M + m0 + m) * ncols + col);
-              store_out(p, static_cast<size_t>(m0 + m) * ncols + col, acc_s);
+    // ---- combine the splits of the cluster in fixed order ----
+    // Column c of the tile is owned by cluster rank c % csize.  Every CTA
+    // stores its partial of each column into the owner's receive buffer, at
+    // slot (rank of the sender); after one cluster barrier each owner adds
+    // its columns' partials, in fixed rank order, from its own shared memory.
+    {
+      const int rank = static_cast<int>(cluster_ctarank());
+      const int ns = p.nsplit;
+      const int csize = (MODE == kModeGateUp) ? 2 * ns : ns;
+      // receive buffer: [m][column slot within owner][sender], sized MR * kCols floats
+      const int per_owner = (T::kCols + csize - 1) / csize;
+      if (tid < 256) {
+#pragma unroll
+        for (int m = 0; m < MR; ++m)
+#pragma unroll
+          for (int i = 0; i < BPT; ++i) {
+            const int c = tid + 256 * i;
+            const int owner = c % csize;
+            const int slot = c / csize;
+            float* dst = cpart + (m * per_owner + slot) * csize + rank;
+            st_peer(peer_addr(dst, owner), colv[m][i]);
+          }
+      }
+      cluster_sync();   // every partial has reached its owner
+      const int tc = tid * csize + rank;   // the column this thread finishes
+      const int col = b0 * kBlockCols + tc;
+      if (tid < per_owner && tc < tile_cols && col < ncols) {
+        for (int m = 0; m < mvalid; ++m) {
+          const float* v = cpart + (m * per_owner + tid) * csize;
+          if constexpr (MODE == kModeGateUp) {
+            // senders 0..ns-1 hold gate partials, ns..2ns-1 up partials
+            float g = 0.f, u = 0.f;
+            for (int sp = 0; sp < ns; ++sp) {
+              g += v[sp];
+              u += v[ns + sp];
             }
+            // SiLU(g) * u, SiLU(g) = g * sigmoid(g)
+            const float silu = g / (1.0f + __expf(-g));
+            p.h[static_cast<size_t>(list[m0 + m]) * ncols + col] = silu * u;
+          } else {
+            float acc_s = 0.f;
+            for (int sp = 0; sp < ns; ++sp) acc_s += v[sp];
+            if constexpr (MODE == kModeGemv)
+              store_out(p, static_cast<size_t>(m0 + m) * ncols + col, acc_s);
+            else
+              p.y[static_cast<size_t>(list[m0 + m]) * ncols + col] = acc_s;
+          }
         }
       }
-    } else {
-      // partial rows are indexed by slot; gate and up partials are separate planes
-      const int which = (p.mode == kModeGateUp) ? (z & 1) : 0;
-      float* part = p.part + static_cast<size_t>(which) * p.nsplit * p.nslots * ncols;
-      if (col_ok)
-        for (int m = 0; m < mvalid; ++m)
-          part[(static_cast<size_t>(split) * p.nslots + list[m0 + m]) * ncols + col] = colv[m];
-    }
-    consumers_sync();   // red and a_s are reused by the next pass
-  }
-
-  if (p.mode != kModeGemv) {
-    const int j = (p.mode == kModeGateUp) ? (z >> 1) : z;
-    const unsigned arrivals = (p.mode == kModeGateUp) ? 2u * p.nsplit : p.nsplit;
-    unsigned* ticket = p.tickets + static_cast<size_t>(j) * gridDim.x + tile;
-    if (!last_arrival(ticket, arrivals, tid, s_misc)) return;
-    const int col = b0 * kBlockCols + tid;
-    if (!((tid < tb * kBlockCols) && (col < ncols))) return;
-    const size_t plane = static_cast<size_t>(p.nsplit) * p.nslots * ncols;
-    for (int m = 0; m < nrows_total; ++m) {
-      const int slot = list[m];
-      if (p.mode == kModeGateUp) {
-        float g = 0.f, u = 0.f;
-        for (int sp = 0; sp < p.nsplit; ++sp) {
-          const size_t o = (static_cast<size_t>(sp) * p.nslots + slot) * ncols + col;
-          g += __ldcg(p.part + o);
-          u += __ldcg(p.part + plane + o);
-        }
-        // SiLU(g) * u, SiLU(g) = g * sigmoid(g)
-        const float silu = g / (1.0f + __expf(-g));
-        p.h[static_cast<size_t>(slot) * ncols + col] = silu * u;
-      } else {
-        float y = 0.f;
-        for (int sp = 0; sp < p.nsplit; ++sp)
-          y += __ldcg(p.part + (static_cast<size_t>(sp) * p.nslots + slot) * ncols + col);
-        p.y[static_cast<size_t>(slot) * ncols + col] = y;
-      }
+      // another pass will push into the receive buffers again: wait until
+      // every owner has read this pass's partials
+      if (pass + 1 < passes) cluster_sync();
     }
   }
 }
@@ -608,41 +696,99 @@ __global__ void __launch_bounds__(256) q4_moe_combine_kernel(float* out, const f
 // ---------------------------------------------------------------------------
 // Host-side launch helpers
 // ---------------------------------------------------------------------------
-template <int MR>
-static cudaError_t launch_mr(const GemvParams& p, dim3 grid, cudaStream_t st, bool pdl) {
-  const SmemPlan plan = smem_plan<MR>(p.rows_per_split, p.list_cap);
-  cudaError_t e = cudaFuncSetAttribute(q4_gemv_kernel<MR>,
+template <int MODE, int MR, int BPT>
+static cudaError_t launch_cfg(const GemvParams& p, dim3 grid, dim3 cluster, cudaStream_t st,
+                              bool pdl) {
+  const SmemPlan plan = smem_plan<MR, BPT>(p.rows_per_split, p.list_cap);
+  cudaError_t e = cudaFuncSetAttribute(q4_gemv_kernel<MODE, MR, BPT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(plan.total));
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(q4_gemv_kernel<MODE, MR, BPT>,
+                           cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(q4_gemv_kernel<MODE, MR, BPT>,
+                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(Crew<MR>::kThreads);
   cfg.dynamicSmemBytes = plan.total;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster.x;
+  attr[0].val.clusterDim.y = cluster.y;
+  attr[0].val.clusterDim.z = cluster.z;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, q4_gemv_kernel<MR>, p);
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, q4_gemv_kernel<MODE, MR, BPT>, p);
 }
 
-cudaError_t launch_gemv(const GemvParams& p, int mr, dim3 grid, cudaStream_t st, bool pdl) {
-  switch (mr) {
-    case 1: return launch_mr<1>(p, grid, st, pdl);
-    case 2: return launch_mr<2>(p, grid, st, pdl);
-    case 4: return launch_mr<4>(p, grid, st, pdl);
+template <int MODE>
+static cudaError_t launch_mode(const GemvParams& p, int mr, int bpt, dim3 grid, dim3 cluster,
+                               cudaStream_t st, bool pdl) {
+  if (bpt == 2 && mr == 1) return launch_cfg<MODE, 1, 2>(p, grid, cluster, st, pdl);
+  if (bpt == 1 && mr == 1) return launch_cfg<MODE, 1, 1>(p, grid, cluster, st, pdl);
+  if (bpt == 1 && mr == 2) return launch_cfg<MODE, 2, 1>(p, grid, cluster, st, pdl);
+  if (bpt == 1 && mr == 4) return launch_cfg<MODE, 4, 1>(p, grid, cluster, st, pdl);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemv(const GemvParams& p, int mr, int bpt, dim3 grid, dim3 cluster,
+                        cudaStream_t st, bool pdl) {
+  switch (p.mode) {
+    case kModeGemv: return launch_mode<kModeGemv>(p, mr, bpt, grid, cluster, st, pdl);
+    case kModeGateUp: return launch_mode<kModeGateUp>(p, mr, bpt, grid, cluster, st, pdl);
+    case kModeDown: return launch_mode<kModeDown>(p, mr, bpt, grid, cluster, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
 
-uint32_t gemv_smem_bytes(int mr, int rows_per_split, int list_cap) {
-  switch (mr) {
-    case 1: return smem_plan<1>(rows_per_split, list_cap).total;
-    case 2: return smem_plan<2>(rows_per_split, list_cap).total;
-    default: return smem_plan<4>(rows_per_split, list_cap).total;
+int max_active_clusters(int mode, int mr, int bpt, int rows_per_split, int list_cap,
+                        dim3 cluster) {
+  // occupancy query for the kernel instance that launch_gemv would pick
+  const void* fn = nullptr;
+#define Q4_PICK(MO)                                                            \
+  if (mode == MO) {                                                            \
+    if (bpt == 2 && mr == 1) fn = (const void*)q4_gemv_kernel<MO, 1, 2>;       \
+    else if (bpt == 1 && mr == 1) fn = (const void*)q4_gemv_kernel<MO, 1, 1>;  \
+    else if (bpt == 1 && mr == 2) fn = (const void*)q4_gemv_kernel<MO, 2, 1>;  \
+    else if (bpt == 1 && mr == 4) fn = (const void*)q4_gemv_kernel<MO, 4, 1>;  \
   }
+  Q4_PICK(kModeGemv)
+  Q4_PICK(kModeGateUp)
+  Q4_PICK(kModeDown)
+#undef Q4_PICK
+  if (!fn) return 0;
+  uint32_t smem = 0;
+  if (bpt == 2) smem = smem_plan<1, 2>(rows_per_split, list_cap).total;
+  else if (mr == 1) smem = smem_plan<1, 1>(rows_per_split, list_cap).total;
+  else if (mr == 2) smem = smem_plan<2, 1>(rows_per_split, list_cap).total;
+  else smem = smem_plan<4, 1>(rows_per_split, list_cap).total;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return 0;
+  cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cluster.x, cluster.y, cluster.z);
+  cfg.blockDim = dim3(mr == 1 ? Crew<1>::kThreads : Crew<2>::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster.x;
+  attr[0].val.clusterDim.y = cluster.y;
+  attr[0].val.clusterDim.z = cluster.z;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 cudaError_t launch_moe_combine(float* out, const float* y, const int32_t* idx, const float* w,
@@ -662,6 +808,46 @@ cudaError_t launch_moe_combine(float* out, const float* y, const int32_t* idx, c
   return cudaLaunchKernelEx(&cfg, q4_moe_combine_kernel, out, y, idx, w, T, topk, E, H);
 }
 
-int gemv_tile_blocks() { return kTileBlocks; }
+int gemv_tile_blocks(int bpt) { return kLanesPerRow * bpt; }
+
+int gemv_stage_rows() { return kRowsPerStage; }
+
+void fill_decode_consts(GemvParams& p) {
+  p.kconst[0] = -(8388608.0f + 8.0f);       // -(2^23 + 8 * 16^0)
+  p.kconst[1] = -(8388608.0f + 128.0f);     // -(2^23 + 8 * 16^1)
+  p.kconst[2] = -(8388608.0f + 2048.0f);    // -(2^23 + 8 * 16^2)
+  p.kconst[3] = -(8388608.0f + 32768.0f);   // -(2^23 + 8 * 16^3)
+  for (int i = 0; i < 4; ++i) p.kmask[i] = 0xFu << (4 * i);
+  p.kmask[4] = kMagic;                      // bits of 2^23
+}
+
+bool encode_weight_tmap(CUtensorMap* map, const void* base, int64_t K, int64_t nb,
+                        int64_t experts, int64_t matrix_bytes, int bpt) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (nb % kLanesPerRow != 0) return false;
+  // uint16 elements: a row is nb*9 halfwords; a box is one tile row segment
+  // (8*bpt blocks = 72*bpt halfwords) by kRowsPerStage rows.
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(nb * 9), static_cast<cuuint64_t>(K),
+                              static_cast<cuuint64_t>(experts)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(nb * kBlockBytes),
+                                 static_cast<cuuint64_t>(matrix_bytes)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kLanesPerRow * bpt * 9),
+                             static_cast<cuuint32_t>(kRowsPerStage), 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims,
+                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 }  // namespace q4

@@ -3,23 +3,31 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace q4 {
 
 enum : int { kModeGemv = 0, kModeGateUp = 1, kModeDown = 2 };
 
-// Arguments of q4_gemv_kernel (one struct, passed by value).
+// Arguments of q4_gemv_kernel (one struct, passed by value as a __grid_constant__
+// parameter so that the tensor maps inside it are addressable by TMA).
 struct GemvParams {
+  // TMA tensor maps of the weights (B and B2) as 3-D uint16 tensors
+  // [experts][K rows][nb*9 halfwords]; valid when use_tma != 0.
+  CUtensorMap tmap[2];
+  int use_tma;
   int mode;
   // weights: one matrix (GEMV) or expert stacks (B = gate or down, B2 = up)
   const uint8_t* B;
   const uint8_t* B2;
   long long b_stride;   // bytes per expert matrix
   int K, N, nb;
-  // split-K tiling (grid.x = column tiles of 8 blocks, grid.y = splits)
+  // split-K tiling (grid.x = column tiles of 8*BPT blocks, grid.y = splits;
+  // the splits of a tile form one thread-block cluster)
   int nsplit, rows_per_split;
-  int bulk;             // row segments may use TMA bulk copies
+  float kconst[4];      // nibble-decoding constants (fill_decode_consts)
+  uint32_t kmask[5];
   // activations
   const void* A;
   int a_dtype;          // 0 fp32, 1 bf16
@@ -28,8 +36,6 @@ struct GemvParams {
   // outputs
   void* C;
   int c_dtype;
-  float* part;          // split partials
-  unsigned* tickets;    // one per (z-group, tile); zero between launches
   // routed experts
   const int32_t* topk_idx;
   int nslots, topk, E;
@@ -39,9 +45,25 @@ struct GemvParams {
   unsigned* err;        // device status word
 };
 
-cudaError_t launch_gemv(const GemvParams& p, int mr, dim3 grid, cudaStream_t st, bool pdl);
-uint32_t gemv_smem_bytes(int mr, int rows_per_split, int list_cap);
-int gemv_tile_blocks();
+// mr: rows of A per pass (1, 2 or 4); bpt: blocks per thread (1 or 2; 2 only with mr 1).
+// cluster: (1, nsplit, 1), or (1, nsplit, 2) for the gate/up kernel.
+cudaError_t launch_gemv(const GemvParams& p, int mr, int bpt, dim3 grid, dim3 cluster,
+                        cudaStream_t st, bool pdl);
+constexpr int kMaxCluster = 16;   // non-portable thread-block cluster size limit
+// Clusters of shape `cluster` that can be resident at once for that kernel
+// configuration (0 if the configuration cannot launch).
+int max_active_clusters(int mode, int mr, int bpt, int rows_per_split, int list_cap,
+                        dim3 cluster);
+// Rows of one TMA box (one pipeline stage) of the GEMV kernel.
+int gemv_stage_rows();
+// Blocks per column tile for `bpt` blocks per thread.
+int gemv_tile_blocks(int bpt);
+void fill_decode_consts(GemvParams& p);
+// Encodes the tensor map of `experts` stacked K x nb-block Q4_0 matrices,
+// `matrix_bytes` apart, with boxes of one tile row segment (8*bpt blocks) by one
+// stage of rows.  Needs nb % 8 == 0 and a 16-byte aligned base.
+bool encode_weight_tmap(CUtensorMap* map, const void* base, int64_t K, int64_t nb,
+                        int64_t experts, int64_t matrix_bytes, int bpt);
 cudaError_t launch_moe_combine(float* out, const float* y, const int32_t* idx, const float* w,
                                int T, int topk, int E, int H, cudaStream_t st, bool pdl);
 

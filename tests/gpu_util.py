@@ -44,3 +44,13 @@ def same_f32(a, b):
     na, nb = np.isnan(a), np.isnan(b)
     return bool(np.array_equal(na, nb) and np.array_equal(f32_bits(np.where(na, 0, a)),
                                                           f32_bits(np.where(nb, 0, b))))
+
+
+def same_bf16(a, b):
+    """Bit-identical bf16 codes, any NaN code matching any NaN code (NaN
+    payloads are not pinned by the block definition)."""
+    a = np.asarray(a, np.uint16)
+    b = np.asarray(b, np.uint16)
+    na = ((a & 0x7F80) == 0x7F80) & ((a & 0x7F) != 0)
+    nb = ((b & 0x7F80) == 0x7F80) & ((b & 0x7F) != 0)
+    return bool(np.array_equal(na, nb) and np.array_equal(np.where(na, 0, a), np.where(nb, 0, b)))

@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 import seeded_inputs as si
-from gpu_util import device, same_f32, to_dev, torch
+from gpu_util import device, same_bf16, same_f32, to_dev, torch
 from test_oracle_pins import _golden_blocks
 
 import quantized_weight_q4_gb300 as q4
@@ -42,7 +42,7 @@ def test_golden_blocks_on_gpu():
 def test_dequant_bit_exact(K, N):
     B = si.q4_weights(K, N, seed=K + N, d_lo=-30.0, d_hi=30.0)
     assert same_f32(_gpu_dequant(B, K, N), oracle.dequant_f32(B, K, N))
-    assert np.array_equal(_gpu_dequant(B, K, N, bf16=True), oracle.dequant_bf16(B, K, N))
+    assert same_bf16(_gpu_dequant(B, K, N, bf16=True), oracle.dequant_bf16(B, K, N))
 
 
 def test_dequant_every_scale_code():
@@ -55,7 +55,7 @@ def test_dequant_every_scale_code():
     B[:, :, 2:] = ramp
     B = B.reshape(K, 8 * 18)
     assert same_f32(_gpu_dequant(B, K, 256), oracle.dequant_f32(B, K, 256))
-    assert np.array_equal(_gpu_dequant(B, K, 256, bf16=True), oracle.dequant_bf16(B, K, 256))
+    assert same_bf16(_gpu_dequant(B, K, 256, bf16=True), oracle.dequant_bf16(B, K, 256))
 
 
 @pytest.mark.parametrize("K,N", [(1, 32), (3, 40), (33, 1000), (128, 4096)])

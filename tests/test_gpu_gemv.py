@@ -121,20 +121,33 @@ def test_batched_decode_5120x12288(M):
     assert_within_matmul_tol(got, C64, S, f"M={M}")
 
 
-def test_workspace_errors_and_explicit_workspace():
+def test_gemv_needs_no_workspace():
+    """Split-K partial sums are combined on chip: no workspace is needed, and
+    a caller-provided one is ignored."""
     M, K, N = 1, 4096, 4096
-    need = q4.q4_matmul_workspace_size(M, N, K)
-    assert need > 0
+    assert q4.q4_matmul_workspace_size(M, N, K) == 0
     A = si.activations_f32(M, K, seed=1)
     B = si.q4_weights(K, N, seed=1)
-    small = torch.zeros(need // 2, dtype=torch.uint8, device=device())
-    with pytest.raises(q4.Q4Error) as e:
-        run(A, B, M, N, K, workspace=small)
-    assert e.value.status == q4.Q4_ERR_WORKSPACE
-    ws = torch.zeros(need, dtype=torch.uint8, device=device())
+    ws = torch.zeros(256, dtype=torch.uint8, device=device())
     c1 = run(A, B, M, N, K, workspace=ws)
     c2 = run(A, B, M, N, K)
     assert torch.equal(c1, c2)
+
+
+def test_moe_workspace_too_small_rejected():
+    T, topk, E, H, I = 2, 2, 4, 256, 64
+    need = q4.q4_moe_workspace_size(T, topk, E, H, I)
+    assert need > 0
+    out = torch.empty((T, H), dtype=torch.float32, device=device())
+    x = to_dev(si.activations_bf16(T, H, 1))
+    W = to_dev(np.zeros((E, H, 2 * 18), np.uint8))
+    Wd = to_dev(np.zeros((E, I, 8 * 18), np.uint8))
+    idx = to_dev(np.zeros((T, topk), np.int32))
+    w = to_dev(np.zeros((T, topk), np.float32))
+    small = torch.zeros(need // 2, dtype=torch.uint8, device=device())
+    with pytest.raises(q4.Q4Error) as e:
+        q4.q4_moe_experts_ex(out, x, W, W, Wd, idx, w, T, topk, E, H, I, workspace=small)
+    assert e.value.status == q4.Q4_ERR_WORKSPACE
 
 
 def test_misaligned_pointer_rejected():

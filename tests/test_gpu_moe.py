@@ -100,3 +100,21 @@ def test_moe_deepseek_v2_shape(T, deepseek_v2_experts):
         ref, tol, _ = oracle.moe(x[t:t + 1], Wg, Wu, Wd, idx[t:t + 1], w[t:t + 1], 1, topk, E, H, I)
         check(got[t:t + 1], ref, tol, f"T={T} token {t}")
     assert q4.q4_get_device_status() == q4.Q4_OK
+
+
+def test_moe_after_gemv_shares_library_workspace():
+    """A GEMV and the expert path, back to back on the library-owned workspace."""
+    from test_gpu_gemv import run as gemv_run
+    M, K, N = 2, 300, 520
+    A = si.activations_f32(M, K, seed=0)
+    B = si.q4_weights(K, N, seed=0)
+    gemv_run(A, B, M, N, K)
+    T, topk, E, H, I = 2, 3, 5, 256, 64
+    x, Wg, Wu, Wd, idx, w = make(T, topk, E, H, I, seed=1)
+    for _ in range(2):
+        got = run(x, Wg, Wu, Wd, idx, w, T, topk, E, H, I)
+        ref, tol, _ = oracle.moe(x, Wg, Wu, Wd, idx, w, T, topk, E, H, I)
+        check(got, ref, tol, "after gemv")
+        C = gemv_run(A, B, M, N, K)
+        C64, S = oracle.matmul(A, B, M, N, K)
+        assert np.all(np.abs(C.cpu().numpy() - C64) <= 1e-3 * S + 1e-6)
