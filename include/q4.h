@@ -135,6 +135,30 @@ Q4_API int q4_moe_experts_ex(float *out, const void *x, int x_dtype, const void 
 Q4_API size_t q4_moe_workspace_size(int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I);
 
 /*
+ * q4_moe_experts_noalloc -- q4_moe_experts_ex without a workspace argument,
+ * for callers that cannot allocate device memory: code running while a CUDA
+ * graph is captured in global mode, loops that must not allocate once
+ * started, or hosts whose own allocator owns all device memory.  (This entry
+ * point has no counterpart on the pages: it only changes where the scratch
+ * lives.)
+ *   The scratch is a fixed device array built into the library, of
+ *   q4_moe_static_scratch_bytes() bytes (8 MiB) on every GPU that loads the
+ *   library, held until the process exits.  Calls whose
+ *   q4_moe_workspace_size(T, topk, E, H, I) exceeds it return
+ *   Q4_ERR_WORKSPACE.  No call allocates or frees device memory.
+ *   The first call on a device looks up the array's device address; make it
+ *   before capturing a stream into a CUDA graph.
+ *   All calls on a device share the one array and leave their intermediate
+ *   rows in it; nothing needs to start at zero.  Calls that overlap on the
+ *   GPU (different streams without ordering) race on the array.
+ */
+Q4_API int q4_moe_experts_noalloc(float *out, const void *x, int x_dtype, const void *W_gate,
+                                  const void *W_up, const void *W_down,
+                                  const int32_t *topk_idx, const float *topk_w, int64_t T,
+                                  int64_t topk, int64_t E, int64_t H, int64_t I, void *stream);
+Q4_API size_t q4_moe_static_scratch_bytes(void);
+
+/*
  * q4_repack / q4_unpack -- lossless change of layout, bit-exact both ways.
  * Q4_LAYOUT_PLANAR for K x N: the fp16 scales d[K][nb] (little-endian), then,
  * from byte offset q4_planar_qs_offset(K, N) (a multiple of 16), the nibble

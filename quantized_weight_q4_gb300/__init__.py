@@ -49,6 +49,9 @@ SIGNATURES = {
     "q4_moe_experts_ex": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _vp, _vp,
                                  _i64, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
     "q4_moe_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _i64]),
+    "q4_moe_experts_noalloc": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _vp, _vp,
+                                      _i64, _i64, _i64, _i64, _i64, _vp]),
+    "q4_moe_static_scratch_bytes": (_sz, []),
     "q4_repack": (_int, [_vp, _vp, _i64, _i64, _vp]),
     "q4_unpack": (_int, [_vp, _vp, _i64, _i64, _vp]),
     "q4_planar_qs_offset": (_sz, [_i64, _i64]),
@@ -172,6 +175,20 @@ def q4_moe_experts_ex(out, x, W_gate, W_up, W_down, topk_idx, topk_w, T: int, to
 
 def q4_moe_workspace_size(T: int, topk: int, E: int, H: int, I: int) -> int:
     return lib().q4_moe_workspace_size(T, topk, E, H, I)
+
+
+def q4_moe_experts_noalloc(out, x, W_gate, W_up, W_down, topk_idx, topk_w, T: int, topk: int,
+                           E: int, H: int, I: int, stream=None) -> None:
+    """Routed experts with the library's built-in scratch: no device memory
+    is allocated, for callers that cannot allocate (see include/q4.h)."""
+    _require_cuda(out, x, W_gate, W_up, W_down, topk_idx, topk_w)
+    _check("q4_moe_experts_noalloc", lib().q4_moe_experts_noalloc(
+        _ptr(out), _ptr(x), _dtype_code(x), _ptr(W_gate), _ptr(W_up), _ptr(W_down),
+        _ptr(topk_idx), _ptr(topk_w), T, topk, E, H, I, _stream(stream)))
+
+
+def q4_moe_static_scratch_bytes() -> int:
+    return lib().q4_moe_static_scratch_bytes()
 
 
 def q4_repack(dst, src, K: int, N: int, stream=None) -> None:
