@@ -7,9 +7,11 @@ Default workload (``--workload decode_sweep_7b``): one decode token through a
 3,642,753,024 bytes of weights, run back to back from one CUDA graph.  One
 step = one pass of the 224 GEMVs.  Metric: weight bytes streamed per second.
 
-Other workloads (``--workload``): gemv_4096 (one 4096 x 4096 GEMV),
-batched_5120x12288 (bf16 A, M rows via --m), moe_deepseek_v2 (top-6 of 160
-experts, H=5120, I=1536, T via --tokens).
+Other workloads (``--workload``), each printing its own line: ``gemv`` (one
+GEMV, fp32 A, default K = N = 4096, --m/--k/--n), ``batched`` (K = 5120,
+N = 12288, bf16 A with --m rows), ``moe`` (top-6 of 160 experts, H = 5120,
+I = 1536, --tokens).  Weight copies or routings rotate so that each pass reads
+at least four times the L2 capacity.
 
 ``--impl reference`` times the fp64 CPU oracle on the host cores on a bounded
 sample of the same workload and prints the same JSON line with
@@ -55,7 +57,10 @@ def measured_peaks():
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel,
 # from an ncu capture, keyed by the hash of the kernel sources it was taken on.
 # A changed source hash makes the figure stale and the bench reports null.
-TRAFFIC = {}
+TRAFFIC = {
+    # profiles/q4_gemv_kernel_decode_sweep_7b.md: mean over the sweep's 4:2:1 shape mix
+    "2976a5ba50371215": 16314843,
+}
 
 
 def kernel_source_hash() -> str:
@@ -234,7 +239,7 @@ def run_ours(args, ws, rank, local):
     hbm_peak, bf16_peak, peak_src = measured_peaks()
 
     if args.workload != "decode_sweep_7b":
-        raise SystemExit(f"workload {args.workload} not wired into the JSON line yet")
+        return run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src)
 
     # CPU baseline first (rank 0 at N = 1 only), while the GPU is idle
     cpu = None
@@ -313,7 +318,7 @@ def run_ours(args, ws, rank, local):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "q4_gemv_kernel<1>",
+            "kernel": "q4_gemv_kernel<0,1,2> (GEMV, one row of A, 2 blocks per thread)",
             "achieved": round(achieved, 2),
             "peak": hbm_peak,
             "unit": "GB/s",
@@ -335,6 +340,126 @@ def run_ours(args, ws, rank, local):
         "clocks": clk.summary(),
     }
     return line
+
+
+# ---------------------------------------------------------------------------
+# other workloads: one GEMV, batched decode, routed experts
+# ---------------------------------------------------------------------------
+class GraphOf:
+    """A list of callables captured once into a CUDA graph."""
+
+    def __init__(self, torch, fns):
+        self.torch, self.fns = torch, fns
+        self.stream = torch.cuda.Stream()
+        with torch.cuda.stream(self.stream):
+            for f in fns:
+                f()
+        self.stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            for f in fns:
+                f()
+
+    def time(self, steps, warmup):
+        torch = self.torch
+        with torch.cuda.stream(self.stream):
+            for _ in range(warmup):
+                self.graph.replay()
+        torch.cuda.synchronize()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            s.record()
+            for _ in range(steps):
+                self.graph.replay()
+            e.record()
+        e.synchronize()
+        return s.elapsed_time(e) / 1e3
+
+
+def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    if args.workload in ("gemv", "batched"):
+        M = args.m if args.workload == "gemv" else args.m
+        K = args.k if args.k else (4096 if args.workload == "gemv" else 5120)
+        N = args.n if args.n else (4096 if args.workload == "gemv" else 12288)
+        wbytes = K * si.nblocks(N) * 18
+        copies = max(1, -(-4 * l2 // wbytes))   # >= 4x L2 of distinct weights per pass
+        bf16 = args.workload == "batched"
+        fns, keep = [], []
+        for i in range(copies):
+            B = to_dev(si.q4_weights(K, N, seed=0, stream=500 + i))
+            A = si.activations_bf16(M, K, 0, 600 + i) if bf16 else si.activations_f32(M, K, 0, 600 + i)
+            A = to_dev(A.view(np.int16)).view(torch.bfloat16) if bf16 else to_dev(A)
+            C = torch.empty((M, N), dtype=torch.float32, device=dev)
+            keep += [A, B, C]
+            fns.append(lambda C=C, A=A, B=B: q4.q4_matmul_ex(C, A, B, M, N, K))
+        g = GraphOf(torch, fns)
+        barrier(ws)
+        with ClockSampler(local) as clk:
+            t = g.time(args.steps, args.warmup)
+        barrier(ws)
+        t = max_over_ranks(ws, t)
+        per_launch = t / (args.steps * copies)
+        value = ws * wbytes / per_launch / 1e9
+        flops = 2.0 * M * K * N
+        cfg = {"workload": args.workload, "M": M, "K": K, "N": N,
+               "a_dtype": "bf16" if bf16 else "f32", "c_dtype": "f32",
+               "weight_bytes_per_launch": wbytes, "weight_copies_rotated": copies,
+               "l2": f"{copies} distinct weight copies per pass ({copies * wbytes} B >= 4x L2)",
+               "parallelism": f"replicas x{ws}", "tflops": round(flops / per_launch / 1e12, 3)}
+        units = copies
+    elif args.workload == "moe":
+        T, E, H, I, topk = args.tokens, 160, 5120, 1536, 6
+        Wg, Wu, Wd = si.moe_weights(E, H, I, seed=0)
+        dWg, dWu, dWd = to_dev(Wg), to_dev(Wu), to_dev(Wd)
+        del Wg, Wu, Wd
+        R = args.routings
+        fns, keep, uniq = [], [], 0
+        per_expert = (2 * H * si.nblocks(I) + I * si.nblocks(H)) * 18
+        wsz = q4.q4_moe_workspace_size(T, topk, E, H, I)
+        wspace = torch.empty(wsz, dtype=torch.uint8, device=dev)
+        for r in range(R):
+            idx, w = si.routing(T, E, topk, seed=r)
+            x = si.activations_bf16(T, H, seed=r)
+            uniq += len(set(idx.reshape(-1).tolist())) * per_expert
+            dx = to_dev(x.view(np.int16)).view(torch.bfloat16)
+            di, dw = to_dev(idx), to_dev(w)
+            out = torch.empty((T, H), dtype=torch.float32, device=dev)
+            keep += [dx, di, dw, out]
+            fns.append(lambda out=out, dx=dx, di=di, dw=dw: q4.q4_moe_experts_ex(
+                out, dx, dWg, dWu, dWd, di, dw, T, topk, E, H, I, workspace=wspace))
+        g = GraphOf(torch, fns)
+        barrier(ws)
+        with ClockSampler(local) as clk:
+            t = g.time(args.steps, args.warmup)
+        barrier(ws)
+        t = max_over_ranks(ws, t)
+        per_call = t / (args.steps * R)
+        wbytes = uniq / R
+        value = ws * wbytes / per_call / 1e9
+        cfg = {"workload": "moe", "T": T, "E": E, "H": H, "I": I, "topk": topk,
+               "routings_rotated": R, "unique_expert_bytes_per_call": round(wbytes),
+               "l2": f"{R} seeded routings rotate over 160 experts (2.12 GB of weights)",
+               "parallelism": f"replicas x{ws}"}
+        units = R
+    else:
+        raise SystemExit(f"unknown workload {args.workload}")
+    status = q4.q4_get_device_status()
+    if status != q4.Q4_OK:
+        raise SystemExit(f"device status {status} after the timed region")
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t / args.steps * 1e3, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded)", "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": round(value / ws, 2), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(value / ws / hbm_peak, 4),
+                     "peak_source": peak_src, "traffic": None},
+        "gpu_launches": None, "clocks": clk.summary(), "launches_per_step": units,
+    }
 
 
 # ---------------------------------------------------------------------------
@@ -392,6 +517,11 @@ def main():
     ap.add_argument("--cpu-layers", type=int, default=24)
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--m", type=int, default=1, help="rows of A (gemv, batched)")
+    ap.add_argument("--k", type=int, default=0)
+    ap.add_argument("--n", type=int, default=0)
+    ap.add_argument("--tokens", type=int, default=1, help="tokens (moe)")
+    ap.add_argument("--routings", type=int, default=32, help="seeded routings rotated (moe)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
