@@ -10,8 +10,9 @@ step = one pass of the 224 GEMVs.  Metric: weight bytes streamed per second.
 Other workloads (``--workload``), each printing its own line: ``gemv`` (one
 GEMV, fp32 A, default K = N = 4096, --m/--k/--n), ``batched`` (K = 5120,
 N = 12288, bf16 A with --m rows), ``moe`` (top-6 of 160 experts, H = 5120,
-I = 1536, --tokens).  Weight copies or routings rotate so that each pass reads
-at least four times the L2 capacity.
+I = 1536, --tokens), ``prefill`` (M = 2048, K = 5120, N = 12288, bf16 A and
+C on the tensor cores; metric TFLOP/s).  Weight copies or routings rotate so
+that each pass reads at least four times the L2 capacity.
 
 ``--impl reference`` times the fp64 CPU oracle on the host cores on a bounded
 sample of the same workload and prints the same JSON line with
@@ -444,6 +445,51 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
                "l2": f"{R} seeded routings rotate over 160 experts (2.12 GB of weights)",
                "parallelism": f"replicas x{ws}"}
         units = R
+    elif args.workload == "prefill":
+        M = args.m if args.m > 64 else 2048
+        K = args.k if args.k else 5120
+        N = args.n if args.n else 12288
+        wbytes = K * si.nblocks(N) * 18
+        per_copy = wbytes + M * K * 2 + M * N * 2
+        copies = max(1, -(-4 * l2 // per_copy))   # >= 4x L2 of distinct A, B and C per pass
+        fns, keep = [], []
+        for i in range(copies):
+            B = to_dev(si.q4_weights(K, N, seed=0, stream=700 + i))
+            A = to_dev(si.activations_bf16(M, K, 0, 800 + i).view(np.int16)).view(torch.bfloat16)
+            C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            keep += [A, B, C]
+            fns.append(lambda C=C, A=A, B=B: q4.q4_matmul_ex(C, A, B, M, N, K))
+        g = GraphOf(torch, fns)
+        barrier(ws)
+        with ClockSampler(local) as clk:
+            t = g.time(args.steps, args.warmup)
+        barrier(ws)
+        t = max_over_ranks(ws, t)
+        per_launch = t / (args.steps * copies)
+        flops = 2.0 * M * K * N
+        value = ws * flops / per_launch / 1e12
+        status = q4.q4_get_device_status()
+        if status != q4.Q4_OK:
+            raise SystemExit(f"device status {status} after the timed region")
+        tf_peak = measured_peaks()[1]
+        return {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t / args.steps * 1e3, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded)",
+            "config": {"workload": "prefill", "M": M, "K": K, "N": N, "a_dtype": "bf16",
+                       "c_dtype": "bf16", "flops_per_launch": flops,
+                       "weight_bytes_per_launch": wbytes, "copies_rotated": copies,
+                       "l2": f"{copies} distinct (A, B, C) sets per pass ({copies * per_copy} B >= 4x L2)",
+                       "parallelism": f"replicas x{ws}",
+                       "weight_gbs": round(wbytes / per_launch / 1e9, 2)},
+            "roofline": {"bound": "tensor", "achieved": round(value / ws, 2), "peak": tf_peak,
+                         "unit": "TFLOP/s", "frac": round(value / ws / tf_peak, 4),
+                         "peak_source": peak_src + " (bf16 burst)", "traffic": None},
+            "gpu_launches": args.steps * copies, "clocks": clk.summary(),
+            "launches_per_step": copies,
+        }
     else:
         raise SystemExit(f"unknown workload {args.workload}")
     status = q4.q4_get_device_status()

@@ -132,6 +132,30 @@ def matmul(A: np.ndarray, B: np.ndarray, M: int, N: int, K: int, with_abs: bool 
     return C, S
 
 
+def matmul_bf16_tiles(A: np.ndarray, B: np.ndarray, M: int, N: int, K: int):
+    """(C64 [M,N], S [M,N]): A . bf16_rn(W) in fp64, with S = sum_k |a * bf16_rn(w)|.
+
+    The product of the tensor-core prefill path, which batches a prompt's
+    tokens into one matmul (C++ DeepSeek engine page, §5.2) and dequantises
+    each weight to a bf16 tile element before the multiply.  Reading: the
+    pages fix no tile precision; bf16 is the tensor cores' input type, and
+    each weight is rounded once, to nearest even, from its exact value.
+    Steps: the C oracle's bf16 dequantisation, the bf16 bit patterns widened
+    to fp64 (16 zero bits appended to make the fp32 pattern), then one fp64
+    matmul (a library primitive).  Every product is exact in fp64 (8-bit
+    bf16 times an 8-bit bf16 or 24-bit fp32 activation).
+    """
+    A = np.ascontiguousarray(A)
+    if A.dtype == np.uint16:
+        A64 = (A.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    else:
+        A64 = A.astype(np.float32).astype(np.float64)
+    Wb = dequant_bf16(B, K, N)
+    W64 = (Wb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    A64 = A64.reshape(M, K)
+    return A64 @ W64, np.abs(A64) @ np.abs(W64)
+
+
 def matmul_naive(A: np.ndarray, B: np.ndarray, M: int, N: int, K: int) -> np.ndarray:
     A, dt = _act(A)
     B = np.ascontiguousarray(B, dtype=np.uint8)

@@ -67,6 +67,24 @@ bool encode_weight_tmap(CUtensorMap* map, const void* base, int64_t K, int64_t n
 cudaError_t launch_moe_combine(float* out, const float* y, const int32_t* idx, const float* w,
                                int T, int topk, int E, int H, cudaStream_t st, bool pdl);
 
+// q4_gemm_sm103.cu: the prefill GEMM on the tensor cores.
+struct GemmParams {
+  CUtensorMap tmap_a;   // A: bf16 [M][K], boxes of 64 K x 256 rows, 128-byte swizzle
+  CUtensorMap tmap_b;   // weights: uint16 [K][nb*9], boxes of 72 halfwords x 64 rows
+  void* C;              // [M][N] fp32 (c_dtype 0) or bf16 (1)
+  int c_dtype;
+  int M, N, K;
+  unsigned* err;        // device status word
+};
+// Shapes the tensor-core GEMM accepts: nb = ceil(N/32) a multiple of 8 (whole
+// 256-column tiles of blocks, 16-byte row pitch) and K a multiple of 8
+// (16-byte row pitch of A).
+bool gemm_supported(int64_t M, int64_t N, int64_t K);
+// A: bf16, 16-byte aligned; B: blocks layout, 16-byte aligned.  `sms` bounds the
+// persistent grid.
+cudaError_t launch_gemm(void* C, int c_dtype, const void* A, const void* B, int64_t M, int64_t N,
+                        int64_t K, unsigned* err, int sms, cudaStream_t st);
+
 // q4_misc.cu
 cudaError_t launch_dequant(void* W, int w_dtype, const uint8_t* B, int64_t K, int64_t N,
                            cudaStream_t st);

@@ -1,0 +1,186 @@
+"""GPU prefill GEMM (M > 64, bf16 A: the tensor-core path) against the oracle.
+
+The path dequantises every weight to a bf16 tile element, bf16_rn((q-8)*d),
+and accumulates bf16 x bf16 products in fp32.  Its own oracle is therefore
+A . bf16_rn(W) in fp64 (oracle.matmul_bf16_tiles), and parity is checked
+against it element by element within 1e-4 * sum|a*bf16(w)| + 1e-6, ten times
+tighter than the matmul tolerance (only the fp32 accumulation differs).
+
+Against the exact product A.W each weight carries up to 2^-9 relative
+rounding, so the bound that holds at every K is
+|gpu - A.W| <= 2^-9 * S + 1e-4 * S + 1e-6 (S = sum|a*w|); at the prefill
+size (K = 5120) the matmul tolerance 1e-3 * S + 1e-6 holds as well, because
+the rounding errors have random signs and average out over K terms.
+Exact cases: one-hot rows reproduce the bf16 tile values bit for bit; the
+bf16 output is the fp32 output rounded to nearest even; results repeat.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+from gpu_util import assert_within_matmul_tol, device, to_dev, to_host64, torch
+
+import quantized_weight_q4_gb300 as q4
+
+pytestmark = pytest.mark.gpu
+
+
+def run(A, B, M, N, K, c_dtype=torch.float32):
+    C = torch.empty((M, N), dtype=c_dtype, device=device())
+    q4.q4_matmul_ex(C, to_dev(A), to_dev(B), M, N, K)
+    torch.cuda.synchronize()
+    assert q4.q4_get_device_status() == q4.Q4_OK
+    return C
+
+
+def assert_exact_bound(got, C64, S, what):
+    """|gpu - A.W| <= 2^-9 * S + 1e-4 * S + 1e-6: bf16 tile rounding plus fp32
+    accumulation.  Returns max |err| / S."""
+    err = np.abs(got - C64)
+    tol = (2.0 ** -9 + 1e-4) * S + 1e-6
+    bad = ~(err <= tol)
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {bad.sum()} elements beyond the bf16 rounding bound, "
+                             f"first {i}: gpu {got[i]!r} oracle {C64[i]!r} tol {tol[i]!r}")
+    return float(np.max(err / np.maximum(S, 1e-300)))
+
+
+def assert_tile_tol(got, Cb, Sb, what):
+    err = np.abs(got - Cb)
+    tol = 1e-4 * Sb + 1e-6
+    bad = ~(err <= tol)
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {bad.sum()} elements beyond the bf16-tile tolerance, "
+                             f"first {i}: gpu {got[i]!r} bf16-tile oracle {Cb[i]!r} tol {tol[i]!r}")
+
+
+# (M, K, N): single and several tiles in M and N, K tails (K % 64 != 0), an N
+# tail inside a tile (N = 250) and M tails.
+SHAPES = [
+    (65, 64, 256), (128, 520, 256), (256, 64, 512), (300, 520, 1000),
+    (513, 1000, 250), (700, 1024, 2048),
+]
+
+
+@pytest.mark.parametrize("M,K,N", SHAPES)
+def test_gemm_parity(M, K, N):
+    A = si.activations_bf16(M, K, seed=M + K)
+    B = si.q4_weights(K, N, seed=N)
+    C = to_host64(run(A, B, M, N, K))
+    Cb, Sb = oracle.matmul_bf16_tiles(A, B, M, N, K)
+    assert_tile_tol(C, Cb, Sb, f"M={M} K={K} N={N}")
+    C64, S = oracle.matmul(A, B, M, N, K)
+    assert_exact_bound(C, C64, S, f"M={M} K={K} N={N}")
+
+
+def test_one_hot_rows_give_bf16_tiles():
+    """Row i of A = e_{k_i}: C row i is the bf16 tile row k_i exactly (one
+    nonzero product per sum), which pins the in-kernel dequantisation, the
+    swizzled tile layout and the descriptors."""
+    M, K, N = 130, 520, 1000
+    B = si.q4_weights(K, N, seed=31)
+    ks = si.rng(31, 2).choice(K, size=M, replace=False)
+    A = np.zeros((M, K), np.float32)
+    A[np.arange(M), ks] = 1.0
+    C = run(si.f32_to_bf16_bits(A), B, M, N, K).cpu().numpy()
+    Wb = oracle.dequant_bf16(B, K, N)
+    want = (Wb[ks].astype(np.uint32) << 16).view(np.float32)
+    assert np.array_equal(C, want)
+
+
+def test_golden_tile_blocks_through_gemm():
+    """Hand-rounded bf16 tile values (ties to even) come out of the GEMM."""
+    import test_oracle_pins as pins
+    recs = pins._golden_bf16_blocks()
+    K, N, M = 64, 256, 128
+    blocks = [blk for _, blk, _ in recs]
+    B = np.frombuffer(b"".join(blocks[(k + b) % len(blocks)] for k in range(K) for b in range(8)),
+                      np.uint8).reshape(K, 8 * 18)
+    A = np.zeros((M, K), np.float32)
+    A[np.arange(M), np.arange(M) % K] = 1.0
+    C = run(si.f32_to_bf16_bits(A), B, M, N, K).cpu().numpy()
+    for i in range(M):
+        k = i % K
+        for b in range(8):
+            want = np.array(recs[(k + b) % len(recs)][2], np.float32)
+            assert np.array_equal(C[i, 32 * b:32 * b + 32], want), (i, b)
+
+
+@pytest.mark.parametrize("M,K,N", [(300, 520, 1000), (2048, 512, 4096)])
+def test_bf16_output_is_rounded_fp32(M, K, N):
+    A = si.activations_bf16(M, K, seed=3)
+    B = si.q4_weights(K, N, seed=3)
+    C32 = run(A, B, M, N, K)
+    C16 = run(A, B, M, N, K, c_dtype=torch.bfloat16)
+    assert torch.equal(C32.to(torch.bfloat16).view(torch.int16), C16.view(torch.int16))
+
+
+def test_deterministic_and_padding_free():
+    M, K, N = 257, 640, 1000
+    A = si.activations_bf16(M, K, seed=5)
+    B = si.q4_weights(K, N, seed=5)
+    Br = si.randomise_padding(B, K, N, seed=5, stream=99)
+    c1 = run(A, B, M, N, K)
+    c2 = run(A, B, M, N, K)
+    c3 = run(A, Br, M, N, K)
+    assert torch.equal(c1, c2)
+    assert torch.equal(c1, c3)
+
+
+def test_zero_weights_and_activations():
+    M, K, N = 200, 256, 512
+    B = si.q4_weights(K, N, seed=2)
+    Z = B.reshape(K, -1, 18).copy()
+    Z[:, :, 2:] = 0x88
+    A = si.activations_bf16(M, K, seed=2)
+    assert not run(A, Z.reshape(K, -1), M, N, K).any()
+    assert not run(np.zeros((M, K), np.uint16), B, M, N, K).any()
+
+
+def test_persistent_tiles_more_than_sms():
+    """More output tiles than SMs: CTAs loop over several tiles and reuse the
+    accumulators.  Sampled rows, every column."""
+    M, K, N = 1024, 192, 256 * 48   # 4 x 48 = 192 tiles
+    A = si.activations_bf16(M, K, seed=7)
+    B = si.q4_weights(K, N, seed=7)
+    C = to_host64(run(A, B, M, N, K))
+    rows = np.unique(np.concatenate([si.rng(7, 3).choice(M, 12, replace=False), [0, 255, 256, M - 1]]))
+    Cb, Sb = oracle.matmul_bf16_tiles(A[rows], B, len(rows), N, K)
+    assert_tile_tol(C[rows], Cb, Sb, "persistent")
+    C64, S = oracle.matmul(A[rows], B, len(rows), N, K)
+    assert_exact_bound(C[rows], C64, S, "persistent")
+
+
+def test_prefill_2048x5120x12288():
+    """The prefill workload: M = 2048 tokens, K = 5120, N = 12288, bf16 A and
+    bf16 output.  16 sampled rows (all 12288 columns) against both oracles;
+    the bf16 output equals the fp32 output rounded."""
+    M, K, N = 2048, 5120, 12288
+    A = si.activations_bf16(M, K, seed=0)
+    B = si.q4_weights(K, N, seed=0)
+    C32 = run(A, B, M, N, K)
+    C16 = run(A, B, M, N, K, c_dtype=torch.bfloat16)
+    assert torch.equal(C32.to(torch.bfloat16).view(torch.int16), C16.view(torch.int16))
+    C = to_host64(C32)
+    rows = np.unique(np.concatenate([si.rng(0, 4).choice(M, 14, replace=False), [0, M - 1]]))
+    Cb, Sb = oracle.matmul_bf16_tiles(A[rows], B, len(rows), N, K)
+    assert_tile_tol(C[rows], Cb, Sb, "prefill")
+    C64, S = oracle.matmul(A[rows], B, len(rows), N, K)
+    ratio = assert_within_matmul_tol(C[rows], C64, S, "prefill")
+    rel = assert_exact_bound(C[rows], C64, S, "prefill")
+    print(f"prefill: max |err|/S = {rel:.3e}, max |err|/(1e-3 S + 1e-6) = {ratio:.3e}")
+
+
+def test_fp32_activations_above_64_rows_use_gemv():
+    """fp32 A with M > 64 keeps the split-K GEMV path (the tensor-core GEMM
+    takes bf16 A): still within the exact tolerance."""
+    M, K, N = 100, 300, 520
+    A = si.activations_f32(M, K, seed=9)
+    B = si.q4_weights(K, N, seed=9)
+    C = to_host64(run(A, B, M, N, K))
+    C64, S = oracle.matmul(A, B, M, N, K)
+    assert_within_matmul_tol(C, C64, S, "fp32 A, M = 100")

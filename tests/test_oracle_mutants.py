@@ -8,6 +8,7 @@ at least one pin must fail.  The real oracle is restored afterwards.
 import os
 import subprocess
 
+import numpy as np
 import pytest
 
 import oracle
@@ -42,6 +43,9 @@ BATTERY = [
     pins.test_fused_equals_textbook,
     pins.test_moe_closed_form,
     lambda: pins.test_silu_closed_forms(oracle),
+    pins.test_bf16_tiles_hand_rounded,
+    pins.test_bf16_tiles_equal_exact_product_when_representable,
+    pins.test_bf16_tiles_within_rounding_bound,
 ]
 
 
@@ -71,3 +75,47 @@ def test_pins_catch_mutant(name, tmp_path):
         assert failed, f"no pin caught the mutant '{name}'"
     finally:
         oracle.use(None)
+
+
+# Mistakes in the bf16-tile product (a Python composition of oracle steps):
+# each replaces the tile dequantisation and must fail a bf16-tile pin.
+def _tiles_truncated(B, K, N):
+    W = oracle.dequant_f32(B, K, N)
+    return (W.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _tiles_ties_up(B, K, N):
+    W = oracle.dequant_f32(B, K, N).view(np.uint32).astype(np.uint64)
+    return ((W + 0x8000) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("mutant", [_tiles_truncated, _tiles_ties_up])
+def test_bf16_tile_pins_catch_mutant(mutant, monkeypatch):
+    monkeypatch.setattr(oracle, "dequant_bf16", mutant)
+    tiles = [pins.test_bf16_tiles_hand_rounded,
+             pins.test_bf16_tiles_equal_exact_product_when_representable,
+             pins.test_bf16_tiles_within_rounding_bound]
+    failed = 0
+    for t in tiles:
+        try:
+            t()
+        except AssertionError:
+            failed += 1
+    assert failed > 0
+
+
+def test_bf16_tile_pins_catch_unrounded_tiles(monkeypatch):
+    """Tiles that keep the exact fp32 weight (no bf16 rounding at all)."""
+    real = oracle.matmul_bf16_tiles
+
+    def unrounded(A, B, M, N, K):
+        A = np.ascontiguousarray(A)
+        A64 = ((A.astype(np.uint32) << 16).view(np.float32) if A.dtype == np.uint16
+               else A.astype(np.float32)).astype(np.float64).reshape(M, K)
+        W = oracle.dequant_f32(B, K, N).astype(np.float64)
+        return A64 @ W, np.abs(A64) @ np.abs(W)
+
+    monkeypatch.setattr(oracle, "matmul_bf16_tiles", unrounded)
+    with pytest.raises(AssertionError):
+        pins.test_bf16_tiles_hand_rounded()
+    monkeypatch.setattr(oracle, "matmul_bf16_tiles", real)

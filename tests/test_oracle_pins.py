@@ -402,3 +402,72 @@ def test_moe_single_expert_is_matmul_chain():
     assert np.array_equal(g[0], g2[0]) and np.array_equal(u[0], u2[0])
     hv = np.array([oracle.silu(float(v)) for v in g2[0]]) * u2[0]
     assert np.allclose(h[0], hv, rtol=1e-15, atol=0)
+
+
+# ---------------------------------------------------------------- bf16 tiles
+
+GOLDEN_BF16 = os.path.join(os.path.dirname(__file__), "golden", "q4_0_bf16_tiles.txt")
+
+
+def _golden_bf16_blocks():
+    recs = []
+    with open(GOLDEN_BF16) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, d, qs, vals = [p.strip() for p in line.split("|")]
+            dbits = int(d, 16)
+            blk = bytes([dbits & 0xFF, dbits >> 8]) + bytes(int(x, 16) for x in qs.split())
+            v = [float(t) for t in vals.split()]
+            assert len(blk) == 18 and len(v) == 32
+            recs.append((name, blk, v))
+    return recs
+
+
+def test_bf16_tiles_hand_rounded():
+    """One-hot rows of A select the bf16 tile values of hand-built blocks
+    (rounded by hand, ties to even, in the fixture)."""
+    import oracle
+    recs = _golden_bf16_blocks()
+    K, N = len(recs), 32
+    B = np.frombuffer(b"".join(blk for _, blk, _ in recs), np.uint8).reshape(K, 18)
+    A = si.f32_to_bf16_bits(np.eye(K, dtype=np.float32))
+    C, S = oracle.matmul_bf16_tiles(A, B, K, N, K)
+    for k, (name, _, vals) in enumerate(recs):
+        assert np.array_equal(C[k], np.array(vals)), name
+        assert np.array_equal(S[k], np.abs(np.array(vals))), name
+
+
+def test_bf16_tiles_equal_exact_product_when_representable():
+    """With power-of-two scales every weight (q-8)*d has at most 4 significant
+    bits, so bf16 rounding changes nothing: the bf16-tile product equals the
+    exact fused product up to fp64 summation order."""
+    import oracle
+    M, K, N = 5, 300, 96
+    B = si.q4_weights(K, N, seed=21).reshape(K, -1, 18).copy()
+    e = si.rng(21, 5).integers(-12, 2, size=B.shape[:2])
+    d16 = np.ldexp(1.0, e).astype(np.float16).view(np.uint16)
+    B[:, :, 0] = (d16 & 0xFF).astype(np.uint8)
+    B[:, :, 1] = (d16 >> 8).astype(np.uint8)
+    B = B.reshape(K, -1)
+    A = si.activations_bf16(M, K, seed=21)
+    Cb, Sb = oracle.matmul_bf16_tiles(A, B, M, N, K)
+    C, S = oracle.matmul(A, B, M, N, K)
+    assert np.all(np.abs(Cb - C) <= 1e-13 * S)
+    assert np.allclose(Sb, S, rtol=1e-13, atol=0)
+
+
+def test_bf16_tiles_within_rounding_bound():
+    """Each bf16 weight is within 2^-9 (half an ulp, relative) of the exact
+    one, so |A.bf16(W) - A.W| <= 2^-9 * sum_k |a*w|; with fp16 scales of 11
+    significant bits the rounding is not a no-op."""
+    import oracle
+    M, K, N = 4, 257, 160
+    A = si.activations_bf16(M, K, seed=22)
+    B = si.q4_weights(K, N, seed=22)
+    Cb, _ = oracle.matmul_bf16_tiles(A, B, M, N, K)
+    C, S = oracle.matmul(A, B, M, N, K)
+    err = np.abs(Cb - C)
+    assert np.all(err <= 2.0 ** -9 * S + 1e-300)
+    assert err.max() > 0
