@@ -10,7 +10,7 @@
 // Structure (one CTA per SM, persistent over 256 x 256 output tiles):
 //  * warp 0, producer: TMA loads of A (64 K x 256 rows, 128-byte swizzle,
 //    K-major) and of the raw Q4 tile (64 rows x 8 blocks) into rings;
-//  * warps 2..5, dequant + epilogue: decode each raw block (one K row, 32
+//  * warps 2..9, dequant + epilogue: decode each raw block (one K row, 32
 //    consecutive N) into 64 contiguous bytes of an MN-major, 128-byte-swizzled
 //    bf16 B tile; after a tile's last K step, read the accumulators out of
 //    tensor memory and store C;
@@ -40,8 +40,8 @@ constexpr int kABytes = BM * BK * 2;                   // 32768
 constexpr int kBBytes = BN * BK * 2;                   // 32768
 constexpr int kRawRowBytes = (BN / kBlockCols) * kBlockBytes;   // 144
 constexpr int kRawBytes = BK * kRawRowBytes;           // 9216
-constexpr int kDequantWarps = 4;
-constexpr int kThreads = (2 + kDequantWarps) * 32;     // 192
+constexpr int kDequantWarps = 8;
+constexpr int kThreads = (2 + kDequantWarps) * 32;     // 320
 constexpr uint32_t kTmemCols = 512;
 
 struct Smem {
@@ -175,22 +175,28 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
   return r;
 }
 
-// Thread (warp wd, lane): block b = lane & 7 of rows k = (lane >> 3) + 4*wd + 16*i.
+// Warp wd decodes K rows 8*wd .. 8*wd+7 of the stage: lane = 8*s + r takes
+// row 8*wd + r and blocks 2*s (first pass) and 2*s + 1 (second pass).
+//  * 16-byte stores are served eight lanes at a time; those eight lanes hold
+//    eight different rows of one block, i.e. eight different chunk positions
+//    of the 128-byte swizzle: no bank conflict.
+//  * 32-bit raw reads: the rows are 36 words apart (4 banks), and the even
+//    (odd) blocks start at words 0, 9, 18, 27 (4, 13, 22, 31) of a row, one
+//    per residue mod 4: the 32 lanes hit 32 different banks.
 __device__ __forceinline__ void dequant_stage(const uint8_t* raw, uint8_t* btile, int wd,
                                               int lane) {
-  const int b = lane & 7;
-  const uint32_t boff = static_cast<uint32_t>(b * kBlockBytes);
+  const int k = wd * 8 + (lane & 7);
+  const f32x2 c01 = pack2(-(8388608.0f + 8.0f), -(8388608.0f + 128.0f));
+  const f32x2 c23 = pack2(-(8388608.0f + 2048.0f), -(8388608.0f + 32768.0f));
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int k = (lane >> 3) + 4 * wd + 16 * i;
+  for (int par = 0; par < 2; ++par) {
+    const int b = 2 * (lane >> 3) + par;
     uint32_t dbits, qs[4];
-    load_block_smem(raw + k * kRawRowBytes, boff, dbits, qs);
+    load_block_smem(raw + k * kRawRowBytes, static_cast<uint32_t>(b * kBlockBytes), dbits, qs);
     const float d = fp16_bits_to_f32(dbits);
     // exact (q - 8) * d per nibble: (bits(2^23) | q << 4p) - (2^23 + 8*16^p), times d*16^-p
     const f32x2 s01 = pack2(d, d * 0.0625f);
     const f32x2 s23 = pack2(d * 0.00390625f, d * 0.000244140625f);
-    const f32x2 c01 = pack2(-(8388608.0f + 8.0f), -(8388608.0f + 128.0f));
-    const f32x2 c23 = pack2(-(8388608.0f + 2048.0f), -(8388608.0f + 32768.0f));
     uint32_t out[16];
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
@@ -381,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ================= dequant + epilogue =================
-    const int wd = warp - 2;   // 0..3
+    const int wd = warp - 2;   // 0..7
     int gr = 0, gb = 0, tl = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < ntiles && ok && !*s_fail; tile += gridDim.x, ++tl) {
@@ -412,8 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int q = warp & 3;   // the tensor-memory lane quarter this warp may access
-#pragma unroll 1
-      for (int mt = 0; mt < 2; ++mt) {
+      {
+        const int mt = wd >> 2;   // warps 2..5 drain the first accumulator, 6..9 the second
         const int row = m0 + mt * 128 + q * 32 + lane;
 #pragma unroll 1
         for (int cc = 0; cc < BN / 32; ++cc) {
