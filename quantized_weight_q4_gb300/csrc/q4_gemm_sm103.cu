@@ -4,8 +4,8 @@
 // the C++ DeepSeek engine page (§2.2-§2.3: K rows of ceil(N/32) 18-byte
 // blocks, each spanning 32 output columns) and fp32 accumulation; the page
 // batches the prompt's tokens into one big matmul (§5.2).  Each weight is
-// dequantised once per CTA tile to bf16: bf16_rn((q - 8) * d), computed
-// exactly in fp32 and rounded once.
+// dequantised once per CTA tile to bf16: bf16_rn((q - 8) * d), the exact
+// product rounded once (bf16x2 arithmetic on a split of d, see split_scale).
 //
 // Structure (one CTA per SM, persistent over 256 x 256 output tiles):
 //  * warp 0, producer: TMA loads of A (64 K x 256 rows, 128-byte swizzle,
@@ -169,10 +169,52 @@ __device__ __forceinline__ uint32_t b_offset(int k, int n) {
   return static_cast<uint32_t>((na * 8 + ka) * 1024 + kr * 128 + ((c ^ kr) << 4));
 }
 
-__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
+// bf16x2 arithmetic, round to nearest even.
+__device__ __forceinline__ uint32_t bf2_add(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Column order inside each 8-column chunk of a B tile: the decode packs
+// nibbles j and j + 4 of a 32-bit word into one bf16 pair, so slot s of a
+// chunk holds column chunk_col(s) of it.  The epilogue applies the inverse.
+__host__ __device__ constexpr int chunk_col(int s) { return (s >> 1) + 4 * (s & 1); }
+
+// Scale of one block for the bf16 decode: d = dh + dl with dh the bf16
+// truncation of d (toward zero) and dl the remaining (at most 3) low bits of
+// the fp16 significand, carrying d's sign also when it is zero.  Non-finite d
+// keeps dh = d (a canonical NaN for NaN) and dl = signed zero.
+__device__ __forceinline__ void split_scale(uint32_t dbits16, uint32_t& dh2, uint32_t& dl2) {
+  const float d = fp16_bits_to_f32(dbits16);
+  const uint32_t db = __float_as_uint(d);
+  const bool finite = (db & 0x7F800000u) != 0x7F800000u;
+  const uint32_t hb = (d != d) ? 0x7FC00000u : (db & 0xFFFF0000u);
+  const float dl = finite ? d - __uint_as_float(hb) : 0.0f;   // exact: at most 3 bits
+  const uint32_t lb = __float_as_uint(dl) | (db & 0x80000000u);
+  const uint32_t h16 = hb >> 16, l16 = lb >> 16;                // dl is exact in bf16
+  dh2 = h16 | (h16 << 16);
+  dl2 = l16 | (l16 << 16);
+}
+
+// bf16_rn((q - 8) * d) for nibbles j (low half) and j + 4 (high half) of w:
+// x = bf16(128 + q) from the bits, q - 8 exactly by one add, (q - 8) * dl
+// exactly (at most 7 significant bits), then (q - 8) * dh plus that, rounded
+// once.
+__device__ __forceinline__ uint32_t decode_pair(uint32_t w_shifted, uint32_t dh2, uint32_t dl2) {
+  const uint32_t x = (w_shifted & 0x000F000Fu) | 0x43004300u;   // 128 + q, 128 + q'
+  const uint32_t xq = bf2_add(x, 0xC308C308u);                    // - 136
+  return bf2_fma(xq, dh2, bf2_mul(xq, dl2));
 }
 
 // Warp wd decodes K rows 8*wd .. 8*wd+7 of the stage: lane = 8*s + r takes
@@ -186,40 +228,21 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
 __device__ __forceinline__ void dequant_stage(const uint8_t* raw, uint8_t* btile, int wd,
                                               int lane) {
   const int k = wd * 8 + (lane & 7);
-  const f32x2 c01 = pack2(-(8388608.0f + 8.0f), -(8388608.0f + 128.0f));
-  const f32x2 c23 = pack2(-(8388608.0f + 2048.0f), -(8388608.0f + 32768.0f));
 #pragma unroll
   for (int par = 0; par < 2; ++par) {
     const int b = 2 * (lane >> 3) + par;
     uint32_t dbits, qs[4];
     load_block_smem(raw + k * kRawRowBytes, static_cast<uint32_t>(b * kBlockBytes), dbits, qs);
-    const float d = fp16_bits_to_f32(dbits);
-    // exact (q - 8) * d per nibble: (bits(2^23) | q << 4p) - (2^23 + 8*16^p), times d*16^-p
-    const f32x2 s01 = pack2(d, d * 0.0625f);
-    const f32x2 s23 = pack2(d * 0.00390625f, d * 0.000244140625f);
-    uint32_t out[16];
+    uint32_t dh2, dl2;
+    split_scale(dbits, dh2, dl2);
+    // word t holds columns 8t .. 8t+7 of the block (nibble j = column 8t + j);
+    // it becomes chunk t, slots in chunk_col order
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      const uint32_t w = qs[t], y = w >> 16;
-      float a0, a1, a2, a3, a4, a5, a6, a7;
-      unpack2(mul2(add2(pack2(__uint_as_float((w & 0x000Fu) | kMagic),
-                              __uint_as_float((w & 0x00F0u) | kMagic)), c01), s01), a0, a1);
-      unpack2(mul2(add2(pack2(__uint_as_float((w & 0x0F00u) | kMagic),
-                              __uint_as_float((w & 0xF000u) | kMagic)), c23), s23), a2, a3);
-      unpack2(mul2(add2(pack2(__uint_as_float((y & 0x000Fu) | kMagic),
-                              __uint_as_float((y & 0x00F0u) | kMagic)), c01), s01), a4, a5);
-      unpack2(mul2(add2(pack2(__uint_as_float((y & 0x0F00u) | kMagic),
-                              __uint_as_float((y & 0xF000u) | kMagic)), c23), s23), a6, a7);
-      out[4 * t + 0] = bf16x2_rn(a0, a1);   // columns 8t, 8t+1
-      out[4 * t + 1] = bf16x2_rn(a2, a3);
-      out[4 * t + 2] = bf16x2_rn(a4, a5);
-      out[4 * t + 3] = bf16x2_rn(a6, a7);
-    }
-    // 32 columns n = 32b .. 32b+31 of K row k: four 16-byte chunks
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint4* dst = reinterpret_cast<uint4*>(btile + b_offset(k, b * 32 + c * 8));
-      *dst = make_uint4(out[4 * c], out[4 * c + 1], out[4 * c + 2], out[4 * c + 3]);
+      const uint32_t w = qs[t];
+      const uint4 o = make_uint4(decode_pair(w, dh2, dl2), decode_pair(w >> 4, dh2, dl2),
+                                 decode_pair(w >> 8, dh2, dl2), decode_pair(w >> 12, dh2, dl2));
+      *reinterpret_cast<uint4*>(btile + b_offset(k, b * 32 + t * 8)) = o;
     }
   }
 }
@@ -230,7 +253,13 @@ __device__ __forceinline__ uint32_t bf16_bits(float v) {
 
 // 32 consecutive accumulators of one row of C, columns col0 .. col0+31 (< N).
 __device__ __forceinline__ void store_row32(const GemmParams& p, int row, int col0,
-                                            const uint32_t (&v)[32]) {
+                                            const uint32_t (&acc)[32]) {
+  // tensor-memory column 8t + s holds output column 8t + chunk_col(s)
+  uint32_t v[32];
+#pragma unroll
+  for (int t = 0; t < 4; ++t)
+#pragma unroll
+    for (int s = 0; s < 8; ++s) v[8 * t + chunk_col(s)] = acc[8 * t + s];
   const size_t base = static_cast<size_t>(row) * p.N + col0;
   const bool whole = col0 + 32 <= p.N && (p.N & 7) == 0;
   if (p.c_dtype == 0) {
