@@ -34,8 +34,8 @@ namespace gemm {
 
 constexpr int BM = 256, BN = 256, BK = 64;
 constexpr int kStagesA = 3;     // A ring: 3 x 32 KB
-constexpr int kStagesRaw = 4;   // raw Q4 ring: 4 x 9 KB
-constexpr int kStagesB = 2;     // dequantised B ring: 2 x 32 KB
+constexpr int kStagesRaw = 3;   // raw Q4 ring: 3 x 9 KB
+constexpr int kStagesB = 3;     // dequantised B ring: 3 x 32 KB
 constexpr int kABytes = BM * BK * 2;                   // 32768
 constexpr int kBBytes = BN * BK * 2;                   // 32768
 constexpr int kRawRowBytes = (BN / kBlockCols) * kBlockBytes;   // 144
