@@ -64,9 +64,16 @@ TRAFFIC = {
 }
 
 
-def kernel_source_hash() -> str:
+# The same for the prefill GEMM kernel (q4_gemm_tc_kernel), one launch of
+# M = 2048, K = 5120, N = 12288 (profiles/q4_gemm_tc_kernel_prefill_2048x5120x12288.md).
+TRAFFIC_GEMM = {
+    "e1f9361c9499bd19": 68202240,
+}
+
+
+def kernel_source_hash(names=("q4_gemv.cu", "q4_device.cuh", "q4_kernels.h")) -> str:
     h = hashlib.sha256()
-    for name in ("q4_gemv.cu", "q4_device.cuh", "q4_kernels.h"):
+    for name in names:
         with open(os.path.join(ROOT, "quantized_weight_q4_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -472,6 +479,7 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
         if status != q4.Q4_OK:
             raise SystemExit(f"device status {status} after the timed region")
         tf_peak = measured_peaks()[1]
+        ghash = kernel_source_hash(("q4_gemm_sm103.cu", "q4_device.cuh", "q4_kernels.h"))
         return {
             "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup,
@@ -486,7 +494,9 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
                        "weight_gbs": round(wbytes / per_launch / 1e9, 2)},
             "roofline": {"bound": "tensor", "achieved": round(value / ws, 2), "peak": tf_peak,
                          "unit": "TFLOP/s", "frac": round(value / ws / tf_peak, 4),
-                         "peak_source": peak_src + " (bf16 burst)", "traffic": None},
+                         "peak_source": peak_src + " (bf16 burst)",
+                         "kernel": "q4_gemm_tc_kernel", "kernel_source_hash": ghash,
+                         "traffic": TRAFFIC_GEMM.get(ghash)},
             "gpu_launches": args.steps * copies, "clocks": clk.summary(),
             "launches_per_step": copies,
         }

@@ -83,9 +83,18 @@ Q4_API int q4_matmul(float *C, const float *A, const void *B, int64_t M, int64_t
  *   workspace  unused by this entry point (q4_matmul_workspace_size returns
  *              0); accepted for interface stability, may be NULL.
  *   stream     cudaStream_t (NULL = legacy default stream)
- * Kernel choice: the split-K GEMV on the CUDA cores, in chunks of up to 4
- * rows of A.  The splits of each column tile run as one thread-block cluster
- * and are added on chip in fixed order: results are deterministic.
+ * Kernel choice:
+ *   - M <= 64, or fp32 A, or a shape the GEMM below does not take: the
+ *     split-K GEMV on the CUDA cores, in chunks of up to 4 rows of A.  The
+ *     splits of each column tile run as one thread-block cluster and are
+ *     added on chip in fixed order.  Exact fp32 dequantisation.
+ *   - M > 64 with bf16 A, ceil(N/32) % 8 == 0 and K % 8 == 0: the
+ *     tensor-core GEMM (prompt batching, engine page §5.2).  Each weight is
+ *     dequantised to a bf16 tile element bf16_rn((q - 8) * d) and the
+ *     products are accumulated in fp32; the result is A . bf16_rn(W), whose
+ *     deviation from A . W is bounded by 2^-9 * sum|a*w| plus the fp32
+ *     accumulation error.
+ *   Both are deterministic (no floating-point atomics, fixed orders).
  * Launches use programmatic dependent launch: a kernel may start streaming
  * its weights while the previous kernel on the stream finishes, and reads A
  * only after that kernel has completed.  Consequently B must not be written

@@ -33,11 +33,20 @@ namespace q4 {
 namespace gemm {
 
 constexpr int BM = 256, BN = 256, BK = 64;
+// CTAs of a thread-block cluster take the same rows of A and adjacent column
+// tiles: each loads 1/kCluster of the A tile and multicasts it to all.
+constexpr int kCluster = 1;
+constexpr int kASlice = BM / kCluster;                 // A rows loaded per CTA
+constexpr uint16_t kClusterMask = (1u << kCluster) - 1;
 constexpr int kStagesA = 3;     // A ring: 3 x 32 KB
 constexpr int kStagesRaw = 3;   // raw Q4 ring: 3 x 9 KB
 constexpr int kStagesB = 3;     // dequantised B ring: 3 x 32 KB
 constexpr int kABytes = BM * BK * 2;                   // 32768
 constexpr int kBBytes = BN * BK * 2;                   // 32768
+// A rows are BK * 2 bytes: one swizzle span of that width (128 or 64 bytes)
+constexpr int kARowBytes = BK * 2;
+static_assert(kARowBytes == 128 || kARowBytes == 64, "A rows must fill one swizzle span");
+constexpr int kBarBytes = 512;
 constexpr int kRawRowBytes = (BN / kBlockCols) * kBlockBytes;   // 144
 constexpr int kRawBytes = BK * kRawRowBytes;           // 9216
 constexpr int kDequantWarps = 8;
@@ -48,14 +57,16 @@ struct Smem {
   uint32_t a, b, raw, bars, total;
 };
 __host__ __device__ constexpr Smem plan() {
-  // A and B stages need 1024-byte alignment (128-byte swizzle atoms)
+  // A and B stages need 1024-byte alignment (swizzle atoms)
   return Smem{0, kStagesA * kABytes, kStagesA * kABytes + kStagesB * kBBytes,
               kStagesA * kABytes + kStagesB * kBBytes + kStagesRaw * kRawBytes,
-              kStagesA * kABytes + kStagesB * kBBytes + kStagesRaw * kRawBytes + 256 + 1024};
+              kStagesA * kABytes + kStagesB * kBBytes + kStagesRaw * kRawBytes + kBarBytes + 1024};
 }
 
-static_assert(plan().raw % 1024 == 0 && kRawBytes % 128 == 0, "TMA destinations need alignment");
-static_assert((2 * kStagesA + 2 * kStagesRaw + 2 * kStagesB + 3) * 8 + 8 <= 256,
+static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0 && plan().raw % 1024 == 0 &&
+                  kRawBytes % 128 == 0 && plan().bars % 8 == 0,
+              "TMA destinations need alignment");
+static_assert((2 * kStagesA + 2 * kStagesRaw + 2 * kStagesB + 3) * 8 + 8 <= kBarBytes,
               "barrier region overflows");
 static_assert(plan().total <= 227 * 1024, "shared memory plan exceeds the per-CTA limit");
 
@@ -66,6 +77,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int c0,
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// The same box into the same shared offset of every CTA in `mask`; each
+// destination's mbarrier (same offset) receives the bytes it got.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const void* tmap, int c0, int c1,
+                                               uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(mask)
       : "memory");
 }
 
@@ -92,6 +114,15 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
           smem_u32(bar))
       : "memory");
 }
+// Arrives once on the mbarrier at this offset in every CTA of `mask` when the
+// MMAs issued so far by this thread are complete.
+__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem desc] . B[smem desc]
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                        uint32_t idesc, uint32_t accumulate) {
@@ -123,16 +154,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 // Shared-memory matrix descriptor: start address, leading and stride byte
 // offsets (16-byte units), descriptor version 1, swizzle mode in bits 61-63
-// (2 = 128-byte swizzle).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// (2 = 128-byte swizzle, 4 = 64-byte swizzle).
+constexpr uint64_t kSwizzle128 = 2, kSwizzle64 = 4;
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint64_t swizzle) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
+  d |= swizzle << 61;
   return d;
 }
+// A (K-major): rows of kARowBytes, 8-row swizzle atoms kARowBytes * 8 apart.
+constexpr uint64_t kASwizzle = (kARowBytes == 128) ? kSwizzle128 : kSwizzle64;
+constexpr uint32_t kASbo = kARowBytes * 8;
 
 // Instruction descriptor of kind::f16: fp32 D, bf16 A and B, A K-major,
 // B MN-major, N = 256, M = 128.
@@ -159,14 +195,15 @@ __device__ __forceinline__ bool gwait(uint64_t* bar, uint32_t parity, volatile i
 }
 
 // ---- dequant of one raw stage into an MN-major swizzled bf16 B tile --------
-// B tile layout (K = 64 rows, N = 256): 128-byte swizzle atoms of 8 K rows x
-// 64 N; atom (na, ka) at (na * 8 + ka) * 1024 bytes; inside it K row kr is
+// B tile layout (K = BK rows, N = 256): 128-byte swizzle atoms of 8 K rows x
+// 64 N; atom (na, ka) at (na * BK/8 + ka) * 1024 bytes; inside it K row kr is
 // 128 bytes at kr * 128 with 16-byte chunk c stored at chunk c ^ kr.
-// Descriptor: leading byte offset (between atoms along N) 8192, stride byte
-// offset (between atoms along K) 1024.
+// Descriptor: leading byte offset (between atoms along N) BK/8 * 1024, stride
+// byte offset (between atoms along K) 1024.
+constexpr uint32_t kBLbo = (BK / 8) * 1024;
 __device__ __forceinline__ uint32_t b_offset(int k, int n) {
   const int ka = k >> 3, kr = k & 7, na = n >> 6, c = (n & 63) >> 3;
-  return static_cast<uint32_t>((na * 8 + ka) * 1024 + kr * 128 + ((c ^ kr) << 4));
+  return static_cast<uint32_t>((na * (BK / 8) + ka) * 1024 + kr * 128 + ((c ^ kr) << 4));
 }
 
 // bf16x2 arithmetic, round to nearest even.
@@ -217,8 +254,9 @@ __device__ __forceinline__ uint32_t decode_pair(uint32_t w_shifted, uint32_t dh2
   return bf2_fma(xq, dh2, bf2_mul(xq, dl2));
 }
 
-// Warp wd decodes K rows 8*wd .. 8*wd+7 of the stage: lane = 8*s + r takes
-// row 8*wd + r and blocks 2*s (first pass) and 2*s + 1 (second pass).
+// A stage is BK/8 row groups x 2 parities of (8 rows x 4 blocks) units; warp
+// wd decodes units wd * BK/32 + i, i < BK/32.  In unit u (row group u/2,
+// parity u%2), lane = 8*s + r takes row 8*(u/2) + r and block 2*s + u%2.
 //  * 16-byte stores are served eight lanes at a time; those eight lanes hold
 //    eight different rows of one block, i.e. eight different chunk positions
 //    of the 128-byte swizzle: no bank conflict.
@@ -227,10 +265,11 @@ __device__ __forceinline__ uint32_t decode_pair(uint32_t w_shifted, uint32_t dh2
 //    per residue mod 4: the 32 lanes hit 32 different banks.
 __device__ __forceinline__ void dequant_stage(const uint8_t* raw, uint8_t* btile, int wd,
                                               int lane) {
-  const int k = wd * 8 + (lane & 7);
 #pragma unroll
-  for (int par = 0; par < 2; ++par) {
-    const int b = 2 * (lane >> 3) + par;
+  for (int i = 0; i < BK / 32; ++i) {
+    const int u = wd * (BK / 32) + i;
+    const int k = (u >> 1) * 8 + (lane & 7);
+    const int b = 2 * (lane >> 3) + (u & 1);
     uint32_t dbits, qs[4];
     load_block_smem(raw + k * kRawRowBytes, static_cast<uint32_t>(b * kBlockBytes), dbits, qs);
     uint32_t dh2, dl2;
@@ -297,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr Smem L = plan();
   // 128-byte swizzled stages need 1024-byte aligned shared addresses
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  static_assert(BK == 32 || BK == 64, "the dequant mapping covers BK = 32 or 64");
   uint8_t* sA = smem + L.a;
   uint8_t* sB = smem + L.b;
   uint8_t* sRaw = smem + L.raw;
@@ -315,15 +355,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // work unit: a group of kCluster adjacent column tiles of one row tile; the
+  // CTAs of a cluster take the group's tiles by rank
+  const int rank = static_cast<int>(cluster_ctarank());
   const int tiles_m = (p.M + BM - 1) / BM;
-  const int tiles_n = (p.N + BN - 1) / BN;
-  const int ntiles = tiles_m * tiles_n;
+  const int groups_n = (p.N + BN * kCluster - 1) / (BN * kCluster);
+  const int ngroups = tiles_m * groups_n;
+  const int first = blockIdx.x / kCluster, stride = gridDim.x / kCluster;
   const int ksteps = (p.K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStagesA; ++i) {
       mbar_init(&full_a[i], 1);
-      mbar_init(&empty_a[i], 1);
+      mbar_init(&empty_a[i], kCluster);   // one commit from every CTA's MMA thread
     }
     for (int i = 0; i < kStagesRaw; ++i) {
       mbar_init(&full_raw[i], 1);
@@ -341,7 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
-  __syncthreads();
+  // every CTA's barriers are initialised before any peer multicasts into them
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -349,14 +394,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================= producer =================
     if (lane == 0) {
       int ga = 0, gr = 0;   // loads issued into the A and raw rings
-      for (int tile = blockIdx.x; tile < ntiles && !*s_fail; tile += gridDim.x) {
-        const int m0 = (tile % tiles_m) * BM, n0 = (tile / tiles_m) * BN;
+      for (int g = first; g < ngroups && !*s_fail; g += stride) {
+        const int m0 = (g % tiles_m) * BM, n0 = ((g / tiles_m) * kCluster + rank) * BN;
         for (int ks = 0; ks < ksteps; ++ks) {
           const int sa = ga % kStagesA, sr = gr % kStagesRaw;
+          // the stage is free once the MMAs of every CTA in the cluster read it
           if (ga >= kStagesA && !gwait(&empty_a[sa], ((ga / kStagesA) - 1) & 1, s_fail, p.err))
             break;
           mbar_arrive_expect_tx(&full_a[sa], kABytes);
-          tma_load_2d(sA + sa * kABytes, &p.tmap_a, ks * BK, m0, &full_a[sa]);
+          tma_load_2d_mc(sA + sa * kABytes + rank * kASlice * (BK * 2), &p.tmap_a, ks * BK,
+                         m0 + rank * kASlice, &full_a[sa], kClusterMask);
           ++ga;
           if (gr >= kStagesRaw &&
               !gwait(&empty_raw[sr], ((gr / kStagesRaw) - 1) & 1, s_fail, p.err))
@@ -379,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================= MMA issuer =================
     if (lane == 0) {
       int ga = 0, gb = 0, tl = 0;
-      for (int tile = blockIdx.x; tile < ntiles && !*s_fail; tile += gridDim.x, ++tl) {
+      for (int g = first; g < ngroups && !*s_fail; g += stride, ++tl) {
         // the epilogue of the previous tile must have drained the accumulators
         if (tl > 0 && !gwait(tmem_empty, (tl - 1) & 1, s_fail, p.err)) break;
         tc_fence_after();
@@ -395,15 +442,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // B: MN-major, one K16 step = two 8-row swizzle atoms = 2048 bytes
-            const uint64_t bdesc = smem_desc(b_base + kk * 2048, 8192, 1024);
+            const uint64_t bdesc = smem_desc(b_base + kk * 2048, kBLbo, 1024, kSwizzle128);
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
-              // A: K-major 128-byte swizzle, 32 bytes per K16 step, 16 KB per 128 rows
-              const uint64_t adesc = smem_desc(a_base + mt * 16384 + kk * 32, 16, 1024);
+              // A: K-major, 32 bytes per K16 step, 128 rows per accumulator
+              const uint64_t adesc =
+                  smem_desc(a_base + mt * 128 * kARowBytes + kk * 32, 16, kASbo, kASwizzle);
               tc_mma(tmem + mt * BN, adesc, bdesc, kIdesc, (ks > 0 || kk > 0) ? 1u : 0u);
             }
           }
-          tc_commit(&empty_a[sa]);   // frees the A and B stages once these MMAs are done
+          // frees the A stage (in every CTA of the cluster) and the B stage
+          // once these MMAs are done
+          tc_commit_mc(&empty_a[sa], kClusterMask);
           tc_commit(&empty_b[sb]);
         }
         if (!ok) break;
@@ -419,8 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wd = warp - 2;   // 0..7
     int gr = 0, gb = 0, tl = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < ntiles && ok && !*s_fail; tile += gridDim.x, ++tl) {
-      const int m0 = (tile % tiles_m) * BM, n0 = (tile / tiles_m) * BN;
+    for (int g = first; g < ngroups && ok && !*s_fail; g += stride, ++tl) {
+      const int m0 = (g % tiles_m) * BM, n0 = ((g / tiles_m) * kCluster + rank) * BN;
       for (int ks = 0; ks < ksteps; ++ks, ++gr, ++gb) {
         const int sr = gr % kStagesRaw, sb = gb % kStagesB;
         int w = 1;
@@ -471,6 +521,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // no CTA leaves while a peer may still multicast into it or arrive on its
+  // barriers (every wait above is bounded, so all CTAs get here)
+  cluster_sync();
 }
 
 }  // namespace gemm
@@ -504,14 +557,16 @@ cudaError_t launch_gemm(void* C, int c_dtype, const void* A, const void* B, int6
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
   GemmParams p;
-  // A: bf16 [M][K], box 64 (K) x 256 (rows), 128-byte swizzle
+  // A: bf16 [M][K], box BK x kASlice rows (one CTA's share), swizzled rows
   {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 2)};
-    const cuuint32_t box[2] = {BK, BM};
+    const cuuint32_t box[2] = {BK, kASlice};
+    const CUtensorMapSwizzle swz =
+        (kARowBytes == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     const cuuint32_t es[2] = {1, 1};
     if (encode(&p.tmap_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A), dims, strides,
-               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -520,7 +575,7 @@ cudaError_t launch_gemm(void* C, int c_dtype, const void* A, const void* B, int6
     const int64_t nb = (N + 31) / 32;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nb * 9), static_cast<cuuint64_t>(K)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nb * kBlockBytes)};
-    const cuuint32_t box[2] = {72, BK};
+    const cuuint32_t box[2] = {72, BK};   // 8 blocks x BK rows
     const cuuint32_t es[2] = {1, 1};
     if (encode(&p.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(B), dims, strides,
                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -533,14 +588,40 @@ cudaError_t launch_gemm(void* C, int c_dtype, const void* A, const void* B, int6
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.err = err;
-  const int ntiles = static_cast<int>(((M + BM - 1) / BM) * ((N + BN - 1) / BN));
-  const int grid = ntiles < sms ? ntiles : sms;
   const uint32_t smem = plan().total;
   cudaError_t e = cudaFuncSetAttribute(gemm::q4_gemm_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  gemm::q4_gemm_tc_kernel<<<grid, kThreads, smem, st>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // persistent grid: as many clusters as can be resident at once (one CTA per
+  // SM), at most one per work group
+  static int resident[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (resident[dev] == 0) {
+    cfg.gridDim = dim3(static_cast<unsigned>((sms / kCluster) * kCluster));
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, gemm::q4_gemm_tc_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorInvalidConfiguration;
+    resident[dev] = n;
+  }
+  const int64_t groups = ((M + BM - 1) / BM) * ((N + BN * kCluster - 1) / (BN * kCluster));
+  const int64_t clusters = groups < resident[dev] ? groups : resident[dev];
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * kCluster));
+  e = cudaLaunchKernelEx(&cfg, gemm::q4_gemm_tc_kernel, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
