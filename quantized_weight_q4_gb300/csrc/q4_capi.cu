@@ -20,9 +20,10 @@ __device__ unsigned int g_q4_status = 0u;
 constexpr int kMaxDevices = 64;
 // The rows of A a CTA uses are copied to shared memory: MR * rows * 4 bytes.
 constexpr int64_t kMaxASliceBytes = 64 * 1024;
-// Up to this many rows of A a matmul runs as split-K GEMVs on the CUDA cores;
-// above it (bf16 A) as a tensor-core GEMM.
-constexpr int64_t kMaxGemvRows = 64;
+// From this many rows of bf16 A on, a matmul runs on the tensor cores (the
+// split-K small-M form up to 128 rows, the persistent prefill form above);
+// below it, and for fp32 A, as split-K GEMVs on the CUDA cores.
+constexpr int64_t kMinTensorRows = 8;
 
 struct GemvShape {
   int mr, bpt, nchunks, ntiles, nsplit, rows_per_split;
@@ -245,7 +246,8 @@ int q4_matmul_ex(void* C, int c_dtype, const void* A, int a_dtype, const void* B
   DeviceState* s = nullptr;
   int rc = current_state(&s);
   if (rc != Q4_OK) return rc;
-  if (M > kMaxGemvRows && a_dtype == Q4_BF16 && q4::gemm_supported(M, N, K))
+  if (M >= kMinTensorRows && a_dtype == Q4_BF16 && q4::gemm_supported(M, N, K) &&
+      (M > 128 || q4::gemm_small_split(M, N, K, s->sms) > 0))
     return launch_status(q4::launch_gemm(C, c_dtype, A, B, M, N, K, s->status, s->sms,
                                          static_cast<cudaStream_t>(stream)));
   const GemvShape& g = cached_gemv_shape(s, M, N, K);

@@ -1,4 +1,4 @@
-// Prefill Q4_0 GEMM on the 5th-generation tensor cores (sm_103a).
+// Q4_0 GEMM on the 5th-generation tensor cores (sm_103a).
 //
 // C[M, N] = A[M, K] . W[K, N] with bf16 A, the weights W in the block layout of
 // the C++ DeepSeek engine page (§2.2-§2.3: K rows of ceil(N/32) 18-byte
@@ -7,20 +7,25 @@
 // dequantised once per CTA tile to bf16: bf16_rn((q - 8) * d), the exact
 // product rounded once (bf16x2 arithmetic on a split of d, see split_scale).
 //
-// Structure (one CTA per SM, persistent over 256 x 256 output tiles):
-//  * warp 0, producer: TMA loads of A (64 K x 256 rows, 128-byte swizzle,
+// One kernel template, two forms:
+//  * prefill (MT = 2): one CTA per SM, persistent over 256 x 256 output tiles;
+//  * small M (MT = 1, SPLIT): 128 x 256 output tiles, each split along K over
+//    the S CTAs of a thread-block cluster; the partial sums meet in shared
+//    memory over DSMEM and are added in rank order (deterministic).
+// Roles inside a CTA:
+//  * warp 0, producer: TMA loads of A (64 K x 128*MT rows, 128-byte swizzle,
 //    K-major) and of the raw Q4 tile (64 rows x 8 blocks) into rings;
-//  * warps 2..9, dequant + epilogue: decode each raw block (one K row, 32
-//    consecutive N) into 64 contiguous bytes of an MN-major, 128-byte-swizzled
-//    bf16 B tile; after a tile's last K step, read the accumulators out of
-//    tensor memory and store C;
-//  * warp 1, MMA: allocates 512 tensor-memory columns (two 128 x 256 fp32
-//    accumulators), issues tcgen05.mma (M = 128, N = 256, K = 16; two per K16
-//    step, one per half of the tile's rows, both reading the same B tile) and
-//    signals stage and accumulator readiness with tcgen05.commit.
+//  * warps 2 .. DW+1, dequant + epilogue: decode each raw block (one K row,
+//    32 consecutive N) into 64 bytes of an MN-major, 128-byte-swizzled bf16 B
+//    tile; after a tile's last K step, read the accumulators out of tensor
+//    memory and store C (or push the partial sums to their owner);
+//  * warp 1, MMA: allocates MT*256 tensor-memory columns (MT accumulators of
+//    128 x 256 fp32), issues tcgen05.mma (M = 128, N = 256, K = 16; MT per
+//    K16 step, all reading the same B tile) and signals stage and
+//    accumulator readiness with tcgen05.commit.
 // Every wait on an mbarrier is bounded: on a timeout the CTA records an error
 // in the device status word, stops issuing work, drains the tensor core and
-// frees its tensor memory before returning.
+// its copies and frees its tensor memory before returning.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -32,43 +37,56 @@
 namespace q4 {
 namespace gemm {
 
-constexpr int BM = 256, BN = 256, BK = 64;
-// CTAs of a thread-block cluster take the same rows of A and adjacent column
-// tiles: each loads 1/kCluster of the A tile and multicasts it to all.
-constexpr int kCluster = 1;
-constexpr int kASlice = BM / kCluster;                 // A rows loaded per CTA
-constexpr uint16_t kClusterMask = (1u << kCluster) - 1;
-constexpr int kStagesA = 3;     // A ring: 3 x 32 KB
-constexpr int kStagesRaw = 3;   // raw Q4 ring: 3 x 9 KB
-constexpr int kStagesB = 3;     // dequantised B ring: 3 x 32 KB
-constexpr int kABytes = BM * BK * 2;                   // 32768
-constexpr int kBBytes = BN * BK * 2;                   // 32768
+constexpr int BN = 256, BK = 64;
+constexpr int kBBytes = BN * BK * 2;                            // 32768
+constexpr int kRawRowBytes = (BN / kBlockCols) * kBlockBytes;   // 144
+constexpr int kRawBytes = BK * kRawRowBytes;                    // 9216
 // A rows are BK * 2 bytes: one swizzle span of that width (128 or 64 bytes)
 constexpr int kARowBytes = BK * 2;
 static_assert(kARowBytes == 128 || kARowBytes == 64, "A rows must fill one swizzle span");
-constexpr int kBarBytes = 512;
-constexpr int kRawRowBytes = (BN / kBlockCols) * kBlockBytes;   // 144
-constexpr int kRawBytes = BK * kRawRowBytes;           // 9216
-constexpr int kDequantWarps = 8;
-constexpr int kThreads = (2 + kDequantWarps) * 32;     // 320
-constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxSplit = 16;   // non-portable thread-block cluster size limit
 
-struct Smem {
-  uint32_t a, b, raw, bars, total;
+// Compile-time shape of one kernel form.
+template <int MT, int DW, bool SPLIT>
+struct Cfg {
+  static constexpr int kBM = 128 * MT;                 // rows of A per tile
+  static constexpr int kThreads = (2 + DW) * 32;
+  // ring depths: the prefill form re-reads A from L2 for every column tile
+  // and needs its A ring deep; the small-M form streams each weight once
+  // from HBM and needs its raw ring deep
+  static constexpr int kStagesA = (MT == 2) ? 3 : 4;   // 32 KB or 16 KB per stage
+  static constexpr int kStagesB = (MT == 2) ? 3 : 2;   // 32 KB per stage
+  static constexpr int kStagesRaw = (MT == 2) ? 3 : 8; // 9 KB per stage
+  static constexpr int kABytes = kBM * BK * 2;
+  static constexpr uint32_t kTmemCols = MT * BN;
+  // dequant units (8 rows x 4 blocks) per warp and stage
+  static constexpr int kUnitsPerWarp = (BK / 4) / DW;
+  // epilogue: the DW/4 warps of one tensor-memory lane quarter split the
+  // MT * BN accumulator columns
+  static constexpr int kEpiCols = MT * BN / (DW / 4);
+  // shared memory plan; A and B stages need 1024-byte alignment
+  static constexpr uint32_t kOffB = kStagesA * kABytes;
+  static constexpr uint32_t kOffRaw = kOffB + kStagesB * kBBytes;
+  static constexpr uint32_t kOffBars = kOffRaw + kStagesRaw * kRawBytes;
+  static constexpr uint32_t kBarBytes = 256;
+  static constexpr uint32_t kSmemBytes = kOffBars + kBarBytes + 1024;
+  static_assert(MT == 1 || (MT == 2 && !SPLIT), "forms: prefill (MT 2) and split small M (MT 1)");
+  static_assert(kUnitsPerWarp >= 1 && (BK / 4) % DW == 0 && DW % 4 == 0, "dequant warps");
+  static_assert(kEpiCols % 32 == 0 && BN % kEpiCols == 0, "epilogue column split");
+  static_assert(kABytes % 1024 == 0 && kOffRaw % 1024 == 0 && kRawBytes % 128 == 0,
+                "TMA destinations need alignment");
+  static_assert((2 * kStagesA + 2 * kStagesRaw + 2 * kStagesB + 3) * 8 + 8 <= kBarBytes,
+                "barrier region overflows");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory plan exceeds the per-CTA limit");
 };
-__host__ __device__ constexpr Smem plan() {
-  // A and B stages need 1024-byte alignment (swizzle atoms)
-  return Smem{0, kStagesA * kABytes, kStagesA * kABytes + kStagesB * kBBytes,
-              kStagesA * kABytes + kStagesB * kBBytes + kStagesRaw * kRawBytes,
-              kStagesA * kABytes + kStagesB * kBBytes + kStagesRaw * kRawBytes + kBarBytes + 1024};
-}
 
-static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0 && plan().raw % 1024 == 0 &&
-                  kRawBytes % 128 == 0 && plan().bars % 8 == 0,
-              "TMA destinations need alignment");
-static_assert((2 * kStagesA + 2 * kStagesRaw + 2 * kStagesB + 3) * 8 + 8 <= kBarBytes,
-              "barrier region overflows");
-static_assert(plan().total <= 227 * 1024, "shared memory plan exceeds the per-CTA limit");
+// Split form: the partial sums of a 128 x 256 tile travel as rows of 32
+// columns, padded to 36 floats (16-byte aligned, conflict-free 16-byte
+// stores of eight consecutive rows).  Owner of 32-column chunk c: rank c % S.
+constexpr int kRedRowFloats = 36;
+__host__ __device__ constexpr uint32_t red_bytes(int S, int rows) {
+  return static_cast<uint32_t>(((BN / 32 + S - 1) / S) * S * rows * kRedRowFloats * 4);
+}
 
 // ---- tcgen05 / TMA wrappers ------------------------------------------------
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int c0, int c1,
@@ -77,17 +95,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int c0,
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// The same box into the same shared offset of every CTA in `mask`; each
-// destination's mbarrier (same offset) receives the bytes it got.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const void* tmap, int c0, int c1,
-                                               uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(mask)
       : "memory");
 }
 
@@ -114,15 +121,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
           smem_u32(bar))
       : "memory");
 }
-// Arrives once on the mbarrier at this offset in every CTA of `mask` when the
-// MMAs issued so far by this thread are complete.
-__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-
 // D[tmem] (+)= A[smem desc] . B[smem desc]
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                        uint32_t idesc, uint32_t accumulate) {
@@ -255,7 +253,7 @@ __device__ __forceinline__ uint32_t decode_pair(uint32_t w_shifted, uint32_t dh2
 }
 
 // A stage is BK/8 row groups x 2 parities of (8 rows x 4 blocks) units; warp
-// wd decodes units wd * BK/32 + i, i < BK/32.  In unit u (row group u/2,
+// wd decodes units wd * UPW + i, i < UPW.  In unit u (row group u/2,
 // parity u%2), lane = 8*s + r takes row 8*(u/2) + r and block 2*s + u%2.
 //  * 16-byte stores are served eight lanes at a time; those eight lanes hold
 //    eight different rows of one block, i.e. eight different chunk positions
@@ -263,11 +261,12 @@ __device__ __forceinline__ uint32_t decode_pair(uint32_t w_shifted, uint32_t dh2
 //  * 32-bit raw reads: the rows are 36 words apart (4 banks), and the even
 //    (odd) blocks start at words 0, 9, 18, 27 (4, 13, 22, 31) of a row, one
 //    per residue mod 4: the 32 lanes hit 32 different banks.
+template <int UPW>
 __device__ __forceinline__ void dequant_stage(const uint8_t* raw, uint8_t* btile, int wd,
                                               int lane) {
 #pragma unroll
-  for (int i = 0; i < BK / 32; ++i) {
-    const int u = wd * (BK / 32) + i;
+  for (int i = 0; i < UPW; ++i) {
+    const int u = wd * UPW + i;
     const int k = (u >> 1) * 8 + (lane & 7);
     const int b = 2 * (lane >> 3) + (u & 1);
     uint32_t dbits, qs[4];
@@ -329,18 +328,78 @@ __device__ __forceinline__ void store_row32(const GemmParams& p, int row, int co
   }
 }
 
+
+// Four consecutive fp32 results of one row of C, columns col .. col+3.
+__device__ __forceinline__ void store_group4(const GemmParams& p, int row, int col, float4 v) {
+  if (row >= p.M || col >= p.N) return;
+  const size_t base = static_cast<size_t>(row) * p.N + col;
+  const bool whole = col + 4 <= p.N && (p.N & 3) == 0;
+  if (p.c_dtype == 0) {
+    float* dst = reinterpret_cast<float*>(p.C) + base;
+    if (whole) {
+      *reinterpret_cast<float4*>(dst) = v;
+    } else {
+      const float f[4] = {v.x, v.y, v.z, v.w};
+      for (int j = 0; j < 4 && col + j < p.N; ++j) dst[j] = f[j];
+    }
+  } else {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(p.C) + base;
+    if (whole) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(bf16_bits(v.x) | (bf16_bits(v.y) << 16),
+                                                  bf16_bits(v.z) | (bf16_bits(v.w) << 16));
+    } else {
+      const float f[4] = {v.x, v.y, v.z, v.w};
+      for (int j = 0; j < 4 && col + j < p.N; ++j) dst[j] = static_cast<uint16_t>(bf16_bits(f[j]));
+    }
+  }
+}
+
+// A unit of work: one output tile (rows m0.., columns n0..) over K steps
+// [kb, ke) of BK rows.
+struct Work {
+  int m0, n0, kb, ke;
+};
+
+// The it-th unit of this CTA (false when there is none).  Prefill: tiles
+// blockIdx.x, blockIdx.x + gridDim.x, ... over all K.  Split: the one tile of
+// the cluster, this CTA's share of K (cluster rank = blockIdx.x % S).
+template <int MT, bool SPLIT>
+__device__ __forceinline__ bool work_item(const GemmParams& p, int it, Work& w) {
+  constexpr int kBM = 128 * MT;
+  const int tiles_m = (p.M + kBM - 1) / kBM;
+  const int tiles_n = (p.N + BN - 1) / BN;
+  const int ksteps = (p.K + BK - 1) / BK;
+  int tile;
+  if (SPLIT) {
+    if (it > 0) return false;
+    tile = blockIdx.x / p.nsplit;
+    const int s = blockIdx.x % p.nsplit;
+    w.kb = s * ksteps / p.nsplit;
+    w.ke = (s + 1) * ksteps / p.nsplit;
+  } else {
+    tile = blockIdx.x + it * gridDim.x;
+    w.kb = 0;
+    w.ke = ksteps;
+  }
+  if (tile >= tiles_m * tiles_n) return false;
+  w.m0 = (tile % tiles_m) * kBM;
+  w.n0 = (tile / tiles_m) * BN;
+  return true;
+}
+
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MT, int DW, bool SPLIT>
+__global__ void __launch_bounds__(Cfg<MT, DW, SPLIT>::kThreads, 1)
     q4_gemm_tc_kernel(const __grid_constant__ GemmParams p) {
+  using C = Cfg<MT, DW, SPLIT>;
+  constexpr int kStagesA = C::kStagesA, kStagesB = C::kStagesB, kStagesRaw = C::kStagesRaw;
   extern __shared__ uint8_t smem_raw[];
-  constexpr Smem L = plan();
-  // 128-byte swizzled stages need 1024-byte aligned shared addresses
+  // swizzled stages need 1024-byte aligned shared addresses
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  static_assert(BK == 32 || BK == 64, "the dequant mapping covers BK = 32 or 64");
-  uint8_t* sA = smem + L.a;
-  uint8_t* sB = smem + L.b;
-  uint8_t* sRaw = smem + L.raw;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::kOffB;
+  uint8_t* sRaw = smem + C::kOffRaw;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
   uint64_t* full_a = bars;                          // [kStagesA]
   uint64_t* empty_a = full_a + kStagesA;            // [kStagesA]
   uint64_t* full_raw = empty_a + kStagesA;          // [kStagesRaw]
@@ -355,38 +414,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // work unit: a group of kCluster adjacent column tiles of one row tile; the
-  // CTAs of a cluster take the group's tiles by rank
-  const int rank = static_cast<int>(cluster_ctarank());
-  const int tiles_m = (p.M + BM - 1) / BM;
-  const int groups_n = (p.N + BN * kCluster - 1) / (BN * kCluster);
-  const int ngroups = tiles_m * groups_n;
-  const int first = blockIdx.x / kCluster, stride = gridDim.x / kCluster;
-  const int ksteps = (p.K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStagesA; ++i) {
       mbar_init(&full_a[i], 1);
-      mbar_init(&empty_a[i], kCluster);   // one commit from every CTA's MMA thread
+      mbar_init(&empty_a[i], 1);
     }
     for (int i = 0; i < kStagesRaw; ++i) {
       mbar_init(&full_raw[i], 1);
-      mbar_init(&empty_raw[i], kDequantWarps);
+      mbar_init(&empty_raw[i], DW);
     }
     for (int i = 0; i < kStagesB; ++i) {
-      mbar_init(&full_b[i], kDequantWarps);
+      mbar_init(&full_b[i], DW);
       mbar_init(&empty_b[i], 1);
     }
     mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, kDequantWarps);
+    mbar_init(tmem_empty, DW);
     mbar_init(drain, 1);
     *s_fail = 0;
     fence_barrier_init();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
   tc_fence_before();
-  // every CTA's barriers are initialised before any peer multicasts into them
-  cluster_sync();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -394,29 +444,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================= producer =================
     if (lane == 0) {
       int ga = 0, gr = 0;   // loads issued into the A and raw rings
-      for (int g = first; g < ngroups && !*s_fail; g += stride) {
-        const int m0 = (g % tiles_m) * BM, n0 = ((g / tiles_m) * kCluster + rank) * BN;
-        for (int ks = 0; ks < ksteps; ++ks) {
+      Work w;
+      for (int it = 0; work_item<MT, SPLIT>(p, it, w) && !*s_fail; ++it) {
+        for (int ks = w.kb; ks < w.ke; ++ks) {
           const int sa = ga % kStagesA, sr = gr % kStagesRaw;
-          // the stage is free once the MMAs of every CTA in the cluster read it
           if (ga >= kStagesA && !gwait(&empty_a[sa], ((ga / kStagesA) - 1) & 1, s_fail, p.err))
             break;
-          mbar_arrive_expect_tx(&full_a[sa], kABytes);
-          tma_load_2d_mc(sA + sa * kABytes + rank * kASlice * (BK * 2), &p.tmap_a, ks * BK,
-                         m0 + rank * kASlice, &full_a[sa], kClusterMask);
+          // the A box holds p.a_rows rows (the tile's rows, rounded up to 16);
+          // the MMA also reads the stage's remaining rows, whose accumulator
+          // rows are never stored
+          mbar_arrive_expect_tx(&full_a[sa], static_cast<uint32_t>(p.a_rows * kARowBytes));
+          tma_load_2d(sA + sa * C::kABytes, &p.tmap_a, ks * BK, w.m0, &full_a[sa]);
           ++ga;
           if (gr >= kStagesRaw &&
               !gwait(&empty_raw[sr], ((gr / kStagesRaw) - 1) & 1, s_fail, p.err))
             break;
           mbar_arrive_expect_tx(&full_raw[sr], kRawBytes);
-          tma_load_2d(sRaw + sr * kRawBytes, &p.tmap_b, (n0 / kBlockCols) * (kBlockBytes / 2),
+          tma_load_2d(sRaw + sr * kRawBytes, &p.tmap_b, (w.n0 / kBlockCols) * (kBlockBytes / 2),
                       ks * BK, &full_raw[sr]);
           ++gr;
         }
       }
-      // No copy may still be writing shared memory when the CTA exits: wait
-      // (bounded) for the last load issued into every stage.  On the normal
-      // path these phases completed long ago.
+      // No copy may still be writing shared memory when the CTA exits or the
+      // rings are reused: wait (bounded) for the last load issued into every
+      // stage.  On the normal path these phases completed long ago.
       for (int g = ga - 1; g >= 0 && g >= ga - kStagesA; --g)
         (void)mbar_wait(&full_a[g % kStagesA], (g / kStagesA) & 1);
       for (int g = gr - 1; g >= 0 && g >= gr - kStagesRaw; --g)
@@ -425,63 +476,65 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ================= MMA issuer =================
     if (lane == 0) {
-      int ga = 0, gb = 0, tl = 0;
-      for (int g = first; g < ngroups && !*s_fail; g += stride, ++tl) {
+      int ga = 0, gb = 0;
+      Work w;
+      for (int it = 0; work_item<MT, SPLIT>(p, it, w) && !*s_fail; ++it) {
         // the epilogue of the previous tile must have drained the accumulators
-        if (tl > 0 && !gwait(tmem_empty, (tl - 1) & 1, s_fail, p.err)) break;
+        if (it > 0 && !gwait(tmem_empty, (it - 1) & 1, s_fail, p.err)) break;
         tc_fence_after();
         bool ok = true;
-        for (int ks = 0; ks < ksteps; ++ks, ++ga, ++gb) {
+        for (int ks = w.kb; ks < w.ke; ++ks, ++ga, ++gb) {
           const int sa = ga % kStagesA, sb = gb % kStagesB;
           ok = gwait(&full_a[sa], (ga / kStagesA) & 1, s_fail, p.err) &&
                gwait(&full_b[sb], (gb / kStagesB) & 1, s_fail, p.err);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + sa * kABytes);
+          const uint32_t a_base = smem_u32(sA + sa * C::kABytes);
           const uint32_t b_base = smem_u32(sB + sb * kBBytes);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // B: MN-major, one K16 step = two 8-row swizzle atoms = 2048 bytes
             const uint64_t bdesc = smem_desc(b_base + kk * 2048, kBLbo, 1024, kSwizzle128);
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
+            for (int mt = 0; mt < MT; ++mt) {
               // A: K-major, 32 bytes per K16 step, 128 rows per accumulator
               const uint64_t adesc =
                   smem_desc(a_base + mt * 128 * kARowBytes + kk * 32, 16, kASbo, kASwizzle);
-              tc_mma(tmem + mt * BN, adesc, bdesc, kIdesc, (ks > 0 || kk > 0) ? 1u : 0u);
+              tc_mma(tmem + mt * BN, adesc, bdesc, kIdesc, (ks > w.kb || kk > 0) ? 1u : 0u);
             }
           }
-          // frees the A stage (in every CTA of the cluster) and the B stage
-          // once these MMAs are done
-          tc_commit_mc(&empty_a[sa], kClusterMask);
+          // frees the A and B stages once these MMAs are done
+          tc_commit(&empty_a[sa]);
           tc_commit(&empty_b[sb]);
         }
         if (!ok) break;
         tc_commit(tmem_full);
       }
       // every MMA this thread issued must be complete before the tensor memory
-      // is freed and the CTA exits (bounded wait, also after a failure)
+      // is freed, the rings are reused or the CTA exits (bounded wait, also
+      // after a failure)
       tc_commit(drain);
       (void)mbar_wait(drain, 0);
     }
   } else {
     // ================= dequant + epilogue =================
-    const int wd = warp - 2;   // 0..7
-    int gr = 0, gb = 0, tl = 0;
+    const int wd = warp - 2;   // 0 .. DW-1
+    const int q = warp & 3;    // the tensor-memory lane quarter this warp may access
+    int gr = 0, gb = 0;
     bool ok = true;
-    for (int g = first; g < ngroups && ok && !*s_fail; g += stride, ++tl) {
-      const int m0 = (g % tiles_m) * BM, n0 = ((g / tiles_m) * kCluster + rank) * BN;
-      for (int ks = 0; ks < ksteps; ++ks, ++gr, ++gb) {
+    Work w;
+    for (int it = 0; ok && work_item<MT, SPLIT>(p, it, w) && !*s_fail; ++it) {
+      for (int ks = w.kb; ks < w.ke; ++ks, ++gr, ++gb) {
         const int sr = gr % kStagesRaw, sb = gb % kStagesB;
-        int w = 1;
+        int v = 1;
         if (lane == 0) {
-          w = gwait(&full_raw[sr], (gr / kStagesRaw) & 1, s_fail, p.err) ? 1 : 0;
-          if (w && gb >= kStagesB)
-            w = gwait(&empty_b[sb], ((gb / kStagesB) - 1) & 1, s_fail, p.err) ? 1 : 0;
+          v = gwait(&full_raw[sr], (gr / kStagesRaw) & 1, s_fail, p.err) ? 1 : 0;
+          if (v && gb >= kStagesB)
+            v = gwait(&empty_b[sb], ((gb / kStagesB) - 1) & 1, s_fail, p.err) ? 1 : 0;
         }
-        ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+        ok = __shfl_sync(0xffffffffu, v, 0) != 0;
         if (!ok) break;
-        dequant_stage(sRaw + sr * kRawBytes, sB + sb * kBBytes, wd, lane);
+        dequant_stage<C::kUnitsPerWarp>(sRaw + sr * kRawBytes, sB + sb * kBBytes, wd, lane);
         fence_async_smem();   // the tensor core reads B through the async proxy
         __syncwarp();
         if (lane == 0) {
@@ -490,22 +543,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      // ---- epilogue: accumulators -> C ----
-      int w = 1;
-      if (lane == 0) w = gwait(tmem_full, tl & 1, s_fail, p.err) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+      int v = 1;
+      if (lane == 0) v = gwait(tmem_full, it & 1, s_fail, p.err) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, v, 0) != 0;
       if (!ok) break;
       tc_fence_after();
-      const int q = warp & 3;   // the tensor-memory lane quarter this warp may access
+      if (SPLIT) break;   // the split form's epilogue follows below
+      // ---- epilogue: accumulators -> C ----
       {
-        const int mt = wd >> 2;   // warps 2..5 drain the first accumulator, 6..9 the second
-        const int row = m0 + mt * 128 + q * 32 + lane;
+        // column c of the MT x BN accumulator columns is column c % BN of
+        // accumulator c / BN; the warps of one lane quarter split them
+        const int c0 = (wd >> 2) * C::kEpiCols;
+        const int mt = c0 / BN;
+        const int row = w.m0 + mt * 128 + q * 32 + lane;
 #pragma unroll 1
-        for (int cc = 0; cc < BN / 32; ++cc) {
-          uint32_t v[32];
-          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + mt * BN + cc * 32, v);
-          const int col0 = n0 + cc * 32;
-          if (row < p.M && col0 < p.N) store_row32(p, row, col0, v);
+        for (int c = c0; c < c0 + C::kEpiCols; c += 32) {
+          uint32_t acc[32];
+          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, acc);
+          const int col0 = w.n0 + (c - mt * BN);
+          if (row < p.M && col0 < p.N) store_row32(p, row, col0, acc);
         }
       }
       tc_fence_before();
@@ -513,17 +569,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(tmem_empty);
     }
   }
+
+  if (SPLIT) {
+    // ---- split-K combine over the cluster ----
+    // (1) Every CTA of the cluster is past its main loop: its MMAs and copies
+    //     are complete (the MMA thread and the producer waited for them), so
+    //     its rings (A, B and raw) may take partial sums.
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const int S = p.nsplit;
+    const int rank = static_cast<int>(cluster_ctarank());
+    Work w;
+    const bool have = work_item<MT, SPLIT>(p, 0, w);
+    const int rows = min(p.M - w.m0, 128);   // valid rows of the tile
+    float* red = reinterpret_cast<float*>(smem);
+    if (warp >= 2 && have && !*s_fail) {
+      // (2) push: each warp reads its lane quarter's columns of the
+      //     accumulator and stores the 32-column chunks, in output column
+      //     order, into the owning CTA's buffer [chunk/S][source rank][row]
+      const int wd = warp - 2, q = warp & 3;
+      const int c0 = (wd >> 2) * C::kEpiCols;
+      const int row = q * 32 + lane;
+#pragma unroll 1
+      for (int c = c0; c < c0 + C::kEpiCols; c += 32) {
+        uint32_t acc[32], v[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, acc);
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+          for (int s = 0; s < 8; ++s) v[8 * t + chunk_col(s)] = acc[8 * t + s];
+        const int chunk = c / 32, owner = chunk % S, jj = chunk / S;
+        if (row < rows) {
+          const uint32_t dst = peer_addr(
+              red + ((static_cast<size_t>(jj) * S + rank) * rows + row) * kRedRowFloats, owner);
+#pragma unroll
+          for (int j = 0; j < 32; j += 4)
+            asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + j * 4),
+                         "r"(v[j]), "r"(v[j + 1]), "r"(v[j + 2]), "r"(v[j + 3])
+                         : "memory");
+        }
+      }
+    }
+    // (3) all partial sums have arrived
+    tc_fence_before();
+    cluster_sync();
+    if (warp >= 2 && have && !*s_fail) {
+      // (4) the owner adds the S partial sums of its chunks in rank order and
+      //     stores C: consecutive threads take consecutive 4-column groups
+      const int mine = (BN / 32 - rank + S - 1) / S;   // chunks rank, rank + S, ...
+      const int items = mine * rows * 8;
+      for (int i = threadIdx.x - 64; i < items; i += DW * 32) {
+        const int jj = i / (rows * 8), r = (i / 8) % rows, g4 = i % 8;
+        const float* src = red + (static_cast<size_t>(jj) * S * rows + r) * kRedRowFloats + g4 * 4;
+        float4 acc = *reinterpret_cast<const float4*>(src);
+        for (int s = 1; s < S; ++s) {
+          const float4 t =
+              *reinterpret_cast<const float4*>(src + static_cast<size_t>(s) * rows * kRedRowFloats);
+          acc.x += t.x;
+          acc.y += t.y;
+          acc.z += t.z;
+          acc.w += t.w;
+        }
+        store_group4(p, w.m0 + r, w.n0 + (rank + jj * S) * 32 + g4 * 4, acc);
+      }
+    }
+  }
+
   // everyone (the MMA thread after its drain) meets here before the tensor
   // memory is released
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
-  // no CTA leaves while a peer may still multicast into it or arrive on its
-  // barriers (every wait above is bounded, so all CTAs get here)
-  cluster_sync();
 }
 
 }  // namespace gemm
@@ -531,7 +651,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -544,85 +666,160 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return encode;
 }
 
+// Dequant warps of the small-M form.
+constexpr int kSmallDW = 16;
+using PrefillCfg = gemm::Cfg<2, 8, false>;
+using SmallCfg = gemm::Cfg<1, kSmallDW, true>;
+
+template <int MT, int DW, bool SPLIT>
+cudaLaunchConfig_t make_cfg(cudaLaunchAttribute* attr, int grid, int S, cudaStream_t st) {
+  using C = gemm::Cfg<MT, DW, SPLIT>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <int MT, int DW, bool SPLIT>
+cudaError_t prepare() {
+  using C = gemm::Cfg<MT, DW, SPLIT>;
+  cudaError_t e = cudaFuncSetAttribute(gemm::q4_gemm_tc_kernel<MT, DW, SPLIT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(C::kSmemBytes));
+  if (e != cudaSuccess) return e;
+  if (SPLIT)
+    e = cudaFuncSetAttribute(gemm::q4_gemm_tc_kernel<MT, DW, SPLIT>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+// Clusters of S CTAs of the small-M form that fit on the device at once
+// (cached per device; 0 if that size cannot launch).
+int small_resident(int S) {
+  static int cache[64][gemm::kMaxSplit + 1] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev][S] == 0) {
+    if (prepare<1, kSmallDW, true>() != cudaSuccess) return 0;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = make_cfg<1, kSmallDW, true>(attr, S, S, nullptr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm::q4_gemm_tc_kernel<1, kSmallDW, true>, &cfg) !=
+        cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    cache[dev][S] = n > 0 ? n : -1;
+  }
+  return cache[dev][S] > 0 ? cache[dev][S] : 0;
+}
+
+bool encode_maps(GemmParams& p, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
+                 int a_rows) {
+  p.a_rows = a_rows;
+  auto encode = get_encode();
+  if (!encode) return false;
+  // A: bf16 [M][K], boxes of BK x a_rows, rows swizzled in their 128 bytes
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 2)};
+    const cuuint32_t box[2] = {gemm::BK, static_cast<cuuint32_t>(a_rows)};
+    const cuuint32_t es[2] = {1, 1};
+    const CUtensorMapSwizzle swz =
+        (gemm::kARowBytes == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (encode(&p.tmap_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A), dims, strides,
+               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  // raw Q4: uint16 [K][nb*9], boxes of 72 halfwords (8 blocks) x BK rows
+  {
+    const int64_t nb = (N + 31) / 32;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nb * 9), static_cast<cuuint64_t>(K)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nb * kBlockBytes)};
+    const cuuint32_t box[2] = {72, gemm::BK};
+    const cuuint32_t es[2] = {1, 1};
+    if (encode(&p.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(B), dims, strides,
+               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
+}
+
+}  // namespace
+
 bool gemm_supported(int64_t M, int64_t N, int64_t K) {
   const int64_t nb = (N + 31) / 32;
   return M >= 1 && nb % 8 == 0 && K % 8 == 0 && K >= 1 && M <= (1LL << 30) && N <= (1LL << 30);
 }
 
-uint32_t gemm_smem_bytes() { return gemm::plan().total; }
+int gemm_small_split(int64_t M, int64_t N, int64_t K, int sms) {
+  (void)sms;
+  if (M > 128) return 0;
+  const int64_t tiles = (N + gemm::BN - 1) / gemm::BN;
+  const int64_t ksteps = (K + gemm::BK - 1) / gemm::BK;
+  const int rows = static_cast<int>(M);
+  int best = 0;
+  int64_t best_cost = 0;
+  for (int S = 1; S <= gemm::kMaxSplit && S <= ksteps; ++S) {
+    // the partial sums take the A, B and raw rings (free after the main loop)
+    if (gemm::red_bytes(S, rows) > SmallCfg::kOffBars) continue;
+    const int active = small_resident(S);
+    if (active <= 0) continue;
+    const int64_t waves = (tiles + active - 1) / active;
+    // a wave also pays its start (first loads) and the combine: about as
+    // long as kWaveSteps K steps
+    constexpr int64_t kWaveSteps = 10;
+    const int64_t cost = waves * ((ksteps + S - 1) / S + kWaveSteps);
+    if (best == 0 || cost < best_cost) {
+      best = S;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
 
 cudaError_t launch_gemm(void* C, int c_dtype, const void* A, const void* B, int64_t M, int64_t N,
                         int64_t K, unsigned* err, int sms, cudaStream_t st) {
-  using namespace gemm;
-  auto encode = get_encode();
-  if (!encode) return cudaErrorNotSupported;
   GemmParams p;
-  // A: bf16 [M][K], box BK x kASlice rows (one CTA's share), swizzled rows
-  {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 2)};
-    const cuuint32_t box[2] = {BK, kASlice};
-    const CUtensorMapSwizzle swz =
-        (kARowBytes == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    const cuuint32_t es[2] = {1, 1};
-    if (encode(&p.tmap_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A), dims, strides,
-               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  // raw Q4: uint16 [K][nb*9], box 72 halfwords (8 blocks) x 64 rows, no swizzle
-  {
-    const int64_t nb = (N + 31) / 32;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nb * 9), static_cast<cuuint64_t>(K)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nb * kBlockBytes)};
-    const cuuint32_t box[2] = {72, BK};   // 8 blocks x BK rows
-    const cuuint32_t es[2] = {1, 1};
-    if (encode(&p.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(B), dims, strides,
-               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
   p.C = C;
   p.c_dtype = c_dtype;
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.err = err;
-  const uint32_t smem = plan().total;
-  cudaError_t e = cudaFuncSetAttribute(gemm::q4_gemm_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kCluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // persistent grid: as many clusters as can be resident at once (one CTA per
-  // SM), at most one per work group
-  static int resident[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (resident[dev] == 0) {
-    cfg.gridDim = dim3(static_cast<unsigned>((sms / kCluster) * kCluster));
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, gemm::q4_gemm_tc_kernel, &cfg);
+  if (M > 128) {
+    // prefill form: persistent, one CTA per SM at most
+    if (!encode_maps(p, A, B, M, N, K, PrefillCfg::kBM)) return cudaErrorInvalidValue;
+    p.nsplit = 1;
+    cudaError_t e = prepare<2, 8, false>();
     if (e != cudaSuccess) return e;
-    if (n <= 0) return cudaErrorInvalidConfiguration;
-    resident[dev] = n;
+    const int64_t tiles = ((M + PrefillCfg::kBM - 1) / PrefillCfg::kBM) * ((N + gemm::BN - 1) / gemm::BN);
+    const int grid = static_cast<int>(tiles < sms ? tiles : sms);
+    cudaLaunchConfig_t cfg = make_cfg<2, 8, false>(attr, grid, 1, st);
+    return cudaLaunchKernelEx(&cfg, gemm::q4_gemm_tc_kernel<2, 8, false>, p);
   }
-  const int64_t groups = ((M + BM - 1) / BM) * ((N + BN * kCluster - 1) / (BN * kCluster));
-  const int64_t clusters = groups < resident[dev] ? groups : resident[dev];
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters * kCluster));
-  e = cudaLaunchKernelEx(&cfg, gemm::q4_gemm_tc_kernel, p);
+  // small-M form: one 128 x 256 tile per cluster of S CTAs splitting K
+  const int S = gemm_small_split(M, N, K, sms);
+  if (S <= 0) return cudaErrorInvalidConfiguration;
+  const int a_rows = static_cast<int>(((M + 15) / 16) * 16);   // M <= 128
+  if (!encode_maps(p, A, B, M, N, K, a_rows)) return cudaErrorInvalidValue;
+  p.nsplit = S;
+  cudaError_t e = prepare<1, kSmallDW, true>();
   if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  const int64_t tiles = (N + gemm::BN - 1) / gemm::BN;
+  cudaLaunchConfig_t cfg = make_cfg<1, kSmallDW, true>(attr, static_cast<int>(tiles * S), S, st);
+  return cudaLaunchKernelEx(&cfg, gemm::q4_gemm_tc_kernel<1, kSmallDW, true>, p);
 }
 
 }  // namespace q4

@@ -74,16 +74,21 @@ struct GemmParams {
   void* C;              // [M][N] fp32 (c_dtype 0) or bf16 (1)
   int c_dtype;
   int M, N, K;
+  int nsplit;           // small-M form: K splits per tile (the cluster size)
+  int a_rows;           // rows of one A box (tile rows, or M rounded up to 16)
   unsigned* err;        // device status word
 };
 // Shapes the tensor-core GEMM accepts: nb = ceil(N/32) a multiple of 8 (whole
 // 256-column tiles of blocks, 16-byte row pitch) and K a multiple of 8
 // (16-byte row pitch of A).
 bool gemm_supported(int64_t M, int64_t N, int64_t K);
-// A: bf16, 16-byte aligned; B: blocks layout, 16-byte aligned.  `sms` bounds the
-// persistent grid.
+// A: bf16, 16-byte aligned; B: blocks layout, 16-byte aligned.  M > 128 runs
+// the persistent prefill form (`sms` bounds its grid), M <= 128 the split-K
+// small-M form.
 cudaError_t launch_gemm(void* C, int c_dtype, const void* A, const void* B, int64_t M, int64_t N,
                         int64_t K, unsigned* err, int sms, cudaStream_t st);
+// K splits the small-M form uses for this shape (0: the form cannot take it).
+int gemm_small_split(int64_t M, int64_t N, int64_t K, int sms);
 
 // q4_misc.cu
 cudaError_t launch_dequant(void* W, int w_dtype, const uint8_t* B, int64_t K, int64_t N,

@@ -1,4 +1,5 @@
-"""GPU prefill GEMM (M > 64, bf16 A: the tensor-core path) against the oracle.
+"""GPU tensor-core GEMM (bf16 A, M >= 8: the split-K small-M form up to 128
+rows, the persistent prefill form above) against the oracle.
 
 The path dequantises every weight to a bf16 tile element, bf16_rn((q-8)*d),
 and accumulates bf16 x bf16 products in fp32.  Its own oracle is therefore
@@ -66,7 +67,15 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("M,K,N", SHAPES)
+# The split-K small-M form (8 <= M <= 128): K split over a cluster, partial
+# sums combined on chip; K tails, N tails and single-step splits.
+SMALL_SHAPES = [
+    (8, 64, 256), (8, 5120, 1024), (16, 520, 1000), (33, 1000, 250), (64, 2048, 4096),
+    (100, 4096, 512), (128, 320, 2048), (9, 128, 256),
+]
+
+
+@pytest.mark.parametrize("M,K,N", SHAPES + SMALL_SHAPES)
 def test_gemm_parity(M, K, N):
     A = si.activations_bf16(M, K, seed=M + K)
     B = si.q4_weights(K, N, seed=N)
@@ -184,3 +193,28 @@ def test_fp32_activations_above_64_rows_use_gemv():
     C = to_host64(run(A, B, M, N, K))
     C64, S = oracle.matmul(A, B, M, N, K)
     assert_within_matmul_tol(C, C64, S, "fp32 A, M = 100")
+
+
+@pytest.mark.parametrize("M", [8, 16, 32, 64])
+def test_small_m_bf16_output_and_determinism(M):
+    K, N = 5120, 2048
+    A = si.activations_bf16(M, K, seed=40 + M)
+    B = si.q4_weights(K, N, seed=40)
+    c1 = run(A, B, M, N, K)
+    c2 = run(A, B, M, N, K)
+    c16 = run(A, B, M, N, K, c_dtype=torch.bfloat16)
+    assert torch.equal(c1, c2)
+    assert torch.equal(c1.to(torch.bfloat16).view(torch.int16), c16.view(torch.int16))
+
+
+def test_small_m_one_hot_rows_give_bf16_tiles():
+    """The split-K combine adds exact zeros from the other splits: one-hot
+    rows still reproduce the bf16 tile values bit for bit."""
+    M, K, N = 24, 3000, 1000
+    B = si.q4_weights(K, N, seed=41)
+    ks = si.rng(41, 2).choice(K, size=M, replace=False)
+    A = np.zeros((M, K), np.float32)
+    A[np.arange(M), ks] = 1.0
+    C = run(si.f32_to_bf16_bits(A), B, M, N, K).cpu().numpy()
+    Wb = oracle.dequant_bf16(B, K, N)
+    assert np.array_equal(C, (Wb[ks].astype(np.uint32) << 16).view(np.float32))
