@@ -55,12 +55,16 @@ struct Cfg {
   // and needs its A ring deep; the small-M form streams each weight once
   // from HBM and needs its raw ring deep
   static constexpr int kStagesA = (MT == 2) ? 3 : 4;   // 32 KB or 16 KB per stage
-  static constexpr int kStagesB = (MT == 2) ? 3 : 2;   // 32 KB per stage
-  static constexpr int kStagesRaw = (MT == 2) ? 3 : 8; // 9 KB per stage
+  static constexpr int kStagesB = 3;                   // 32 KB per stage
+  static constexpr int kStagesRaw = (MT == 2) ? 3 : 6; // 9 KB per stage
   static constexpr int kABytes = kBM * BK * 2;
   static constexpr uint32_t kTmemCols = MT * BN;
-  // dequant units (8 rows x 4 blocks) per warp and stage
-  static constexpr int kUnitsPerWarp = (BK / 4) / DW;
+  // with kGroups > 1 the dequant warps form groups that take alternate
+  // stages; both forms measured faster with one group (every warp on every
+  // stage).  Dequant units (8 rows x 4 blocks) per warp and stage follow.
+  static constexpr int kGroups = 1;
+  static constexpr int kGroupWarps = DW / kGroups;
+  static constexpr int kUnitsPerWarp = (BK / 4) / kGroupWarps;
   // epilogue: the DW/4 warps of one tensor-memory lane quarter split the
   // MT * BN accumulator columns
   static constexpr int kEpiCols = MT * BN / (DW / 4);
@@ -71,7 +75,9 @@ struct Cfg {
   static constexpr uint32_t kBarBytes = 256;
   static constexpr uint32_t kSmemBytes = kOffBars + kBarBytes + 1024;
   static_assert(MT == 1 || (MT == 2 && !SPLIT), "forms: prefill (MT 2) and split small M (MT 1)");
-  static_assert(kUnitsPerWarp >= 1 && (BK / 4) % DW == 0 && DW % 4 == 0, "dequant warps");
+  static_assert(kUnitsPerWarp >= 1 && (BK / 4) % kGroupWarps == 0 && DW % 4 == 0 &&
+                    DW % kGroups == 0,
+                "dequant warps");
   static_assert(kEpiCols % 32 == 0 && BN % kEpiCols == 0, "epilogue column split");
   static_assert(kABytes % 1024 == 0 && kOffRaw % 1024 == 0 && kRawBytes % 128 == 0,
                 "TMA destinations need alignment");
@@ -422,10 +428,10 @@ __global__ void __launch_bounds__(Cfg<MT, DW, SPLIT>::kThreads, 1)
     }
     for (int i = 0; i < kStagesRaw; ++i) {
       mbar_init(&full_raw[i], 1);
-      mbar_init(&empty_raw[i], DW);
+      mbar_init(&empty_raw[i], C::kGroupWarps);
     }
     for (int i = 0; i < kStagesB; ++i) {
-      mbar_init(&full_b[i], DW);
+      mbar_init(&full_b[i], C::kGroupWarps);
       mbar_init(&empty_b[i], 1);
     }
     mbar_init(tmem_full, 1);
@@ -520,11 +526,13 @@ __global__ void __launch_bounds__(Cfg<MT, DW, SPLIT>::kThreads, 1)
     // ================= dequant + epilogue =================
     const int wd = warp - 2;   // 0 .. DW-1
     const int q = warp & 3;    // the tensor-memory lane quarter this warp may access
+    const int grp = wd / C::kGroupWarps, wg = wd % C::kGroupWarps;
     int gr = 0, gb = 0;
     bool ok = true;
     Work w;
     for (int it = 0; ok && work_item<MT, SPLIT>(p, it, w) && !*s_fail; ++it) {
       for (int ks = w.kb; ks < w.ke; ++ks, ++gr, ++gb) {
+        if (gb % C::kGroups != grp) continue;   // the other group's stage
         const int sr = gr % kStagesRaw, sb = gb % kStagesB;
         int v = 1;
         if (lane == 0) {
@@ -534,7 +542,7 @@ __global__ void __launch_bounds__(Cfg<MT, DW, SPLIT>::kThreads, 1)
         }
         ok = __shfl_sync(0xffffffffu, v, 0) != 0;
         if (!ok) break;
-        dequant_stage<C::kUnitsPerWarp>(sRaw + sr * kRawBytes, sB + sb * kBBytes, wd, lane);
+        dequant_stage<C::kUnitsPerWarp>(sRaw + sr * kRawBytes, sB + sb * kBBytes, wg, lane);
         fence_async_smem();   // the tensor core reads B through the async proxy
         __syncwarp();
         if (lane == 0) {
@@ -667,7 +675,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 // Dequant warps of the small-M form.
-constexpr int kSmallDW = 16;
+constexpr int kSmallDW = 8;
 using PrefillCfg = gemm::Cfg<2, 8, false>;
 using SmallCfg = gemm::Cfg<1, kSmallDW, true>;
 
