@@ -283,20 +283,24 @@ __device__ __forceinline__ void produce_stage(const StreamDesc& sd, int s, uint8
   const int r0 = s * kRowsPerStage;
   if (sd.tmap) {
     // one box of 32 rows x 144*BPT bytes; rows past K and blocks past the row
-    // read as zero, rows past this slice are loaded but never used
+    // read as zero (a slice is a whole number of boxes, except the last one,
+    // which ends at K)
     if (lane == 0) {
       mbar_arrive_expect_tx(full, T::kStageBytes);
       tma_load_3d(stage, sd.tmap, sd.b0 * (kBlockBytes / 2), sd.k0 + r0, sd.expert, full);
     }
   } else {
-    // 2-byte aligned rows: copy with 16-bit loads (every block offset is even)
+    // 2-byte aligned rows: copy with 16-bit loads (every block offset is even);
+    // rows past the slice and blocks past the row are written as zeros, as
+    // the tensor copy does, so that the consumers need no bounds checks
     const int nr = min(kRowsPerStage, sd.rows - r0);
     const int halves = sd.tb * (kBlockBytes / 2);
-    for (int r = 0; r < nr; ++r) {
+    for (int r = 0; r < kRowsPerStage; ++r) {
       const uint16_t* src = reinterpret_cast<const uint16_t*>(
           sd.B + (static_cast<size_t>(sd.k0 + r0 + r) * sd.nb + sd.b0) * kBlockBytes);
       uint16_t* dst = reinterpret_cast<uint16_t*>(stage + r * T::kRowBytes);
-      for (int h = lane; h < halves; h += 32) dst[h] = __ldg(src + h);
+      for (int h = lane; h < T::kRowBytes / 2; h += 32)
+        dst[h] = (r < nr && h < halves) ? __ldg(src + h) : static_cast<uint16_t>(0);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(full);
@@ -591,14 +595,12 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
     for (int s = group; s < nstages; s += Crew<MR>::kGroups) {
       const int gs = pass * nstages + s;   // the producer's stage counter
       const int slot = gs % T::kStages;
-      // one lane per warp waits on the stage; the warp barrier then orders the
-      // other lanes' shared-memory reads after that wait
-      int ok = 1;
-      if (lane == 0) ok = wait_or_fail(&full[slot], (gs / T::kStages) & 1, s_fail, p.err) ? 1 : 0;
-      __syncwarp();   // orders the other lanes' reads after lane 0's wait
-      const bool ready = __shfl_sync(0xffffffffu, ok, 0) != 0;
+      // every lane waits on the stage itself (no divergence, no broadcast).
+      // Rows past the slice need no check: they exist only past K, where the
+      // stage holds zeros and the rows of A are zero too.
+      const bool ready = wait_or_fail(&full[slot], (gs / T::kStages) & 1, s_fail, p.err);
       const int r = s * kRowsPerStage + rp;   // row of the slice handled by this thread
-      if (ready && r < rows) {
+      if (ready) {
         const uint8_t* row = ring + slot * T::kStageBytes + rp * T::kRowBytes;
         uint32_t dbits[BPT], qs[BPT][4];
         load_blocks<BPT>(row, boff, odd, dbits, qs);
