@@ -68,7 +68,7 @@ struct TileCfg {
   static constexpr int kCols = kBlocks * kBlockCols;              // 256 * BPT
   static constexpr int kRowBytes = kBlocks * kBlockBytes;         // 144 * BPT
   static constexpr int kStageBytes = kRowsPerStage * kRowBytes;   // 4608 * BPT
-  static constexpr int kStages = (BPT == 1) ? 16 : 8;             // ~74 KB in flight
+  static constexpr int kStages = (BPT == 1) ? 32 : 16;            // ~147 KB in flight
   // TMA tensor copies need 128-byte-aligned shared destinations; a block's
   // word-aligned 20-byte read ends at most at the row's last byte, so rows
   // carry no padding.
