@@ -50,11 +50,12 @@ constexpr int kLanesPerRow = 8;     // consumer lanes sharing one row
 constexpr int kGroupWarps = 8;      // a warp group covers one stage: 8 warps x 4 rows
 
 // Consumer warps: one group of 8 per ring stage in flight for compute.  With
-// one row of A (the register-light case) two groups alternate stages, which
-// doubles the warps that hide latency; heavier configurations keep one group.
+// one or two rows of A two groups alternate stages, which doubles the warps
+// that hide latency; four rows keep one group (their accumulators need the
+// registers).
 template <int MR>
 struct Crew {
-  static constexpr int kGroups = (MR == 1) ? 2 : 1;
+  static constexpr int kGroups = (MR <= 2) ? 2 : 1;
   static constexpr int kWarps = kGroups * kGroupWarps;
   static constexpr int kConsumers = kWarps * 32;
   static constexpr int kThreads = kConsumers + 32;   // + producer warp
@@ -776,7 +777,7 @@ int max_active_clusters(int mode, int mr, int bpt, int rows_per_split, int list_
   cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster.x, cluster.y, cluster.z);
-  cfg.blockDim = dim3(mr == 1 ? Crew<1>::kThreads : Crew<2>::kThreads);
+  cfg.blockDim = dim3(mr == 1 ? Crew<1>::kThreads : mr == 2 ? Crew<2>::kThreads : Crew<4>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
