@@ -105,11 +105,13 @@ int64_t split_rows(int64_t K, int64_t nsplit) {
                                        q4::gemv_stage_rows()));
 }
 
+constexpr double kCtaFixedBytes = 48.0 * 1024;
+
 // Picks the blocks-per-thread and the split count (at most `max_split`; the
 // splits of a column tile form one cluster of `pair * nsplit` CTAs) that
 // minimise the bytes the busiest SM must stream: waves of resident clusters
 // (from the occupancy query) times the CTAs per SM within a wave times the
-// bytes per CTA.  Ties go to fewer CTAs.
+// bytes per CTA plus its fixed cost.  Ties go to fewer CTAs.
 void choose_split(int mode, int mr, int list_cap, int64_t K, int64_t nb, int64_t z_groups, int pair,
                   int sms, int max_split, bool allow_bpt2, int* bpt_out, int* nsplit_out,
                   int* rows_out, int* ntiles_out) {
@@ -135,7 +137,10 @@ void choose_split(int mode, int mr, int list_cap, int64_t K, int64_t nb, int64_t
       if (active <= 0) continue;
       const int64_t waves = ceil_div(clusters, active);
       const int64_t per_wave = (clusters < active ? clusters : active) * csize;
-      const double per_cta = static_cast<double>(rows) * q4::gemv_tile_blocks(bpt) * 18.0;
+      // a CTA's fixed cost (first loads, reduction, cluster combine: ~2.5 us)
+      // is worth about kCtaFixedBytes of streaming
+      const double per_cta = static_cast<double>(rows) * q4::gemv_tile_blocks(bpt) * 18.0 +
+                             kCtaFixedBytes;
       double cost = per_cta * static_cast<double>(waves * ceil_div(per_wave, sms));
       if (bpt == 1 && allow_bpt2) cost *= 1.03;   // more instructions per weight
       if (best < 0 || cost < best * 0.999 || (cost <= best * 1.001 && ctas < best_ctas)) {
