@@ -193,6 +193,19 @@ Q4_API int q4_dequant_bf16(uint16_t *W, const void *B, int64_t K, int64_t N, voi
 Q4_API int q4_get_device_status(void *stream);
 Q4_API unsigned int q4_last_device_flags(void);
 
+/*
+ * q4_selftest_wait -- failure-detection self-test; no counterpart on the
+ * pages.  Launches one CTA that waits on a pipeline barrier with the same
+ * bounded wait every kernel uses, but with a limit of `limit_ns`
+ * (1 .. 1e9 ns; the kernels use 1 s).  With arrive = 0 nothing completes
+ * the barrier: the wait runs out, records Q4_DEVERR_TIMEOUT in the device
+ * status word and the kernel returns (no trap, no hang; the context stays
+ * usable).  With arrive = 1 the CTA completes the barrier first and the wait
+ * succeeds.  Read the outcome with q4_get_device_status(stream).
+ * Returns Q4_OK, Q4_ERR_ARG (limit or arrive out of range) or Q4_ERR_CUDA.
+ */
+Q4_API int q4_selftest_wait(int64_t limit_ns, int arrive, void *stream);
+
 /* Human-readable text of a status code (static storage). */
 Q4_API const char *q4_status_str(int status);
 

@@ -58,6 +58,7 @@ SIGNATURES = {
     "q4_planar_bytes": (_sz, [_i64, _i64]),
     "q4_dequant": (_int, [_vp, _vp, _i64, _i64, _vp]),
     "q4_dequant_bf16": (_int, [_vp, _vp, _i64, _i64, _vp]),
+    "q4_selftest_wait": (_int, [_i64, _int, _vp]),
     "q4_get_device_status": (_int, [_vp]),
     "q4_last_device_flags": (ctypes.c_uint, []),
     "q4_status_str": (ctypes.c_char_p, [_int]),
@@ -217,6 +218,12 @@ def q4_dequant(W, B, K: int, N: int, stream=None) -> None:
 def q4_dequant_bf16(W, B, K: int, N: int, stream=None) -> None:
     _require_cuda(W, B)
     _check("q4_dequant_bf16", lib().q4_dequant_bf16(_ptr(W), _ptr(B), K, N, _stream(stream)))
+
+
+def q4_selftest_wait(limit_ns: int, arrive: bool, stream=None) -> None:
+    """One bounded pipeline wait run to its limit (arrive=False) or completed."""
+    _check("q4_selftest_wait", lib().q4_selftest_wait(int(limit_ns), 1 if arrive else 0,
+                                                      _stream(stream)))
 
 
 def q4_get_device_status(stream=None) -> int:

@@ -435,6 +435,17 @@ int q4_dequant_bf16(uint16_t* W, const void* B, int64_t K, int64_t N, void* stre
                                           static_cast<cudaStream_t>(stream)));
 }
 
+int q4_selftest_wait(int64_t limit_ns, int arrive, void* stream) {
+  if (limit_ns <= 0 || limit_ns > 1000000000LL || (arrive != 0 && arrive != 1)) return Q4_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  int rc = current_state(&s);
+  if (rc != Q4_OK) return rc;
+  return launch_status(q4::launch_wait_selftest(s->status,
+                                                static_cast<unsigned long long>(limit_ns),
+                                                arrive != 0, static_cast<cudaStream_t>(stream)));
+}
+
 int q4_get_device_status(void* stream) {
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* s = nullptr;

@@ -92,6 +92,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// The wait every kernel uses on its pipeline barriers: returns true once phase
+// `parity` of `bar` completes.  Gives up (returns false) if the CTA already
+// failed, or after `limit_ns`: then it marks the CTA failed (`*fail`) and
+// records Q4_DEVERR_TIMEOUT in the device status word, so that no thread of
+// the CTA waits again and the host learns of it.  Between tries the thread is
+// suspended in the barrier (hint 2 us) rather than spinning.
+__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, volatile int* fail,
+                                             unsigned* err,
+                                             unsigned long long limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  if (*fail) return false;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i)
+      if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
+    if (*fail) return false;
+    if (globaltimer() - t0 > limit_ns) {
+      *fail = 1;
+      atomicOr(err, kDevErrTimeout);
+      return false;
+    }
+  }
+}
+
 // ---- TMA bulk copy (non-tensor): global -> shared, completes on an mbarrier --
 // Requirements: dst and src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,

@@ -179,23 +179,10 @@ constexpr uint32_t kASbo = kARowBytes * 8;
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
                             (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
 
-// Bounded wait that leaves the failure visible to the whole CTA.
+// Bounded wait that leaves the failure visible to the whole CTA (bounded_wait).
 __device__ __forceinline__ bool gwait(uint64_t* bar, uint32_t parity, volatile int* fail,
                                       unsigned* err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  if (*fail) return false;
-  const unsigned long long t0 = globaltimer();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 8; ++i)
-      if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
-    if (*fail) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
-      *fail = 1;
-      atomicOr(err, kDevErrTimeout);
-      return false;
-    }
-  }
+  return bounded_wait(bar, parity, fail, err);
 }
 
 // ---- dequant of one raw stage into an MN-major swizzled bf16 B tile --------

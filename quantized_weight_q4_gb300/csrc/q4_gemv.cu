@@ -242,27 +242,12 @@ __device__ __forceinline__ void load_blocks(const uint8_t* row, uint32_t off, bo
   }
 }
 
-// Waits on `bar`, unless the CTA has already failed; on a timeout records the
-// error and marks the CTA failed so that no thread waits again.  Threads never
-// leave their loops early, so every named barrier is still reached.
+// Waits on `bar` (bounded_wait: gives up if the CTA failed or after the wait
+// limit, recording the timeout).  Threads never leave their loops early, so
+// every named barrier is still reached.
 __device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, volatile int* fail,
                                              unsigned* err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  if (*fail) return false;
-  const unsigned long long t0 = globaltimer();
-  while (true) {
-    // sleep in the barrier rather than spin: waiting warps leave the issue
-    // slots to warps that have data
-#pragma unroll 1
-    for (int i = 0; i < 8; ++i)
-      if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
-    if (*fail) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
-      *fail = 1;
-      atomicOr(err, kDevErrTimeout);
-      return false;
-    }
-  }
+  return bounded_wait(bar, parity, fail, err);
 }
 
 // ---------------------------------------------------------------------------

@@ -95,5 +95,8 @@ cudaError_t launch_dequant(void* W, int w_dtype, const uint8_t* B, int64_t K, in
                            cudaStream_t st);
 cudaError_t launch_repack(uint8_t* dst, const uint8_t* src, int64_t K, int64_t N, bool to_planar,
                           cudaStream_t st);
+// One bounded pipeline wait run to its limit (arrive = false) or completed.
+cudaError_t launch_wait_selftest(unsigned* err, unsigned long long limit_ns, bool arrive,
+                                 cudaStream_t st);
 
 }  // namespace q4

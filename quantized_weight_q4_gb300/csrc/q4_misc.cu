@@ -104,4 +104,31 @@ cudaError_t launch_repack(uint8_t* dst, const uint8_t* src, int64_t K, int64_t N
   return cudaGetLastError();
 }
 
+// One CTA waits, with bounded_wait and a limit of `limit_ns`, on an mbarrier
+// that only `arrive` ever completes: the path every pipeline wait takes, run
+// to its timeout on purpose (no fault, no hang: the wait gives up, records
+// Q4_DEVERR_TIMEOUT in the status word and the kernel returns).
+__global__ void __launch_bounds__(32) q4_wait_selftest_kernel(unsigned* err,
+                                                              unsigned long long limit_ns,
+                                                              int arrive) {
+  __shared__ uint64_t bar;
+  __shared__ int fail;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fail = 0;
+    fence_barrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) {
+    if (arrive) mbar_arrive(&bar);
+    (void)bounded_wait(&bar, 0, &fail, err, limit_ns);
+  }
+}
+
+cudaError_t launch_wait_selftest(unsigned* err, unsigned long long limit_ns, bool arrive,
+                                 cudaStream_t st) {
+  q4_wait_selftest_kernel<<<1, 32, 0, st>>>(err, limit_ns, arrive ? 1 : 0);
+  return cudaGetLastError();
+}
+
 }  // namespace q4

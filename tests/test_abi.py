@@ -82,3 +82,6 @@ def test_argument_errors_on_host(L):
                                None) == q4.Q4_ERR_DTYPE
     assert L.q4_repack(bad, good, 4, 64, None) == q4.Q4_ERR_ALIGN
     assert L.q4_dequant(good, good, 0, 64, None) == q4.Q4_ERR_ARG
+    # the failure-detection self-test checks its limit and mode before any CUDA call
+    for limit, arrive in [(0, 0), (-5, 0), (2_000_000_000, 0), (1000, 2)]:
+        assert L.q4_selftest_wait(limit, arrive, None) == q4.Q4_ERR_ARG
