@@ -252,7 +252,7 @@ int q4_matmul_ex(void* C, int c_dtype, const void* A, int a_dtype, const void* B
   int rc = current_state(&s);
   if (rc != Q4_OK) return rc;
   if (M >= kMinTensorRows && a_dtype == Q4_BF16 && q4::gemm_supported(M, N, K) &&
-      (M > 128 || q4::gemm_small_split(M, N, K, s->sms) > 0))
+      (M > 128 || q4::gemm_small_split(M, N, K) > 0))
     return launch_status(q4::launch_gemm(C, c_dtype, A, B, M, N, K, s->status, s->sms,
                                          static_cast<cudaStream_t>(stream)));
   const GemvShape& g = cached_gemv_shape(s, M, N, K);

@@ -757,8 +757,7 @@ bool gemm_supported(int64_t M, int64_t N, int64_t K) {
   return M >= 1 && nb % 8 == 0 && K % 8 == 0 && K >= 1 && M <= (1LL << 30) && N <= (1LL << 30);
 }
 
-int gemm_small_split(int64_t M, int64_t N, int64_t K, int sms) {
-  (void)sms;
+int gemm_small_split(int64_t M, int64_t N, int64_t K) {
   if (M > 128) return 0;
   const int64_t tiles = (N + gemm::BN - 1) / gemm::BN;
   const int64_t ksteps = (K + gemm::BK - 1) / gemm::BK;
@@ -805,7 +804,7 @@ cudaError_t launch_gemm(void* C, int c_dtype, const void* A, const void* B, int6
     return cudaLaunchKernelEx(&cfg, gemm::q4_gemm_tc_kernel<2, 8, false>, p);
   }
   // small-M form: one 128 x 256 tile per cluster of S CTAs splitting K
-  const int S = gemm_small_split(M, N, K, sms);
+  const int S = gemm_small_split(M, N, K);
   if (S <= 0) return cudaErrorInvalidConfiguration;
   const int a_rows = static_cast<int>(((M + 15) / 16) * 16);   // M <= 128
   if (!encode_maps(p, A, B, M, N, K, a_rows)) return cudaErrorInvalidValue;

@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
   uint64_t* empty = full + T::kStages;
   float* a_s = reinterpret_cast<float*>(smem + plan.a);
   int* list = reinterpret_cast<int*>(smem + plan.list);
-  int* s_misc = list + p.list_cap;   // [0] ticket flag, [1] expert, [2] list length, [3] failed
+  int* s_misc = list + p.list_cap;   // [0] unused, [1] expert, [2] list length, [3] failed
   volatile int* s_fail = s_misc + 3;
 
   const int tid = threadIdx.x;

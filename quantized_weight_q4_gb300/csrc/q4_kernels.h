@@ -88,7 +88,7 @@ bool gemm_supported(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm(void* C, int c_dtype, const void* A, const void* B, int64_t M, int64_t N,
                         int64_t K, unsigned* err, int sms, cudaStream_t st);
 // K splits the small-M form uses for this shape (0: the form cannot take it).
-int gemm_small_split(int64_t M, int64_t N, int64_t K, int sms);
+int gemm_small_split(int64_t M, int64_t N, int64_t K);
 
 // q4_misc.cu
 cudaError_t launch_dequant(void* W, int w_dtype, const uint8_t* B, int64_t K, int64_t N,
