@@ -56,6 +56,7 @@ def bind(path: str) -> ctypes.CDLL:
     L.q4o_dequant_bf16.argtypes = [vp, c_i64, c_i64, vp]
     L.q4o_matmul.argtypes = [vp, ctypes.c_int, vp, c_i64, c_i64, c_i64, vp, vp]
     L.q4o_matmul_naive.argtypes = [vp, ctypes.c_int, vp, c_i64, c_i64, c_i64, vp]
+    L.q4o_moe_gate.argtypes = [vp, c_i64, c_i64, c_i64, vp, vp]
     L.q4o_moe.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, vp,
                           c_i64, c_i64, c_i64, c_i64, c_i64,
                           vp, vp, vp, vp, vp]
@@ -162,6 +163,17 @@ def matmul_naive(A: np.ndarray, B: np.ndarray, M: int, N: int, K: int) -> np.nda
     C = np.empty((M, N), dtype=np.float64)
     lib().q4o_matmul_naive(_p(A), dt, _p(B), M, N, K, _p(C))
     return C
+
+
+def moe_gate(logits, T: int, E: int, topk: int):
+    """(topk_idx int32 [T, topk], topk_w fp64 [T, topk]): softmax of each
+    token's fp32 logits (max subtracted), the topk largest in descending order
+    (ties: lower index first), renormalised; fp64."""
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    idx = np.empty((T, topk), dtype=np.int32)
+    w = np.empty((T, topk), dtype=np.float64)
+    lib().q4o_moe_gate(_p(logits), T, E, topk, _p(idx), _p(w))
+    return idx, w
 
 
 def moe(x, Wg, Wu, Wd, idx, w, T, topk, E, H, I, stages: bool = False):

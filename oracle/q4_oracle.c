@@ -362,3 +362,51 @@ void q4o_moe(const void *x, int x_dtype,
 
 /* SiLU(g) = g * sigmoid(g) in fp64, exposed for its closed-form pins. */
 double q4o_silu(double g) { return g * sigmoid(g); }
+
+/* ------------------------------------------------------------------ */
+/* Router of the routed experts                                        */
+/* ------------------------------------------------------------------ */
+
+/* For each token t [KTransformers page, «规则二»: the gate gives the top-k
+ * indices and weights]: p = softmax(logits[t]) with the largest logit
+ * subtracted before exp [engine page §5.1], the k largest p in descending
+ * order (equal p: the lower expert index first), and their weights
+ * renormalised to sum to one, w_k = p_k / sum_j p_j over the k chosen.  All
+ * arithmetic in fp64. */
+void q4o_moe_gate(const float *logits, int64_t T, int64_t E, int64_t topk,
+                  int32_t *idx, double *w)
+{
+    double *p = (double *)malloc(sizeof(double) * (size_t)(E > 0 ? E : 1));
+    unsigned char *taken = (unsigned char *)malloc((size_t)(E > 0 ? E : 1));
+    for (int64_t t = 0; t < T; t++) {
+        const float *l = logits + t * E;
+        double mx = (double)l[0];
+        for (int64_t e = 1; e < E; e++)
+            if ((double)l[e] > mx)
+                mx = (double)l[e];
+        double sum = 0.0;
+        for (int64_t e = 0; e < E; e++) {
+            p[e] = exp((double)l[e] - mx);
+            sum += p[e];
+        }
+        for (int64_t e = 0; e < E; e++) {
+            p[e] /= sum;
+            taken[e] = 0;
+        }
+        double wsum = 0.0;
+        for (int64_t k = 0; k < topk; k++) {
+            int64_t best = -1;
+            for (int64_t e = 0; e < E; e++)      /* ascending: ties keep the lower index */
+                if (!taken[e] && (best < 0 || p[e] > p[best]))
+                    best = e;
+            taken[best] = 1;
+            idx[t * topk + k] = (int32_t)best;
+            w[t * topk + k] = p[best];
+            wsum += p[best];
+        }
+        for (int64_t k = 0; k < topk; k++)
+            w[t * topk + k] /= wsum;
+    }
+    free(p);
+    free(taken);
+}

@@ -103,9 +103,16 @@ def activations_bf16(M: int, K: int, seed: int = 0, stream: int = 1) -> np.ndarr
     return f32_to_bf16_bits(activations_f32(M, K, seed, stream))
 
 
+def router_logits(T: int, E: int, seed: int = 0, stream: int = 2) -> np.ndarray:
+    """Seeded N(0,1) router logits, fp32 [T, E]."""
+    return rng(seed, stream).standard_normal(size=(T, E), dtype=np.float32)
+
+
 def routing(T: int, E: int, topk: int, seed: int = 0, stream: int = 2):
-    """(topk_idx int32 [T, topk], topk_w fp32 [T, topk]) from seeded N(0,1) logits."""
-    logits = rng(seed, stream).standard_normal(size=(T, E), dtype=np.float32)
+    """(topk_idx int32 [T, topk], topk_w fp32 [T, topk]) from seeded N(0,1) logits:
+    input data for the expert path (the gate itself is checked against the
+    oracle's router)."""
+    logits = router_logits(T, E, seed, stream)
     m = logits.max(axis=1, keepdims=True)
     e = np.exp(logits - m, dtype=np.float32)
     p = (e / e.sum(axis=1, keepdims=True, dtype=np.float32)).astype(np.float32)

@@ -29,6 +29,10 @@ MUTANTS = {
     "routing weight dropped": ("out[t * H + j] += wk * y[j];", "out[t * H + j] += y[j];"),
     "up projection dropped": ("h[i] = silu * u[i];", "h[i] = silu;"),
     "bf16 ties away from zero": ("(diff == 0.5 && fmod(fl, 2.0) != 0.0)", "(diff == 0.5)"),
+    "router ties to the higher index": ("if (!taken[e] && (best < 0 || p[e] > p[best]))", "if (!taken[e] && (best < 0 || p[e] >= p[best]))"),
+    "router weights not renormalised": ("            w[t * topk + k] /= wsum;", "            w[t * topk + k] /= 1.0;"),
+    "router max not subtracted": ("            p[e] = exp((double)l[e] - mx);", "            p[e] = exp((double)l[e]);"),
+    "router picks the smallest": ("if (!taken[e] && (best < 0 || p[e] > p[best]))", "if (!taken[e] && (best < 0 || p[e] < p[best]))"),
 }
 
 BATTERY = [
@@ -46,6 +50,10 @@ BATTERY = [
     pins.test_bf16_tiles_hand_rounded,
     pins.test_bf16_tiles_equal_exact_product_when_representable,
     pins.test_bf16_tiles_within_rounding_bound,
+    pins.test_gate_closed_forms,
+    pins.test_gate_ties_go_to_the_lower_index,
+    pins.test_gate_matches_stable_sort,
+    pins.test_gate_large_logits_stay_finite,
 ]
 
 

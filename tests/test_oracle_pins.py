@@ -471,3 +471,60 @@ def test_bf16_tiles_within_rounding_bound():
     err = np.abs(Cb - C)
     assert np.all(err <= 2.0 ** -9 * S + 1e-300)
     assert err.max() > 0
+
+
+# ---------------------------------------------------------------- router
+
+def _softmax_selected(row, sel):
+    """exp(l - max) / sum over the selected logits, in Python floats."""
+    m = max(float(row[e]) for e in sel)
+    ex = [math.exp(float(row[e]) - m) for e in sel]
+    s = sum(ex)
+    return [v / s for v in ex]
+
+
+def test_gate_closed_forms():
+    """All-equal logits: the first k experts, each weight 1/k.  Logits
+    log(1..8): descending order 7..2 and the renormalised softmax of the
+    chosen six."""
+    import oracle
+    idx, w = oracle.moe_gate(np.zeros((3, 160), np.float32), 3, 160, 6)
+    assert (idx == np.arange(6)).all()
+    assert np.allclose(w, 1.0 / 6.0, rtol=1e-15, atol=0)
+    row = np.log(np.arange(1, 9, dtype=np.float64)).astype(np.float32)
+    idx, w = oracle.moe_gate(row[None], 1, 8, 6)
+    assert idx[0].tolist() == [7, 6, 5, 4, 3, 2]
+    assert np.allclose(w[0], _softmax_selected(row, idx[0]), rtol=1e-14, atol=0)
+
+
+def test_gate_ties_go_to_the_lower_index():
+    import oracle
+    row = np.array([[5, 3, 3, 3, 1, 1]], np.float32)
+    assert oracle.moe_gate(row, 1, 6, 3)[0][0].tolist() == [0, 1, 2]
+    assert oracle.moe_gate(row, 1, 6, 5)[0][0].tolist() == [0, 1, 2, 3, 4]
+    assert oracle.moe_gate(np.array([[1, 2, 2]], np.float32), 1, 3, 1)[0][0].tolist() == [1]
+
+
+def test_gate_matches_stable_sort():
+    """Brute force: the chosen experts are a stable descending sort of the
+    logits (duplicates included), and the weights the softmax over them."""
+    import oracle
+    T, E, k = 64, 160, 6
+    logits = si.router_logits(T, E, seed=5)
+    logits[::3, 10] = logits[::3, 20]          # exact duplicates
+    logits[1::4, :8] = logits[1::4, 8:16]
+    idx, w = oracle.moe_gate(logits, T, E, k)
+    ref = np.argsort(-logits, axis=1, kind="stable")[:, :k]
+    assert np.array_equal(idx, ref)
+    for t in range(T):
+        assert np.allclose(w[t], _softmax_selected(logits[t], idx[t]), rtol=1e-14, atol=0)
+
+
+def test_gate_large_logits_stay_finite():
+    """The max subtraction keeps exp finite for logits near 1000."""
+    import oracle
+    row = np.array([[1000, 1001, 1002, 990, 1003, 998, 1001, 997]], np.float32)
+    idx, w = oracle.moe_gate(row, 1, 8, 4)
+    assert idx[0].tolist() == [4, 2, 1, 6]
+    assert np.isfinite(w).all()
+    assert np.allclose(w[0], _softmax_selected(row[0], idx[0]), rtol=1e-14, atol=0)
