@@ -57,6 +57,8 @@ def bind(path: str) -> ctypes.CDLL:
     L.q4o_matmul.argtypes = [vp, ctypes.c_int, vp, c_i64, c_i64, c_i64, vp, vp]
     L.q4o_matmul_naive.argtypes = [vp, ctypes.c_int, vp, c_i64, c_i64, c_i64, vp]
     L.q4o_moe_gate.argtypes = [vp, c_i64, c_i64, c_i64, vp, vp]
+    L.q4o_moe_block.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, c_i64, c_i64, c_i64, c_i64, c_i64,
+                                vp, vp, vp, c_i64, vp, vp, vp, vp]
     L.q4o_moe.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, vp,
                           c_i64, c_i64, c_i64, c_i64, c_i64,
                           vp, vp, vp, vp, vp]
@@ -174,6 +176,22 @@ def moe_gate(logits, T: int, E: int, topk: int):
     w = np.empty((T, topk), dtype=np.float64)
     lib().q4o_moe_gate(_p(logits), T, E, topk, _p(idx), _p(w))
     return idx, w
+
+
+def moe_block(x, logits, Wg, Wu, Wd, T, topk, E, H, I, Sg=None, Su=None, Sd=None, Is=0):
+    """(out [T,H], tol [T,H], idx [T,topk], w [T,topk]) of one MoE block:
+    router, routed experts, shared expert (Is > 0); fp64."""
+    x, dt = _act(x)
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    Wg, Wu, Wd = (np.ascontiguousarray(a, dtype=np.uint8) for a in (Wg, Wu, Wd))
+    sh = [np.ascontiguousarray(a, dtype=np.uint8) if a is not None else None for a in (Sg, Su, Sd)]
+    out = np.empty((T, H), np.float64)
+    tol = np.empty((T, H), np.float64)
+    idx = np.empty((T, topk), np.int32)
+    w = np.empty((T, topk), np.float64)
+    lib().q4o_moe_block(_p(x), dt, _p(logits), _p(Wg), _p(Wu), _p(Wd), T, topk, E, H, I,
+                        _p(sh[0]), _p(sh[1]), _p(sh[2]), Is, _p(out), _p(tol), _p(idx), _p(w))
+    return out, tol, idx, w
 
 
 def moe(x, Wg, Wu, Wd, idx, w, T, topk, E, H, I, stages: bool = False):

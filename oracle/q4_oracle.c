@@ -289,11 +289,14 @@ static double sigmoid(double g) { return 1.0 / (1.0 + exp(-g)); }
  * order: the gate and up errors through SiLU(g)*u, then through down, then
  * through the weighted sum.
  * g, u, h (may be NULL) receive the per-slot stage values [T*topk, I]. */
-void q4o_moe(const void *x, int x_dtype,
-             const uint8_t *Wg, const uint8_t *Wu, const uint8_t *Wd,
-             const int32_t *idx, const float *w,
-             int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I,
-             double *out, double *tol, double *g_out, double *u_out, double *h_out)
+/* The chain above with the slot weights in fp64 (w64) or fp32 (w32), and an
+ * extra tolerance term wrel * |w_k| * |y_k[j]| for weights known only to a
+ * relative error wrel (0 for exact weights). */
+static void moe_core(const void *x, int x_dtype,
+                     const uint8_t *Wg, const uint8_t *Wu, const uint8_t *Wd,
+                     const int32_t *idx, const float *w32, const double *w64, double wrel,
+                     int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I,
+                     double *out, double *tol, double *g_out, double *u_out, double *h_out)
 {
     int64_t nbI = (I + QO_BLOCK - 1) / QO_BLOCK;
     int64_t nbH = (H + QO_BLOCK - 1) / QO_BLOCK;
@@ -321,7 +324,7 @@ void q4o_moe(const void *x, int x_dtype,
         for (int64_t k = 0; k < topk; k++) {
             int64_t slot = t * topk + k;
             int32_t e = idx[slot];
-            double wk = (double)w[slot];
+            double wk = w64 ? w64[slot] : (double)w32[slot];
             if (e < 0 || e >= E) {
                 if (g_out) for (int64_t i = 0; i < I; i++) g_out[slot * I + i] = 0.0;
                 if (u_out) for (int64_t i = 0; i < I; i++) u_out[slot * I + i] = 0.0;
@@ -352,12 +355,23 @@ void q4o_moe(const void *x, int x_dtype,
                 double *prop = (double *)malloc(sizeof(double) * (size_t)H);
                 row_matmul_abs(dh, wd, H, I, prop);
                 for (int64_t j = 0; j < H; j++)
-                    tol[t * H + j] += fabs(wk) * (1e-3 * sy[j] + 1e-6 + prop[j]);
+                    tol[t * H + j] += fabs(wk) * (1e-3 * sy[j] + 1e-6 + prop[j]
+                                                  + wrel * fabs(y[j]));
                 free(prop);
             }
         }
     }
     free(xt); free(g); free(sg); free(u); free(su); free(h); free(dh); free(y); free(sy);
+}
+
+void q4o_moe(const void *x, int x_dtype,
+             const uint8_t *Wg, const uint8_t *Wu, const uint8_t *Wd,
+             const int32_t *idx, const float *w,
+             int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I,
+             double *out, double *tol, double *g_out, double *u_out, double *h_out)
+{
+    moe_core(x, x_dtype, Wg, Wu, Wd, idx, w, NULL, 0.0, T, topk, E, H, I,
+             out, tol, g_out, u_out, h_out);
 }
 
 /* SiLU(g) = g * sigmoid(g) in fp64, exposed for its closed-form pins. */
@@ -409,4 +423,38 @@ void q4o_moe_gate(const float *logits, int64_t T, int64_t E, int64_t topk,
     }
     free(p);
     free(taken);
+}
+
+/* One MoE block: the router above on the logits, the routed experts with its
+ * fp64 weights, and, when Is > 0, a shared expert (S_gate, S_up: H x Is;
+ * S_down: Is x H) that every token takes with weight 1, added after the
+ * routed sum [KTransformers page, «规则二»: gate then experts; «优化三»: the
+ * shared expert].  out and tol [T, H]; idx, w [T, topk] receive the routing.
+ * tol carries the chain tolerance of both parts plus wrel * |w_k| * |y_k|
+ * for router weights computed in fp32 (wrel = 2e-6). */
+void q4o_moe_block(const void *x, int x_dtype, const float *logits,
+                   const uint8_t *Wg, const uint8_t *Wu, const uint8_t *Wd,
+                   int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I,
+                   const uint8_t *Sg, const uint8_t *Su, const uint8_t *Sd, int64_t Is,
+                   double *out, double *tol, int32_t *idx, double *w)
+{
+    q4o_moe_gate(logits, T, E, topk, idx, w);
+    moe_core(x, x_dtype, Wg, Wu, Wd, idx, NULL, w, 2e-6, T, topk, E, H, I,
+             out, tol, NULL, NULL, NULL);
+    if (Is <= 0)
+        return;
+    int32_t *sidx = (int32_t *)calloc((size_t)T, sizeof(int32_t));
+    double *sw = (double *)malloc(sizeof(double) * (size_t)T);
+    double *so = (double *)malloc(sizeof(double) * (size_t)(T * H));
+    double *st = (double *)malloc(sizeof(double) * (size_t)(T * H));
+    for (int64_t t = 0; t < T; t++)
+        sw[t] = 1.0;
+    moe_core(x, x_dtype, Sg, Su, Sd, sidx, NULL, sw, 0.0, T, 1, 1, H, Is,
+             so, st, NULL, NULL, NULL);
+    for (int64_t i = 0; i < T * H; i++) {
+        out[i] += so[i];
+        if (tol)
+            tol[i] += st[i];
+    }
+    free(sidx); free(sw); free(so); free(st);
 }

@@ -32,6 +32,8 @@ MUTANTS = {
     "router ties to the higher index": ("if (!taken[e] && (best < 0 || p[e] > p[best]))", "if (!taken[e] && (best < 0 || p[e] >= p[best]))"),
     "router weights not renormalised": ("            w[t * topk + k] /= wsum;", "            w[t * topk + k] /= 1.0;"),
     "router max not subtracted": ("            p[e] = exp((double)l[e] - mx);", "            p[e] = exp((double)l[e]);"),
+    "block shared term dropped": ("        out[i] += so[i];", "        out[i] += 0.0 * so[i];"),
+    "block shared weight doubled": ("        sw[t] = 1.0;", "        sw[t] = 2.0;"),
     "router picks the smallest": ("if (!taken[e] && (best < 0 || p[e] > p[best]))", "if (!taken[e] && (best < 0 || p[e] < p[best]))"),
 }
 
@@ -54,6 +56,9 @@ BATTERY = [
     pins.test_gate_ties_go_to_the_lower_index,
     pins.test_gate_matches_stable_sort,
     pins.test_gate_large_logits_stay_finite,
+    pins.test_block_shared_term_is_the_shared_expert,
+    pins.test_block_identical_experts_collapse,
+    pins.test_block_expert_relabelling,
 ]
 
 

@@ -528,3 +528,53 @@ def test_gate_large_logits_stay_finite():
     assert idx[0].tolist() == [4, 2, 1, 6]
     assert np.isfinite(w).all()
     assert np.allclose(w[0], _softmax_selected(row[0], idx[0]), rtol=1e-14, atol=0)
+
+
+# ---------------------------------------------------------------- MoE block
+
+def _block_case(T=3, E=8, H=64, I=32, Is=48, seed=9):
+    x = si.activations_bf16(T, H, seed=seed)
+    logits = si.router_logits(T, E, seed=seed)
+    Wg, Wu, Wd = si.moe_weights(E, H, I, seed=seed)
+    Sg, Su, Sd = (a[0] for a in si.moe_weights(1, H, Is, seed=seed + 100))
+    return x, logits, Wg, Wu, Wd, Sg, Su, Sd
+
+
+def test_block_shared_term_is_the_shared_expert():
+    """block(with shared) - block(without) = the shared expert alone, run as
+    one expert taken by every token with weight 1."""
+    import oracle
+    T, topk, E, H, I, Is = 3, 6, 8, 64, 32, 48
+    x, logits, Wg, Wu, Wd, Sg, Su, Sd = _block_case(T, E, H, I, Is)
+    with_s, _, idx, w = oracle.moe_block(x, logits, Wg, Wu, Wd, T, topk, E, H, I, Sg, Su, Sd, Is)
+    without, _, idx2, w2 = oracle.moe_block(x, logits, Wg, Wu, Wd, T, topk, E, H, I)
+    assert np.array_equal(idx, idx2) and np.array_equal(w, w2)
+    shared, _, _ = oracle.moe(x, Sg[None], Su[None], Sd[None], np.zeros((T, 1), np.int32),
+                              np.ones((T, 1), np.float32), T, 1, 1, H, Is)
+    assert np.allclose(with_s - without, shared, rtol=1e-12, atol=1e-12)
+
+
+def test_block_identical_experts_collapse():
+    """With every routed expert the same matrices, the renormalised weights
+    sum to one and the routed sum is that one expert's output."""
+    import oracle
+    T, topk, E, H, I = 4, 6, 8, 64, 32
+    x, logits, Wg, Wu, Wd, *_ = _block_case(T, E, H, I)
+    Wg1, Wu1, Wd1 = (np.repeat(a[:1], E, axis=0) for a in (Wg, Wu, Wd))
+    out, _, _, w = oracle.moe_block(x, logits, Wg1, Wu1, Wd1, T, topk, E, H, I)
+    assert np.allclose(w.sum(axis=1), 1.0, rtol=1e-15, atol=0)
+    one, _, _ = oracle.moe(x, Wg[:1], Wu[:1], Wd[:1], np.zeros((T, 1), np.int32),
+                           np.ones((T, 1), np.float32), T, 1, 1, H, I)
+    assert np.allclose(out, one, rtol=1e-12, atol=1e-12)
+
+
+def test_block_expert_relabelling():
+    """Permuting the experts together with their logit columns changes nothing."""
+    import oracle
+    T, topk, E, H, I, Is = 3, 6, 8, 64, 32, 48
+    x, logits, Wg, Wu, Wd, Sg, Su, Sd = _block_case(T, E, H, I, Is)
+    perm = si.rng(9, 77).permutation(E)
+    a, _, _, _ = oracle.moe_block(x, logits, Wg, Wu, Wd, T, topk, E, H, I, Sg, Su, Sd, Is)
+    b, _, _, _ = oracle.moe_block(x, logits[:, perm], Wg[perm], Wu[perm], Wd[perm], T, topk, E,
+                                  H, I, Sg, Su, Sd, Is)
+    assert np.allclose(a, b, rtol=1e-12, atol=1e-12)
