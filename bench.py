@@ -10,7 +10,8 @@ step = one pass of the 224 GEMVs.  Metric: weight bytes streamed per second.
 Other workloads (``--workload``), each printing its own line: ``gemv`` (one
 GEMV, fp32 A, default K = N = 4096, --m/--k/--n), ``batched`` (K = 5120,
 N = 12288, bf16 A with --m rows), ``moe`` (top-6 of 160 experts, H = 5120,
-I = 1536, --tokens), ``prefill`` (M = 2048, K = 5120, N = 12288, bf16 A and
+I = 1536, --tokens), ``moe_block`` (router + shared expert + routed experts
+of the same block, --tokens), ``prefill`` (M = 2048, K = 5120, N = 12288, bf16 A and
 C on the tensor cores; metric TFLOP/s).  Weight copies or routings rotate so
 that each pass reads at least four times the L2 capacity.
 
@@ -451,6 +452,46 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
                "routings_rotated": R, "unique_expert_bytes_per_call": round(wbytes),
                "l2": f"{R} seeded routings rotate over 160 experts (2.12 GB of weights)",
                "parallelism": f"replicas x{ws}"}
+        units = R
+    elif args.workload == "moe_block":
+        # router + shared expert + routed experts of one DeepSeek-V2-sized block
+        T, E, H, I, topk, Is = args.tokens, 160, 5120, 1536, 6, 3072
+        Wg, Wu, Wd = si.moe_weights(E, H, I, seed=0)
+        dWg, dWu, dWd = to_dev(Wg), to_dev(Wu), to_dev(Wd)
+        del Wg, Wu, Wd
+        Sg, Su, Sd = (to_dev(a[0]) for a in si.moe_weights(1, H, Is, seed=100))
+        R = args.routings
+        fns, keep, uniq = [], [], 0
+        per_expert = (2 * H * si.nblocks(I) + I * si.nblocks(H)) * 18
+        shared_bytes = (2 * H * si.nblocks(Is) + Is * si.nblocks(H)) * 18
+        wsz = q4.q4_moe_block_workspace_size(T, topk, E, H, I, Is)
+        wspace = torch.empty(wsz, dtype=torch.uint8, device=dev)
+        for r in range(R):
+            logits = si.router_logits(T, E, seed=r)
+            order = np.argsort(-logits, axis=1, kind="stable")[:, :topk]
+            uniq += len(set(order.reshape(-1).tolist())) * per_expert + shared_bytes
+            dx = to_dev(si.activations_bf16(T, H, seed=r).view(np.int16)).view(torch.bfloat16)
+            dl = to_dev(logits)
+            out = torch.empty((T, H), dtype=torch.float32, device=dev)
+            keep += [dx, dl, out]
+            fns.append(lambda out=out, dx=dx, dl=dl: q4.q4_moe_block(
+                out, dx, dl, dWg, dWu, dWd, T, topk, E, H, I, Sg, Su, Sd, Is, workspace=wspace))
+        g = GraphOf(torch, fns)
+        barrier(ws)
+        with ClockSampler(local) as clk:
+            t = g.time(args.steps, args.warmup)
+        barrier(ws)
+        t = max_over_ranks(ws, t)
+        per_call = t / (args.steps * R)
+        wbytes = uniq / R
+        value = ws * wbytes / per_call / 1e9
+        cfg = {"workload": "moe_block", "T": T, "E": E, "H": H, "I": I, "topk": topk,
+               "shared_I": Is, "routings_rotated": R,
+               "weight_bytes_per_call": round(wbytes),
+               "note": "router on the GPU, shared expert (two of I=1536 run as one of 3072), "
+                       "routed experts; the chosen experts' bytes plus the shared expert's",
+               "l2": f"{R} seeded router-logit sets rotate over 160 experts",
+               "parallelism": f"replicas x{ws}", "us_per_call": round(per_call * 1e6, 2)}
         units = R
     elif args.workload == "prefill":
         M = args.m if args.m > 64 else 2048

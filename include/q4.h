@@ -194,6 +194,48 @@ Q4_API int q4_get_device_status(void *stream);
 Q4_API unsigned int q4_last_device_flags(void);
 
 /*
+ * q4_moe_gate -- the router in front of the routed experts
+ * [KTransformers page, «规则二»: the gate gives the top-k indices and weights].
+ *   topk_idx  int32 [T, topk] (out): for each token the topk largest of its
+ *             E logits, in descending order; equal logits: lower index first
+ *   topk_w    fp32 [T, topk] (out): softmax over the E logits with the maximum
+ *             subtracted (engine page §5.1), restricted to the chosen experts
+ *             and renormalised: w_i = exp(l_i - l_max) / sum_j exp(l_j - l_max)
+ *   logits    fp32 [T, E], finite values
+ * The choice compares the fp32 logits exactly.  E <= 1024, topk <= 16 and
+ * topk <= E (else Q4_ERR_SHAPE); pointers 16-byte aligned.  The outputs are
+ * the inputs q4_moe_experts_ex takes.
+ */
+Q4_API int q4_moe_gate(int32_t *topk_idx, float *topk_w, const float *logits,
+                int64_t T, int64_t E, int64_t topk, void *stream);
+
+/*
+ * q4_moe_block -- one DeepSeek-V2-style MoE block on the GPU: router, shared
+ * expert and routed experts, in one call that can be captured into a CUDA
+ * graph [KTransformers page, «规则二» (gate, then the experts) and «优化三»
+ * (the shared expert stays on the GPU with the rest of the block)].
+ *   out[t] = sum_k topk_w[t,k] * expert_{topk_idx[t,k]}(x_t) + shared(x_t)
+ * with (topk_idx, topk_w) = q4_moe_gate(logits), expert_e as in
+ * q4_moe_experts_ex (W_gate, W_up, W_down: E experts, intermediate size I)
+ * and shared(x) = (SiLU(x.S_gate) * (x.S_up)) . S_down with intermediate size
+ * Is (S_gate, S_up: H rows x ceil(Is/32) blocks; S_down: Is rows x
+ * ceil(H/32) blocks).  Is = 0 means no shared expert (S_* may be NULL).  The
+ * routed sum is taken in slot order and the shared term added last.
+ *   out  fp32 [T, H]; x  [T, H] fp32 or bf16 (x_dtype); logits fp32 [T, E]
+ * Workspace: q4_moe_block_workspace_size bytes (no initialisation needed),
+ * or NULL for the library-owned workspace shared with q4_moe_experts_ex.
+ * Limits as for q4_moe_gate and q4_moe_experts_ex.
+ */
+Q4_API int q4_moe_block(float *out, const void *x, int x_dtype, const float *logits,
+                 const void *W_gate, const void *W_up, const void *W_down,
+                 int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I,
+                 const void *S_gate, const void *S_up, const void *S_down, int64_t Is,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
+Q4_API size_t q4_moe_block_workspace_size(int64_t T, int64_t topk, int64_t E, int64_t H,
+                                   int64_t I, int64_t Is);
+
+/*
  * q4_selftest_wait -- failure-detection self-test; no counterpart on the
  * pages.  Launches one CTA that waits on a pipeline barrier with the same
  * bounded wait every kernel uses, but with a limit of `limit_ns`

@@ -58,6 +58,10 @@ SIGNATURES = {
     "q4_planar_bytes": (_sz, [_i64, _i64]),
     "q4_dequant": (_int, [_vp, _vp, _i64, _i64, _vp]),
     "q4_dequant_bf16": (_int, [_vp, _vp, _i64, _i64, _vp]),
+    "q4_moe_gate": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "q4_moe_block": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                            _vp, _vp, _vp, _i64, _vp, _sz, _vp]),
+    "q4_moe_block_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _i64, _i64]),
     "q4_selftest_wait": (_int, [_i64, _int, _vp]),
     "q4_get_device_status": (_int, [_vp]),
     "q4_last_device_flags": (ctypes.c_uint, []),
@@ -186,6 +190,28 @@ def q4_moe_experts_noalloc(out, x, W_gate, W_up, W_down, topk_idx, topk_w, T: in
     _check("q4_moe_experts_noalloc", lib().q4_moe_experts_noalloc(
         _ptr(out), _ptr(x), _dtype_code(x), _ptr(W_gate), _ptr(W_up), _ptr(W_down),
         _ptr(topk_idx), _ptr(topk_w), T, topk, E, H, I, _stream(stream)))
+
+
+def q4_moe_gate(topk_idx, topk_w, logits, T: int, E: int, topk: int, stream=None) -> None:
+    _require_cuda(topk_idx, topk_w, logits)
+    _check("q4_moe_gate", lib().q4_moe_gate(_ptr(topk_idx), _ptr(topk_w), _ptr(logits), T, E,
+                                            topk, _stream(stream)))
+
+
+def q4_moe_block(out, x, logits, W_gate, W_up, W_down, T: int, topk: int, E: int, H: int, I: int,
+                 S_gate=None, S_up=None, S_down=None, Is: int = 0, workspace=None,
+                 stream=None) -> None:
+    """Router + shared expert + routed experts of one MoE block (include/q4.h)."""
+    _require_cuda(out, x, logits, W_gate, W_up, W_down, S_gate, S_up, S_down, workspace)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("q4_moe_block", lib().q4_moe_block(
+        _ptr(out), _ptr(x), _dtype_code(x), _ptr(logits), _ptr(W_gate), _ptr(W_up),
+        _ptr(W_down), T, topk, E, H, I, _ptr(S_gate), _ptr(S_up), _ptr(S_down), Is,
+        _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def q4_moe_block_workspace_size(T: int, topk: int, E: int, H: int, I: int, Is: int = 0) -> int:
+    return lib().q4_moe_block_workspace_size(T, topk, E, H, I, Is)
 
 
 def q4_moe_static_scratch_bytes() -> int:

@@ -209,6 +209,83 @@ int launch_status(cudaError_t e) { return e == cudaSuccess ? Q4_OK : Q4_ERR_CUDA
 
 }  // namespace
 
+namespace {
+
+// The routed-expert kernels (gate/up, down, slot combine) for a validated
+// problem, on a workspace of at least m.total bytes; the combine adds
+// `addend` (fp32 [T, H], or null) after the weighted sum.
+int moe_run(DeviceState* s, const MoeShape& m, float* out, const void* x, int x_dtype,
+            const void* W_gate, const void* W_up, const void* W_down, const int32_t* topk_idx,
+            const float* topk_w, int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I,
+            void* ws, const float* addend, cudaStream_t st) {
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  const int64_t nbI = ceil_div(I, 32), nbH = ceil_div(H, 32);
+  float* h = reinterpret_cast<float*>(w8 + m.off_h);
+  float* y = reinterpret_cast<float*>(w8 + m.off_y);
+
+  q4::GemvParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.topk_idx = topk_idx;
+  p.nslots = m.nslots;
+  p.topk = static_cast<int>(topk);
+  p.E = static_cast<int>(E);
+  p.list_cap = m.list_cap;
+  p.h = h;
+  p.y = y;
+  p.err = s->status;
+  p.c_dtype = 0;
+  q4::fill_decode_consts(p);
+
+  // gate and up: K = H, N = I; A rows are tokens
+  p.mode = q4::kModeGateUp;
+  p.B = static_cast<const uint8_t*>(W_gate);
+  p.B2 = static_cast<const uint8_t*>(W_up);
+  p.b_stride = static_cast<long long>(H) * nbI * 18;
+  p.K = static_cast<int>(H);
+  p.N = static_cast<int>(I);
+  p.nb = static_cast<int>(nbI);
+  p.nsplit = m.nsplit_gu;
+  p.rows_per_split = m.rows_gu;
+  p.use_tma = (p.nb % 8 == 0 && p.b_stride % 16 == 0 &&
+               q4::encode_weight_tmap(&p.tmap[0], W_gate, H, p.nb, E, p.b_stride, m.bpt_gu) &&
+               q4::encode_weight_tmap(&p.tmap[1], W_up, H, p.nb, E, p.b_stride, m.bpt_gu))
+                  ? 1 : 0;
+  p.A = x;
+  p.a_dtype = x_dtype;
+  p.a_ld = H;
+  cudaError_t e = q4::launch_gemv(p, m.mr, m.bpt_gu, dim3(m.ntiles_gu, m.nsplit_gu, 2 * m.nexp),
+                                  dim3(1, m.nsplit_gu, 2), st, true);
+  if (e != cudaSuccess) return Q4_ERR_CUDA;
+
+  // down: K = I, N = H; A rows are slots of h
+  p.mode = q4::kModeDown;
+  p.B = static_cast<const uint8_t*>(W_down);
+  p.B2 = nullptr;
+  p.b_stride = static_cast<long long>(I) * nbH * 18;
+  p.K = static_cast<int>(I);
+  p.N = static_cast<int>(H);
+  p.nb = static_cast<int>(nbH);
+  p.nsplit = m.nsplit_d;
+  p.rows_per_split = m.rows_d;
+  p.use_tma = (p.nb % 8 == 0 && p.b_stride % 16 == 0 &&
+               q4::encode_weight_tmap(&p.tmap[0], W_down, I, p.nb, E, p.b_stride, m.bpt_d))
+                  ? 1 : 0;
+  p.A = h;
+  p.a_dtype = 0;
+  p.a_ld = I;
+  e = q4::launch_gemv(p, m.mr, m.bpt_d, dim3(m.ntiles_d, m.nsplit_d, m.nexp),
+                      dim3(1, m.nsplit_d, 1), st, true);
+  if (e != cudaSuccess) return Q4_ERR_CUDA;
+
+  e = q4::launch_moe_combine(out, y, topk_idx, topk_w, addend, static_cast<int>(T),
+                             static_cast<int>(topk), static_cast<int>(E), static_cast<int>(H), st,
+                             true);
+  return launch_status(e);
+}
+
+
+}  // namespace
+
 extern "C" {
 
 int q4_version(void) { return 100; }
@@ -323,69 +400,8 @@ int q4_moe_experts_ex(float* out, const void* x, int x_dtype, const void* W_gate
     rc = owned_workspace(s, m.total, &ws);
     if (rc != Q4_OK) return rc;
   }
-  uint8_t* w8 = static_cast<uint8_t*>(ws);
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int64_t nbI = ceil_div(I, 32), nbH = ceil_div(H, 32);
-  float* h = reinterpret_cast<float*>(w8 + m.off_h);
-  float* y = reinterpret_cast<float*>(w8 + m.off_y);
-
-  q4::GemvParams p;
-  std::memset(&p, 0, sizeof(p));
-  p.topk_idx = topk_idx;
-  p.nslots = m.nslots;
-  p.topk = static_cast<int>(topk);
-  p.E = static_cast<int>(E);
-  p.list_cap = m.list_cap;
-  p.h = h;
-  p.y = y;
-  p.err = s->status;
-  p.c_dtype = 0;
-  q4::fill_decode_consts(p);
-
-  // gate and up: K = H, N = I; A rows are tokens
-  p.mode = q4::kModeGateUp;
-  p.B = static_cast<const uint8_t*>(W_gate);
-  p.B2 = static_cast<const uint8_t*>(W_up);
-  p.b_stride = static_cast<long long>(H) * nbI * 18;
-  p.K = static_cast<int>(H);
-  p.N = static_cast<int>(I);
-  p.nb = static_cast<int>(nbI);
-  p.nsplit = m.nsplit_gu;
-  p.rows_per_split = m.rows_gu;
-  p.use_tma = (p.nb % 8 == 0 && p.b_stride % 16 == 0 &&
-               q4::encode_weight_tmap(&p.tmap[0], W_gate, H, p.nb, E, p.b_stride, m.bpt_gu) &&
-               q4::encode_weight_tmap(&p.tmap[1], W_up, H, p.nb, E, p.b_stride, m.bpt_gu))
-                  ? 1 : 0;
-  p.A = x;
-  p.a_dtype = x_dtype;
-  p.a_ld = H;
-  cudaError_t e = q4::launch_gemv(p, m.mr, m.bpt_gu, dim3(m.ntiles_gu, m.nsplit_gu, 2 * m.nexp),
-                                  dim3(1, m.nsplit_gu, 2), st, true);
-  if (e != cudaSuccess) return Q4_ERR_CUDA;
-
-  // down: K = I, N = H; A rows are slots of h
-  p.mode = q4::kModeDown;
-  p.B = static_cast<const uint8_t*>(W_down);
-  p.B2 = nullptr;
-  p.b_stride = static_cast<long long>(I) * nbH * 18;
-  p.K = static_cast<int>(I);
-  p.N = static_cast<int>(H);
-  p.nb = static_cast<int>(nbH);
-  p.nsplit = m.nsplit_d;
-  p.rows_per_split = m.rows_d;
-  p.use_tma = (p.nb % 8 == 0 && p.b_stride % 16 == 0 &&
-               q4::encode_weight_tmap(&p.tmap[0], W_down, I, p.nb, E, p.b_stride, m.bpt_d))
-                  ? 1 : 0;
-  p.A = h;
-  p.a_dtype = 0;
-  p.a_ld = I;
-  e = q4::launch_gemv(p, m.mr, m.bpt_d, dim3(m.ntiles_d, m.nsplit_d, m.nexp),
-                      dim3(1, m.nsplit_d, 1), st, true);
-  if (e != cudaSuccess) return Q4_ERR_CUDA;
-
-  e = q4::launch_moe_combine(out, y, topk_idx, topk_w, static_cast<int>(T), static_cast<int>(topk),
-                             static_cast<int>(E), static_cast<int>(H), st, true);
-  return launch_status(e);
+  return moe_run(s, m, out, x, x_dtype, W_gate, W_up, W_down, topk_idx, topk_w, T, topk, E, H, I,
+                 ws, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 int q4_moe_experts(float* out, const void* x, const void* W_gate, const void* W_up,
@@ -393,6 +409,114 @@ int q4_moe_experts(float* out, const void* x, const void* W_gate, const void* W_
                    int64_t E, int64_t H, int64_t I) {
   return q4_moe_experts_ex(out, x, Q4_BF16, W_gate, W_up, W_down, topk_idx, topk_w, T, 6, E, H, I,
                            nullptr, 0, nullptr);
+}
+
+int q4_moe_gate(int32_t* topk_idx, float* topk_w, const float* logits, int64_t T, int64_t E,
+                int64_t topk, void* stream) {
+  if (!topk_idx || !topk_w || !logits || T <= 0 || E <= 0 || topk <= 0) return Q4_ERR_ARG;
+  if (E > q4::kGateMaxExperts || topk > q4::kGateMaxTopk || topk > E || T > (1 << 24))
+    return Q4_ERR_SHAPE;
+  if (!aligned16(topk_idx) || !aligned16(topk_w) || !aligned16(logits)) return Q4_ERR_ALIGN;
+  return launch_status(q4::launch_moe_gate(topk_idx, topk_w, logits, static_cast<int>(T),
+                                           static_cast<int>(E), static_cast<int>(topk), nullptr,
+                                           nullptr, static_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+// Workspace of q4_moe_block: routing, the shared expert's routing and output,
+// then one expert workspace serving the routed and the shared problem in turn.
+struct BlockLayout {
+  size_t idx, w, sidx, sw, ys, moe, total;
+};
+BlockLayout block_layout(int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I, int64_t Is) {
+  BlockLayout b;
+  size_t o = 0;
+  b.idx = o;
+  o += round_up(static_cast<size_t>(T * topk) * 4, 256);
+  b.w = o;
+  o += round_up(static_cast<size_t>(T * topk) * 4, 256);
+  b.sidx = o;
+  o += round_up(static_cast<size_t>(T) * 4, 256);
+  b.sw = o;
+  o += round_up(static_cast<size_t>(T) * 4, 256);
+  b.ys = o;
+  o += (Is > 0) ? round_up(static_cast<size_t>(T * H) * 4, 256) : 0;
+  b.moe = o;
+  size_t need = q4_moe_workspace_size(T, topk, E, H, I);
+  if (Is > 0) {
+    const size_t sneed = q4_moe_workspace_size(T, 1, 1, H, Is);
+    if (sneed > need) need = sneed;
+  }
+  b.total = o + need;
+  return b;
+}
+}  // namespace
+
+size_t q4_moe_block_workspace_size(int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I,
+                                   int64_t Is) {
+  if (T <= 0 || topk <= 0 || E <= 0 || H <= 0 || I <= 0 || Is < 0) return 0;
+  return block_layout(T, topk, E, H, I, Is).total;
+}
+
+int q4_moe_block(float* out, const void* x, int x_dtype, const float* logits, const void* W_gate,
+                 const void* W_up, const void* W_down, int64_t T, int64_t topk, int64_t E,
+                 int64_t H, int64_t I, const void* S_gate, const void* S_up, const void* S_down,
+                 int64_t Is, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!out || !x || !logits || !W_gate || !W_up || !W_down) return Q4_ERR_ARG;
+  if (T <= 0 || topk <= 0 || E <= 0 || H <= 0 || I <= 0 || Is < 0) return Q4_ERR_ARG;
+  if (Is > 0 && (!S_gate || !S_up || !S_down)) return Q4_ERR_ARG;
+  if (E > q4::kGateMaxExperts || topk > q4::kGateMaxTopk || topk > E || T * topk > 8192 ||
+      H > (1 << 24) || I > (1 << 24) || Is > (1 << 24))
+    return Q4_ERR_SHAPE;
+  if (x_dtype != Q4_F32 && x_dtype != Q4_BF16) return Q4_ERR_DTYPE;
+  if (!aligned16(out) || !aligned16(x) || !aligned16(logits) || !aligned16(W_gate) ||
+      !aligned16(W_up) || !aligned16(W_down) || (workspace && !aligned16(workspace)) ||
+      (Is > 0 && (!aligned16(S_gate) || !aligned16(S_up) || !aligned16(S_down))))
+    return Q4_ERR_ALIGN;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  int rc = current_state(&s);
+  if (rc != Q4_OK) return rc;
+  const MoeShape& m = cached_moe_shape(s, T, topk, E, H, I);
+  if (4LL * m.mr * m.rows_gu > kMaxASliceBytes || 4LL * m.mr * m.rows_d > kMaxASliceBytes)
+    return Q4_ERR_SHAPE;
+  const MoeShape* ms = nullptr;
+  if (Is > 0) {
+    ms = &cached_moe_shape(s, T, 1, 1, H, Is);
+    if (4LL * ms->mr * ms->rows_gu > kMaxASliceBytes || 4LL * ms->mr * ms->rows_d > kMaxASliceBytes)
+      return Q4_ERR_SHAPE;
+  }
+  const BlockLayout b = block_layout(T, topk, E, H, I, Is);
+  void* ws = workspace;
+  if (ws) {
+    if (workspace_bytes < b.total) return Q4_ERR_WORKSPACE;
+  } else {
+    rc = owned_workspace(s, b.total, &ws);
+    if (rc != Q4_OK) return rc;
+  }
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  int32_t* idx = reinterpret_cast<int32_t*>(w8 + b.idx);
+  float* w = reinterpret_cast<float*>(w8 + b.w);
+  int32_t* sidx = reinterpret_cast<int32_t*>(w8 + b.sidx);
+  float* sw = reinterpret_cast<float*>(w8 + b.sw);
+  float* ys = reinterpret_cast<float*>(w8 + b.ys);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  // router (and the shared expert's unit routing)
+  cudaError_t e = q4::launch_moe_gate(idx, w, logits, static_cast<int>(T), static_cast<int>(E),
+                                      static_cast<int>(topk), Is > 0 ? sidx : nullptr,
+                                      Is > 0 ? sw : nullptr, st);
+  if (e != cudaSuccess) return Q4_ERR_CUDA;
+  // shared expert: every token, weight 1
+  if (Is > 0) {
+    rc = moe_run(s, *ms, ys, x, x_dtype, S_gate, S_up, S_down, sidx, sw, T, 1, 1, H, Is,
+                 w8 + b.moe, nullptr, st);
+    if (rc != Q4_OK) return rc;
+  }
+  // routed experts; the shared expert's rows are added after the weighted sum
+  return moe_run(s, m, out, x, x_dtype, W_gate, W_up, W_down, idx, w, T, topk, E, H, I,
+                 w8 + b.moe, Is > 0 ? ys : nullptr, st);
 }
 
 size_t q4_planar_qs_offset(int64_t K, int64_t N) {

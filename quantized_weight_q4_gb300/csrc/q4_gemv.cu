@@ -659,10 +659,12 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
   }
 }
 
-// out[t, j] = sum_k w[t, k] * y[t*topk + k, j] in slot order; invalid slots skipped.
+// out[t, j] = sum_k w[t, k] * y[t*topk + k, j] in slot order (invalid slots
+// skipped), then + addend[t, j] when an addend is given.
 __global__ void __launch_bounds__(256) q4_moe_combine_kernel(float* out, const float* y,
                                                              const int32_t* idx, const float* w,
-                                                             int T, int topk, int E, int H) {
+                                                             const float* addend, int T, int topk,
+                                                             int E, int H) {
   pdl_wait();
   pdl_launch_dependents();
   const size_t n = static_cast<size_t>(T) * H;
@@ -677,7 +679,7 @@ __global__ void __launch_bounds__(256) q4_moe_combine_kernel(float* out, const f
       if (e < 0 || e >= E) continue;
       acc = fmaf(w[s], y[static_cast<size_t>(s) * H + j], acc);
     }
-    out[i] = acc;
+    out[i] = addend ? acc + addend[i] : acc;
   }
 }
 
@@ -780,7 +782,8 @@ int max_active_clusters(int mode, int mr, int bpt, int rows_per_split, int list_
 }
 
 cudaError_t launch_moe_combine(float* out, const float* y, const int32_t* idx, const float* w,
-                               int T, int topk, int E, int H, cudaStream_t st, bool pdl) {
+                               const float* addend, int T, int topk, int E, int H,
+                               cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   const size_t n = static_cast<size_t>(T) * H;
   size_t nblocks = (n + 255) / 256;
@@ -793,7 +796,7 @@ cudaError_t launch_moe_combine(float* out, const float* y, const int32_t* idx, c
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, q4_moe_combine_kernel, out, y, idx, w, T, topk, E, H);
+  return cudaLaunchKernelEx(&cfg, q4_moe_combine_kernel, out, y, idx, w, addend, T, topk, E, H);
 }
 
 int gemv_tile_blocks(int bpt) { return kLanesPerRow * bpt; }

@@ -64,8 +64,10 @@ void fill_decode_consts(GemvParams& p);
 // stage of rows.  Needs nb % 8 == 0 and a 16-byte aligned base.
 bool encode_weight_tmap(CUtensorMap* map, const void* base, int64_t K, int64_t nb,
                         int64_t experts, int64_t matrix_bytes, int bpt);
+// out[t] = sum_k w[t,k] * y[t*topk+k] (slot order), plus addend[t] if given.
 cudaError_t launch_moe_combine(float* out, const float* y, const int32_t* idx, const float* w,
-                               int T, int topk, int E, int H, cudaStream_t st, bool pdl);
+                               const float* addend, int T, int topk, int E, int H,
+                               cudaStream_t st, bool pdl);
 
 // q4_gemm_sm103.cu: the prefill GEMM on the tensor cores.
 struct GemmParams {
@@ -95,6 +97,13 @@ cudaError_t launch_dequant(void* W, int w_dtype, const uint8_t* B, int64_t K, in
                            cudaStream_t st);
 cudaError_t launch_repack(uint8_t* dst, const uint8_t* src, int64_t K, int64_t N, bool to_planar,
                           cudaStream_t st);
+// q4_moe_gate.cu: the router (one warp per token).  Optionally also writes the
+// shared expert's routing (index 0, weight 1) for every token.
+constexpr int kGateMaxExperts = 1024;
+constexpr int kGateMaxTopk = 16;
+cudaError_t launch_moe_gate(int32_t* topk_idx, float* topk_w, const float* logits, int T, int E,
+                            int topk, int32_t* shared_idx, float* shared_w, cudaStream_t st);
+
 // One bounded pipeline wait run to its limit (arrive = false) or completed.
 cudaError_t launch_wait_selftest(unsigned* err, unsigned long long limit_ns, bool arrive,
                                  cudaStream_t st);
