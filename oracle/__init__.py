@@ -57,6 +57,9 @@ def bind(path: str) -> ctypes.CDLL:
     L.q4o_matmul.argtypes = [vp, ctypes.c_int, vp, c_i64, c_i64, c_i64, vp, vp]
     L.q4o_matmul_naive.argtypes = [vp, ctypes.c_int, vp, c_i64, c_i64, c_i64, vp]
     L.q4o_moe_gate.argtypes = [vp, c_i64, c_i64, c_i64, vp, vp]
+    L.q4o_f64_to_fp16.argtypes = [ctypes.c_double]
+    L.q4o_f64_to_fp16.restype = ctypes.c_uint16
+    L.q4o_quantize.argtypes = [vp, ctypes.c_int, c_i64, c_i64, vp]
     L.q4o_moe_block.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, c_i64, c_i64, c_i64, c_i64, c_i64,
                                 vp, vp, vp, c_i64, vp, vp, vp, vp]
     L.q4o_moe.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, vp,
@@ -105,6 +108,19 @@ def bf16_to_f64(h: int) -> float:
 
 def f64_to_bf16(x: float) -> int:
     return lib().q4o_f64_to_bf16(x)
+
+
+def f64_to_fp16(x: float) -> int:
+    return lib().q4o_f64_to_fp16(x)
+
+
+def quantize(W: np.ndarray, K: int, N: int) -> np.ndarray:
+    """Q4_0 blocks [K, nb*18] of W (fp32, or bf16 bits as uint16) by the
+    oracle's encoder."""
+    W, dt = _act(W)
+    B = np.empty((K, ((N + 31) // 32) * 18), dtype=np.uint8)
+    lib().q4o_quantize(_p(W), dt, K, N, _p(B))
+    return B
 
 
 def silu(g: float) -> float:

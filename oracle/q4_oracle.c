@@ -458,3 +458,92 @@ void q4o_moe_block(const void *x, int x_dtype, const float *logits,
     }
     free(sidx); free(sw); free(so); free(st);
 }
+
+/* ------------------------------------------------------------------ */
+/* Encoder (quantisation)                                              */
+/* ------------------------------------------------------------------ */
+
+/* x rounded to the nearest IEEE binary16 value, ties to even (5-bit
+ * exponent with bias 15, 10-bit fraction, subnormals from 2^-24, values
+ * that round above 65504 become infinity); returned as its 16 bits. */
+uint16_t q4o_f64_to_fp16(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (isnan(x))
+        return (uint16_t)(sign | 0x7E00);
+    if (isinf(x))
+        return (uint16_t)(sign | 0x7C00);
+    if (a == 0.0)
+        return sign;
+    int e;
+    (void)frexp(a, &e);                   /* a = m * 2^e, m in [0.5, 1) */
+    int expo = e - 1;                     /* a = 1.xxx * 2^expo */
+    int quantum_exp = (expo < -14) ? -24 : expo - 10;
+    double y = ldexp(a, -quantum_exp);    /* a in units of the quantum */
+    double fl = floor(y);
+    double r = fl;
+    double diff = y - fl;
+    if (diff > 0.5 || (diff == 0.5 && fmod(fl, 2.0) != 0.0))
+        r = fl + 1.0;
+    double v = ldexp(r, quantum_exp);
+    if (v >= 65536.0)
+        return (uint16_t)(sign | 0x7C00);
+    if (v < ldexp(1.0, -14))
+        return (uint16_t)(sign | (uint16_t)ldexp(v, 24));   /* subnormal */
+    double m = frexp(v, &e);
+    expo = e - 1;
+    int frac = (int)ldexp(m, 11) - 1024;   /* m*2048 in [1024, 2048) */
+    return (uint16_t)(sign | (uint16_t)((expo + 15) << 10) | (uint16_t)frac);
+}
+
+/* Q4_0 blocks of a K x N matrix W (row-major, fp32 or bf16 bits) in the
+ * layout of [Eng §2.2-§2.3]: for each row k and block b (columns
+ * 32b .. 32b+31), m = the element of largest magnitude (the first on ties),
+ * d = m / -8 so that m maps to code 0, stored as fp16 (nearest even), and
+ * code q_l = min(15, trunc(w_l * (1/d) + 8.5)) with every step an fp32
+ * operation (no fused multiply-add; 1/d := 0 when d = 0); padding columns
+ * (>= N) get code 8 (value 0).  The pages give no scale rule: this one makes
+ * the largest magnitude exact and rounds the rest half up. */
+void q4o_quantize(const void *W, int w_dtype, int64_t K, int64_t N, uint8_t *B)
+{
+    int64_t nb = (N + QO_BLOCK - 1) / QO_BLOCK;
+    for (int64_t k = 0; k < K; k++) {
+        for (int64_t b = 0; b < nb; b++) {
+            float wv[QO_BLOCK];
+            int n = (int)((N - b * QO_BLOCK) < QO_BLOCK ? (N - b * QO_BLOCK) : QO_BLOCK);
+            for (int l = 0; l < n; l++)
+                wv[l] = (float)act_at(W, w_dtype, k * N + b * QO_BLOCK + l);
+            float amax = 0.0f, mx = 0.0f;
+            for (int l = 0; l < n; l++) {
+                float v = wv[l];
+                if (amax < fabsf(v)) {
+                    amax = fabsf(v);
+                    mx = v;
+                }
+            }
+            float d = mx / -8.0f;
+            float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+            uint8_t *blk = B + (k * nb + b) * QO_BLOCK_BYTES;
+            uint16_t h = q4o_f64_to_fp16((double)d);
+            blk[0] = (uint8_t)(h & 0xFF);
+            blk[1] = (uint8_t)(h >> 8);
+            for (int l = 0; l < QO_BLOCK; l++) {
+                int q = 8;
+                if (l < n) {
+                    float t = wv[l] * id;
+                    t = t + 8.5f;
+                    q = (int)t;
+                    if (q > 15)
+                        q = 15;
+                    if (q < 0)
+                        q = 0;
+                }
+                if (l % 2 == 0)
+                    blk[2 + l / 2] = (uint8_t)q;
+                else
+                    blk[2 + l / 2] |= (uint8_t)(q << 4);
+            }
+        }
+    }
+}

@@ -28,12 +28,17 @@ MUTANTS = {
     "sigmoid sign": ("return 1.0 / (1.0 + exp(-g));", "return 1.0 / (1.0 + exp(g));"),
     "routing weight dropped": ("out[t * H + j] += wk * y[j];", "out[t * H + j] += y[j];"),
     "up projection dropped": ("h[i] = silu * u[i];", "h[i] = silu;"),
-    "bf16 ties away from zero": ("(diff == 0.5 && fmod(fl, 2.0) != 0.0)", "(diff == 0.5)"),
+    "bf16 ties away from zero": ("(diff == 0.5 && fmod(fl, 2.0) != 0.0))\n        r = fl + 1.0;\n    double v = ldexp(r, (int)quantum_exp);",
+                                 "(diff == 0.5))\n        r = fl + 1.0;\n    double v = ldexp(r, (int)quantum_exp);"),
     "router ties to the higher index": ("if (!taken[e] && (best < 0 || p[e] > p[best]))", "if (!taken[e] && (best < 0 || p[e] >= p[best]))"),
     "router weights not renormalised": ("            w[t * topk + k] /= wsum;", "            w[t * topk + k] /= 1.0;"),
     "router max not subtracted": ("            p[e] = exp((double)l[e] - mx);", "            p[e] = exp((double)l[e]);"),
     "block shared term dropped": ("        out[i] += so[i];", "        out[i] += 0.0 * so[i];"),
     "block shared weight doubled": ("        sw[t] = 1.0;", "        sw[t] = 2.0;"),
+    "encoder truncates instead of rounding": ("                    t = t + 8.5f;", "                    t = t + 8.0f;"),
+    "encoder takes the largest value, not magnitude": ("                if (amax < fabsf(v)) {\n                    amax = fabsf(v);", "                if (amax < v) {\n                    amax = v;"),
+    "encoder padding code 0": ("                int q = 8;\n                if (l < n) {", "                int q = 0;\n                if (l < n) {"),
+    "fp16 ties away from zero": ("    if (diff > 0.5 || (diff == 0.5 && fmod(fl, 2.0) != 0.0))\n        r = fl + 1.0;\n    double v = ldexp(r, quantum_exp);", "    if (diff >= 0.5)\n        r = fl + 1.0;\n    double v = ldexp(r, quantum_exp);"),
     "router picks the smallest": ("if (!taken[e] && (best < 0 || p[e] > p[best]))", "if (!taken[e] && (best < 0 || p[e] < p[best]))"),
 }
 
@@ -59,6 +64,10 @@ BATTERY = [
     pins.test_block_shared_term_is_the_shared_expert,
     pins.test_block_identical_experts_collapse,
     pins.test_block_expert_relabelling,
+    lambda: pins.test_fp16_encode_matches_numpy(oracle),
+    pins.test_quantize_closed_forms,
+    pins.test_quantize_matches_fp32_restatement,
+    pins.test_quantize_round_trip_bound,
 ]
 
 

@@ -578,3 +578,111 @@ def test_block_expert_relabelling():
     b, _, _, _ = oracle.moe_block(x, logits[:, perm], Wg[perm], Wu[perm], Wd[perm], T, topk, E,
                                   H, I, Sg, Su, Sd, Is)
     assert np.allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- encoder
+
+def test_fp16_encode_matches_numpy(oracle_lib):
+    """fp64 -> binary16 nearest-even equals numpy's cast: every fp16 value,
+    random fp32 values over the whole range, exact ties, the overflow edge."""
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = codes.view(np.float16).astype(np.float64)
+    for c in range(65536):
+        if not math.isnan(vals[c]):
+            assert oracle_lib.f64_to_fp16(float(vals[c])) == c, hex(c)
+    g = np.random.default_rng(4)
+    xs = np.concatenate([
+        (g.standard_normal(3000) * np.exp2(g.integers(-30, 17, 3000))).astype(np.float32),
+        np.array([65504.0, 65519.99, 65520.0, 1e6, -65520.0, 2.0 ** -25, 2.0 ** -26, 3e-8],
+                 np.float32)])
+    # ties: the midpoint of two neighbouring fp16 values, both parities
+    h = np.array([0x3C00, 0x3C01, 0x0401, 0x0002, 0x7BFE], np.uint16).view(np.float16)
+    mids = ((h.astype(np.float64) + np.nextafter(h, np.float16(np.inf)).astype(np.float64)) / 2)
+    for x in list(xs.astype(np.float64)) + list(mids):
+        want = int(np.array([x]).astype(np.float16).view(np.uint16)[0])
+        assert oracle_lib.f64_to_fp16(float(x)) == want, x
+
+
+def _codes(B, K, N):
+    nb = (N + 31) // 32
+    blk = B.reshape(K, nb, 18)
+    q = np.empty((K, nb, 32), np.int64)
+    q[:, :, 0::2] = blk[:, :, 2:] & 0xF
+    q[:, :, 1::2] = blk[:, :, 2:] >> 4
+    d = blk[:, :, 0].astype(np.uint16) | (blk[:, :, 1].astype(np.uint16) << 8)
+    return q, d
+
+
+def test_quantize_closed_forms():
+    import oracle
+    # largest magnitude negative: d = 1/8, codes are the pattern itself
+    pat = np.array(list(range(16)) * 2)
+    W = ((pat - 8) / 8.0).astype(np.float32)[None]
+    q, d = _codes(oracle.quantize(W, 1, 32), 1, 32)
+    assert q[0, 0].tolist() == pat.tolist() and d[0, 0] == 0x3000
+    # largest magnitude positive: d = -1/8 (negative scale), 1 -> code 0
+    W = np.zeros((1, 32), np.float32)
+    W[0, :4] = [1.0, 0.5, -0.25, 0.0]
+    q, d = _codes(oracle.quantize(W, 1, 32), 1, 32)
+    assert d[0, 0] == 0xB000 and q[0, 0, :4].tolist() == [0, 4, 10, 8]
+    # all zeros: scale -0, every code 8
+    q, d = _codes(oracle.quantize(np.zeros((2, 64), np.float32), 2, 64), 2, 64)
+    assert (q == 8).all() and (d == 0x8000).all()
+    # a half step rounds up: -0.4375 = -3.5 steps of 1/8 -> code 5
+    W = np.zeros((1, 32), np.float32)
+    W[0, 0], W[0, 1] = -1.0, -0.4375
+    q, _ = _codes(oracle.quantize(W, 1, 32), 1, 32)
+    assert q[0, 0, 1] == 5
+    # padding columns (>= N) hold code 8
+    q, _ = _codes(oracle.quantize(np.ones((1, 40), np.float32), 1, 40), 1, 40)
+    assert (q[0, 1, 8:] == 8).all() and (q[0, 1, :8] == 0).all()
+
+
+def test_quantize_matches_fp32_restatement():
+    """The codes equal a numpy fp32 restatement of the same rule (largest
+    magnitude first-on-ties, d = m/-8, trunc(w*(1/d) + 8.5) capped at 15)."""
+    import oracle
+    K, N = 37, 200
+    W = (si.rng(8, 1).standard_normal((K, N)) * 0.02).astype(np.float32)
+    W[3, 64:96] = 0.0
+    W[5, 40], W[5, 41] = 0.05, -0.05             # equal magnitudes: the first wins
+    q, d = _codes(oracle.quantize(W, K, N), K, N)
+    nb = (N + 31) // 32
+    Wp = np.zeros((K, nb * 32), np.float32)
+    Wp[:, :N] = W
+    Wb = Wp.reshape(K, nb, 32)
+    first = np.argmax(np.abs(Wb) == np.abs(Wb).max(axis=2, keepdims=True), axis=2)
+    m = np.take_along_axis(Wb, first[..., None], axis=2)[..., 0]
+    dd = (m / np.float32(-8.0)).astype(np.float32)
+    with np.errstate(divide="ignore"):
+        idd = np.where(dd != 0, np.float32(1.0) / dd, np.float32(0.0)).astype(np.float32)
+    t = (Wb * idd[..., None]).astype(np.float32)
+    t = (t + np.float32(8.5)).astype(np.float32)
+    qq = np.minimum(t.astype(np.int64), 15)
+    col = np.arange(nb * 32).reshape(nb, 32)
+    qq[:, col >= N] = 8
+    assert np.array_equal(q, qq)
+    assert np.array_equal(d, dd.astype(np.float16).view(np.uint16))
+
+
+def test_quantize_round_trip_bound():
+    """Dequantising the codes gives back each weight within half a step of
+    the fp32 scale (a full step where code 16 would be needed and 15 is
+    stored) plus 8 times the scale's fp16 rounding."""
+    import oracle
+    K, N = 64, 320
+    W = (si.rng(9, 1).standard_normal((K, N)) * 0.05).astype(np.float32)
+    B = oracle.quantize(W, K, N)
+    R = oracle.dequant_f32(B, K, N).astype(np.float64)
+    nb = N // 32
+    Wb = W.astype(np.float64).reshape(K, nb, 32)
+    d32 = -np.abs(Wb).max(axis=2) * np.sign(np.take_along_axis(
+        Wb, np.abs(Wb).argmax(axis=2)[..., None], axis=2)[..., 0]) / 8.0
+    q, dh = _codes(B, K, N)
+    d16 = dh.view(np.float16).astype(np.float64)
+    steps = Wb / d32[..., None]                 # w in units of the fp32 scale
+    half = np.where(steps > 7.5, 1.0, 0.5)      # capped at code 15
+    bound = half * np.abs(d32)[..., None] + 8 * np.abs(d32 - d16)[..., None] + 1e-12
+    err = np.abs(R.reshape(K, nb, 32) - Wb)
+    assert (err <= bound * 1.000001).all()
+    assert (steps > 7.5).any()                  # the capped case occurs in the data
