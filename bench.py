@@ -11,7 +11,8 @@ Other workloads (``--workload``), each printing its own line: ``gemv`` (one
 GEMV, fp32 A, default K = N = 4096, --m/--k/--n), ``batched`` (K = 5120,
 N = 12288, bf16 A with --m rows), ``moe`` (top-6 of 160 experts, H = 5120,
 I = 1536, --tokens), ``moe_block`` (router + shared expert + routed experts
-of the same block, --tokens), ``prefill`` (M = 2048, K = 5120, N = 12288, bf16 A and
+of the same block, --tokens), ``quantize`` (the Q4_0 encoder on a fp32
+--k x --n matrix; GB/s of input plus output), ``prefill`` (M = 2048, K = 5120, N = 12288, bf16 A and
 C on the tensor cores; metric TFLOP/s).  Weight copies or routings rotate so
 that each pass reads at least four times the L2 capacity.
 
@@ -453,6 +454,32 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
                "l2": f"{R} seeded routings rotate over 160 experts (2.12 GB of weights)",
                "parallelism": f"replicas x{ws}"}
         units = R
+    elif args.workload == "quantize":
+        # the Q4_0 encoder on a fp32 matrix (HBM-bound: read W, write blocks)
+        K = args.k if args.k else 5120
+        N = args.n if args.n else 12288
+        nbytes = K * N * 4 + K * si.nblocks(N) * 18
+        copies = max(1, -(-4 * l2 // nbytes))
+        fns, keep = [], []
+        for i in range(copies):
+            W = to_dev((si.rng(0, 900 + i).standard_normal((K, N)) * 0.02).astype(np.float32))
+            B = torch.empty((K, si.nblocks(N) * 18), dtype=torch.uint8, device=dev)
+            keep += [W, B]
+            fns.append(lambda B=B, W=W: q4.q4_quantize(B, W, K, N))
+        g = GraphOf(torch, fns)
+        barrier(ws)
+        with ClockSampler(local) as clk:
+            t = g.time(args.steps, args.warmup)
+        barrier(ws)
+        t = max_over_ranks(ws, t)
+        per_launch = t / (args.steps * copies)
+        wbytes = nbytes
+        value = ws * nbytes / per_launch / 1e9
+        cfg = {"workload": "quantize", "K": K, "N": N, "w_dtype": "f32",
+               "bytes_per_launch": nbytes, "copies_rotated": copies,
+               "l2": f"{copies} distinct inputs per pass ({copies * nbytes} B >= 4x L2)",
+               "parallelism": f"replicas x{ws}", "us_per_launch": round(per_launch * 1e6, 2)}
+        units = copies
     elif args.workload == "moe_block":
         # router + shared expert + routed experts of one DeepSeek-V2-sized block
         T, E, H, I, topk, Is = args.tokens, 160, 5120, 1536, 6, 3072

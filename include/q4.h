@@ -194,6 +194,18 @@ Q4_API int q4_get_device_status(void *stream);
 Q4_API unsigned int q4_last_device_flags(void);
 
 /*
+ * q4_quantize -- Q4_0 encoder: W [K, N] row-major (w_dtype Q4_F32 or Q4_BF16)
+ * -> B [K, ceil(N/32) * 18 bytes] in Q4_LAYOUT_BLOCKS (engine page §2.2-§2.3).
+ * The pages give no scale rule; this one, per block (row k, 32 consecutive
+ * columns): m = the element of largest magnitude (the first on ties),
+ * d = m / -8 (so that m maps to code 0 exactly), stored as fp16 rounded to
+ * nearest even; code q = min(15, trunc(w * (1/d) + 8.5)), each step one
+ * fp32 operation; 1/d is taken as 0 when d = 0; columns >= N get code 8.
+ * Values must be finite.  Pointers 16-byte aligned; B is overwritten.
+ */
+Q4_API int q4_quantize(void *B, const void *W, int w_dtype, int64_t K, int64_t N, void *stream);
+
+/*
  * q4_moe_gate -- the router in front of the routed experts
  * [KTransformers page, «规则二»: the gate gives the top-k indices and weights].
  *   topk_idx  int32 [T, topk] (out): for each token the topk largest of its

@@ -58,6 +58,7 @@ SIGNATURES = {
     "q4_planar_bytes": (_sz, [_i64, _i64]),
     "q4_dequant": (_int, [_vp, _vp, _i64, _i64, _vp]),
     "q4_dequant_bf16": (_int, [_vp, _vp, _i64, _i64, _vp]),
+    "q4_quantize": (_int, [_vp, _vp, _int, _i64, _i64, _vp]),
     "q4_moe_gate": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "q4_moe_block": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                             _vp, _vp, _vp, _i64, _vp, _sz, _vp]),
@@ -190,6 +191,13 @@ def q4_moe_experts_noalloc(out, x, W_gate, W_up, W_down, topk_idx, topk_w, T: in
     _check("q4_moe_experts_noalloc", lib().q4_moe_experts_noalloc(
         _ptr(out), _ptr(x), _dtype_code(x), _ptr(W_gate), _ptr(W_up), _ptr(W_down),
         _ptr(topk_idx), _ptr(topk_w), T, topk, E, H, I, _stream(stream)))
+
+
+def q4_quantize(B, W, K: int, N: int, stream=None) -> None:
+    """Q4_0 blocks of W (fp32 or bf16) into B (uint8 [K, ceil(N/32)*18])."""
+    _require_cuda(B, W)
+    _check("q4_quantize", lib().q4_quantize(_ptr(B), _ptr(W), _dtype_code(W), K, N,
+                                            _stream(stream)))
 
 
 def q4_moe_gate(topk_idx, topk_w, logits, T: int, E: int, topk: int, stream=None) -> None:

@@ -519,6 +519,15 @@ int q4_moe_block(float* out, const void* x, int x_dtype, const float* logits, co
                  w8 + b.moe, Is > 0 ? ys : nullptr, st);
 }
 
+int q4_quantize(void* B, const void* W, int w_dtype, int64_t K, int64_t N, void* stream) {
+  if (!B || !W || K <= 0 || N <= 0) return Q4_ERR_ARG;
+  if (K > (1LL << 30) || N > (1LL << 30)) return Q4_ERR_SHAPE;
+  if (w_dtype != Q4_F32 && w_dtype != Q4_BF16) return Q4_ERR_DTYPE;
+  if (!aligned16(B) || !aligned16(W)) return Q4_ERR_ALIGN;
+  return launch_status(q4::launch_quantize(static_cast<uint8_t*>(B), W, w_dtype, K, N,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 size_t q4_planar_qs_offset(int64_t K, int64_t N) {
   if (K <= 0 || N <= 0) return 0;
   return round_up(static_cast<size_t>(K * ceil_div(N, 32)) * 2, 16);

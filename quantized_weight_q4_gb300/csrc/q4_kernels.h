@@ -97,6 +97,10 @@ cudaError_t launch_dequant(void* W, int w_dtype, const uint8_t* B, int64_t K, in
                            cudaStream_t st);
 cudaError_t launch_repack(uint8_t* dst, const uint8_t* src, int64_t K, int64_t N, bool to_planar,
                           cudaStream_t st);
+// q4_misc.cu: the Q4_0 encoder (w_dtype 0 fp32, 1 bf16).
+cudaError_t launch_quantize(uint8_t* B, const void* W, int w_dtype, int64_t K, int64_t N,
+                            cudaStream_t st);
+
 // q4_moe_gate.cu: the router (one warp per token).  Optionally also writes the
 // shared expert's routing (index 0, weight 1) for every token.
 constexpr int kGateMaxExperts = 1024;

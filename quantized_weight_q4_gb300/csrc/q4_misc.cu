@@ -104,6 +104,86 @@ cudaError_t launch_repack(uint8_t* dst, const uint8_t* src, int64_t K, int64_t N
   return cudaGetLastError();
 }
 
+// Q4_0 encoder [C++ DeepSeek engine page §2.2-§2.3 block layout; the pages
+// give no scale rule]: per block (row k, columns 32b .. 32b+31), m = the
+// element of largest magnitude (first on ties), d = m / -8 stored as fp16
+// (nearest even), code q = min(15, trunc(w * (1/d) + 8.5)) with each step
+// one fp32 operation (explicitly rounded: no fused multiply-add), 1/d := 0
+// when d = 0; padding columns (>= N) get code 8.  One thread per block.
+template <bool BF16>
+__global__ void __launch_bounds__(256) q4_quantize_kernel(uint8_t* B, const void* W, int64_t K,
+                                                          int64_t N, int64_t nb) {
+  const int64_t nblk = K * nb;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nblk;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t k = i / nb;
+    const int64_t b = i - k * nb;
+    const int64_t c0 = b * kBlockCols;
+    const int n = static_cast<int>((N - c0) < kBlockCols ? (N - c0) : kBlockCols);
+    float v[kBlockCols];
+    const size_t base = static_cast<size_t>(k) * N + c0;
+    if (BF16) {
+      const uint16_t* w = static_cast<const uint16_t*>(W) + base;
+#pragma unroll
+      for (int l = 0; l < kBlockCols; ++l) v[l] = (l < n) ? bf16_bits_to_f32(w[l]) : 0.f;
+    } else {
+      const float* w = static_cast<const float*>(W) + base;
+      if (n == kBlockCols && (N & 3) == 0) {
+#pragma unroll
+        for (int l = 0; l < kBlockCols; l += 4) {
+          const float4 f = *reinterpret_cast<const float4*>(w + l);
+          v[l] = f.x;
+          v[l + 1] = f.y;
+          v[l + 2] = f.z;
+          v[l + 3] = f.w;
+        }
+      } else {
+#pragma unroll
+        for (int l = 0; l < kBlockCols; ++l) v[l] = (l < n) ? w[l] : 0.f;
+      }
+    }
+    float amax = 0.f, mx = 0.f;
+#pragma unroll
+    for (int l = 0; l < kBlockCols; ++l) {
+      if (l < n && amax < fabsf(v[l])) {
+        amax = fabsf(v[l]);
+        mx = v[l];
+      }
+    }
+    const float d = __fdiv_rn(mx, -8.0f);
+    const float id = (d != 0.f) ? __fdiv_rn(1.0f, d) : 0.f;
+    uint32_t packed[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int l = 0; l < kBlockCols; ++l) {
+      int q = 8;
+      if (l < n) {
+        const float t = __fadd_rn(__fmul_rn(v[l], id), 8.5f);
+        q = __float2int_rz(t);
+        q = q > 15 ? 15 : (q < 0 ? 0 : q);
+      }
+      packed[l >> 3] |= static_cast<uint32_t>(q) << (4 * (l & 7));
+    }
+    uint16_t* dst = reinterpret_cast<uint16_t*>(B + i * kBlockBytes);   // 2-byte aligned
+    dst[0] = __half_as_ushort(__float2half_rn(d));
+#pragma unroll
+    for (int h = 0; h < 8; ++h)
+      dst[1 + h] = static_cast<uint16_t>(packed[h >> 1] >> (16 * (h & 1)));
+  }
+}
+
+cudaError_t launch_quantize(uint8_t* B, const void* W, int w_dtype, int64_t K, int64_t N,
+                            cudaStream_t st) {
+  const int64_t nb = (N + kBlockCols - 1) / kBlockCols;
+  const int64_t nblk = K * nb;
+  int64_t grid = (nblk + 255) / 256;
+  if (grid > 65536) grid = 65536;
+  if (w_dtype == 1)
+    q4_quantize_kernel<true><<<static_cast<unsigned>(grid), 256, 0, st>>>(B, W, K, N, nb);
+  else
+    q4_quantize_kernel<false><<<static_cast<unsigned>(grid), 256, 0, st>>>(B, W, K, N, nb);
+  return cudaGetLastError();
+}
+
 // One CTA waits, with bounded_wait and a limit of `limit_ns`, on an mbarrier
 // that only `arrive` ever completes: the path every pipeline wait takes, run
 // to its timeout on purpose (no fault, no hang: the wait gives up, records
