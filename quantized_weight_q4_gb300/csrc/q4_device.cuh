@@ -213,23 +213,7 @@ __device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
   return d;
 }
 
-// ---- Q4_0 nibble decoding ---------------------------------------------------
-// A nibble q placed at bit 4p (p = 0..4) of a word ORed with the bit pattern of
-// 2^23 reads as the float 2^23 + q*16^p exactly (it lies in [2^23, 2^24), where
-// floats are the integers).  Subtracting 2^23 + 8*16^p, also exact, leaves
-// 16^p * (q - 8): the signed weight code, scaled by a power of two that the
-// per-block scale factor absorbs.
-constexpr uint32_t kMagic = 0x4B000000u;   // bit pattern of 2^23
-
-__device__ __forceinline__ float nib_f(uint32_t w, uint32_t mask) {
-  return __uint_as_float((w & mask) | kMagic);
-}
-
-// -(2^23 + 8 * 16^p) for p = 0..4
-__device__ __forceinline__ float neg_bias(int p) {
-  return -(8388608.0f + 8.0f * static_cast<float>(1u << (4 * p)));
-}
-
+// ---- Q4_0 blocks in shared memory -------------------------------------------
 // Reads the 18-byte block at byte offset `off` of a 4-byte-aligned shared
 // row: returns the fp16 scale bits and the four 32-bit words of qs.
 __device__ __forceinline__ void load_block_smem(const uint8_t* row, uint32_t off, uint32_t& dbits,

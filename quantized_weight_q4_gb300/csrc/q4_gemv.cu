@@ -23,12 +23,18 @@
 //  * Programmatic dependent launch: the producer streams weights before
 //    griddepcontrol.wait; A is read, and workspace written, only after.
 //
-// Nibble decoding (exact): a nibble q at bit 4p of a word ORed with the bits of
-// 2^23 reads as 2^23 + q*16^p; subtracting 2^23 + 8*16^p (exact) leaves
-// 16^p*(q - 8), and the per-block factor a*d*16^-p (or d*16^-p) turns it into
-// the weight's contribution.  Word w (columns 8t..8t+7 as nibbles 0..7) is
-// decoded as pairs (0,1) and (2,3) of w and of w >> 16, so only the positions
-// p = 0..3 and four constant pairs occur.
+// Nibble decoding (exact, one AND per weight): a word masked down to its
+// nibble q at bits 4p..4p+3 (p <= 3), read as an fp32 bit pattern, is the
+// subnormal number q * 16^p * 2^-149, exactly.  Multiplying it by
+// a' = (a * 2^64) * d in a fused multiply-add adds a*d*q*16^p*2^-85 with one
+// rounding: subnormal operands are taken at full precision (no flush to zero)
+// and, for |a*d| >= 2^-41, the product is a normal number.  The -8 of every
+// code is not applied per weight: C = sum a*d*q - 8 * sum a*d, and each
+// thread keeps sum a' for each of its blocks and subtracts 8 times it once,
+// after its last stage, when it also removes the power-of-two factors.
+// Preconditions: |a| and |a*d| below 2^64 (so that a' stays finite).  Word w
+// (columns 8t..8t+7 as nibbles 0..7) is decoded as pairs (0,1) and (2,3) of w
+// and of w >> 16, so only the positions p = 0..3 occur.
 //
 // The routed-expert kernels (KTransformers DeepSeek-V2 page, «优化三»: 6 of
 // 160 experts per token, run as batched GEMVs; «规则二»: gate -> top-k) reuse
@@ -108,104 +114,95 @@ __host__ __device__ inline SmemPlan smem_plan(int rows_per_split, int list_cap) 
 // ---------------------------------------------------------------------------
 // Consumer arithmetic
 // ---------------------------------------------------------------------------
-// Registers held across the main loop (loaded from the parameters so that the
-// compiler keeps them in registers instead of re-creating immediates):
-// the nibble masks 0xF << 4p, the bits of 2^23, and the bias pairs
-// -(2^23 + 8*16^p) in both halves, p = 0..3.
+// The nibble masks 0xF << 4p, p = 0..3, held in registers across the main
+// loop (loaded from the parameters so that the compiler does not re-create
+// immediates).
 struct DecodeConsts {
   uint32_t mask[4];
-  uint32_t magic;
-  f32x2 bias[4];
 };
 
 __device__ __forceinline__ DecodeConsts load_consts(const GemvParams& p) {
   DecodeConsts c;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    c.mask[i] = p.kmask[i];
-    c.bias[i] = dup2(p.kconst[i]);
-  }
-  c.magic = p.kmask[4];
+  for (int i = 0; i < 4; ++i) c.mask[i] = p.kmask[i];
   return c;
 }
 
-// (2^23 + q0*16^p, 2^23 + q1*16^p) for nibble p of words w0 and w1: one
-// three-input logic op per half, both written into one register pair.
-__device__ __forceinline__ f32x2 nib_pair(uint32_t w0, uint32_t w1, uint32_t mask,
-                                          uint32_t magic) {
+// The subnormals (q0 * 16^p * 2^-149, q1 * 16^p * 2^-149) of nibble p of
+// words w0 and w1: one AND per half, both written into one register pair.
+__device__ __forceinline__ f32x2 code_pair(uint32_t w0, uint32_t w1, uint32_t mask) {
   f32x2 r;
   asm("{\n\t.reg .b32 lo, hi;\n\t"
-      "lop3.b32 lo, %1, %3, %4, 0xEA;\n\t"   // (w0 & mask) | magic
-      "lop3.b32 hi, %2, %3, %4, 0xEA;\n\t"   // (w1 & mask) | magic
+      "and.b32 lo, %1, %3;\n\t"
+      "and.b32 hi, %2, %3;\n\t"
       "mov.b64 %0, {lo, hi};\n\t}"
       : "=l"(r)
-      : "r"(w0), "r"(w1), "r"(mask), "r"(magic));
+      : "r"(w0), "r"(w1), "r"(mask));
   return r;
 }
+
+// 2^64: the factor of the activations staged in shared memory.
+constexpr float kAScale = 18446744073709551616.0f;
 
 // Accumulator layout of one block (32 columns, 16 pairs): words t = 2h and
 // 2h + 1 are decoded together, nibble p of each forming a pair, so
 //   acc[8h + p]     holds columns (16h + p,     16h + 8 + p)
 //   acc[8h + 4 + p] holds columns (16h + 4 + p, 16h + 12 + p)
-// each scaled by 16^p; acc_col_pair() maps a pair back to its columns and
-// rescale_block() removes the power-of-two factors, which is exact.
+// each scaled by 16^p * 2^-85; acc_col_pair() maps a pair back to its columns
+// and finish_acc() removes the power-of-two factors (exact) and the -8.
 __device__ __forceinline__ int acc_col_pair(int j) {   // first column of pair j
   const int h = j >> 3, p = j & 3, hi = (j >> 2) & 1;
   return 16 * h + 4 * hi + p;                            // second column is +8
 }
 
-template <int MR>
-__device__ __forceinline__ void accumulate_block(f32x2* acc0, int acc_stride, uint32_t dbits,
+// Adds block bb of a staged row (scale bits dbits, codes qs) for MR rows of A
+// (a[m * a_ld], already times 2^64): acc[m][16bb + j] += a'_m * codes of pair
+// j, sad[m][bb] += a'_m.
+template <int MR, int BPT>
+__device__ __forceinline__ void accumulate_block(f32x2 (&acc)[MR][16 * BPT],
+                                                 float (&sad)[MR][BPT], int bb, uint32_t dbits,
                                                  const uint32_t (&qs)[4], const float* a,
                                                  int a_ld, const DecodeConsts& k) {
   const float d = fp16_bits_to_f32(dbits);
-  if constexpr (MR == 1) {
-    // acc += (a*d) * 16^p (q - 8)
-    const f32x2 ad = dup2(a[0] * d);
+  f32x2 ad[MR];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t w0 = qs[2 * h], w1 = qs[2 * h + 1];
-      const uint32_t y0 = w0 >> 16, y1 = w1 >> 16;
+  for (int m = 0; m < MR; ++m) {
+    const float x = a[m * a_ld] * d;
+    sad[m][bb] += x;
+    ad[m] = dup2(x);
+  }
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        f32x2* acc = acc0 + 8 * h;
-        acc[p] = fma2(ad, add2(nib_pair(w0, w1, k.mask[p], k.magic), k.bias[p]), acc[p]);
-        acc[4 + p] = fma2(ad, add2(nib_pair(y0, y1, k.mask[p], k.magic), k.bias[p]), acc[4 + p]);
-      }
-    }
-  } else {
-    // w' = d * 16^p (q - 8), exact; acc[m] += a_m * w'
-    const f32x2 dd = dup2(d);
-    f32x2 am[MR];
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t w0 = qs[2 * h], w1 = qs[2 * h + 1];
+    const uint32_t y0 = w0 >> 16, y1 = w1 >> 16;
 #pragma unroll
-    for (int m = 0; m < MR; ++m) am[m] = dup2(a[m * a_ld]);
+    for (int p = 0; p < 4; ++p) {
+      const f32x2 lo = code_pair(w0, w1, k.mask[p]);
+      const f32x2 hi = code_pair(y0, y1, k.mask[p]);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t w0 = qs[2 * h], w1 = qs[2 * h + 1];
-      const uint32_t y0 = w0 >> 16, y1 = w1 >> 16;
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const f32x2 wa = mul2(add2(nib_pair(w0, w1, k.mask[p], k.magic), k.bias[p]), dd);
-        const f32x2 wb = mul2(add2(nib_pair(y0, y1, k.mask[p], k.magic), k.bias[p]), dd);
-#pragma unroll
-        for (int m = 0; m < MR; ++m) {
-          f32x2* acc = acc0 + m * acc_stride + 8 * h;
-          acc[p] = fma2(am[m], wa, acc[p]);
-          acc[4 + p] = fma2(am[m], wb, acc[4 + p]);
-        }
+      for (int m = 0; m < MR; ++m) {
+        f32x2* acc0 = &acc[m][16 * bb + 8 * h];
+        acc0[p] = fma2(ad[m], lo, acc0[p]);
+        acc0[4 + p] = fma2(ad[m], hi, acc0[4 + p]);
       }
     }
   }
 }
 
-// Multiplies pair j of every block by 16^-p (p = j & 3): exact.
+// Turns the accumulators into sums of a*w: pair j of block bb becomes
+// acc * 2^(85 - 4p) - 8 * sad * 2^-64 (p = j & 3; the scalings are exact).
 template <int MR, int BPT>
-__device__ __forceinline__ void rescale_acc(f32x2 (&acc)[MR][16 * BPT]) {
-  const f32x2 sc[4] = {dup2(1.0f), dup2(0.0625f), dup2(0.00390625f), dup2(0.000244140625f)};
+__device__ __forceinline__ void finish_acc(f32x2 (&acc)[MR][16 * BPT],
+                                           const float (&sad)[MR][BPT]) {
+  const f32x2 sc[4] = {dup2(0x1p85f), dup2(0x1p81f), dup2(0x1p77f), dup2(0x1p73f)};
 #pragma unroll
   for (int m = 0; m < MR; ++m)
 #pragma unroll
-    for (int j = 0; j < 16 * BPT; ++j) acc[m][j] = mul2(acc[m][j], sc[j & 3]);
+    for (int bb = 0; bb < BPT; ++bb) {
+      const f32x2 corr = dup2(sad[m][bb] * -0x1p-61f);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[m][16 * bb + j] = fma2(acc[m][16 * bb + j], sc[j & 3], corr);
+    }
 }
 
 // The BPT consecutive blocks a thread owns in one staged row.  `off` is the
@@ -567,16 +564,21 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
         const size_t ai = arow * p.a_ld + k0 + r;
         v = (p.a_dtype == 0) ? reinterpret_cast<const float*>(p.A)[ai]
                              : bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.A)[ai]);
+        v *= kAScale;
       }
       a_s[m * a_ld_s + r] = v;
     }
     consumers_sync<MR>();
 
     f32x2 acc[MR][16 * BPT];
+    float sad[MR][BPT];
 #pragma unroll
-    for (int m = 0; m < MR; ++m)
+    for (int m = 0; m < MR; ++m) {
 #pragma unroll
       for (int i = 0; i < 16 * BPT; ++i) acc[m][i] = 0ull;
+#pragma unroll
+      for (int bb = 0; bb < BPT; ++bb) sad[m][bb] = 0.f;
+    }
 
     for (int s = group; s < nstages; s += Crew<MR>::kGroups) {
       const int gs = pass * nstages + s;   // the producer's stage counter
@@ -592,14 +594,14 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
         load_blocks<BPT>(row, boff, odd, dbits, qs);
 #pragma unroll
         for (int bb = 0; bb < BPT; ++bb)
-          accumulate_block<MR>(&acc[0][16 * bb], 16 * BPT, dbits[bb], qs[bb], a_s + r, a_ld_s, kc);
+          accumulate_block<MR, BPT>(acc, sad, bb, dbits[bb], qs[bb], a_s + r, a_ld_s, kc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
 
     // ---- reduce the 32 row phases ----
-    rescale_acc<MR, BPT>(acc);
+    finish_acc<MR, BPT>(acc, sad);
     float colv[MR][BPT];
     reduce_tile<MR, BPT>(acc, red, warp, lane, tid, colv);
 
@@ -804,12 +806,7 @@ int gemv_tile_blocks(int bpt) { return kLanesPerRow * bpt; }
 int gemv_stage_rows() { return kRowsPerStage; }
 
 void fill_decode_consts(GemvParams& p) {
-  p.kconst[0] = -(8388608.0f + 8.0f);       // -(2^23 + 8 * 16^0)
-  p.kconst[1] = -(8388608.0f + 128.0f);     // -(2^23 + 8 * 16^1)
-  p.kconst[2] = -(8388608.0f + 2048.0f);    // -(2^23 + 8 * 16^2)
-  p.kconst[3] = -(8388608.0f + 32768.0f);   // -(2^23 + 8 * 16^3)
   for (int i = 0; i < 4; ++i) p.kmask[i] = 0xFu << (4 * i);
-  p.kmask[4] = kMagic;                      // bits of 2^23
 }
 
 bool encode_weight_tmap(CUtensorMap* map, const void* base, int64_t K, int64_t nb,

@@ -26,8 +26,7 @@ struct GemvParams {
   // split-K tiling (grid.x = column tiles of 8*BPT blocks, grid.y = splits;
   // the splits of a tile form one thread-block cluster)
   int nsplit, rows_per_split;
-  float kconst[4];      // nibble-decoding constants (fill_decode_consts)
-  uint32_t kmask[5];
+  uint32_t kmask[4];    // nibble masks (fill_decode_consts)
   // activations
   const void* A;
   int a_dtype;          // 0 fp32, 1 bf16
