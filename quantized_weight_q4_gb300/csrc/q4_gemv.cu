@@ -53,21 +53,21 @@ namespace q4 {
 
 constexpr int kRowsPerStage = 32;   // rows of one TMA box
 constexpr int kLanesPerRow = 8;     // consumer lanes sharing one row
-constexpr int kGroupWarps = 8;      // a warp group covers one stage: 8 warps x 4 rows
+constexpr int kRowsPerThread = 2;   // rows of a stage each consumer thread decodes
+constexpr int kGroupWarps = 4;      // a warp group covers one stage: 4 warps x 4 rows x 2
 
-// Consumer warps: one group of 8 per ring stage in flight for compute.  With
-// one or two rows of A two groups alternate stages, which doubles the warps
-// that hide latency; four rows keep one group (their accumulators need the
+// Consumer warps: groups of 4 take the ring stages in turn.  One or two rows
+// of A: 16 warps (4 groups); four rows: 8 warps (their accumulators need the
 // registers).
 template <int MR>
 struct Crew {
-  static constexpr int kGroups = (MR <= 2) ? 2 : 1;
-  static constexpr int kWarps = kGroups * kGroupWarps;
+  static constexpr int kWarps = (MR <= 2) ? 16 : 8;
+  static constexpr int kGroups = kWarps / kGroupWarps;
   static constexpr int kConsumers = kWarps * 32;
   static constexpr int kThreads = kConsumers + 32;   // + producer warp
 };
-static_assert(kGroupWarps * 32 / kLanesPerRow == kRowsPerStage,
-              "a warp group handles one row per consumer thread per stage");
+static_assert(kGroupWarps * 32 / kLanesPerRow * kRowsPerThread == kRowsPerStage,
+              "a warp group handles kRowsPerThread rows per consumer thread per stage");
 
 template <int BPT>
 struct TileCfg {
@@ -296,7 +296,7 @@ __device__ __forceinline__ void consumers_sync() {
 }
 
 // ---------------------------------------------------------------------------
-// Reduction of the 32 row phases of a tile: warp shuffles (halving exchange
+// Reduction of the row phases of a tile: warp shuffles (halving exchange
 // over the four rows of a warp), then across warps through shared memory.
 // out[m][i] = column tid + 256*i of the tile for row m.
 // ---------------------------------------------------------------------------
@@ -540,7 +540,8 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
   const DecodeConsts kc = load_consts(p);
   const int pi = lane & 7;                                 // lane within its row
   const int group = warp / kGroupWarps;                    // stages s = group mod kGroups
-  const int rp = (warp % kGroupWarps) * 4 + (lane >> 3);   // row phase 0..31
+  // row phase 0..15: the thread decodes rows rp and rp + 16 of each stage
+  const int rp = (warp % kGroupWarps) * 4 + (lane >> 3);
   const uint32_t boff = static_cast<uint32_t>(pi * BPT * kBlockBytes);
   const bool odd = (boff & 2u) != 0;
   const int ncols = p.N;
@@ -587,20 +588,24 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
       // Rows past the slice need no check: they exist only past K, where the
       // stage holds zeros and the rows of A are zero too.
       const bool ready = wait_or_fail(&full[slot], (gs / T::kStages) & 1, s_fail, p.err);
-      const int r = s * kRowsPerStage + rp;   // row of the slice handled by this thread
       if (ready) {
-        const uint8_t* row = ring + slot * T::kStageBytes + rp * T::kRowBytes;
-        uint32_t dbits[BPT], qs[BPT][4];
-        load_blocks<BPT>(row, boff, odd, dbits, qs);
 #pragma unroll
-        for (int bb = 0; bb < BPT; ++bb)
-          accumulate_block<MR, BPT>(acc, sad, bb, dbits[bb], qs[bb], a_s + r, a_ld_s, kc);
+        for (int rr = 0; rr < kRowsPerThread; ++rr) {
+          const int rs = rp + rr * (kRowsPerStage / kRowsPerThread);   // row within the stage
+          const uint8_t* row = ring + slot * T::kStageBytes + rs * T::kRowBytes;
+          uint32_t dbits[BPT], qs[BPT][4];
+          load_blocks<BPT>(row, boff, odd, dbits, qs);
+          const float* a = a_s + s * kRowsPerStage + rs;
+#pragma unroll
+          for (int bb = 0; bb < BPT; ++bb)
+            accumulate_block<MR, BPT>(acc, sad, bb, dbits[bb], qs[bb], a, a_ld_s, kc);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
 
-    // ---- reduce the 32 row phases ----
+    // ---- reduce the row phases ----
     finish_acc<MR, BPT>(acc, sad);
     float colv[MR][BPT];
     reduce_tile<MR, BPT>(acc, red, warp, lane, tid, colv);
