@@ -27,6 +27,7 @@ constexpr int64_t kMinTensorRows = 8;
 
 struct GemvShape {
   int mr, bpt, nchunks, ntiles, nsplit, rows_per_split;
+  bool big;
 };
 
 struct MoeShape {
@@ -34,6 +35,7 @@ struct MoeShape {
   int nslots, nexp, list_cap;
   int bpt_gu, ntiles_gu, nsplit_gu, rows_gu;
   int bpt_d, ntiles_d, nsplit_d, rows_d;
+  bool big_gu, big_d;
   size_t off_h, off_y, total;
 };
 
@@ -100,12 +102,17 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // GEMV launch shape
 // ---------------------------------------------------------------------------
 // Rows per split for `nsplit` splits: a multiple of the TMA box height.
-int64_t split_rows(int64_t K, int64_t nsplit) {
+int64_t split_rows(int64_t K, int64_t nsplit, int bpt, bool big) {
   return static_cast<int64_t>(round_up(static_cast<size_t>(ceil_div(K, nsplit)),
-                                       q4::gemv_stage_rows()));
+                                       q4::gemv_stage_rows(bpt, big)));
 }
 
 constexpr double kCtaFixedBytes = 48.0 * 1024;
+// Slices of at least this many 18 KB stages stream with them; shorter slices
+// keep 32-row stages, which fill and drain the pipeline sooner.  With two or
+// four rows of A the decode per stage is longer and the 18 KB stages pay off
+// sooner (measured on GB300).
+int64_t big_min_stages(int mr) { return mr == 1 ? 16 : 4; }
 
 // Picks the blocks-per-thread and the split count (at most `max_split`; the
 // splits of a column tile form one cluster of `pair * nsplit` CTAs) that
@@ -114,24 +121,26 @@ constexpr double kCtaFixedBytes = 48.0 * 1024;
 // bytes per CTA plus its fixed cost.  Ties go to fewer CTAs.
 void choose_split(int mode, int mr, int list_cap, int64_t K, int64_t nb, int64_t z_groups, int pair,
                   int sms, int max_split, bool allow_bpt2, int* bpt_out, int* nsplit_out,
-                  int* rows_out, int* ntiles_out) {
+                  int* rows_out, int* ntiles_out, bool* big_out) {
   double best = -1.0;
   int64_t best_ctas = 0;
   *bpt_out = 1;
   *nsplit_out = 1;
-  *rows_out = static_cast<int>(split_rows(K, 1));
+  *big_out = false;
+  *rows_out = static_cast<int>(split_rows(K, 1, 1, false));
   *ntiles_out = static_cast<int>(ceil_div(nb, q4::gemv_tile_blocks(1)));
   for (int bpt = 2; bpt >= 1; --bpt) {
     if (bpt == 2 && !allow_bpt2) continue;
     const int64_t ntiles = ceil_div(nb, q4::gemv_tile_blocks(bpt));
     for (int64_t ns = 1; ns <= max_split; ++ns) {
-      const int64_t rows = split_rows(K, ns);
+      const int64_t rows = split_rows(K, ns, bpt, false);
       const int64_t nsplit = ceil_div(K, rows);
       if (nsplit != ns) continue;
       const int64_t csize = pair * nsplit;
       const int64_t clusters = ntiles * z_groups;
       const int64_t ctas = clusters * csize;
-      const int active = q4::max_active_clusters(mode, mr, bpt, static_cast<int>(rows), list_cap,
+      const int active = q4::max_active_clusters(mode, mr, bpt, false, static_cast<int>(rows),
+                                                 list_cap,
                                                  dim3(1, static_cast<unsigned>(nsplit),
                                                       static_cast<unsigned>(pair)));
       if (active <= 0) continue;
@@ -153,6 +162,20 @@ void choose_split(int mode, int mr, int list_cap, int64_t K, int64_t nb, int64_t
       }
     }
   }
+  // long slices: the same split with 18 KB stages, if it keeps its split count
+  // and its residency
+  const int bpt = *bpt_out;
+  const int64_t big_rows = q4::gemv_stage_rows(bpt, true);
+  if (*rows_out >= big_min_stages(mr) * big_rows) {
+    const int64_t rows = split_rows(K, *nsplit_out, bpt, true);
+    const dim3 cl(1, static_cast<unsigned>(*nsplit_out), static_cast<unsigned>(pair));
+    if (ceil_div(K, rows) == *nsplit_out &&
+        q4::max_active_clusters(mode, mr, bpt, true, static_cast<int>(rows), list_cap, cl) >=
+            q4::max_active_clusters(mode, mr, bpt, false, *rows_out, list_cap, cl)) {
+      *big_out = true;
+      *rows_out = static_cast<int>(rows);
+    }
+  }
 }
 
 GemvShape gemv_shape(int64_t M, int64_t N, int64_t K, int sms) {
@@ -161,7 +184,7 @@ GemvShape gemv_shape(int64_t M, int64_t N, int64_t K, int sms) {
   g.mr = (M == 1) ? 1 : (M == 2) ? 2 : 4;
   g.nchunks = static_cast<int>(ceil_div(M, g.mr));
   choose_split(q4::kModeGemv, g.mr, 0, K, nb, g.nchunks, 1, sms, q4::kMaxCluster, g.mr == 1,
-               &g.bpt, &g.nsplit, &g.rows_per_split, &g.ntiles);
+               &g.bpt, &g.nsplit, &g.rows_per_split, &g.ntiles, &g.big);
   return g;
 }
 
@@ -177,9 +200,10 @@ MoeShape moe_shape(int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I, int
   m.list_cap = static_cast<int>(m.nslots > ceil_div(E, 32) ? m.nslots : ceil_div(E, 32));
   // gate and up of one expert tile share a cluster: at most 8 splits each
   choose_split(q4::kModeGateUp, m.mr, m.list_cap, H, ceil_div(I, 32), m.nexp, 2, sms,
-               q4::kMaxCluster / 2, m.mr == 1, &m.bpt_gu, &m.nsplit_gu, &m.rows_gu, &m.ntiles_gu);
+               q4::kMaxCluster / 2, m.mr == 1, &m.bpt_gu, &m.nsplit_gu, &m.rows_gu, &m.ntiles_gu,
+               &m.big_gu);
   choose_split(q4::kModeDown, m.mr, m.list_cap, I, ceil_div(H, 32), m.nexp, 1, sms,
-               q4::kMaxCluster, m.mr == 1, &m.bpt_d, &m.nsplit_d, &m.rows_d, &m.ntiles_d);
+               q4::kMaxCluster, m.mr == 1, &m.bpt_d, &m.nsplit_d, &m.rows_d, &m.ntiles_d, &m.big_d);
   size_t o = 0;
   m.off_h = o;
   o += round_up(static_cast<size_t>(m.nslots) * I * 4, 256);
@@ -247,13 +271,15 @@ int moe_run(DeviceState* s, const MoeShape& m, float* out, const void* x, int x_
   p.nsplit = m.nsplit_gu;
   p.rows_per_split = m.rows_gu;
   p.use_tma = (p.nb % 8 == 0 && p.b_stride % 16 == 0 &&
-               q4::encode_weight_tmap(&p.tmap[0], W_gate, H, p.nb, E, p.b_stride, m.bpt_gu) &&
-               q4::encode_weight_tmap(&p.tmap[1], W_up, H, p.nb, E, p.b_stride, m.bpt_gu))
+               q4::encode_weight_tmap(&p.tmap[0], W_gate, H, p.nb, E, p.b_stride, m.bpt_gu,
+                                      m.big_gu) &&
+               q4::encode_weight_tmap(&p.tmap[1], W_up, H, p.nb, E, p.b_stride, m.bpt_gu,
+                                      m.big_gu))
                   ? 1 : 0;
   p.A = x;
   p.a_dtype = x_dtype;
   p.a_ld = H;
-  cudaError_t e = q4::launch_gemv(p, m.mr, m.bpt_gu, dim3(m.ntiles_gu, m.nsplit_gu, 2 * m.nexp),
+  cudaError_t e = q4::launch_gemv(p, m.mr, m.bpt_gu, m.big_gu, dim3(m.ntiles_gu, m.nsplit_gu, 2 * m.nexp),
                                   dim3(1, m.nsplit_gu, 2), st, true);
   if (e != cudaSuccess) return Q4_ERR_CUDA;
 
@@ -268,12 +294,12 @@ int moe_run(DeviceState* s, const MoeShape& m, float* out, const void* x, int x_
   p.nsplit = m.nsplit_d;
   p.rows_per_split = m.rows_d;
   p.use_tma = (p.nb % 8 == 0 && p.b_stride % 16 == 0 &&
-               q4::encode_weight_tmap(&p.tmap[0], W_down, I, p.nb, E, p.b_stride, m.bpt_d))
+               q4::encode_weight_tmap(&p.tmap[0], W_down, I, p.nb, E, p.b_stride, m.bpt_d, m.big_d))
                   ? 1 : 0;
   p.A = h;
   p.a_dtype = 0;
   p.a_ld = I;
-  e = q4::launch_gemv(p, m.mr, m.bpt_d, dim3(m.ntiles_d, m.nsplit_d, m.nexp),
+  e = q4::launch_gemv(p, m.mr, m.bpt_d, m.big_d, dim3(m.ntiles_d, m.nsplit_d, m.nexp),
                       dim3(1, m.nsplit_d, 1), st, true);
   if (e != cudaSuccess) return Q4_ERR_CUDA;
 
@@ -346,7 +372,7 @@ int q4_matmul_ex(void* C, int c_dtype, const void* A, int a_dtype, const void* B
   p.rows_per_split = g.rows_per_split;
   q4::fill_decode_consts(p);
   p.use_tma = (p.nb % 8 == 0 &&
-               q4::encode_weight_tmap(&p.tmap[0], B, K, p.nb, 1, K * p.nb * 18, g.bpt))
+               q4::encode_weight_tmap(&p.tmap[0], B, K, p.nb, 1, K * p.nb * 18, g.bpt, g.big))
                   ? 1 : 0;
   p.A = A;
   p.a_dtype = a_dtype;
@@ -357,7 +383,7 @@ int q4_matmul_ex(void* C, int c_dtype, const void* A, int a_dtype, const void* B
   p.list_cap = 0;
   p.err = s->status;
   const dim3 grid(g.ntiles, g.nsplit, g.nchunks);
-  return launch_status(q4::launch_gemv(p, g.mr, g.bpt, grid, dim3(1, g.nsplit, 1),
+  return launch_status(q4::launch_gemv(p, g.mr, g.bpt, g.big, grid, dim3(1, g.nsplit, 1),
                                        static_cast<cudaStream_t>(stream), true));
 }
 

@@ -8,7 +8,7 @@
 // How (GB300-first, not the page's CPU loop):
 //  * A CTA owns a column tile of 8*BPT blocks (256*BPT columns) and a
 //    contiguous slice of rows (split-K).  One producer warp streams the slice
-//    into a shared-memory ring, one 32-row box per TMA tensor copy
+//    into a shared-memory ring, one 18 KB box (64 or 128 rows) per TMA tensor copy
 //    (cp.async.bulk.tensor, completion on mbarriers); eight consumer warps
 //    decode nibbles in registers and accumulate in fp32 with packed fp32x2
 //    arithmetic.  Eight consecutive lanes share a row, each owning BPT
@@ -51,31 +51,35 @@
 
 namespace q4 {
 
-constexpr int kRowsPerStage = 32;   // rows of one TMA box
 constexpr int kLanesPerRow = 8;     // consumer lanes sharing one row
-constexpr int kRowsPerThread = 2;   // rows of a stage each consumer thread decodes
-constexpr int kGroupWarps = 4;      // a warp group covers one stage: 4 warps x 4 rows x 2
 
-// Consumer warps: groups of 4 take the ring stages in turn.  One or two rows
-// of A: 16 warps (4 groups); four rows: 8 warps (their accumulators need the
-// registers).
+// Consumer warps: one or two rows of A, 16 warps; four rows, 8 warps (their
+// accumulators need the registers).  They work in groups that take the ring
+// stages in turn (TileCfg).
 template <int MR>
 struct Crew {
   static constexpr int kWarps = (MR <= 2) ? 16 : 8;
-  static constexpr int kGroups = kWarps / kGroupWarps;
   static constexpr int kConsumers = kWarps * 32;
   static constexpr int kThreads = kConsumers + 32;   // + producer warp
 };
-static_assert(kGroupWarps * 32 / kLanesPerRow * kRowsPerThread == kRowsPerStage,
-              "a warp group handles kRowsPerThread rows per consumer thread per stage");
 
-template <int BPT>
+// A stage is one TMA box.  Long slices use 18 KB boxes (BIG): bulk copies of
+// that size keep HBM near its copy bandwidth from 128 SMs, where 9 KB boxes
+// reach about two thirds of it (measured on GB300, data movement alone).
+// Short slices use 32-row boxes: fewer rows per stage fill and drain the
+// pipeline sooner.  Either way the ring holds ~147 KB.
+template <int BPT, bool BIG>
 struct TileCfg {
-  static constexpr int kBlocks = kLanesPerRow * BPT;              // blocks per column tile
-  static constexpr int kCols = kBlocks * kBlockCols;              // 256 * BPT
-  static constexpr int kRowBytes = kBlocks * kBlockBytes;         // 144 * BPT
-  static constexpr int kStageBytes = kRowsPerStage * kRowBytes;   // 4608 * BPT
-  static constexpr int kStages = (BPT == 1) ? 32 : 16;            // ~147 KB in flight
+  static constexpr int kBlocks = kLanesPerRow * BPT;                // blocks per column tile
+  static constexpr int kCols = kBlocks * kBlockCols;                // 256 * BPT
+  static constexpr int kRowBytes = kBlocks * kBlockBytes;           // 144 * BPT
+  static constexpr int kRows = BIG ? 128 / BPT : 32;                // rows of one stage
+  static constexpr int kStageBytes = kRows * kRowBytes;
+  static constexpr int kStages = (147456 / kStageBytes);            // 8, 16 or 32
+  static constexpr int kGroupWarps = BIG ? 8 : 4;                   // warps sharing a stage
+  static constexpr int kGroupRows = kGroupWarps * 32 / kLanesPerRow;
+  static constexpr int kRowsPerThread = kRows / kGroupRows;         // per consumer thread per stage
+  static_assert(kRows % kGroupRows == 0, "a warp group covers a stage in whole passes");
   // TMA tensor copies need 128-byte-aligned shared destinations; a block's
   // word-aligned 20-byte read ends at most at the row's last byte, so rows
   // carry no padding.
@@ -97,16 +101,16 @@ struct SmemPlan {
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-template <int MR, int BPT>
+template <int MR, int BPT, bool BIG>
 __host__ __device__ inline SmemPlan smem_plan(int rows_per_split, int list_cap) {
-  using T = TileCfg<BPT>;
+  using T = TileCfg<BPT, BIG>;
   SmemPlan p;
   p.ring = 0;   // the dynamic shared-memory base is 128-byte aligned
   p.red = align_up(T::kStages * T::kStageBytes, 16);
   p.cpart = p.red + Crew<MR>::kWarps * MR * kRedStride<BPT> * 4;
   p.bars = p.cpart + MR * (T::kCols + 2 * kMaxCluster) * 4;   // partials received from the cluster
   p.a = p.bars + 2 * T::kStages * 8;
-  p.list = align_up(p.a + MR * align_up(rows_per_split, kRowsPerStage) * 4, 16);
+  p.list = align_up(p.a + MR * align_up(rows_per_split, T::kRows) * 4, 16);
   p.total = align_up(p.list + list_cap * 4 + 64, 128);
   return p;
 }
@@ -259,13 +263,13 @@ struct StreamDesc {
   int k0, rows;       // row slice
 };
 
-template <int BPT>
+template <int BPT, bool BIG>
 __device__ __forceinline__ void produce_stage(const StreamDesc& sd, int s, uint8_t* stage,
                                               uint64_t* full, int lane) {
-  using T = TileCfg<BPT>;
-  const int r0 = s * kRowsPerStage;
+  using T = TileCfg<BPT, BIG>;
+  const int r0 = s * T::kRows;
   if (sd.tmap) {
-    // one box of 32 rows x 144*BPT bytes; rows past K and blocks past the row
+    // one box of kRows rows x 144*BPT bytes; rows past K and blocks past the row
     // read as zero (a slice is a whole number of boxes, except the last one,
     // which ends at K)
     if (lane == 0) {
@@ -276,9 +280,9 @@ __device__ __forceinline__ void produce_stage(const StreamDesc& sd, int s, uint8
     // 2-byte aligned rows: copy with 16-bit loads (every block offset is even);
     // rows past the slice and blocks past the row are written as zeros, as
     // the tensor copy does, so that the consumers need no bounds checks
-    const int nr = min(kRowsPerStage, sd.rows - r0);
+    const int nr = min(T::kRows, sd.rows - r0);
     const int halves = sd.tb * (kBlockBytes / 2);
-    for (int r = 0; r < kRowsPerStage; ++r) {
+    for (int r = 0; r < T::kRows; ++r) {
       const uint16_t* src = reinterpret_cast<const uint16_t*>(
           sd.B + (static_cast<size_t>(sd.k0 + r0 + r) * sd.nb + sd.b0) * kBlockBytes);
       uint16_t* dst = reinterpret_cast<uint16_t*>(stage + r * T::kRowBytes);
@@ -303,7 +307,6 @@ __device__ __forceinline__ void consumers_sync() {
 template <int MR, int BPT>
 __device__ __forceinline__ void reduce_tile(f32x2 (&acc)[MR][16 * BPT], float* red, int warp,
                                             int lane, int tid, float (&out)[MR][BPT]) {
-  using T = TileCfg<BPT>;
   constexpr int P = 16 * BPT;   // pairs per thread
   const bool hi16 = (lane & 16) != 0;
   const bool hi8 = (lane & 8) != 0;
@@ -418,12 +421,13 @@ __device__ __forceinline__ void store_out(const GemvParams& p, size_t i, float v
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int MODE, int MR, int BPT>
+template <int MODE, int MR, int BPT, bool BIG>
 __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
     q4_gemv_kernel(const __grid_constant__ GemvParams p) {
-  using T = TileCfg<BPT>;
+  using T = TileCfg<BPT, BIG>;
+  constexpr int kGroups = Crew<MR>::kWarps / T::kGroupWarps;
   extern __shared__ __align__(128) uint8_t smem[];
-  const SmemPlan plan = smem_plan<MR, BPT>(p.rows_per_split, p.list_cap);
+  const SmemPlan plan = smem_plan<MR, BPT, BIG>(p.rows_per_split, p.list_cap);
   uint8_t* ring = smem + plan.ring;
   float* red = reinterpret_cast<float*>(smem + plan.red);
   float* cpart = reinterpret_cast<float*>(smem + plan.cpart);
@@ -487,7 +491,7 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
   const int tb = min(T::kBlocks, p.nb - b0);
   const int k0 = split * p.rows_per_split;
   const int rows = min(p.rows_per_split, p.K - k0);
-  const int nstages = (rows + kRowsPerStage - 1) / kRowsPerStage;
+  const int nstages = (rows + T::kRows - 1) / T::kRows;
   const int m_begin = (MODE == kModeGemv) ? z * MR : 0;
   const int passes = (MODE == kModeGemv) ? 1 : (nrows_total + MR - 1) / MR;
   if (rows <= 0 || passes <= 0) return;
@@ -495,7 +499,7 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < T::kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kGroupWarps);
+      mbar_init(&empty[i], T::kGroupWarps);
     }
     *s_fail = 0;
     fence_barrier_init();
@@ -526,7 +530,7 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
           failed = !__shfl_sync(0xffffffffu, ok ? 1 : 0, 0);   // failed: issue nothing more
           if (failed) break;
         }
-        produce_stage<BPT>(sd, s, ring + slot * T::kStageBytes, &full[slot], lane);
+        produce_stage<BPT, BIG>(sd, s, ring + slot * T::kStageBytes, &full[slot], lane);
       }
       // the cluster barriers of this pass's combine (see the consumers)
       cluster_sync();
@@ -539,14 +543,14 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
   pdl_wait();   // A (and the workspace) may belong to the previous kernel
   const DecodeConsts kc = load_consts(p);
   const int pi = lane & 7;                                 // lane within its row
-  const int group = warp / kGroupWarps;                    // stages s = group mod kGroups
-  // row phase 0..15: the thread decodes rows rp and rp + 16 of each stage
-  const int rp = (warp % kGroupWarps) * 4 + (lane >> 3);
+  const int group = warp / T::kGroupWarps;                 // stages s = group mod kGroups
+  // row phase: the thread decodes rows rp, rp + kGroupRows, ... of each stage
+  const int rp = (warp % T::kGroupWarps) * 4 + (lane >> 3);
   const uint32_t boff = static_cast<uint32_t>(pi * BPT * kBlockBytes);
   const bool odd = (boff & 2u) != 0;
   const int ncols = p.N;
   const int tile_cols = tb * kBlockCols;
-  const int a_ld_s = nstages * kRowsPerStage;   // rows of A in shared memory, stage-padded
+  const int a_ld_s = nstages * T::kRows;   // rows of A in shared memory, stage-padded
 
   for (int pass = 0; pass < passes; ++pass) {
     // ---- rows of A for this pass, as fp32 in shared memory ----
@@ -581,7 +585,7 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
       for (int bb = 0; bb < BPT; ++bb) sad[m][bb] = 0.f;
     }
 
-    for (int s = group; s < nstages; s += Crew<MR>::kGroups) {
+    for (int s = group; s < nstages; s += kGroups) {
       const int gs = pass * nstages + s;   // the producer's stage counter
       const int slot = gs % T::kStages;
       // every lane waits on the stage itself (no divergence, no broadcast).
@@ -589,13 +593,14 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
       // stage holds zeros and the rows of A are zero too.
       const bool ready = wait_or_fail(&full[slot], (gs / T::kStages) & 1, s_fail, p.err);
       if (ready) {
-#pragma unroll
-        for (int rr = 0; rr < kRowsPerThread; ++rr) {
-          const int rs = rp + rr * (kRowsPerStage / kRowsPerThread);   // row within the stage
+        // two rows at a time: more would keep too many words live for MR > 1
+#pragma unroll 2
+        for (int rr = 0; rr < T::kRowsPerThread; ++rr) {
+          const int rs = rp + rr * T::kGroupRows;   // row within the stage
           const uint8_t* row = ring + slot * T::kStageBytes + rs * T::kRowBytes;
           uint32_t dbits[BPT], qs[BPT][4];
           load_blocks<BPT>(row, boff, odd, dbits, qs);
-          const float* a = a_s + s * kRowsPerStage + rs;
+          const float* a = a_s + s * T::kRows + rs;
 #pragma unroll
           for (int bb = 0; bb < BPT; ++bb)
             accumulate_block<MR, BPT>(acc, sad, bb, dbits[bb], qs[bb], a, a_ld_s, kc);
@@ -693,18 +698,18 @@ __global__ void __launch_bounds__(256) q4_moe_combine_kernel(float* out, const f
 // ---------------------------------------------------------------------------
 // Host-side launch helpers
 // ---------------------------------------------------------------------------
-template <int MODE, int MR, int BPT>
+template <int MODE, int MR, int BPT, bool BIG>
 static cudaError_t launch_cfg(const GemvParams& p, dim3 grid, dim3 cluster, cudaStream_t st,
                               bool pdl) {
-  const SmemPlan plan = smem_plan<MR, BPT>(p.rows_per_split, p.list_cap);
-  cudaError_t e = cudaFuncSetAttribute(q4_gemv_kernel<MODE, MR, BPT>,
+  const SmemPlan plan = smem_plan<MR, BPT, BIG>(p.rows_per_split, p.list_cap);
+  cudaError_t e = cudaFuncSetAttribute(q4_gemv_kernel<MODE, MR, BPT, BIG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(plan.total));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(q4_gemv_kernel<MODE, MR, BPT>,
+  e = cudaFuncSetAttribute(q4_gemv_kernel<MODE, MR, BPT, BIG>,
                            cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(q4_gemv_kernel<MODE, MR, BPT>,
+  e = cudaFuncSetAttribute(q4_gemv_kernel<MODE, MR, BPT, BIG>,
                            cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -721,50 +726,64 @@ static cudaError_t launch_cfg(const GemvParams& p, dim3 grid, dim3 cluster, cuda
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, q4_gemv_kernel<MODE, MR, BPT>, p);
+  return cudaLaunchKernelEx(&cfg, q4_gemv_kernel<MODE, MR, BPT, BIG>, p);
 }
 
-template <int MODE>
+template <int MODE, bool BIG>
 static cudaError_t launch_mode(const GemvParams& p, int mr, int bpt, dim3 grid, dim3 cluster,
                                cudaStream_t st, bool pdl) {
-  if (bpt == 2 && mr == 1) return launch_cfg<MODE, 1, 2>(p, grid, cluster, st, pdl);
-  if (bpt == 1 && mr == 1) return launch_cfg<MODE, 1, 1>(p, grid, cluster, st, pdl);
-  if (bpt == 1 && mr == 2) return launch_cfg<MODE, 2, 1>(p, grid, cluster, st, pdl);
-  if (bpt == 1 && mr == 4) return launch_cfg<MODE, 4, 1>(p, grid, cluster, st, pdl);
+  if (bpt == 2 && mr == 1) return launch_cfg<MODE, 1, 2, BIG>(p, grid, cluster, st, pdl);
+  if (bpt == 1 && mr == 1) return launch_cfg<MODE, 1, 1, BIG>(p, grid, cluster, st, pdl);
+  if (bpt == 1 && mr == 2) return launch_cfg<MODE, 2, 1, BIG>(p, grid, cluster, st, pdl);
+  if (bpt == 1 && mr == 4) return launch_cfg<MODE, 4, 1, BIG>(p, grid, cluster, st, pdl);
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_gemv(const GemvParams& p, int mr, int bpt, dim3 grid, dim3 cluster,
-                        cudaStream_t st, bool pdl) {
+template <bool BIG>
+static cudaError_t launch_big(const GemvParams& p, int mr, int bpt, dim3 grid, dim3 cluster,
+                              cudaStream_t st, bool pdl) {
   switch (p.mode) {
-    case kModeGemv: return launch_mode<kModeGemv>(p, mr, bpt, grid, cluster, st, pdl);
-    case kModeGateUp: return launch_mode<kModeGateUp>(p, mr, bpt, grid, cluster, st, pdl);
-    case kModeDown: return launch_mode<kModeDown>(p, mr, bpt, grid, cluster, st, pdl);
+    case kModeGemv: return launch_mode<kModeGemv, BIG>(p, mr, bpt, grid, cluster, st, pdl);
+    case kModeGateUp: return launch_mode<kModeGateUp, BIG>(p, mr, bpt, grid, cluster, st, pdl);
+    case kModeDown: return launch_mode<kModeDown, BIG>(p, mr, bpt, grid, cluster, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
 
-int max_active_clusters(int mode, int mr, int bpt, int rows_per_split, int list_cap,
-                        dim3 cluster) {
-  // occupancy query for the kernel instance that launch_gemv would pick
-  const void* fn = nullptr;
-#define Q4_PICK(MO)                                                            \
-  if (mode == MO) {                                                            \
-    if (bpt == 2 && mr == 1) fn = (const void*)q4_gemv_kernel<MO, 1, 2>;       \
-    else if (bpt == 1 && mr == 1) fn = (const void*)q4_gemv_kernel<MO, 1, 1>;  \
-    else if (bpt == 1 && mr == 2) fn = (const void*)q4_gemv_kernel<MO, 2, 1>;  \
-    else if (bpt == 1 && mr == 4) fn = (const void*)q4_gemv_kernel<MO, 4, 1>;  \
+cudaError_t launch_gemv(const GemvParams& p, int mr, int bpt, bool big, dim3 grid, dim3 cluster,
+                        cudaStream_t st, bool pdl) {
+  return big ? launch_big<true>(p, mr, bpt, grid, cluster, st, pdl)
+             : launch_big<false>(p, mr, bpt, grid, cluster, st, pdl);
+}
+
+template <bool BIG>
+static void pick_instance(int mode, int mr, int bpt, int rows_per_split, int list_cap,
+                          const void** fn, uint32_t* smem) {
+#define Q4_PICK(MO)                                                                 \
+  if (mode == MO) {                                                                 \
+    if (bpt == 2 && mr == 1) *fn = (const void*)q4_gemv_kernel<MO, 1, 2, BIG>;      \
+    else if (bpt == 1 && mr == 1) *fn = (const void*)q4_gemv_kernel<MO, 1, 1, BIG>; \
+    else if (bpt == 1 && mr == 2) *fn = (const void*)q4_gemv_kernel<MO, 2, 1, BIG>; \
+    else if (bpt == 1 && mr == 4) *fn = (const void*)q4_gemv_kernel<MO, 4, 1, BIG>; \
   }
   Q4_PICK(kModeGemv)
   Q4_PICK(kModeGateUp)
   Q4_PICK(kModeDown)
 #undef Q4_PICK
-  if (!fn) return 0;
+  if (bpt == 2) *smem = smem_plan<1, 2, BIG>(rows_per_split, list_cap).total;
+  else if (mr == 1) *smem = smem_plan<1, 1, BIG>(rows_per_split, list_cap).total;
+  else if (mr == 2) *smem = smem_plan<2, 1, BIG>(rows_per_split, list_cap).total;
+  else *smem = smem_plan<4, 1, BIG>(rows_per_split, list_cap).total;
+}
+
+int max_active_clusters(int mode, int mr, int bpt, bool big, int rows_per_split, int list_cap,
+                        dim3 cluster) {
+  // occupancy query for the kernel instance that launch_gemv would pick
+  const void* fn = nullptr;
   uint32_t smem = 0;
-  if (bpt == 2) smem = smem_plan<1, 2>(rows_per_split, list_cap).total;
-  else if (mr == 1) smem = smem_plan<1, 1>(rows_per_split, list_cap).total;
-  else if (mr == 2) smem = smem_plan<2, 1>(rows_per_split, list_cap).total;
-  else smem = smem_plan<4, 1>(rows_per_split, list_cap).total;
+  if (big) pick_instance<true>(mode, mr, bpt, rows_per_split, list_cap, &fn, &smem);
+  else pick_instance<false>(mode, mr, bpt, rows_per_split, list_cap, &fn, &smem);
+  if (!fn) return 0;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return 0;
   cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -808,14 +827,17 @@ cudaError_t launch_moe_combine(float* out, const float* y, const int32_t* idx, c
 
 int gemv_tile_blocks(int bpt) { return kLanesPerRow * bpt; }
 
-int gemv_stage_rows() { return kRowsPerStage; }
+int gemv_stage_rows(int bpt, bool big) {
+  if (big) return bpt == 2 ? TileCfg<2, true>::kRows : TileCfg<1, true>::kRows;
+  return bpt == 2 ? TileCfg<2, false>::kRows : TileCfg<1, false>::kRows;
+}
 
 void fill_decode_consts(GemvParams& p) {
   for (int i = 0; i < 4; ++i) p.kmask[i] = 0xFu << (4 * i);
 }
 
 bool encode_weight_tmap(CUtensorMap* map, const void* base, int64_t K, int64_t nb,
-                        int64_t experts, int64_t matrix_bytes, int bpt) {
+                        int64_t experts, int64_t matrix_bytes, int bpt, bool big) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -828,13 +850,13 @@ bool encode_weight_tmap(CUtensorMap* map, const void* base, int64_t K, int64_t n
   }
   if (nb % kLanesPerRow != 0) return false;
   // uint16 elements: a row is nb*9 halfwords; a box is one tile row segment
-  // (8*bpt blocks = 72*bpt halfwords) by kRowsPerStage rows.
+  // (8*bpt blocks = 72*bpt halfwords) by the stage's rows.
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(nb * 9), static_cast<cuuint64_t>(K),
                               static_cast<cuuint64_t>(experts)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(nb * kBlockBytes),
                                  static_cast<cuuint64_t>(matrix_bytes)};
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(kLanesPerRow * bpt * 9),
-                             static_cast<cuuint32_t>(kRowsPerStage), 1u};
+                             static_cast<cuuint32_t>(gemv_stage_rows(bpt, big)), 1u};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims,
                             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

@@ -44,17 +44,19 @@ struct GemvParams {
   unsigned* err;        // device status word
 };
 
-// mr: rows of A per pass (1, 2 or 4); bpt: blocks per thread (1 or 2; 2 only with mr 1).
+// mr: rows of A per pass (1, 2 or 4); bpt: blocks per thread (1 or 2; 2 only with mr 1);
+// big: 18 KB pipeline stages instead of 32-row ones (rows_per_split a multiple of
+// gemv_stage_rows(bpt, big) either way).
 // cluster: (1, nsplit, 1), or (1, nsplit, 2) for the gate/up kernel.
-cudaError_t launch_gemv(const GemvParams& p, int mr, int bpt, dim3 grid, dim3 cluster,
+cudaError_t launch_gemv(const GemvParams& p, int mr, int bpt, bool big, dim3 grid, dim3 cluster,
                         cudaStream_t st, bool pdl);
 constexpr int kMaxCluster = 16;   // non-portable thread-block cluster size limit
 // Clusters of shape `cluster` that can be resident at once for that kernel
 // configuration (0 if the configuration cannot launch).
-int max_active_clusters(int mode, int mr, int bpt, int rows_per_split, int list_cap,
+int max_active_clusters(int mode, int mr, int bpt, bool big, int rows_per_split, int list_cap,
                         dim3 cluster);
 // Rows of one TMA box (one pipeline stage) of the GEMV kernel.
-int gemv_stage_rows();
+int gemv_stage_rows(int bpt, bool big);
 // Blocks per column tile for `bpt` blocks per thread.
 int gemv_tile_blocks(int bpt);
 void fill_decode_consts(GemvParams& p);
@@ -62,7 +64,7 @@ void fill_decode_consts(GemvParams& p);
 // `matrix_bytes` apart, with boxes of one tile row segment (8*bpt blocks) by one
 // stage of rows.  Needs nb % 8 == 0 and a 16-byte aligned base.
 bool encode_weight_tmap(CUtensorMap* map, const void* base, int64_t K, int64_t nb,
-                        int64_t experts, int64_t matrix_bytes, int bpt);
+                        int64_t experts, int64_t matrix_bytes, int bpt, bool big);
 // out[t] = sum_k w[t,k] * y[t*topk+k] (slot order), plus addend[t] if given.
 cudaError_t launch_moe_combine(float* out, const float* y, const int32_t* idx, const float* w,
                                const float* addend, int T, int topk, int E, int H,
