@@ -12,8 +12,11 @@ GEMV, fp32 A, default K = N = 4096, --m/--k/--n), ``batched`` (K = 5120,
 N = 12288, bf16 A with --m rows), ``moe`` (top-6 of 160 experts, H = 5120,
 I = 1536, --tokens), ``moe_block`` (router + shared expert + routed experts
 of the same block, --tokens), ``quantize`` (the Q4_0 encoder on a fp32
---k x --n matrix; GB/s of input plus output), ``prefill`` (M = 2048, K = 5120, N = 12288, bf16 A and
-C on the tensor cores; metric TFLOP/s).  Weight copies or routings rotate so
+--k x --n matrix; GB/s of input plus output), ``host_stream`` (the decode
+sweep with its weights in pinned host memory, copied into --slots device slots
+while earlier GEMVs run; roofline: the host-to-device copy rate measured in
+the same run), ``prefill`` (M = 2048, K = 5120, N = 12288, bf16 A and C on the
+tensor cores; metric TFLOP/s).  Weight copies or routings rotate so
 that each pass reads at least four times the L2 capacity.
 
 ``--impl reference`` times the fp64 CPU oracle on the host cores on a bounded
@@ -520,6 +523,8 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
                "l2": f"{R} seeded router-logit sets rotate over 160 experts",
                "parallelism": f"replicas x{ws}", "us_per_call": round(per_call * 1e6, 2)}
         units = R
+    elif args.workload == "host_stream":
+        return run_host_stream(args, ws, local, torch, q4, dev)
     elif args.workload == "prefill":
         M = args.m if args.m > 64 else 2048
         K = args.k if args.k else 5120
@@ -586,6 +591,84 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
     }
 
 
+def run_host_stream(args, ws, local, torch, q4, dev):
+    """The decode sweep with its weights in pinned host memory: each GEMV's
+    blocks cross the host link into a ring of device slots while earlier GEMVs
+    run (q4_matmul_host_stream), the whole sequence captured in a CUDA graph.
+    The roofline is the host-to-device copy rate measured in the same run."""
+    shapes, wbytes = sweep_plan(args.layers)
+    ops, keep = [], []
+    for i, (K, N) in enumerate(shapes):
+        Bh = torch.from_numpy(si.q4_weights(K, N, seed=0, stream=100 + i)).pin_memory()
+        A = torch.from_numpy(si.activations_f32(1, K, 0, 10000 + i)).to(dev)
+        C = torch.empty((1, N), dtype=torch.float32, device=dev)
+        ops.append((C, A, Bh, 1, N, K))
+        keep += [A, C]
+    slots = args.slots
+    staging = torch.empty(q4.q4_host_stream_slot_bytes(ops) * slots, dtype=torch.uint8, device=dev)
+    st, cp = torch.cuda.Stream(), torch.cuda.Stream()
+    # the link alone: pinned host -> device copies of the same bytes, back to back
+    big = max(K * si.nblocks(N) * 18 for K, N in shapes)
+    src = torch.empty(big, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(big, dtype=torch.uint8, device=dev)
+    n_copy = max(8, (1 << 30) // big)
+    for _ in range(3):
+        dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(cp):
+        e0.record()
+        for _ in range(n_copy):
+            dst.copy_(src, non_blocking=True)
+        e1.record()
+    e1.synchronize()
+    link_gbs = big * n_copy / (e0.elapsed_time(e1) / 1e3) / 1e9
+    # the sequence, captured once and replayed
+    q4.q4_matmul_host_stream(ops, staging, slots, stream=st, copy_stream=cp)
+    st.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        q4.q4_matmul_host_stream(ops, staging, slots, stream=st, copy_stream=cp)
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    barrier(ws)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(st):
+            e0.record()
+            for _ in range(args.steps):
+                g.replay()
+            e1.record()
+        e1.synchronize()
+    t = max_over_ranks(ws, e0.elapsed_time(e1) / 1e3)
+    barrier(ws)
+    status = q4.q4_get_device_status()
+    if status != q4.Q4_OK:
+        raise SystemExit(f"device status {status} after the timed region")
+    value = ws * wbytes * args.steps / t / 1e9
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t / args.steps * 1e3, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
+        "config": {"workload": "host_stream", "layers": args.layers, "gemvs_per_step": len(shapes),
+                   "weight_bytes_per_step": wbytes, "weights": "pinned host memory",
+                   "slots": slots, "slot_bytes": q4.q4_host_stream_slot_bytes(ops),
+                   "launch": "one CUDA graph: per GEMV a host-to-device copy on a copy stream "
+                             "and the GEMV from its slot, ordered by events",
+                   "l2": "no flush: each step copies 3.64 GB from the host",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"bound": "host link", "achieved": round(value / ws, 2),
+                     "peak": round(link_gbs, 2), "unit": "GB/s",
+                     "frac": round(value / ws / link_gbs, 4),
+                     "peak_source": f"measured in this run: {n_copy} pinned host-to-device "
+                                    f"copies of {big} B on one stream",
+                     "traffic": None},
+        "gpu_launches": args.steps * len(shapes), "clocks": clk.summary(),
+        "launches_per_step": len(shapes),
+    }
+
+
 # ---------------------------------------------------------------------------
 # reference arm: the oracle on the host cores
 # ---------------------------------------------------------------------------
@@ -641,6 +724,7 @@ def main():
     ap.add_argument("--cpu-layers", type=int, default=24)
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--slots", type=int, default=4, help="host_stream: device weight slots")
     ap.add_argument("--m", type=int, default=1, help="rows of A (gemv, batched)")
     ap.add_argument("--k", type=int, default=0)
     ap.add_argument("--n", type=int, default=0)

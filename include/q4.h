@@ -187,6 +187,49 @@ Q4_API size_t q4_planar_bytes(int64_t K, int64_t N);
 Q4_API int q4_dequant(float *W, const void *B, int64_t K, int64_t N, void *stream);
 Q4_API int q4_dequant_bf16(uint16_t *W, const void *B, int64_t K, int64_t N, void *stream);
 
+/*
+ * Host-streamed weights [AirLLM deep-dive page, §1.2: layers kept in pinned
+ * host memory and brought in by a worker while the GPU computes the previous
+ * one; §6: the packed quantised bytes cross the link, expansion on the GPU].
+ *
+ * q4_seq_op -- one matmul C = A . W of a sequence; C and A are DEVICE
+ * pointers as everywhere else, B is a PAGE-LOCKED HOST pointer
+ * (cudaHostAlloc / cudaHostRegister, e.g. torch pin_memory) to Q4_0 blocks.
+ */
+typedef struct q4_seq_op {
+  void *C;            /* device [M, N], c_dtype                 */
+  const void *A;      /* device [M, K], a_dtype                 */
+  const void *B;      /* pinned host, K x ceil(N/32) blocks      */
+  int64_t M, N, K;
+  int a_dtype, c_dtype;
+} q4_seq_op;
+
+/* Bytes of one staging slot for `ops`: the largest B, rounded up to 256.
+ * 0 if ops is NULL, n <= 0 or a size is <= 0. */
+Q4_API size_t q4_host_stream_slot_bytes(const q4_seq_op *ops, int n);
+
+/*
+ * q4_matmul_host_stream -- runs ops[0..n) in order on `stream`, each as
+ * q4_matmul_ex would (same kernels, same results bit for bit), with its
+ * weights copied from host memory into one of `slots` device slots of
+ * `staging` on `copy_stream` while earlier matmuls run.  Copy i reuses slot
+ * i % slots only after matmul i - slots has finished; matmul i waits for copy
+ * i.  `copy_stream` is forked from and joined back into `stream`: the
+ * sequence follows earlier work on `stream`, later work on `stream` follows
+ * it, and it can be captured into a CUDA graph.
+ *   staging      device buffer, 256-byte aligned, >= slots *
+ *                q4_host_stream_slot_bytes(ops, n) bytes (else
+ *                Q4_ERR_WORKSPACE); owned by the caller and in use until the
+ *                sequence completes.
+ *   slots        >= 1 (2 or more overlap copies with matmuls).
+ *   copy_stream  a stream other than `stream` (else Q4_ERR_ARG).
+ * Every op is checked before anything is enqueued: a B that is not
+ * page-locked host memory, or a bad size, gives Q4_ERR_ARG; dtype and
+ * alignment errors as in q4_matmul_ex.
+ */
+Q4_API int q4_matmul_host_stream(const q4_seq_op *ops, int n, void *staging, size_t staging_bytes,
+                                 int slots, void *stream, void *copy_stream);
+
 /* Synchronises `stream`, then reads and clears the device status word of the
  * current device: Q4_OK, Q4_ERR_DEVICE (bits in q4_last_device_flags()) or
  * Q4_ERR_CUDA. */

@@ -40,6 +40,14 @@ _i64 = ctypes.c_int64
 _sz = ctypes.c_size_t
 _int = ctypes.c_int
 
+
+class SeqOp(ctypes.Structure):
+    """q4_seq_op of include/q4.h: one matmul of a host-streamed sequence."""
+    _fields_ = [("C", ctypes.c_void_p), ("A", ctypes.c_void_p), ("B", ctypes.c_void_p),
+                ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("a_dtype", ctypes.c_int), ("c_dtype", ctypes.c_int)]
+
+
 # name -> (restype, argtypes), as declared in include/q4.h
 SIGNATURES = {
     "q4_matmul": (_int, [_vp, _vp, _vp, _i64, _i64, _i64]),
@@ -64,6 +72,8 @@ SIGNATURES = {
                             _vp, _vp, _vp, _i64, _vp, _sz, _vp]),
     "q4_moe_block_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _i64, _i64]),
     "q4_selftest_wait": (_int, [_i64, _int, _vp]),
+    "q4_host_stream_slot_bytes": (_sz, [ctypes.POINTER(SeqOp), _int]),
+    "q4_matmul_host_stream": (_int, [ctypes.POINTER(SeqOp), _int, _vp, _sz, _int, _vp, _vp]),
     "q4_get_device_status": (_int, [_vp]),
     "q4_last_device_flags": (ctypes.c_uint, []),
     "q4_status_str": (ctypes.c_char_p, [_int]),
@@ -155,6 +165,30 @@ def q4_matmul_ex(C, A, B, M: int, N: int, K: int, workspace=None, stream=None,
     _check("q4_matmul_ex", lib().q4_matmul_ex(
         _ptr(C), _dtype_code(C), _ptr(A), _dtype_code(A), _ptr(B), b_layout,
         M, N, K, _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def _seq_ops(ops):
+    """ops: list of (C, A, B_host, M, N, K): C and A CUDA tensors, B a pinned CPU tensor."""
+    arr = (SeqOp * len(ops))()
+    for i, (C, A, B, M, N, K) in enumerate(ops):
+        _require_cuda(C, A)
+        arr[i] = SeqOp(_ptr(C), _ptr(A), B.data_ptr(), M, N, K, _dtype_code(A), _dtype_code(C))
+    return arr
+
+
+def q4_host_stream_slot_bytes(ops) -> int:
+    return lib().q4_host_stream_slot_bytes(_seq_ops(ops), len(ops))
+
+
+def q4_matmul_host_stream(ops, staging, slots: int, stream=None, copy_stream=None) -> None:
+    """Runs ops [(C, A, B_host, M, N, K), ...] in order on `stream`, copying each
+    pinned host B into one of `slots` slots of the device buffer `staging` on
+    `copy_stream` while earlier matmuls run."""
+    _require_cuda(staging)
+    arr = _seq_ops(ops)
+    nbytes = staging.numel() * staging.element_size()
+    _check("q4_matmul_host_stream", lib().q4_matmul_host_stream(
+        arr, len(ops), _ptr(staging), nbytes, slots, _stream(stream), _stream(copy_stream)))
 
 
 def q4_matmul_workspace_size(M: int, N: int, K: int) -> int:

@@ -85,3 +85,26 @@ def test_argument_errors_on_host(L):
     # the failure-detection self-test checks its limit and mode before any CUDA call
     for limit, arrive in [(0, 0), (-5, 0), (2_000_000_000, 0), (1000, 2)]:
         assert L.q4_selftest_wait(limit, arrive, None) == q4.Q4_ERR_ARG
+
+
+def test_host_stream_checks_on_host(L):
+    """The host-streamed sequence checks every op before any CUDA call."""
+    vp = ctypes.c_void_p
+    good, bad = 0x10000, 0x10004
+    ops = (q4.SeqOp * 2)(q4.SeqOp(good, good, good, 1, 64, 32, 0, 0),
+                         q4.SeqOp(good, good, good, 2, 40, 96, 1, 0))
+    # slot: the larger B, 96 x 2 blocks x 18 = 3456 -> 3584 (256-byte rounding)
+    assert L.q4_host_stream_slot_bytes(ops, 2) == 3584
+    assert L.q4_host_stream_slot_bytes(ops, 0) == 0
+    s1, s2 = vp(0x1000), vp(0x2000)
+    assert L.q4_matmul_host_stream(None, 2, vp(good), 1 << 20, 2, s1, s2) == q4.Q4_ERR_ARG
+    assert L.q4_matmul_host_stream(ops, 2, vp(good), 1 << 20, 0, s1, s2) == q4.Q4_ERR_ARG
+    assert L.q4_matmul_host_stream(ops, 2, vp(good), 1 << 20, 2, s1, s1) == q4.Q4_ERR_ARG
+    assert L.q4_matmul_host_stream(ops, 2, vp(good + 16), 1 << 20, 2, s1, s2) == q4.Q4_ERR_ALIGN
+    assert L.q4_matmul_host_stream(ops, 2, vp(good), 3584, 2, s1, s2) == q4.Q4_ERR_WORKSPACE
+    ops[1].K = 0
+    assert L.q4_matmul_host_stream(ops, 2, vp(good), 1 << 20, 2, s1, s2) == q4.Q4_ERR_ARG
+    ops[1].K, ops[1].a_dtype = 96, 3
+    assert L.q4_matmul_host_stream(ops, 2, vp(good), 1 << 20, 2, s1, s2) == q4.Q4_ERR_DTYPE
+    ops[1].a_dtype, ops[1].C = 1, bad
+    assert L.q4_matmul_host_stream(ops, 2, vp(good), 1 << 20, 2, s1, s2) == q4.Q4_ERR_ALIGN
