@@ -60,6 +60,8 @@ def bind(path: str) -> ctypes.CDLL:
     L.q4o_f64_to_fp16.argtypes = [ctypes.c_double]
     L.q4o_f64_to_fp16.restype = ctypes.c_uint16
     L.q4o_quantize.argtypes = [vp, ctypes.c_int, c_i64, c_i64, vp]
+    L.q4o_q8_dequant_f32.argtypes = [vp, c_i64, c_i64, vp]
+    L.q4o_q8_matmul.argtypes = [vp, ctypes.c_int, vp, c_i64, c_i64, c_i64, vp, vp]
     L.q4o_moe_block.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, c_i64, c_i64, c_i64, c_i64, c_i64,
                                 vp, vp, vp, c_i64, vp, vp, vp, vp]
     L.q4o_moe.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, vp,
@@ -148,6 +150,24 @@ def matmul(A: np.ndarray, B: np.ndarray, M: int, N: int, K: int, with_abs: bool 
     C = np.empty((M, N), dtype=np.float64)
     S = np.empty((M, N), dtype=np.float64) if with_abs else None
     lib().q4o_matmul(_p(A), dt, _p(B), M, N, K, _p(C), _p(S))
+    return C, S
+
+
+def q8_dequant_f32(B: np.ndarray, K: int, N: int) -> np.ndarray:
+    """Q8_0 blocks (34 bytes: fp16 d, int8 q[32]) -> W [K, N] fp32 = q * d."""
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    W = np.empty((K, N), dtype=np.float32)
+    lib().q4o_q8_dequant_f32(_p(B), K, N, _p(W))
+    return W
+
+
+def q8_matmul(A: np.ndarray, B: np.ndarray, M: int, N: int, K: int, with_abs: bool = True):
+    """(C64 [M,N], S [M,N] or None) for Q8_0 weights."""
+    A, dt = _act(A)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    C = np.empty((M, N), dtype=np.float64)
+    S = np.empty((M, N), dtype=np.float64) if with_abs else None
+    lib().q4o_q8_matmul(_p(A), dt, _p(B), M, N, K, _p(C), _p(S))
     return C, S
 
 

@@ -21,6 +21,9 @@
  * at most 24 significant bits, w = (q-8)*d at most 15), so the only error of
  * the oracle is the fp64 summation, at most about K*2^-53*sum|a*w|.
  *
+ * Q8_0 (q4o_q8_*): [Eng §2.1-§2.2] names the format but prints no layout;
+ * the reading used here is stated beside the functions.
+ *
  * Pins: every function here is pinned by a CPU test against something other
  * than itself (library conversions over all 65536 codes, hand-built blocks,
  * exact rational sums, one-hot and zero cases, linearity, padding invariance,
@@ -543,6 +546,63 @@ void q4o_quantize(const void *W, int w_dtype, int64_t K, int64_t N, uint8_t *B)
                     blk[2 + l / 2] = (uint8_t)q;
                 else
                     blk[2 + l / 2] |= (uint8_t)(q << 4);
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Q8_0 (a second format behind the same interface)                    */
+/* ------------------------------------------------------------------ */
+/* [Eng §2.1-§2.2] names Q8_0 beside Q4_0 (8-bit codes, about 60% of Q4_0's
+ * decode speed on its CPU) but prints no layout for it.  Reading, by analogy
+ * with the page's block_q4_0 and its §2.3 layout: a block is { fp16 d
+ * (little-endian); int8 q[32] } = 34 bytes covering 32 consecutive output
+ * columns of one row k; K rows of nb = ceil(N/32) blocks; element l of a block
+ * is the two's-complement byte q[l]; W[k, 32b + l] = q * d.  Columns >= N are
+ * padding and never read into an output. */
+#define QO_Q8_BYTES 34
+
+static double q8_weight_at(const uint8_t *B, int64_t nb, int64_t k, int64_t j)
+{
+    const uint8_t *blk = B + (k * nb + j / QO_BLOCK) * QO_Q8_BYTES;
+    int q = (int)blk[2 + j % QO_BLOCK];
+    if (q >= 128)
+        q -= 256;                          /* two's complement */
+    return (double)q * block_scale(blk);
+}
+
+/* W [K, N] fp32 = q * d: at most 8 x 11 significant bits, exact in fp32. */
+void q4o_q8_dequant_f32(const uint8_t *B, int64_t K, int64_t N, float *W)
+{
+    int64_t nb = (N + QO_BLOCK - 1) / QO_BLOCK;
+    for (int64_t k = 0; k < K; k++)
+        for (int64_t j = 0; j < N; j++)
+            W[k * N + j] = (float)q8_weight_at(B, nb, k, j);
+}
+
+/* C [M, N] = A . W for Q8_0 weights, S = sum_k |A[i,k] * W[k,j]| (may be
+ * NULL), in fp64 with the k -> block -> l order of [Eng §3.4].  Each product
+ * is exact in fp64 (24 + 19 bits). */
+void q4o_q8_matmul(const void *A, int a_dtype, const uint8_t *B,
+                   int64_t M, int64_t N, int64_t K, double *C, double *S)
+{
+    int64_t nb = (N + QO_BLOCK - 1) / QO_BLOCK;
+    for (int64_t i = 0; i < M; i++) {
+        double *c = C + i * N;
+        double *s = S ? S + i * N : NULL;
+        for (int64_t j = 0; j < N; j++) {
+            c[j] = 0.0;
+            if (s)
+                s[j] = 0.0;
+        }
+        for (int64_t k = 0; k < K; k++) {
+            double av = act_at(A, a_dtype, i * K + k);
+            for (int64_t j = 0; j < N; j++) {
+                double p = av * q8_weight_at(B, nb, k, j);
+                c[j] += p;
+                if (s)
+                    s[j] += fabs(p);
             }
         }
     }

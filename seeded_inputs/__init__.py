@@ -54,6 +54,25 @@ def q4_weights(K: int, N: int, seed: int = 0, stream: int = 0,
     return out.reshape(K, nb * BLOCK_BYTES)
 
 
+Q8_BLOCK_BYTES = 34
+
+
+def q8_weights(K: int, N: int, seed: int = 0, stream: int = 0,
+               d_lo: float = 0.001, d_hi: float = 0.01) -> np.ndarray:
+    """Q8_0 blocks of a K x N matrix as uint8 [K, nb*34]: per block an fp16
+    scale drawn as for Q4_0 and 32 uniform random bytes (int8 codes); padding
+    codes are 0."""
+    nb = nblocks(N)
+    g = rng(seed, stream)
+    out = np.empty((K, nb, Q8_BLOCK_BYTES), dtype=np.uint8)
+    d = g.uniform(d_lo, d_hi, size=(K, nb)).astype(np.float16)
+    out[:, :, 0:2] = d.view(np.uint8).reshape(K, nb, 2)
+    out[:, :, 2:] = g.integers(0, 256, size=(K, nb, BLOCK), dtype=np.uint8)
+    first = N - (nb - 1) * BLOCK
+    out[:, nb - 1, 2 + first:] = 0
+    return out.reshape(K, nb * Q8_BLOCK_BYTES)
+
+
 def _fill_padding(blocks: np.ndarray, N: int, q: int) -> None:
     """Write nibble value q into every padding column of the last block."""
     nb = blocks.shape[1]

@@ -13,6 +13,7 @@ import pytest
 
 import oracle
 import test_oracle_pins as pins
+import test_oracle_q8_pins as q8pins
 
 MUTANTS = {
     "nibble order swapped": ("(packed & 0x0F) : (packed >> 4)", "(packed >> 4) : (packed & 0x0F)"),
@@ -40,6 +41,10 @@ MUTANTS = {
     "encoder padding code 0": ("                int q = 8;\n                if (l < n) {", "                int q = 0;\n                if (l < n) {"),
     "fp16 ties away from zero": ("    if (diff > 0.5 || (diff == 0.5 && fmod(fl, 2.0) != 0.0))\n        r = fl + 1.0;\n    double v = ldexp(r, quantum_exp);", "    if (diff >= 0.5)\n        r = fl + 1.0;\n    double v = ldexp(r, quantum_exp);"),
     "router picks the smallest": ("if (!taken[e] && (best < 0 || p[e] > p[best]))", "if (!taken[e] && (best < 0 || p[e] < p[best]))"),
+    "q8 codes read unsigned": ("    if (q >= 128)\n        q -= 256;                          /* two's complement */", "    (void)0;"),
+    "q8 codes offset by one byte": ("    int q = (int)blk[2 + j % QO_BLOCK];", "    int q = (int)blk[1 + j % QO_BLOCK];"),
+    "q8 blocks 18 bytes apart": ("    const uint8_t *blk = B + (k * nb + j / QO_BLOCK) * QO_Q8_BYTES;", "    const uint8_t *blk = B + (k * nb + j / QO_BLOCK) * QO_BLOCK_BYTES;"),
+    "q8 activation row stride": ("            double av = act_at(A, a_dtype, i * K + k);", "            double av = act_at(A, a_dtype, i + k);"),
 }
 
 BATTERY = [
@@ -68,6 +73,11 @@ BATTERY = [
     pins.test_quantize_closed_forms,
     pins.test_quantize_matches_fp32_restatement,
     pins.test_quantize_round_trip_bound,
+    q8pins.test_hand_written_blocks,
+    lambda: q8pins.test_equals_pinned_q4_on_reencoded_weights(2, 64, 96),
+    q8pins.test_layout_one_hot,
+    lambda: q8pins.test_exact_rational(2, 5, 40),
+    q8pins.test_padding_and_linearity,
 ]
 
 
