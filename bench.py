@@ -176,17 +176,18 @@ def max_over_ranks(ws, x: float) -> float:
 # ---------------------------------------------------------------------------
 # workloads
 # ---------------------------------------------------------------------------
-def sweep_plan(layers):
+def sweep_plan(layers, block_bytes=18):
     shapes = si.sweep_shapes(layers)
-    wbytes = sum(K * si.nblocks(N) * 18 for K, N in shapes)
+    wbytes = sum(K * si.nblocks(N) * block_bytes for K, N in shapes)
     return shapes, wbytes
 
 
-def build_sweep(torch, dev, layers, seed=0):
+def build_sweep(torch, dev, layers, seed=0, fmt="q4_0"):
     """Device weights, one contiguous A buffer and one contiguous C buffer."""
-    import quantized_weight_q4_gb300 as q4  # noqa: F401
+    import quantized_weight_q4_gb300 as q4
     from quantized_weight_q4_gb300.graph import MatmulSequence
-    shapes, wbytes = sweep_plan(layers)
+    q8 = fmt == "q8_0"
+    shapes, wbytes = sweep_plan(layers, 34 if q8 else 18)
     a_off, c_off, oa, oc = [], [], 0, 0
     for K, N in shapes:
         a_off.append(oa)
@@ -200,13 +201,14 @@ def build_sweep(torch, dev, layers, seed=0):
     calls = []
     weights = []
     for i, (K, N) in enumerate(shapes):
-        B = torch.from_numpy(si.q4_weights(K, N, seed=seed, stream=100 + i)).to(dev)
+        gen = si.q8_weights if q8 else si.q4_weights
+        B = torch.from_numpy(gen(K, N, seed=seed, stream=100 + i)).to(dev)
         weights.append(B)
         hA[a_off[i]:a_off[i] + K] = torch.from_numpy(si.activations_f32(1, K, seed, 10000 + i)[0])
         calls.append((dC[c_off[i]:c_off[i] + N].view(1, N), dA[a_off[i]:a_off[i] + K].view(1, K),
                       B, 1, N, K))
     dA.copy_(hA)
-    seq = MatmulSequence(calls)
+    seq = MatmulSequence(calls, b_layout=q4.Q4_LAYOUT_Q8_0 if q8 else q4.Q4_LAYOUT_BLOCKS)
     return dict(seq=seq, dA=dA, dC=dC, hA=hA, hC=hC, weights=weights, shapes=shapes,
                 wbytes=wbytes, launches_per_step=len(shapes))
 
@@ -227,16 +229,17 @@ def time_graph(torch, seq, steps, warmup):
     return s.elapsed_time(e) / 1e3
 
 
-def cpu_baseline_sweep(layers_sample, seed=0):
+def cpu_baseline_sweep(layers_sample, seed=0, fmt="q4_0"):
     """The oracle, single-threaded, on the first `layers_sample` layers."""
     import oracle
     shapes, _ = sweep_plan(layers_sample)
     total_bytes, total_t = 0, 0.0
+    q8 = fmt == "q8_0"
     for i, (K, N) in enumerate(shapes):
-        B = si.q4_weights(K, N, seed=seed, stream=100 + i)
+        B = (si.q8_weights if q8 else si.q4_weights)(K, N, seed=seed, stream=100 + i)
         A = si.activations_f32(1, K, seed, 10000 + i)
         t = time.perf_counter()
-        oracle.matmul(A, B, 1, N, K, with_abs=False)
+        (oracle.q8_matmul if q8 else oracle.matmul)(A, B, 1, N, K, with_abs=False)
         total_t += time.perf_counter() - t
         total_bytes += B.nbytes
     return total_bytes, total_t
@@ -257,12 +260,12 @@ def run_ours(args, ws, rank, local):
     # CPU baseline first (rank 0 at N = 1 only), while the GPU is idle
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        nbytes, t = cpu_baseline_sweep(args.cpu_layers)
+        nbytes, t = cpu_baseline_sweep(args.cpu_layers, fmt=args.format)
         cpu = {"value": nbytes / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"first {args.cpu_layers} of 32 layers ({7 * args.cpu_layers} GEMVs, "
                          f"{nbytes} weight bytes), fp64 oracle, 1 thread, {t:.1f} s"}
 
-    w = build_sweep(torch, dev, args.layers)
+    w = build_sweep(torch, dev, args.layers, fmt=args.format)
     seq = w["seq"]
     torch.cuda.synchronize()
 
@@ -303,7 +306,7 @@ def run_ours(args, ws, rank, local):
     avg_launch_s = elapsed / (args.steps * w["launches_per_step"])
     achieved = per_launch_bytes / avg_launch_s / 1e9
     h = kernel_source_hash()
-    traffic = TRAFFIC.get(h)
+    traffic = TRAFFIC.get(h) if args.format == "q4_0" else None
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -319,6 +322,7 @@ def run_ours(args, ws, rank, local):
         "data": "synthetic (seeded: q ~ U{0..15}, d = fp16(U[0.001, 0.01]), A ~ N(0,1))",
         "config": {
             "workload": "decode_sweep_7b",
+            "format": args.format,
             "layers": args.layers,
             "gemvs_per_step": w["launches_per_step"],
             "shapes_per_layer": "4x(K=4096,N=4096) 2x(4096,11008) 1x(11008,4096)",
@@ -331,7 +335,8 @@ def run_ours(args, ws, rank, local):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "q4_gemv_kernel<0,1,2> (GEMV, one row of A, 2 blocks per thread)",
+            "kernel": "q4_gemv_kernel (GEMV, one row of A, 2 blocks per thread, 32-row stages"
+                      + (", Q8_0 blocks)" if args.format == "q8_0" else ")"),
             "achieved": round(achieved, 2),
             "peak": hbm_peak,
             "unit": "GB/s",
@@ -397,17 +402,19 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
         M = args.m if args.workload == "gemv" else args.m
         K = args.k if args.k else (4096 if args.workload == "gemv" else 5120)
         N = args.n if args.n else (4096 if args.workload == "gemv" else 12288)
-        wbytes = K * si.nblocks(N) * 18
+        q8 = args.format == "q8_0"
+        wbytes = K * si.nblocks(N) * (34 if q8 else 18)
+        layout = q4.Q4_LAYOUT_Q8_0 if q8 else q4.Q4_LAYOUT_BLOCKS
         copies = max(1, -(-4 * l2 // wbytes))   # >= 4x L2 of distinct weights per pass
         bf16 = args.workload == "batched"
         fns, keep = [], []
         for i in range(copies):
-            B = to_dev(si.q4_weights(K, N, seed=0, stream=500 + i))
+            B = to_dev((si.q8_weights if q8 else si.q4_weights)(K, N, seed=0, stream=500 + i))
             A = si.activations_bf16(M, K, 0, 600 + i) if bf16 else si.activations_f32(M, K, 0, 600 + i)
             A = to_dev(A.view(np.int16)).view(torch.bfloat16) if bf16 else to_dev(A)
             C = torch.empty((M, N), dtype=torch.float32, device=dev)
             keep += [A, B, C]
-            fns.append(lambda C=C, A=A, B=B: q4.q4_matmul_ex(C, A, B, M, N, K))
+            fns.append(lambda C=C, A=A, B=B: q4.q4_matmul_ex(C, A, B, M, N, K, b_layout=layout))
         g = GraphOf(torch, fns)
         barrier(ws)
         with ClockSampler(local) as clk:
@@ -417,7 +424,7 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
         per_launch = t / (args.steps * copies)
         value = ws * wbytes / per_launch / 1e9
         flops = 2.0 * M * K * N
-        cfg = {"workload": args.workload, "M": M, "K": K, "N": N,
+        cfg = {"workload": args.workload, "format": args.format, "M": M, "K": K, "N": N,
                "a_dtype": "bf16" if bf16 else "f32", "c_dtype": "f32",
                "weight_bytes_per_launch": wbytes, "weight_copies_rotated": copies,
                "l2": f"{copies} distinct weight copies per pass ({copies * wbytes} B >= 4x L2)",
@@ -725,6 +732,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--slots", type=int, default=4, help="host_stream: device weight slots")
+    ap.add_argument("--format", choices=("q4_0", "q8_0"), default="q4_0",
+                    help="weight format (decode sweep, gemv, batched)")
     ap.add_argument("--m", type=int, default=1, help="rows of A (gemv, batched)")
     ap.add_argument("--k", type=int, default=0)
     ap.add_argument("--n", type=int, default=0)

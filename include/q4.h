@@ -66,6 +66,8 @@ extern "C" {
 /* ---- weight layouts ---- */
 #define Q4_LAYOUT_BLOCKS 0   /* the 18-byte block_q4_0 array described above */
 #define Q4_LAYOUT_PLANAR 1   /* q4_repack output: scales plane then nibble plane */
+#define Q4_LAYOUT_Q8_0   2   /* Q8_0 blocks {fp16 d; int8 q[32]} (34 bytes), laid out
+                                as the Q4_0 blocks above: w = q * d (see q4_matmul_ex) */
 
 /*
  * q4_matmul -- C = A . W, fp32 A [M, K], fp32 C [M, N], B in Q4_LAYOUT_BLOCKS,
@@ -79,17 +81,24 @@ Q4_API int q4_matmul(float *C, const float *A, const void *B, int64_t M, int64_t
  * q4_matmul_ex -- C = A . W with explicit types, layout, workspace and stream.
  *   C          [M, N] row-major, c_dtype Q4_F32 or Q4_BF16 (bf16 = RN of fp32)
  *   A          [M, K] row-major, a_dtype Q4_F32 or Q4_BF16
- *   B          weights in b_layout (Q4_LAYOUT_BLOCKS or Q4_LAYOUT_PLANAR)
+ *   B          weights in b_layout: Q4_LAYOUT_BLOCKS; or Q4_LAYOUT_Q8_0, the
+ *              second format (the engine page, §2.1-§2.2, names Q8_0 but
+ *              prints no layout; reading: blocks {fp16 d; int8 q[32]} of 34
+ *              bytes, 32 output columns of one row each, K rows of
+ *              ceil(N/32) blocks, w = q * d), for M <= 64 only (else
+ *              Q4_ERR_SHAPE); Q4_LAYOUT_PLANAR is a storage form for
+ *              q4_repack/q4_unpack and gives Q4_ERR_SHAPE here
  *   workspace  unused by this entry point (q4_matmul_workspace_size returns
  *              0); accepted for interface stability, may be NULL.
  *   stream     cudaStream_t (NULL = legacy default stream)
  * Kernel choice:
- *   - M <= 64, or fp32 A, or a shape the GEMM below does not take: the
- *     split-K GEMV on the CUDA cores, in chunks of up to 4 rows of A.  The
- *     splits of each column tile run as one thread-block cluster and are
- *     added on chip in fixed order.  Exact fp32 dequantisation.
- *   - M > 64 with bf16 A, ceil(N/32) % 8 == 0 and K % 8 == 0: the
- *     tensor-core GEMM (prompt batching, engine page §5.2).  Each weight is
+ *   - M < 8, or fp32 A, or Q8_0 weights, or a shape the GEMM below does not
+ *     take: the split-K GEMV on the CUDA cores, in chunks of up to 4 rows of
+ *     A.  The splits of each column tile run as one thread-block cluster and
+ *     are added on chip in fixed order.  Exact fp32 dequantisation.
+ *   - M >= 8 with bf16 A, ceil(N/32) % 8 == 0 and K % 8 == 0 (and, for
+ *     M <= 128, a shape its split-K form takes): the tensor-core GEMM
+ *     (prompt batching, engine page §5.2).  Each weight is
  *     dequantised to a bf16 tile element bf16_rn((q - 8) * d) and the
  *     products are accumulated in fp32; the result is A . bf16_rn(W), whose
  *     deviation from A . W is bounded by 2^-9 * sum|a*w| plus the fp32

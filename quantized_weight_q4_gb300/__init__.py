@@ -31,6 +31,7 @@ Q4_F32 = 0
 Q4_BF16 = 1
 Q4_LAYOUT_BLOCKS = 0
 Q4_LAYOUT_PLANAR = 1
+Q4_LAYOUT_Q8_0 = 2
 
 _lock = threading.Lock()
 _lib = None

@@ -46,7 +46,7 @@ struct DeviceState {
   void* ws = nullptr;           // library-owned workspace
   size_t ws_bytes = 0;
   // launch shapes already chosen for a problem size (the choice runs occupancy queries)
-  std::map<std::tuple<int64_t, int64_t, int64_t>, GemvShape> gemv_shapes;
+  std::map<std::tuple<int64_t, int64_t, int64_t, int>, GemvShape> gemv_shapes;
   std::map<std::tuple<int64_t, int64_t, int64_t, int64_t, int64_t>, MoeShape> moe_shapes;
 };
 
@@ -119,9 +119,10 @@ int64_t big_min_stages(int mr) { return mr == 1 ? 16 : 4; }
 // minimise the bytes the busiest SM must stream: waves of resident clusters
 // (from the occupancy query) times the CTAs per SM within a wave times the
 // bytes per CTA plus its fixed cost.  Ties go to fewer CTAs.
-void choose_split(int mode, int mr, int list_cap, int64_t K, int64_t nb, int64_t z_groups, int pair,
-                  int sms, int max_split, bool allow_bpt2, int* bpt_out, int* nsplit_out,
-                  int* rows_out, int* ntiles_out, bool* big_out) {
+void choose_split(int mode, int mr, int fmt, int list_cap, int64_t K, int64_t nb, int64_t z_groups,
+                  int pair, int sms, int max_split, bool allow_bpt2, int* bpt_out,
+                  int* nsplit_out, int* rows_out, int* ntiles_out, bool* big_out) {
+  const double block_bytes = (fmt == q4::kFmtQ8) ? 34.0 : 18.0;
   double best = -1.0;
   int64_t best_ctas = 0;
   *bpt_out = 1;
@@ -139,7 +140,7 @@ void choose_split(int mode, int mr, int list_cap, int64_t K, int64_t nb, int64_t
       const int64_t csize = pair * nsplit;
       const int64_t clusters = ntiles * z_groups;
       const int64_t ctas = clusters * csize;
-      const int active = q4::max_active_clusters(mode, mr, bpt, false, static_cast<int>(rows),
+      const int active = q4::max_active_clusters(mode, mr, bpt, false, fmt, static_cast<int>(rows),
                                                  list_cap,
                                                  dim3(1, static_cast<unsigned>(nsplit),
                                                       static_cast<unsigned>(pair)));
@@ -148,7 +149,7 @@ void choose_split(int mode, int mr, int list_cap, int64_t K, int64_t nb, int64_t
       const int64_t per_wave = (clusters < active ? clusters : active) * csize;
       // a CTA's fixed cost (first loads, reduction, cluster combine: ~2.5 us)
       // is worth about kCtaFixedBytes of streaming
-      const double per_cta = static_cast<double>(rows) * q4::gemv_tile_blocks(bpt) * 18.0 +
+      const double per_cta = static_cast<double>(rows) * q4::gemv_tile_blocks(bpt) * block_bytes +
                              kCtaFixedBytes;
       double cost = per_cta * static_cast<double>(waves * ceil_div(per_wave, sms));
       if (bpt == 1 && allow_bpt2) cost *= 1.03;   // more instructions per weight
@@ -166,24 +167,24 @@ void choose_split(int mode, int mr, int list_cap, int64_t K, int64_t nb, int64_t
   // and its residency
   const int bpt = *bpt_out;
   const int64_t big_rows = q4::gemv_stage_rows(bpt, true);
-  if (*rows_out >= big_min_stages(mr) * big_rows) {
+  if (fmt == q4::kFmtQ4 && *rows_out >= big_min_stages(mr) * big_rows) {
     const int64_t rows = split_rows(K, *nsplit_out, bpt, true);
     const dim3 cl(1, static_cast<unsigned>(*nsplit_out), static_cast<unsigned>(pair));
     if (ceil_div(K, rows) == *nsplit_out &&
-        q4::max_active_clusters(mode, mr, bpt, true, static_cast<int>(rows), list_cap, cl) >=
-            q4::max_active_clusters(mode, mr, bpt, false, *rows_out, list_cap, cl)) {
+        q4::max_active_clusters(mode, mr, bpt, true, fmt, static_cast<int>(rows), list_cap, cl) >=
+            q4::max_active_clusters(mode, mr, bpt, false, fmt, *rows_out, list_cap, cl)) {
       *big_out = true;
       *rows_out = static_cast<int>(rows);
     }
   }
 }
 
-GemvShape gemv_shape(int64_t M, int64_t N, int64_t K, int sms) {
+GemvShape gemv_shape(int64_t M, int64_t N, int64_t K, int fmt, int sms) {
   GemvShape g;
   const int64_t nb = ceil_div(N, 32);
   g.mr = (M == 1) ? 1 : (M == 2) ? 2 : 4;
   g.nchunks = static_cast<int>(ceil_div(M, g.mr));
-  choose_split(q4::kModeGemv, g.mr, 0, K, nb, g.nchunks, 1, sms, q4::kMaxCluster, g.mr == 1,
+  choose_split(q4::kModeGemv, g.mr, fmt, 0, K, nb, g.nchunks, 1, sms, q4::kMaxCluster, g.mr == 1,
                &g.bpt, &g.nsplit, &g.rows_per_split, &g.ntiles, &g.big);
   return g;
 }
@@ -199,10 +200,10 @@ MoeShape moe_shape(int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I, int
   m.mr = (T == 1) ? 1 : 2;
   m.list_cap = static_cast<int>(m.nslots > ceil_div(E, 32) ? m.nslots : ceil_div(E, 32));
   // gate and up of one expert tile share a cluster: at most 8 splits each
-  choose_split(q4::kModeGateUp, m.mr, m.list_cap, H, ceil_div(I, 32), m.nexp, 2, sms,
+  choose_split(q4::kModeGateUp, m.mr, q4::kFmtQ4, m.list_cap, H, ceil_div(I, 32), m.nexp, 2, sms,
                q4::kMaxCluster / 2, m.mr == 1, &m.bpt_gu, &m.nsplit_gu, &m.rows_gu, &m.ntiles_gu,
                &m.big_gu);
-  choose_split(q4::kModeDown, m.mr, m.list_cap, I, ceil_div(H, 32), m.nexp, 1, sms,
+  choose_split(q4::kModeDown, m.mr, q4::kFmtQ4, m.list_cap, I, ceil_div(H, 32), m.nexp, 1, sms,
                q4::kMaxCluster, m.mr == 1, &m.bpt_d, &m.nsplit_d, &m.rows_d, &m.ntiles_d, &m.big_d);
   size_t o = 0;
   m.off_h = o;
@@ -213,10 +214,11 @@ MoeShape moe_shape(int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I, int
   return m;
 }
 
-const GemvShape& cached_gemv_shape(DeviceState* s, int64_t M, int64_t N, int64_t K) {
-  const auto key = std::make_tuple(M, N, K);
+const GemvShape& cached_gemv_shape(DeviceState* s, int64_t M, int64_t N, int64_t K, int fmt) {
+  const auto key = std::make_tuple(M, N, K, fmt);
   auto it = s->gemv_shapes.find(key);
-  if (it == s->gemv_shapes.end()) it = s->gemv_shapes.emplace(key, gemv_shape(M, N, K, s->sms)).first;
+  if (it == s->gemv_shapes.end())
+    it = s->gemv_shapes.emplace(key, gemv_shape(M, N, K, fmt, s->sms)).first;
   return it->second;
 }
 
@@ -258,7 +260,7 @@ int moe_run(DeviceState* s, const MoeShape& m, float* out, const void* x, int x_
   p.y = y;
   p.err = s->status;
   p.c_dtype = 0;
-  q4::fill_decode_consts(p);
+  q4::fill_decode_consts(p, q4::kFmtQ4);
 
   // gate and up: K = H, N = I; A rows are tokens
   p.mode = q4::kModeGateUp;
@@ -272,14 +274,15 @@ int moe_run(DeviceState* s, const MoeShape& m, float* out, const void* x, int x_
   p.rows_per_split = m.rows_gu;
   p.use_tma = (p.nb % 8 == 0 && p.b_stride % 16 == 0 &&
                q4::encode_weight_tmap(&p.tmap[0], W_gate, H, p.nb, E, p.b_stride, m.bpt_gu,
-                                      m.big_gu) &&
+                                      m.big_gu, q4::kFmtQ4) &&
                q4::encode_weight_tmap(&p.tmap[1], W_up, H, p.nb, E, p.b_stride, m.bpt_gu,
-                                      m.big_gu))
+                                      m.big_gu, q4::kFmtQ4))
                   ? 1 : 0;
   p.A = x;
   p.a_dtype = x_dtype;
   p.a_ld = H;
-  cudaError_t e = q4::launch_gemv(p, m.mr, m.bpt_gu, m.big_gu, dim3(m.ntiles_gu, m.nsplit_gu, 2 * m.nexp),
+  cudaError_t e = q4::launch_gemv(p, m.mr, m.bpt_gu, m.big_gu, q4::kFmtQ4,
+                                  dim3(m.ntiles_gu, m.nsplit_gu, 2 * m.nexp),
                                   dim3(1, m.nsplit_gu, 2), st, true);
   if (e != cudaSuccess) return Q4_ERR_CUDA;
 
@@ -294,12 +297,13 @@ int moe_run(DeviceState* s, const MoeShape& m, float* out, const void* x, int x_
   p.nsplit = m.nsplit_d;
   p.rows_per_split = m.rows_d;
   p.use_tma = (p.nb % 8 == 0 && p.b_stride % 16 == 0 &&
-               q4::encode_weight_tmap(&p.tmap[0], W_down, I, p.nb, E, p.b_stride, m.bpt_d, m.big_d))
+               q4::encode_weight_tmap(&p.tmap[0], W_down, I, p.nb, E, p.b_stride, m.bpt_d, m.big_d,
+                                      q4::kFmtQ4))
                   ? 1 : 0;
   p.A = h;
   p.a_dtype = 0;
   p.a_ld = I;
-  e = q4::launch_gemv(p, m.mr, m.bpt_d, m.big_d, dim3(m.ntiles_d, m.nsplit_d, m.nexp),
+  e = q4::launch_gemv(p, m.mr, m.bpt_d, m.big_d, q4::kFmtQ4, dim3(m.ntiles_d, m.nsplit_d, m.nexp),
                       dim3(1, m.nsplit_d, 1), st, true);
   if (e != cudaSuccess) return Q4_ERR_CUDA;
 
@@ -344,7 +348,10 @@ int q4_matmul_ex(void* C, int c_dtype, const void* A, int a_dtype, const void* B
   if (M > (1LL << 30) || N > (1LL << 30) || K > (1LL << 30)) return Q4_ERR_SHAPE;
   if ((c_dtype != Q4_F32 && c_dtype != Q4_BF16) || (a_dtype != Q4_F32 && a_dtype != Q4_BF16))
     return Q4_ERR_DTYPE;
-  if (b_layout != Q4_LAYOUT_BLOCKS) return (b_layout == Q4_LAYOUT_PLANAR) ? Q4_ERR_SHAPE : Q4_ERR_ARG;
+  if (b_layout == Q4_LAYOUT_PLANAR) return Q4_ERR_SHAPE;
+  if (b_layout != Q4_LAYOUT_BLOCKS && b_layout != Q4_LAYOUT_Q8_0) return Q4_ERR_ARG;
+  const int fmt = (b_layout == Q4_LAYOUT_Q8_0) ? q4::kFmtQ8 : q4::kFmtQ4;
+  if (fmt == q4::kFmtQ8 && M > 64) return Q4_ERR_SHAPE;   // Q8_0: the GEMV (M <= 64) only
   if (!aligned16(C) || !aligned16(A) || !aligned16(B) || (workspace && !aligned16(workspace)))
     return Q4_ERR_ALIGN;
 
@@ -354,11 +361,11 @@ int q4_matmul_ex(void* C, int c_dtype, const void* A, int a_dtype, const void* B
   DeviceState* s = nullptr;
   int rc = current_state(&s);
   if (rc != Q4_OK) return rc;
-  if (M >= kMinTensorRows && a_dtype == Q4_BF16 && q4::gemm_supported(M, N, K) &&
-      (M > 128 || q4::gemm_small_split(M, N, K) > 0))
+  if (fmt == q4::kFmtQ4 && M >= kMinTensorRows && a_dtype == Q4_BF16 &&
+      q4::gemm_supported(M, N, K) && (M > 128 || q4::gemm_small_split(M, N, K) > 0))
     return launch_status(q4::launch_gemm(C, c_dtype, A, B, M, N, K, s->status, s->sms,
                                          static_cast<cudaStream_t>(stream)));
-  const GemvShape& g = cached_gemv_shape(s, M, N, K);
+  const GemvShape& g = cached_gemv_shape(s, M, N, K, fmt);
   if (g.nchunks > 65535 || 4LL * g.mr * g.rows_per_split > kMaxASliceBytes) return Q4_ERR_SHAPE;
 
   q4::GemvParams p;
@@ -370,9 +377,11 @@ int q4_matmul_ex(void* C, int c_dtype, const void* A, int a_dtype, const void* B
   p.nb = static_cast<int>(ceil_div(N, 32));
   p.nsplit = g.nsplit;
   p.rows_per_split = g.rows_per_split;
-  q4::fill_decode_consts(p);
+  q4::fill_decode_consts(p, fmt);
+  const int64_t block_bytes = (fmt == q4::kFmtQ8) ? 34 : 18;
   p.use_tma = (p.nb % 8 == 0 &&
-               q4::encode_weight_tmap(&p.tmap[0], B, K, p.nb, 1, K * p.nb * 18, g.bpt, g.big))
+               q4::encode_weight_tmap(&p.tmap[0], B, K, p.nb, 1, K * p.nb * block_bytes, g.bpt,
+                                      g.big, fmt))
                   ? 1 : 0;
   p.A = A;
   p.a_dtype = a_dtype;
@@ -383,7 +392,7 @@ int q4_matmul_ex(void* C, int c_dtype, const void* A, int a_dtype, const void* B
   p.list_cap = 0;
   p.err = s->status;
   const dim3 grid(g.ntiles, g.nsplit, g.nchunks);
-  return launch_status(q4::launch_gemv(p, g.mr, g.bpt, g.big, grid, dim3(1, g.nsplit, 1),
+  return launch_status(q4::launch_gemv(p, g.mr, g.bpt, g.big, fmt, grid, dim3(1, g.nsplit, 1),
                                        static_cast<cudaStream_t>(stream), true));
 }
 

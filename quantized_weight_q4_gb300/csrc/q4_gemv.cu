@@ -63,17 +63,42 @@ struct Crew {
   static constexpr int kThreads = kConsumers + 32;   // + producer warp
 };
 
+// Weight formats behind the same kernel (the block runs along the output
+// columns of one row in both):
+//   kFmtQ4: block_q4_0 {fp16 d; 16 bytes of nibbles}, w = (q - 8) * d;
+//   kFmtQ8: Q8_0 {fp16 d; int8 q[32]}, w = q * d (decoded as b = q + 128,
+//           so the offset removed per block is 128).
+template <int FMT>
+struct Fmt;
+template <>
+struct Fmt<kFmtQ4> {
+  static constexpr int kBytes = 18;        // bytes per block
+  static constexpr int kWords = 4;         // 32-bit words of codes per block
+  static constexpr int kBias = 8;          // code offset removed after the loop
+  static constexpr int kPairGap = 8;       // second column of an accumulator pair
+  static constexpr int kTmaElem = 2;       // tensor-map element size (uint16)
+};
+template <>
+struct Fmt<kFmtQ8> {
+  static constexpr int kBytes = 34;
+  static constexpr int kWords = 8;
+  static constexpr int kBias = 128;
+  static constexpr int kPairGap = 4;
+  static constexpr int kTmaElem = 4;       // uint32: a 2-block-per-thread row segment is 544 B
+};
+
 // A stage is one TMA box.  Long slices use 18 KB boxes (BIG): bulk copies of
 // that size keep HBM near its copy bandwidth from 128 SMs, where 9 KB boxes
 // reach about two thirds of it (measured on GB300, data movement alone).
 // Short slices use 32-row boxes: fewer rows per stage fill and drain the
-// pipeline sooner.  Either way the ring holds ~147 KB.
-template <int BPT, bool BIG>
+// pipeline sooner.  Either way the ring holds ~147 KB.  (Q8_0 rows are
+// already 272 or 544 bytes: it keeps 32-row boxes.)
+template <int BPT, bool BIG, int FMT = kFmtQ4>
 struct TileCfg {
   static constexpr int kBlocks = kLanesPerRow * BPT;                // blocks per column tile
   static constexpr int kCols = kBlocks * kBlockCols;                // 256 * BPT
-  static constexpr int kRowBytes = kBlocks * kBlockBytes;           // 144 * BPT
-  static constexpr int kRows = BIG ? 128 / BPT : 32;                // rows of one stage
+  static constexpr int kRowBytes = kBlocks * Fmt<FMT>::kBytes;      // 144 or 272 per BPT
+  static constexpr int kRows = (BIG && FMT == kFmtQ4) ? 128 / BPT : 32;   // rows of one stage
   static constexpr int kStageBytes = kRows * kRowBytes;
   static constexpr int kStages = (147456 / kStageBytes);            // 8, 16 or 32
   static constexpr int kGroupWarps = BIG ? 8 : 4;                   // warps sharing a stage
@@ -101,9 +126,9 @@ struct SmemPlan {
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-template <int MR, int BPT, bool BIG>
+template <int MR, int BPT, bool BIG, int FMT>
 __host__ __device__ inline SmemPlan smem_plan(int rows_per_split, int list_cap) {
-  using T = TileCfg<BPT, BIG>;
+  using T = TileCfg<BPT, BIG, FMT>;
   SmemPlan p;
   p.ring = 0;   // the dynamic shared-memory base is 128-byte aligned
   p.red = align_up(T::kStages * T::kStageBytes, 16);
@@ -118,9 +143,10 @@ __host__ __device__ inline SmemPlan smem_plan(int rows_per_split, int list_cap) 
 // ---------------------------------------------------------------------------
 // Consumer arithmetic
 // ---------------------------------------------------------------------------
-// The nibble masks 0xF << 4p, p = 0..3, held in registers across the main
-// loop (loaded from the parameters so that the compiler does not re-create
-// immediates).
+// The code masks, held in registers across the main loop (loaded from the
+// parameters so that the compiler does not re-create immediates): Q4_0, the
+// nibble masks 0xF << 4p, p = 0..3; Q8_0, the byte masks 0xFF << 8p,
+// p = 0..2, and the sign flips 0x80808080.
 struct DecodeConsts {
   uint32_t mask[4];
 };
@@ -145,28 +171,56 @@ __device__ __forceinline__ f32x2 code_pair(uint32_t w0, uint32_t w1, uint32_t ma
   return r;
 }
 
+// Q8_0: the subnormals ((byte p of w0 ^ 0x80) * 256^p * 2^-149, same for w1),
+// p = 0..2: one three-input logic op per half, (w ^ flip) & mask.
+__device__ __forceinline__ f32x2 byte_pair(uint32_t w0, uint32_t w1, uint32_t mask,
+                                           uint32_t flip) {
+  f32x2 r;
+  asm("{\n\t.reg .b32 lo, hi;\n\t"
+      "lop3.b32 lo, %1, %4, %3, 0x28;\n\t"   // (w0 ^ flip) & mask
+      "lop3.b32 hi, %2, %4, %3, 0x28;\n\t"   // (w1 ^ flip) & mask
+      "mov.b64 %0, {lo, hi};\n\t}"
+      : "=l"(r)
+      : "r"(w0), "r"(w1), "r"(mask), "r"(flip));
+  return r;
+}
+
+// Q8_0 byte 3 of w0 and w1 as ((w >> 24) ^ 0x80) * 2^-149.
+__device__ __forceinline__ f32x2 top_byte_pair(uint32_t w0, uint32_t w1) {
+  return pack2(__uint_as_float((w0 >> 24) ^ 0x80u), __uint_as_float((w1 >> 24) ^ 0x80u));
+}
+
 // 2^64: the factor of the activations staged in shared memory.
 constexpr float kAScale = 18446744073709551616.0f;
 
-// Accumulator layout of one block (32 columns, 16 pairs): words t = 2h and
-// 2h + 1 are decoded together, nibble p of each forming a pair, so
+// Accumulator layout of one block (32 columns, 16 pairs).  Q4_0: words t = 2h
+// and 2h + 1 are decoded together, nibble p of each forming a pair, so
 //   acc[8h + p]     holds columns (16h + p,     16h + 8 + p)
 //   acc[8h + 4 + p] holds columns (16h + 4 + p, 16h + 12 + p)
-// each scaled by 16^p * 2^-85; acc_col_pair() maps a pair back to its columns
-// and finish_acc() removes the power-of-two factors (exact) and the -8.
+// each scaled by 16^p * 2^-85.  Q8_0: words 2h and 2h + 1, byte p of each:
+//   acc[4h + p]     holds columns (8h + p, 8h + 4 + p), scaled by
+// 256^p * 2^-85 for p < 3 and 2^-85 for p = 3.  acc_col_pair() maps a pair
+// back to its first column (the second is kPairGap further) and finish_acc()
+// removes the power-of-two factors (exact) and the code offset.
+template <int FMT>
 __device__ __forceinline__ int acc_col_pair(int j) {   // first column of pair j
-  const int h = j >> 3, p = j & 3, hi = (j >> 2) & 1;
-  return 16 * h + 4 * hi + p;                            // second column is +8
+  if constexpr (FMT == kFmtQ8) {
+    return 8 * (j >> 2) + (j & 3);
+  } else {
+    const int h = j >> 3, p = j & 3, hi = (j >> 2) & 1;
+    return 16 * h + 4 * hi + p;
+  }
 }
 
 // Adds block bb of a staged row (scale bits dbits, codes qs) for MR rows of A
 // (a[m * a_ld], already times 2^64): acc[m][16bb + j] += a'_m * codes of pair
 // j, sad[m][bb] += a'_m.
-template <int MR, int BPT>
+template <int MR, int BPT, int FMT>
 __device__ __forceinline__ void accumulate_block(f32x2 (&acc)[MR][16 * BPT],
                                                  float (&sad)[MR][BPT], int bb, uint32_t dbits,
-                                                 const uint32_t (&qs)[4], const float* a,
-                                                 int a_ld, const DecodeConsts& k) {
+                                                 const uint32_t (&qs)[Fmt<FMT>::kWords],
+                                                 const float* a, int a_ld,
+                                                 const DecodeConsts& k) {
   const float d = fp16_bits_to_f32(dbits);
   f32x2 ad[MR];
 #pragma unroll
@@ -174,6 +228,24 @@ __device__ __forceinline__ void accumulate_block(f32x2 (&acc)[MR][16 * BPT],
     const float x = a[m * a_ld] * d;
     sad[m][bb] += x;
     ad[m] = dup2(x);
+  }
+  if constexpr (FMT == kFmtQ8) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const uint32_t w0 = qs[2 * h], w1 = qs[2 * h + 1];
+      f32x2 code[4];
+#pragma unroll
+      for (int p = 0; p < 3; ++p) code[p] = byte_pair(w0, w1, k.mask[p], k.mask[3]);
+      code[3] = top_byte_pair(w0, w1);
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+#pragma unroll
+        for (int m = 0; m < MR; ++m) {
+          f32x2* acc0 = &acc[m][16 * bb + 4 * h];
+          acc0[p] = fma2(ad[m], code[p], acc0[p]);
+        }
+    }
+    return;
   }
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -194,28 +266,68 @@ __device__ __forceinline__ void accumulate_block(f32x2 (&acc)[MR][16 * BPT],
 }
 
 // Turns the accumulators into sums of a*w: pair j of block bb becomes
-// acc * 2^(85 - 4p) - 8 * sad * 2^-64 (p = j & 3; the scalings are exact).
-template <int MR, int BPT>
+// acc * (power of two of its position) - bias * sad * 2^-64 (Q4_0: 2^(85-4p),
+// p = j & 3, bias 8; Q8_0: 2^(85-8p) for p = j & 3 < 3, 2^85 for p = 3,
+// bias 128; the scalings are exact).
+template <int MR, int BPT, int FMT>
 __device__ __forceinline__ void finish_acc(f32x2 (&acc)[MR][16 * BPT],
                                            const float (&sad)[MR][BPT]) {
-  const f32x2 sc[4] = {dup2(0x1p85f), dup2(0x1p81f), dup2(0x1p77f), dup2(0x1p73f)};
+  f32x2 sc[4];
+  if constexpr (FMT == kFmtQ8) {
+    sc[0] = dup2(0x1p85f); sc[1] = dup2(0x1p77f); sc[2] = dup2(0x1p69f); sc[3] = dup2(0x1p85f);
+  } else {
+    sc[0] = dup2(0x1p85f); sc[1] = dup2(0x1p81f); sc[2] = dup2(0x1p77f); sc[3] = dup2(0x1p73f);
+  }
+  constexpr float kCorr = -static_cast<float>(Fmt<FMT>::kBias) * 0x1p-64f;   // exact
 #pragma unroll
   for (int m = 0; m < MR; ++m)
 #pragma unroll
     for (int bb = 0; bb < BPT; ++bb) {
-      const f32x2 corr = dup2(sad[m][bb] * -0x1p-61f);
+      const f32x2 corr = dup2(sad[m][bb] * kCorr);
 #pragma unroll
       for (int j = 0; j < 16; ++j) acc[m][16 * bb + j] = fma2(acc[m][16 * bb + j], sc[j & 3], corr);
     }
 }
 
 // The BPT consecutive blocks a thread owns in one staged row.  `off` is the
-// byte offset of its first block; for BPT = 2 it is a multiple of 36 (4-byte
-// aligned), for BPT = 1 a multiple of 18 whose parity is fixed per thread.
-template <int BPT>
+// byte offset of its first block; for BPT = 2 it is a multiple of 36 (Q4_0)
+// or 68 (Q8_0), 4-byte aligned; for BPT = 1 a multiple of 18 or 34 whose
+// parity (2 mod 4 or not) is fixed per thread.  Either format's block is a
+// 2-byte scale followed by its code words, so a block that starts 4-byte
+// aligned has its codes 2 bytes off the word grid.
+template <int BPT, int FMT>
 __device__ __forceinline__ void load_blocks(const uint8_t* row, uint32_t off, bool odd,
-                                            uint32_t (&dbits)[BPT], uint32_t (&qs)[BPT][4]) {
-  if constexpr (BPT == 2) {
+                                            uint32_t (&dbits)[BPT],
+                                            uint32_t (&qs)[BPT][Fmt<FMT>::kWords]) {
+  if constexpr (FMT == kFmtQ8) {
+    constexpr int W = Fmt<FMT>::kWords;   // 8
+    if constexpr (BPT == 2) {
+      const uint32_t* wp = reinterpret_cast<const uint32_t*>(row + off);
+      uint32_t w[2 * W + 1];
+#pragma unroll
+      for (int i = 0; i < 2 * W + 1; ++i) w[i] = wp[i];
+      dbits[0] = w[0] & 0xFFFFu;
+#pragma unroll
+      for (int t = 0; t < W; ++t) qs[0][t] = __funnelshift_r(w[t], w[t + 1], 16);
+      dbits[1] = w[W] >> 16;
+#pragma unroll
+      for (int t = 0; t < W; ++t) qs[1][t] = w[W + 1 + t];
+    } else {
+      const uint32_t* wp = reinterpret_cast<const uint32_t*>(row + (off & ~3u));
+      uint32_t w[W + 1];
+#pragma unroll
+      for (int i = 0; i < W + 1; ++i) w[i] = wp[i];
+      if (odd) {
+        dbits[0] = w[0] >> 16;
+#pragma unroll
+        for (int t = 0; t < W; ++t) qs[0][t] = w[t + 1];
+      } else {
+        dbits[0] = w[0] & 0xFFFFu;
+#pragma unroll
+        for (int t = 0; t < W; ++t) qs[0][t] = __funnelshift_r(w[t], w[t + 1], 16);
+      }
+    }
+  } else if constexpr (BPT == 2) {
     const uint32_t* wp = reinterpret_cast<const uint32_t*>(row + off);
     uint32_t w[9];
 #pragma unroll
@@ -263,28 +375,29 @@ struct StreamDesc {
   int k0, rows;       // row slice
 };
 
-template <int BPT, bool BIG>
+template <int BPT, bool BIG, int FMT>
 __device__ __forceinline__ void produce_stage(const StreamDesc& sd, int s, uint8_t* stage,
                                               uint64_t* full, int lane) {
-  using T = TileCfg<BPT, BIG>;
+  using T = TileCfg<BPT, BIG, FMT>;
+  constexpr int kBB = Fmt<FMT>::kBytes;
   const int r0 = s * T::kRows;
   if (sd.tmap) {
-    // one box of kRows rows x 144*BPT bytes; rows past K and blocks past the row
+    // one box of kRows rows x kRowBytes; rows past K and blocks past the row
     // read as zero (a slice is a whole number of boxes, except the last one,
     // which ends at K)
     if (lane == 0) {
       mbar_arrive_expect_tx(full, T::kStageBytes);
-      tma_load_3d(stage, sd.tmap, sd.b0 * (kBlockBytes / 2), sd.k0 + r0, sd.expert, full);
+      tma_load_3d(stage, sd.tmap, sd.b0 * kBB / Fmt<FMT>::kTmaElem, sd.k0 + r0, sd.expert, full);
     }
   } else {
     // 2-byte aligned rows: copy with 16-bit loads (every block offset is even);
     // rows past the slice and blocks past the row are written as zeros, as
     // the tensor copy does, so that the consumers need no bounds checks
     const int nr = min(T::kRows, sd.rows - r0);
-    const int halves = sd.tb * (kBlockBytes / 2);
+    const int halves = sd.tb * (kBB / 2);
     for (int r = 0; r < T::kRows; ++r) {
       const uint16_t* src = reinterpret_cast<const uint16_t*>(
-          sd.B + (static_cast<size_t>(sd.k0 + r0 + r) * sd.nb + sd.b0) * kBlockBytes);
+          sd.B + (static_cast<size_t>(sd.k0 + r0 + r) * sd.nb + sd.b0) * kBB);
       uint16_t* dst = reinterpret_cast<uint16_t*>(stage + r * T::kRowBytes);
       for (int h = lane; h < T::kRowBytes / 2; h += 32)
         dst[h] = (r < nr && h < halves) ? __ldg(src + h) : static_cast<uint16_t>(0);
@@ -304,7 +417,7 @@ __device__ __forceinline__ void consumers_sync() {
 // over the four rows of a warp), then across warps through shared memory.
 // out[m][i] = column tid + 256*i of the tile for row m.
 // ---------------------------------------------------------------------------
-template <int MR, int BPT>
+template <int MR, int BPT, int FMT>
 __device__ __forceinline__ void reduce_tile(f32x2 (&acc)[MR][16 * BPT], float* red, int warp,
                                             int lane, int tid, float (&out)[MR][BPT]) {
   constexpr int P = 16 * BPT;   // pairs per thread
@@ -332,13 +445,13 @@ __device__ __forceinline__ void reduce_tile(f32x2 (&acc)[MR][16 * BPT], float* r
     float* dst = red + (warp * MR + m) * kRedStride<BPT> + pi * BPT * 33;
 #pragma unroll
     for (int i = 0; i < P / 4; ++i) {
-      // pair j = j0 + i: block j >> 4, columns acc_col_pair(j & 15) and +8
+      // pair j = j0 + i: block j >> 4, columns acc_col_pair(j & 15) and + kPairGap
       const int j = j0 + i;
-      const int c = 33 * (j >> 4) + acc_col_pair(j & 15);
+      const int c = 33 * (j >> 4) + acc_col_pair<FMT>(j & 15);
       float v0, v1;
       unpack2(q[i], v0, v1);
       dst[c] = v0;
-      dst[c + 8] = v1;
+      dst[c + Fmt<FMT>::kPairGap] = v1;
     }
   }
   consumers_sync<MR>();
@@ -421,13 +534,13 @@ __device__ __forceinline__ void store_out(const GemvParams& p, size_t i, float v
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int MODE, int MR, int BPT, bool BIG>
+template <int MODE, int MR, int BPT, bool BIG, int FMT>
 __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
     q4_gemv_kernel(const __grid_constant__ GemvParams p) {
-  using T = TileCfg<BPT, BIG>;
+  using T = TileCfg<BPT, BIG, FMT>;
   constexpr int kGroups = Crew<MR>::kWarps / T::kGroupWarps;
   extern __shared__ __align__(128) uint8_t smem[];
-  const SmemPlan plan = smem_plan<MR, BPT, BIG>(p.rows_per_split, p.list_cap);
+  const SmemPlan plan = smem_plan<MR, BPT, BIG, FMT>(p.rows_per_split, p.list_cap);
   uint8_t* ring = smem + plan.ring;
   float* red = reinterpret_cast<float*>(smem + plan.red);
   float* cpart = reinterpret_cast<float*>(smem + plan.cpart);
@@ -530,7 +643,7 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
           failed = !__shfl_sync(0xffffffffu, ok ? 1 : 0, 0);   // failed: issue nothing more
           if (failed) break;
         }
-        produce_stage<BPT, BIG>(sd, s, ring + slot * T::kStageBytes, &full[slot], lane);
+        produce_stage<BPT, BIG, FMT>(sd, s, ring + slot * T::kStageBytes, &full[slot], lane);
       }
       // the cluster barriers of this pass's combine (see the consumers)
       cluster_sync();
@@ -546,7 +659,7 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
   const int group = warp / T::kGroupWarps;                 // stages s = group mod kGroups
   // row phase: the thread decodes rows rp, rp + kGroupRows, ... of each stage
   const int rp = (warp % T::kGroupWarps) * 4 + (lane >> 3);
-  const uint32_t boff = static_cast<uint32_t>(pi * BPT * kBlockBytes);
+  const uint32_t boff = static_cast<uint32_t>(pi * BPT * Fmt<FMT>::kBytes);
   const bool odd = (boff & 2u) != 0;
   const int ncols = p.N;
   const int tile_cols = tb * kBlockCols;
@@ -598,12 +711,12 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
         for (int rr = 0; rr < T::kRowsPerThread; ++rr) {
           const int rs = rp + rr * T::kGroupRows;   // row within the stage
           const uint8_t* row = ring + slot * T::kStageBytes + rs * T::kRowBytes;
-          uint32_t dbits[BPT], qs[BPT][4];
-          load_blocks<BPT>(row, boff, odd, dbits, qs);
+          uint32_t dbits[BPT], qs[BPT][Fmt<FMT>::kWords];
+          load_blocks<BPT, FMT>(row, boff, odd, dbits, qs);
           const float* a = a_s + s * T::kRows + rs;
 #pragma unroll
           for (int bb = 0; bb < BPT; ++bb)
-            accumulate_block<MR, BPT>(acc, sad, bb, dbits[bb], qs[bb], a, a_ld_s, kc);
+            accumulate_block<MR, BPT, FMT>(acc, sad, bb, dbits[bb], qs[bb], a, a_ld_s, kc);
         }
       }
       __syncwarp();
@@ -611,9 +724,9 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
     }
 
     // ---- reduce the row phases ----
-    finish_acc<MR, BPT>(acc, sad);
+    finish_acc<MR, BPT, FMT>(acc, sad);
     float colv[MR][BPT];
-    reduce_tile<MR, BPT>(acc, red, warp, lane, tid, colv);
+    reduce_tile<MR, BPT, FMT>(acc, red, warp, lane, tid, colv);
 
     // ---- combine the splits of the cluster in fixed order ----
     // Column c of the tile is owned by cluster rank c % csize.  Every CTA
@@ -698,19 +811,17 @@ __global__ void __launch_bounds__(256) q4_moe_combine_kernel(float* out, const f
 // ---------------------------------------------------------------------------
 // Host-side launch helpers
 // ---------------------------------------------------------------------------
-template <int MODE, int MR, int BPT, bool BIG>
+template <int MODE, int MR, int BPT, bool BIG, int FMT>
 static cudaError_t launch_cfg(const GemvParams& p, dim3 grid, dim3 cluster, cudaStream_t st,
                               bool pdl) {
-  const SmemPlan plan = smem_plan<MR, BPT, BIG>(p.rows_per_split, p.list_cap);
-  cudaError_t e = cudaFuncSetAttribute(q4_gemv_kernel<MODE, MR, BPT, BIG>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const SmemPlan plan = smem_plan<MR, BPT, BIG, FMT>(p.rows_per_split, p.list_cap);
+  auto fn = q4_gemv_kernel<MODE, MR, BPT, BIG, FMT>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(plan.total));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(q4_gemv_kernel<MODE, MR, BPT, BIG>,
-                           cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(q4_gemv_kernel<MODE, MR, BPT, BIG>,
-                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -726,16 +837,16 @@ static cudaError_t launch_cfg(const GemvParams& p, dim3 grid, dim3 cluster, cuda
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, q4_gemv_kernel<MODE, MR, BPT, BIG>, p);
+  return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
-template <int MODE, bool BIG>
+template <int MODE, bool BIG, int FMT>
 static cudaError_t launch_mode(const GemvParams& p, int mr, int bpt, dim3 grid, dim3 cluster,
                                cudaStream_t st, bool pdl) {
-  if (bpt == 2 && mr == 1) return launch_cfg<MODE, 1, 2, BIG>(p, grid, cluster, st, pdl);
-  if (bpt == 1 && mr == 1) return launch_cfg<MODE, 1, 1, BIG>(p, grid, cluster, st, pdl);
-  if (bpt == 1 && mr == 2) return launch_cfg<MODE, 2, 1, BIG>(p, grid, cluster, st, pdl);
-  if (bpt == 1 && mr == 4) return launch_cfg<MODE, 4, 1, BIG>(p, grid, cluster, st, pdl);
+  if (bpt == 2 && mr == 1) return launch_cfg<MODE, 1, 2, BIG, FMT>(p, grid, cluster, st, pdl);
+  if (bpt == 1 && mr == 1) return launch_cfg<MODE, 1, 1, BIG, FMT>(p, grid, cluster, st, pdl);
+  if (bpt == 1 && mr == 2) return launch_cfg<MODE, 2, 1, BIG, FMT>(p, grid, cluster, st, pdl);
+  if (bpt == 1 && mr == 4) return launch_cfg<MODE, 4, 1, BIG, FMT>(p, grid, cluster, st, pdl);
   return cudaErrorInvalidValue;
 }
 
@@ -743,46 +854,58 @@ template <bool BIG>
 static cudaError_t launch_big(const GemvParams& p, int mr, int bpt, dim3 grid, dim3 cluster,
                               cudaStream_t st, bool pdl) {
   switch (p.mode) {
-    case kModeGemv: return launch_mode<kModeGemv, BIG>(p, mr, bpt, grid, cluster, st, pdl);
-    case kModeGateUp: return launch_mode<kModeGateUp, BIG>(p, mr, bpt, grid, cluster, st, pdl);
-    case kModeDown: return launch_mode<kModeDown, BIG>(p, mr, bpt, grid, cluster, st, pdl);
+    case kModeGemv: return launch_mode<kModeGemv, BIG, kFmtQ4>(p, mr, bpt, grid, cluster, st, pdl);
+    case kModeGateUp: return launch_mode<kModeGateUp, BIG, kFmtQ4>(p, mr, bpt, grid, cluster, st, pdl);
+    case kModeDown: return launch_mode<kModeDown, BIG, kFmtQ4>(p, mr, bpt, grid, cluster, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_gemv(const GemvParams& p, int mr, int bpt, bool big, dim3 grid, dim3 cluster,
-                        cudaStream_t st, bool pdl) {
+cudaError_t launch_gemv(const GemvParams& p, int mr, int bpt, bool big, int fmt, dim3 grid,
+                        dim3 cluster, cudaStream_t st, bool pdl) {
+  if (fmt == kFmtQ8) {   // the plain GEMV, 32-row stages only
+    if (p.mode != kModeGemv || big) return cudaErrorInvalidValue;
+    return launch_mode<kModeGemv, false, kFmtQ8>(p, mr, bpt, grid, cluster, st, pdl);
+  }
   return big ? launch_big<true>(p, mr, bpt, grid, cluster, st, pdl)
              : launch_big<false>(p, mr, bpt, grid, cluster, st, pdl);
 }
 
-template <bool BIG>
+template <bool BIG, int FMT>
 static void pick_instance(int mode, int mr, int bpt, int rows_per_split, int list_cap,
                           const void** fn, uint32_t* smem) {
-#define Q4_PICK(MO)                                                                 \
-  if (mode == MO) {                                                                 \
-    if (bpt == 2 && mr == 1) *fn = (const void*)q4_gemv_kernel<MO, 1, 2, BIG>;      \
-    else if (bpt == 1 && mr == 1) *fn = (const void*)q4_gemv_kernel<MO, 1, 1, BIG>; \
-    else if (bpt == 1 && mr == 2) *fn = (const void*)q4_gemv_kernel<MO, 2, 1, BIG>; \
-    else if (bpt == 1 && mr == 4) *fn = (const void*)q4_gemv_kernel<MO, 4, 1, BIG>; \
+#define Q4_PICK(MO)                                                                      \
+  if (mode == MO) {                                                                      \
+    if (bpt == 2 && mr == 1) *fn = (const void*)q4_gemv_kernel<MO, 1, 2, BIG, FMT>;      \
+    else if (bpt == 1 && mr == 1) *fn = (const void*)q4_gemv_kernel<MO, 1, 1, BIG, FMT>; \
+    else if (bpt == 1 && mr == 2) *fn = (const void*)q4_gemv_kernel<MO, 2, 1, BIG, FMT>; \
+    else if (bpt == 1 && mr == 4) *fn = (const void*)q4_gemv_kernel<MO, 4, 1, BIG, FMT>; \
   }
   Q4_PICK(kModeGemv)
-  Q4_PICK(kModeGateUp)
-  Q4_PICK(kModeDown)
+  if constexpr (FMT == kFmtQ4) {
+    Q4_PICK(kModeGateUp)
+    Q4_PICK(kModeDown)
+  }
 #undef Q4_PICK
-  if (bpt == 2) *smem = smem_plan<1, 2, BIG>(rows_per_split, list_cap).total;
-  else if (mr == 1) *smem = smem_plan<1, 1, BIG>(rows_per_split, list_cap).total;
-  else if (mr == 2) *smem = smem_plan<2, 1, BIG>(rows_per_split, list_cap).total;
-  else *smem = smem_plan<4, 1, BIG>(rows_per_split, list_cap).total;
+  if (bpt == 2) *smem = smem_plan<1, 2, BIG, FMT>(rows_per_split, list_cap).total;
+  else if (mr == 1) *smem = smem_plan<1, 1, BIG, FMT>(rows_per_split, list_cap).total;
+  else if (mr == 2) *smem = smem_plan<2, 1, BIG, FMT>(rows_per_split, list_cap).total;
+  else *smem = smem_plan<4, 1, BIG, FMT>(rows_per_split, list_cap).total;
 }
 
-int max_active_clusters(int mode, int mr, int bpt, bool big, int rows_per_split, int list_cap,
-                        dim3 cluster) {
+int max_active_clusters(int mode, int mr, int bpt, bool big, int fmt, int rows_per_split,
+                        int list_cap, dim3 cluster) {
   // occupancy query for the kernel instance that launch_gemv would pick
   const void* fn = nullptr;
   uint32_t smem = 0;
-  if (big) pick_instance<true>(mode, mr, bpt, rows_per_split, list_cap, &fn, &smem);
-  else pick_instance<false>(mode, mr, bpt, rows_per_split, list_cap, &fn, &smem);
+  if (fmt == kFmtQ8) {
+    if (big || mode != kModeGemv) return 0;
+    pick_instance<false, kFmtQ8>(mode, mr, bpt, rows_per_split, list_cap, &fn, &smem);
+  } else if (big) {
+    pick_instance<true, kFmtQ4>(mode, mr, bpt, rows_per_split, list_cap, &fn, &smem);
+  } else {
+    pick_instance<false, kFmtQ4>(mode, mr, bpt, rows_per_split, list_cap, &fn, &smem);
+  }
   if (!fn) return 0;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return 0;
@@ -832,12 +955,17 @@ int gemv_stage_rows(int bpt, bool big) {
   return bpt == 2 ? TileCfg<2, false>::kRows : TileCfg<1, false>::kRows;
 }
 
-void fill_decode_consts(GemvParams& p) {
-  for (int i = 0; i < 4; ++i) p.kmask[i] = 0xFu << (4 * i);
+void fill_decode_consts(GemvParams& p, int fmt) {
+  if (fmt == kFmtQ8) {
+    for (int i = 0; i < 3; ++i) p.kmask[i] = 0xFFu << (8 * i);
+    p.kmask[3] = 0x80808080u;   // sign flips: b = q + 128 in every byte
+  } else {
+    for (int i = 0; i < 4; ++i) p.kmask[i] = 0xFu << (4 * i);
+  }
 }
 
 bool encode_weight_tmap(CUtensorMap* map, const void* base, int64_t K, int64_t nb,
-                        int64_t experts, int64_t matrix_bytes, int bpt, bool big) {
+                        int64_t experts, int64_t matrix_bytes, int bpt, bool big, int fmt) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -849,16 +977,22 @@ bool encode_weight_tmap(CUtensorMap* map, const void* base, int64_t K, int64_t n
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   if (nb % kLanesPerRow != 0) return false;
-  // uint16 elements: a row is nb*9 halfwords; a box is one tile row segment
-  // (8*bpt blocks = 72*bpt halfwords) by the stage's rows.
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(nb * 9), static_cast<cuuint64_t>(K),
+  // Q4_0: uint16 elements, a row is nb*9 of them; Q8_0: uint32 elements, a
+  // row is nb*34/4 (nb is a multiple of 8, so the tile starts, 8*bpt blocks
+  // apart, are whole elements and 16-byte aligned).  A box is one tile row
+  // segment (8*bpt blocks) by the stage's rows.
+  const bool q8 = (fmt == kFmtQ8);
+  const int64_t bb = q8 ? Fmt<kFmtQ8>::kBytes : Fmt<kFmtQ4>::kBytes;
+  const int64_t es = q8 ? Fmt<kFmtQ8>::kTmaElem : Fmt<kFmtQ4>::kTmaElem;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(nb * bb / es), static_cast<cuuint64_t>(K),
                               static_cast<cuuint64_t>(experts)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(nb * kBlockBytes),
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(nb * bb),
                                  static_cast<cuuint64_t>(matrix_bytes)};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kLanesPerRow * bpt * 9),
-                             static_cast<cuuint32_t>(gemv_stage_rows(bpt, big)), 1u};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kLanesPerRow * bpt * bb / es),
+                             static_cast<cuuint32_t>(q8 ? 32 : gemv_stage_rows(bpt, big)), 1u};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims,
+  const CUresult r = encode(map, q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16,
+                            3, const_cast<void*>(base), dims,
                             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -9,6 +9,10 @@
 namespace q4 {
 
 enum : int { kModeGemv = 0, kModeGateUp = 1, kModeDown = 2 };
+// Weight formats of the GEMV kernel (values of the public Q4_LAYOUT_* codes
+// are not used here: the host maps Q4_LAYOUT_BLOCKS -> kFmtQ4 and
+// Q4_LAYOUT_Q8_0 -> kFmtQ8).
+enum : int { kFmtQ4 = 0, kFmtQ8 = 1 };
 
 // Arguments of q4_gemv_kernel (one struct, passed by value as a __grid_constant__
 // parameter so that the tensor maps inside it are addressable by TMA).
@@ -48,23 +52,24 @@ struct GemvParams {
 // big: 18 KB pipeline stages instead of 32-row ones (rows_per_split a multiple of
 // gemv_stage_rows(bpt, big) either way).
 // cluster: (1, nsplit, 1), or (1, nsplit, 2) for the gate/up kernel.
-cudaError_t launch_gemv(const GemvParams& p, int mr, int bpt, bool big, dim3 grid, dim3 cluster,
-                        cudaStream_t st, bool pdl);
+// fmt: kFmtQ4 (block_q4_0) or kFmtQ8 (Q8_0: plain GEMV mode and big = false only).
+cudaError_t launch_gemv(const GemvParams& p, int mr, int bpt, bool big, int fmt, dim3 grid,
+                        dim3 cluster, cudaStream_t st, bool pdl);
 constexpr int kMaxCluster = 16;   // non-portable thread-block cluster size limit
 // Clusters of shape `cluster` that can be resident at once for that kernel
 // configuration (0 if the configuration cannot launch).
-int max_active_clusters(int mode, int mr, int bpt, bool big, int rows_per_split, int list_cap,
-                        dim3 cluster);
+int max_active_clusters(int mode, int mr, int bpt, bool big, int fmt, int rows_per_split,
+                        int list_cap, dim3 cluster);
 // Rows of one TMA box (one pipeline stage) of the GEMV kernel.
 int gemv_stage_rows(int bpt, bool big);
 // Blocks per column tile for `bpt` blocks per thread.
 int gemv_tile_blocks(int bpt);
-void fill_decode_consts(GemvParams& p);
+void fill_decode_consts(GemvParams& p, int fmt);
 // Encodes the tensor map of `experts` stacked K x nb-block Q4_0 matrices,
 // `matrix_bytes` apart, with boxes of one tile row segment (8*bpt blocks) by one
 // stage of rows.  Needs nb % 8 == 0 and a 16-byte aligned base.
 bool encode_weight_tmap(CUtensorMap* map, const void* base, int64_t K, int64_t nb,
-                        int64_t experts, int64_t matrix_bytes, int bpt, bool big);
+                        int64_t experts, int64_t matrix_bytes, int bpt, bool big, int fmt);
 // out[t] = sum_k w[t,k] * y[t*topk+k] (slot order), plus addend[t] if given.
 cudaError_t launch_moe_combine(float* out, const float* y, const int32_t* idx, const float* w,
                                const float* addend, int T, int topk, int E, int H,

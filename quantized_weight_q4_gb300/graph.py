@@ -10,21 +10,23 @@ from __future__ import annotations
 
 import torch
 
-from . import q4_matmul_ex
+from . import Q4_LAYOUT_BLOCKS, q4_matmul_ex
 
 
 class MatmulSequence:
     """calls: list of (C, A, B, M, N, K) device tensors and sizes, run in order."""
 
-    def __init__(self, calls, workspace=None):
+    def __init__(self, calls, workspace=None, b_layout=Q4_LAYOUT_BLOCKS):
         self.calls = list(calls)
         self.workspace = workspace
+        self.b_layout = b_layout
         self.graph = None
         self.stream = torch.cuda.Stream()
 
     def run_eager(self, stream=None):
         for C, A, B, M, N, K in self.calls:
-            q4_matmul_ex(C, A, B, M, N, K, workspace=self.workspace, stream=stream)
+            q4_matmul_ex(C, A, B, M, N, K, workspace=self.workspace, stream=stream,
+                         b_layout=self.b_layout)
 
     def capture(self):
         # one eager pass first: sizes the library-owned workspace outside capture
