@@ -1,0 +1,62 @@
+"""The benchmark's N > 1 path on the CPU: two gloo ranks.
+
+The path has no exchange step, so several GPUs run independent replicas; what
+needs checking is the host side: the process group comes up from the torchrun
+environment, the timing is the maximum over ranks, and the reference arm runs
+and prints on rank 0 only while the other rank exits cleanly.
+"""
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out_path):
+    os.environ.update({"RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    sys.path.insert(0, ROOT)
+    import bench
+    ws, r, local = bench.dist_setup()
+    assert (ws, r, local) == (world, rank, rank)
+    bench.barrier(ws)
+    m = bench.max_over_ranks(ws, 10.0 + rank)
+    with open(f"{out_path}.{rank}", "w") as f:
+        f.write(repr(m))
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_two_gloo_ranks(tmp_path):
+    import torch.multiprocessing as mp
+    port = _free_port()
+    out = str(tmp_path / "m")
+    mp.start_processes(_worker, args=(2, port, out), nprocs=2, start_method="spawn", join=True)
+    for r in range(2):
+        assert float(open(f"{out}.{r}").read()) == 11.0
+
+
+def test_reference_arm_under_torchrun_prints_once(tmp_path):
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py",
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3",
+           "--ref-rows", "16"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["value"] > 0
