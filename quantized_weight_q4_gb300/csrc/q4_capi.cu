@@ -237,6 +237,41 @@ int launch_status(cudaError_t e) { return e == cudaSuccess ? Q4_OK : Q4_ERR_CUDA
 
 namespace {
 
+// The split-K GEMV of q4_matmul_ex for a validated problem (the caller holds
+// g_mu): C [M, N] = A [M, K] . W, weights in format `fmt`.
+int gemv_run(DeviceState* s, void* C, int c_dtype, const void* A, int a_dtype, const void* B,
+             int fmt, int64_t M, int64_t N, int64_t K, cudaStream_t st) {
+  const GemvShape& g = cached_gemv_shape(s, M, N, K, fmt);
+  if (g.nchunks > 65535 || 4LL * g.mr * g.rows_per_split > kMaxASliceBytes) return Q4_ERR_SHAPE;
+
+  q4::GemvParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.mode = q4::kModeGemv;
+  p.B = static_cast<const uint8_t*>(B);
+  p.K = static_cast<int>(K);
+  p.N = static_cast<int>(N);
+  p.nb = static_cast<int>(ceil_div(N, 32));
+  p.nsplit = g.nsplit;
+  p.rows_per_split = g.rows_per_split;
+  q4::fill_decode_consts(p, fmt);
+  const int64_t block_bytes = (fmt == q4::kFmtQ8) ? 34 : 18;
+  p.use_tma = (p.nb % 8 == 0 &&
+               q4::encode_weight_tmap(&p.tmap[0], B, K, p.nb, 1, K * p.nb * block_bytes, g.bpt,
+                                      g.big, fmt))
+                  ? 1 : 0;
+  p.A = A;
+  p.a_dtype = a_dtype;
+  p.a_ld = K;
+  p.M = static_cast<int>(M);
+  p.C = C;
+  p.c_dtype = c_dtype;
+  p.list_cap = 0;
+  p.err = s->status;
+  const dim3 grid(g.ntiles, g.nsplit, g.nchunks);
+  return launch_status(q4::launch_gemv(p, g.mr, g.bpt, g.big, fmt, grid, dim3(1, g.nsplit, 1),
+                                       st, true));
+}
+
 // The routed-expert kernels (gate/up, down, slot combine) for a validated
 // problem, on a workspace of at least m.total bytes; the combine adds
 // `addend` (fp32 [T, H], or null) after the weighted sum.
@@ -365,35 +400,7 @@ int q4_matmul_ex(void* C, int c_dtype, const void* A, int a_dtype, const void* B
       q4::gemm_supported(M, N, K) && (M > 128 || q4::gemm_small_split(M, N, K) > 0))
     return launch_status(q4::launch_gemm(C, c_dtype, A, B, M, N, K, s->status, s->sms,
                                          static_cast<cudaStream_t>(stream)));
-  const GemvShape& g = cached_gemv_shape(s, M, N, K, fmt);
-  if (g.nchunks > 65535 || 4LL * g.mr * g.rows_per_split > kMaxASliceBytes) return Q4_ERR_SHAPE;
-
-  q4::GemvParams p;
-  std::memset(&p, 0, sizeof(p));
-  p.mode = q4::kModeGemv;
-  p.B = static_cast<const uint8_t*>(B);
-  p.K = static_cast<int>(K);
-  p.N = static_cast<int>(N);
-  p.nb = static_cast<int>(ceil_div(N, 32));
-  p.nsplit = g.nsplit;
-  p.rows_per_split = g.rows_per_split;
-  q4::fill_decode_consts(p, fmt);
-  const int64_t block_bytes = (fmt == q4::kFmtQ8) ? 34 : 18;
-  p.use_tma = (p.nb % 8 == 0 &&
-               q4::encode_weight_tmap(&p.tmap[0], B, K, p.nb, 1, K * p.nb * block_bytes, g.bpt,
-                                      g.big, fmt))
-                  ? 1 : 0;
-  p.A = A;
-  p.a_dtype = a_dtype;
-  p.a_ld = K;
-  p.M = static_cast<int>(M);
-  p.C = C;
-  p.c_dtype = c_dtype;
-  p.list_cap = 0;
-  p.err = s->status;
-  const dim3 grid(g.ntiles, g.nsplit, g.nchunks);
-  return launch_status(q4::launch_gemv(p, g.mr, g.bpt, g.big, fmt, grid, dim3(1, g.nsplit, 1),
-                                       static_cast<cudaStream_t>(stream), true));
+  return gemv_run(s, C, c_dtype, A, a_dtype, B, fmt, M, N, K, static_cast<cudaStream_t>(stream));
 }
 
 int q4_matmul(float* C, const float* A, const void* B, int64_t M, int64_t N, int64_t K) {
@@ -461,8 +468,15 @@ namespace {
 // Workspace of q4_moe_block: routing, the shared expert's routing and output,
 // then one expert workspace serving the routed and the shared problem in turn.
 struct BlockLayout {
-  size_t idx, w, sidx, sw, ys, moe, total;
+  size_t idx, w, sidx, sw, ys, sg, su, sh, moe, total;
 };
+
+// The shared expert runs as one (E = 1) routed expert at T = 1, where gate and
+// up share a kernel; with more tokens it is a dense FFN over all T rows: two
+// GEMVs (gate, up) whose row chunks run side by side, SiLU(g)*u, and a GEMV
+// for down -- rather than one expert kernel passing over its weights once per
+// few tokens.
+bool shared_dense(int64_t T) { return T > 1; }
 BlockLayout block_layout(int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I, int64_t Is) {
   BlockLayout b;
   size_t o = 0;
@@ -476,9 +490,16 @@ BlockLayout block_layout(int64_t T, int64_t topk, int64_t E, int64_t H, int64_t 
   o += round_up(static_cast<size_t>(T) * 4, 256);
   b.ys = o;
   o += (Is > 0) ? round_up(static_cast<size_t>(T * H) * 4, 256) : 0;
+  const size_t tis = (Is > 0 && shared_dense(T)) ? round_up(static_cast<size_t>(T * Is) * 4, 256) : 0;
+  b.sg = o;
+  o += tis;
+  b.su = o;
+  o += tis;
+  b.sh = o;
+  o += tis;
   b.moe = o;
   size_t need = q4_moe_workspace_size(T, topk, E, H, I);
-  if (Is > 0) {
+  if (Is > 0 && !shared_dense(T)) {
     const size_t sneed = q4_moe_workspace_size(T, 1, 1, H, Is);
     if (sneed > need) need = sneed;
   }
@@ -517,10 +538,16 @@ int q4_moe_block(float* out, const void* x, int x_dtype, const float* logits, co
   if (4LL * m.mr * m.rows_gu > kMaxASliceBytes || 4LL * m.mr * m.rows_d > kMaxASliceBytes)
     return Q4_ERR_SHAPE;
   const MoeShape* ms = nullptr;
-  if (Is > 0) {
+  if (Is > 0 && !shared_dense(T)) {
     ms = &cached_moe_shape(s, T, 1, 1, H, Is);
     if (4LL * ms->mr * ms->rows_gu > kMaxASliceBytes || 4LL * ms->mr * ms->rows_d > kMaxASliceBytes)
       return Q4_ERR_SHAPE;
+  }
+  if (Is > 0 && shared_dense(T)) {
+    for (const auto& kn : {std::make_pair(H, Is), std::make_pair(Is, H)}) {
+      const GemvShape& g = cached_gemv_shape(s, T, kn.second, kn.first, q4::kFmtQ4);
+      if (g.nchunks > 65535 || 4LL * g.mr * g.rows_per_split > kMaxASliceBytes) return Q4_ERR_SHAPE;
+    }
   }
   const BlockLayout b = block_layout(T, topk, E, H, I, Is);
   void* ws = workspace;
@@ -544,9 +571,20 @@ int q4_moe_block(float* out, const void* x, int x_dtype, const float* logits, co
                                       Is > 0 ? sw : nullptr, st);
   if (e != cudaSuccess) return Q4_ERR_CUDA;
   // shared expert: every token, weight 1
-  if (Is > 0) {
+  if (Is > 0 && !shared_dense(T)) {
     rc = moe_run(s, *ms, ys, x, x_dtype, S_gate, S_up, S_down, sidx, sw, T, 1, 1, H, Is,
                  w8 + b.moe, nullptr, st);
+    if (rc != Q4_OK) return rc;
+  } else if (Is > 0) {
+    float* sg = reinterpret_cast<float*>(w8 + b.sg);
+    float* su = reinterpret_cast<float*>(w8 + b.su);
+    float* sh = reinterpret_cast<float*>(w8 + b.sh);
+    rc = gemv_run(s, sg, Q4_F32, x, x_dtype, S_gate, q4::kFmtQ4, T, Is, H, st);
+    if (rc == Q4_OK) rc = gemv_run(s, su, Q4_F32, x, x_dtype, S_up, q4::kFmtQ4, T, Is, H, st);
+    if (rc != Q4_OK) return rc;
+    if (q4::launch_silu_mul(sh, sg, su, static_cast<size_t>(T * Is), st) != cudaSuccess)
+      return Q4_ERR_CUDA;
+    rc = gemv_run(s, ys, Q4_F32, sh, Q4_F32, S_down, q4::kFmtQ4, T, H, Is, st);
     if (rc != Q4_OK) return rc;
   }
   // routed experts; the shared expert's rows are added after the weighted sum

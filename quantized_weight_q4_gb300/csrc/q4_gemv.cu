@@ -808,6 +808,34 @@ __global__ void __launch_bounds__(256) q4_moe_combine_kernel(float* out, const f
   }
 }
 
+// h[i] = SiLU(g[i]) * u[i] = g / (1 + exp(-g)) * u, in fp32 (the expert
+// chain's middle step when gate and up run as separate matmuls).
+__global__ void __launch_bounds__(256) q4_silu_mul_kernel(float* h, const float* g, const float* u,
+                                                          size_t n) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float gv = g[i];
+    h[i] = gv / (1.0f + __expf(-gv)) * u[i];
+  }
+}
+
+cudaError_t launch_silu_mul(float* h, const float* g, const float* u, size_t n, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  size_t nblocks = (n + 255) / 256;
+  if (nblocks > 1184) nblocks = 1184;
+  cfg.gridDim = dim3(static_cast<unsigned>(nblocks));
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, q4_silu_mul_kernel, h, g, u, n);
+}
+
 // ---------------------------------------------------------------------------
 // Host-side launch helpers
 // ---------------------------------------------------------------------------

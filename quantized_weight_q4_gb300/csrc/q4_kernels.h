@@ -70,6 +70,8 @@ void fill_decode_consts(GemvParams& p, int fmt);
 // stage of rows.  Needs nb % 8 == 0 and a 16-byte aligned base.
 bool encode_weight_tmap(CUtensorMap* map, const void* base, int64_t K, int64_t nb,
                         int64_t experts, int64_t matrix_bytes, int bpt, bool big, int fmt);
+// h[i] = SiLU(g[i]) * u[i] for i < n, fp32 (programmatic dependent launch).
+cudaError_t launch_silu_mul(float* h, const float* g, const float* u, size_t n, cudaStream_t st);
 // out[t] = sum_k w[t,k] * y[t*topk+k] (slot order), plus addend[t] if given.
 cudaError_t launch_moe_combine(float* out, const float* y, const int32_t* idx, const float* w,
                                const float* addend, int T, int topk, int E, int H,
