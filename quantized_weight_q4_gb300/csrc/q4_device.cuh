@@ -1,5 +1,6 @@
 // Device-side helpers shared by the sm_103a kernels: inline PTX for mbarriers,
-// TMA bulk copies, programmatic dependent launch and packed fp32x2 arithmetic.
+// TMA tensor copies, programmatic dependent launch, clusters and packed fp32x2
+// arithmetic.
 #pragma once
 
 #include <cstdint>
@@ -117,17 +118,6 @@ __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, vol
   }
 }
 
-// ---- TMA bulk copy (non-tensor): global -> shared, completes on an mbarrier --
-// Requirements: dst and src 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
-                                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // ---- TMA tensor copy: a 3-D box of a tensor map -> shared, completes on an mbarrier
 // (coordinates in elements; the tensor map must live in param/const/global space)
 __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int c0, int c1, int c2,
@@ -172,15 +162,6 @@ __device__ __forceinline__ void st_peer(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
-// Loads from a peer's shared memory.  Volatile keeps it after the preceding
-// cluster barrier; without a memory clobber, consecutive loads can be in
-// flight together.
-__device__ __forceinline__ float ld_peer(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-  return v;
-}
-
 // ---- packed fp32x2 arithmetic (sm_100+) -------------------------------------
 typedef unsigned long long f32x2;
 
@@ -205,11 +186,6 @@ __device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
 __device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
   f32x2 d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
-  f32x2 d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 

@@ -21,7 +21,8 @@ def L():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"Q4_API\s+[\w\s\*]+?\b(q4_\w+)\s*\(", text)))
 

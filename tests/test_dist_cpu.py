@@ -44,7 +44,8 @@ def test_max_over_ranks_with_two_gloo_ranks(tmp_path):
     out = str(tmp_path / "m")
     mp.start_processes(_worker, args=(2, port, out), nprocs=2, start_method="spawn", join=True)
     for r in range(2):
-        assert float(open(f"{out}.{r}").read()) == 11.0
+        with open(f"{out}.{r}") as f:
+            assert float(f.read()) == 11.0
 
 
 def test_reference_arm_under_torchrun_prints_once(tmp_path):

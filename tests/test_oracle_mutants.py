@@ -82,7 +82,8 @@ BATTERY = [
 
 
 def _build_mutant(tmp_path, name, old, new):
-    src = open(os.path.join(os.path.dirname(oracle.__file__), "q4_oracle.c")).read()
+    with open(os.path.join(os.path.dirname(oracle.__file__), "q4_oracle.c")) as f:
+        src = f.read()
     assert src.count(old) == 1, f"mutation site for '{name}' not unique"
     path = tmp_path / "mut.c"
     path.write_text(src.replace(old, new))
