@@ -126,14 +126,19 @@ struct SmemPlan {
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
+// owner_splits: 0 for the expert modes (every cluster rank owns a share of
+// the columns); the split count for the plain GEMV, whose rank 0 receives the
+// partial sums of every split for every column.
 template <int MR, int BPT, bool BIG, int FMT>
-__host__ __device__ inline SmemPlan smem_plan(int rows_per_split, int list_cap) {
+__host__ __device__ inline SmemPlan smem_plan(int rows_per_split, int list_cap, int owner_splits) {
   using T = TileCfg<BPT, BIG, FMT>;
   SmemPlan p;
   p.ring = 0;   // the dynamic shared-memory base is 128-byte aligned
   p.red = align_up(T::kStages * T::kStageBytes, 16);
   p.cpart = p.red + Crew<MR>::kWarps * MR * kRedStride<BPT> * 4;
-  p.bars = p.cpart + MR * (T::kCols + 2 * kMaxCluster) * 4;   // partials received from the cluster
+  // partials received from the cluster
+  p.bars = p.cpart + (owner_splits > 0 ? MR * T::kCols * owner_splits
+                                        : MR * (T::kCols + 2 * kMaxCluster)) * 4;
   p.a = p.bars + 2 * T::kStages * 8;
   p.list = align_up(p.a + MR * align_up(rows_per_split, T::kRows) * 4, 16);
   p.total = align_up(p.list + list_cap * 4 + 64, 128);
@@ -540,7 +545,8 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
   using T = TileCfg<BPT, BIG, FMT>;
   constexpr int kGroups = Crew<MR>::kWarps / T::kGroupWarps;
   extern __shared__ __align__(128) uint8_t smem[];
-  const SmemPlan plan = smem_plan<MR, BPT, BIG, FMT>(p.rows_per_split, p.list_cap);
+  const SmemPlan plan = smem_plan<MR, BPT, BIG, FMT>(p.rows_per_split, p.list_cap,
+                                                     MODE == kModeGemv ? p.nsplit : 0);
   uint8_t* ring = smem + plan.ring;
   float* red = reinterpret_cast<float*>(smem + plan.red);
   float* cpart = reinterpret_cast<float*>(smem + plan.cpart);
@@ -729,11 +735,41 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
     reduce_tile<MR, BPT, FMT>(acc, red, warp, lane, tid, colv);
 
     // ---- combine the splits of the cluster in fixed order ----
+    if constexpr (MODE == kModeGemv) {
+      // Plain GEMV (one pass): cluster rank 0 receives every split's partial
+      // of every column, as [m][sender][column], and finishes the tile
+      // alone, adding in fixed rank order; the other CTAs exit right after
+      // the barrier, so that their SMs can take the next kernel's clusters
+      // while rank 0 adds and stores.
+      const int rank = static_cast<int>(cluster_ctarank());
+      const int ns = p.nsplit;
+      if (tid < 256) {
+#pragma unroll
+        for (int m = 0; m < MR; ++m)
+#pragma unroll
+          for (int i = 0; i < BPT; ++i) {
+            float* dst = cpart + (m * ns + rank) * T::kCols + tid + 256 * i;
+            st_peer(peer_addr(dst, 0), colv[m][i]);
+          }
+      }
+      cluster_sync();   // every partial has reached rank 0
+      if (rank == 0) {
+        for (int c = tid; c < tile_cols; c += Crew<MR>::kConsumers) {
+          const int col = b0 * kBlockCols + c;
+          if (col >= ncols) break;
+          for (int m = 0; m < mvalid; ++m) {
+            const float* v = cpart + m * ns * T::kCols + c;
+            float acc_s = 0.f;
+            for (int sp = 0; sp < ns; ++sp) acc_s += v[sp * T::kCols];
+            store_out(p, static_cast<size_t>(m0 + m) * ncols + col, acc_s);
+          }
+        }
+      }
+    } else {
     // Column c of the tile is owned by cluster rank c % csize.  Every CTA
     // stores its partial of each column into the owner's receive buffer, at
     // slot (rank of the sender); after one cluster barrier each owner adds
     // its columns' partials, in fixed rank order, from its own shared memory.
-    {
       const int rank = static_cast<int>(cluster_ctarank());
       const int ns = p.nsplit;
       const int csize = (MODE == kModeGateUp) ? 2 * ns : ns;
@@ -770,10 +806,7 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
           } else {
             float acc_s = 0.f;
             for (int sp = 0; sp < ns; ++sp) acc_s += v[sp];
-            if constexpr (MODE == kModeGemv)
-              store_out(p, static_cast<size_t>(m0 + m) * ncols + col, acc_s);
-            else
-              p.y[static_cast<size_t>(list[m0 + m]) * ncols + col] = acc_s;
+            p.y[static_cast<size_t>(list[m0 + m]) * ncols + col] = acc_s;
           }
         }
       }
@@ -842,7 +875,8 @@ cudaError_t launch_silu_mul(float* h, const float* g, const float* u, size_t n, 
 template <int MODE, int MR, int BPT, bool BIG, int FMT>
 static cudaError_t launch_cfg(const GemvParams& p, dim3 grid, dim3 cluster, cudaStream_t st,
                               bool pdl) {
-  const SmemPlan plan = smem_plan<MR, BPT, BIG, FMT>(p.rows_per_split, p.list_cap);
+  const SmemPlan plan = smem_plan<MR, BPT, BIG, FMT>(p.rows_per_split, p.list_cap,
+                                                     MODE == kModeGemv ? p.nsplit : 0);
   auto fn = q4_gemv_kernel<MODE, MR, BPT, BIG, FMT>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(plan.total));
@@ -901,7 +935,8 @@ cudaError_t launch_gemv(const GemvParams& p, int mr, int bpt, bool big, int fmt,
 
 template <bool BIG, int FMT>
 static void pick_instance(int mode, int mr, int bpt, int rows_per_split, int list_cap,
-                          const void** fn, uint32_t* smem) {
+                          int nsplit, const void** fn, uint32_t* smem) {
+  const int owner_splits = (mode == kModeGemv) ? nsplit : 0;
 #define Q4_PICK(MO)                                                                      \
   if (mode == MO) {                                                                      \
     if (bpt == 2 && mr == 1) *fn = (const void*)q4_gemv_kernel<MO, 1, 2, BIG, FMT>;      \
@@ -915,10 +950,10 @@ static void pick_instance(int mode, int mr, int bpt, int rows_per_split, int lis
     Q4_PICK(kModeDown)
   }
 #undef Q4_PICK
-  if (bpt == 2) *smem = smem_plan<1, 2, BIG, FMT>(rows_per_split, list_cap).total;
-  else if (mr == 1) *smem = smem_plan<1, 1, BIG, FMT>(rows_per_split, list_cap).total;
-  else if (mr == 2) *smem = smem_plan<2, 1, BIG, FMT>(rows_per_split, list_cap).total;
-  else *smem = smem_plan<4, 1, BIG, FMT>(rows_per_split, list_cap).total;
+  if (bpt == 2) *smem = smem_plan<1, 2, BIG, FMT>(rows_per_split, list_cap, owner_splits).total;
+  else if (mr == 1) *smem = smem_plan<1, 1, BIG, FMT>(rows_per_split, list_cap, owner_splits).total;
+  else if (mr == 2) *smem = smem_plan<2, 1, BIG, FMT>(rows_per_split, list_cap, owner_splits).total;
+  else *smem = smem_plan<4, 1, BIG, FMT>(rows_per_split, list_cap, owner_splits).total;
 }
 
 int max_active_clusters(int mode, int mr, int bpt, bool big, int fmt, int rows_per_split,
@@ -928,11 +963,11 @@ int max_active_clusters(int mode, int mr, int bpt, bool big, int fmt, int rows_p
   uint32_t smem = 0;
   if (fmt == kFmtQ8) {
     if (big || mode != kModeGemv) return 0;
-    pick_instance<false, kFmtQ8>(mode, mr, bpt, rows_per_split, list_cap, &fn, &smem);
+    pick_instance<false, kFmtQ8>(mode, mr, bpt, rows_per_split, list_cap, cluster.y, &fn, &smem);
   } else if (big) {
-    pick_instance<true, kFmtQ4>(mode, mr, bpt, rows_per_split, list_cap, &fn, &smem);
+    pick_instance<true, kFmtQ4>(mode, mr, bpt, rows_per_split, list_cap, cluster.y, &fn, &smem);
   } else {
-    pick_instance<false, kFmtQ4>(mode, mr, bpt, rows_per_split, list_cap, &fn, &smem);
+    pick_instance<false, kFmtQ4>(mode, mr, bpt, rows_per_split, list_cap, cluster.y, &fn, &smem);
   }
   if (!fn) return 0;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
