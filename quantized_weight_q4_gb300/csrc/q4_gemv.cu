@@ -126,19 +126,16 @@ struct SmemPlan {
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// owner_splits: 0 for the expert modes (every cluster rank owns a share of
-// the columns); the split count for the plain GEMV, whose rank 0 receives the
-// partial sums of every split for every column.
+// senders: the CTAs of a cluster (the split count; twice it for gate/up),
+// whose partial sums of every column cluster rank 0 receives.
 template <int MR, int BPT, bool BIG, int FMT>
-__host__ __device__ inline SmemPlan smem_plan(int rows_per_split, int list_cap, int owner_splits) {
+__host__ __device__ inline SmemPlan smem_plan(int rows_per_split, int list_cap, int senders) {
   using T = TileCfg<BPT, BIG, FMT>;
   SmemPlan p;
   p.ring = 0;   // the dynamic shared-memory base is 128-byte aligned
   p.red = align_up(T::kStages * T::kStageBytes, 16);
   p.cpart = p.red + Crew<MR>::kWarps * MR * kRedStride<BPT> * 4;
-  // partials received from the cluster
-  p.bars = p.cpart + (owner_splits > 0 ? MR * T::kCols * owner_splits
-                                        : MR * (T::kCols + 2 * kMaxCluster)) * 4;
+  p.bars = p.cpart + MR * T::kCols * senders * 4;   // partials received from the cluster
   p.a = p.bars + 2 * T::kStages * 8;
   p.list = align_up(p.a + MR * align_up(rows_per_split, T::kRows) * 4, 16);
   p.total = align_up(p.list + list_cap * 4 + 64, 128);
@@ -546,7 +543,7 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
   constexpr int kGroups = Crew<MR>::kWarps / T::kGroupWarps;
   extern __shared__ __align__(128) uint8_t smem[];
   const SmemPlan plan = smem_plan<MR, BPT, BIG, FMT>(p.rows_per_split, p.list_cap,
-                                                     MODE == kModeGemv ? p.nsplit : 0);
+                                                     MODE == kModeGateUp ? 2 * p.nsplit : p.nsplit);
   uint8_t* ring = smem + plan.ring;
   float* red = reinterpret_cast<float*>(smem + plan.red);
   float* cpart = reinterpret_cast<float*>(smem + plan.cpart);
@@ -735,20 +732,22 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
     reduce_tile<MR, BPT, FMT>(acc, red, warp, lane, tid, colv);
 
     // ---- combine the splits of the cluster in fixed order ----
-    if constexpr (MODE == kModeGemv) {
-      // Plain GEMV (one pass): cluster rank 0 receives every split's partial
-      // of every column, as [m][sender][column], and finishes the tile
-      // alone, adding in fixed rank order; the other CTAs exit right after
-      // the barrier, so that their SMs can take the next kernel's clusters
-      // while rank 0 adds and stores.
+    // Cluster rank 0 receives every sender's partial of every column, as
+    // [m][sender][column], and finishes the tile alone, adding in fixed rank
+    // order (gate/up: senders 0..ns-1 hold gate partials, ns..2ns-1 up
+    // partials).  After the last pass the other CTAs exit right after the
+    // barrier, so that their SMs can take the next kernel's clusters while
+    // rank 0 adds and stores.
+    {
       const int rank = static_cast<int>(cluster_ctarank());
       const int ns = p.nsplit;
+      const int csize = (MODE == kModeGateUp) ? 2 * ns : ns;
       if (tid < 256) {
 #pragma unroll
         for (int m = 0; m < MR; ++m)
 #pragma unroll
           for (int i = 0; i < BPT; ++i) {
-            float* dst = cpart + (m * ns + rank) * T::kCols + tid + 256 * i;
+            float* dst = cpart + (m * csize + rank) * T::kCols + tid + 256 * i;
             st_peer(peer_addr(dst, 0), colv[m][i]);
           }
       }
@@ -758,60 +757,29 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
           const int col = b0 * kBlockCols + c;
           if (col >= ncols) break;
           for (int m = 0; m < mvalid; ++m) {
-            const float* v = cpart + m * ns * T::kCols + c;
-            float acc_s = 0.f;
-            for (int sp = 0; sp < ns; ++sp) acc_s += v[sp * T::kCols];
-            store_out(p, static_cast<size_t>(m0 + m) * ncols + col, acc_s);
-          }
-        }
-      }
-    } else {
-    // Column c of the tile is owned by cluster rank c % csize.  Every CTA
-    // stores its partial of each column into the owner's receive buffer, at
-    // slot (rank of the sender); after one cluster barrier each owner adds
-    // its columns' partials, in fixed rank order, from its own shared memory.
-      const int rank = static_cast<int>(cluster_ctarank());
-      const int ns = p.nsplit;
-      const int csize = (MODE == kModeGateUp) ? 2 * ns : ns;
-      // receive buffer: [m][column slot within owner][sender], sized MR * kCols floats
-      const int per_owner = (T::kCols + csize - 1) / csize;
-      if (tid < 256) {
-#pragma unroll
-        for (int m = 0; m < MR; ++m)
-#pragma unroll
-          for (int i = 0; i < BPT; ++i) {
-            const int c = tid + 256 * i;
-            const int owner = c % csize;
-            const int slot = c / csize;
-            float* dst = cpart + (m * per_owner + slot) * csize + rank;
-            st_peer(peer_addr(dst, owner), colv[m][i]);
-          }
-      }
-      cluster_sync();   // every partial has reached its owner
-      const int tc = tid * csize + rank;   // the column this thread finishes
-      const int col = b0 * kBlockCols + tc;
-      if (tid < per_owner && tc < tile_cols && col < ncols) {
-        for (int m = 0; m < mvalid; ++m) {
-          const float* v = cpart + (m * per_owner + tid) * csize;
-          if constexpr (MODE == kModeGateUp) {
-            // senders 0..ns-1 hold gate partials, ns..2ns-1 up partials
-            float g = 0.f, u = 0.f;
-            for (int sp = 0; sp < ns; ++sp) {
-              g += v[sp];
-              u += v[ns + sp];
+            const float* v = cpart + m * csize * T::kCols + c;
+            if constexpr (MODE == kModeGateUp) {
+              float g = 0.f, u = 0.f;
+              for (int sp = 0; sp < ns; ++sp) {
+                g += v[sp * T::kCols];
+                u += v[(ns + sp) * T::kCols];
+              }
+              // SiLU(g) * u, SiLU(g) = g * sigmoid(g)
+              const float silu = g / (1.0f + __expf(-g));
+              p.h[static_cast<size_t>(list[m0 + m]) * ncols + col] = silu * u;
+            } else {
+              float acc_s = 0.f;
+              for (int sp = 0; sp < ns; ++sp) acc_s += v[sp * T::kCols];
+              if constexpr (MODE == kModeGemv)
+                store_out(p, static_cast<size_t>(m0 + m) * ncols + col, acc_s);
+              else
+                p.y[static_cast<size_t>(list[m0 + m]) * ncols + col] = acc_s;
             }
-            // SiLU(g) * u, SiLU(g) = g * sigmoid(g)
-            const float silu = g / (1.0f + __expf(-g));
-            p.h[static_cast<size_t>(list[m0 + m]) * ncols + col] = silu * u;
-          } else {
-            float acc_s = 0.f;
-            for (int sp = 0; sp < ns; ++sp) acc_s += v[sp];
-            p.y[static_cast<size_t>(list[m0 + m]) * ncols + col] = acc_s;
           }
         }
       }
-      // another pass will push into the receive buffers again: wait until
-      // every owner has read this pass's partials
+      // another pass will push into rank 0's buffer again: wait until it has
+      // read this pass's partials
       if (pass + 1 < passes) cluster_sync();
     }
   }
@@ -876,7 +844,7 @@ template <int MODE, int MR, int BPT, bool BIG, int FMT>
 static cudaError_t launch_cfg(const GemvParams& p, dim3 grid, dim3 cluster, cudaStream_t st,
                               bool pdl) {
   const SmemPlan plan = smem_plan<MR, BPT, BIG, FMT>(p.rows_per_split, p.list_cap,
-                                                     MODE == kModeGemv ? p.nsplit : 0);
+                                                     MODE == kModeGateUp ? 2 * p.nsplit : p.nsplit);
   auto fn = q4_gemv_kernel<MODE, MR, BPT, BIG, FMT>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(plan.total));
@@ -935,8 +903,7 @@ cudaError_t launch_gemv(const GemvParams& p, int mr, int bpt, bool big, int fmt,
 
 template <bool BIG, int FMT>
 static void pick_instance(int mode, int mr, int bpt, int rows_per_split, int list_cap,
-                          int nsplit, const void** fn, uint32_t* smem) {
-  const int owner_splits = (mode == kModeGemv) ? nsplit : 0;
+                          int senders, const void** fn, uint32_t* smem) {
 #define Q4_PICK(MO)                                                                      \
   if (mode == MO) {                                                                      \
     if (bpt == 2 && mr == 1) *fn = (const void*)q4_gemv_kernel<MO, 1, 2, BIG, FMT>;      \
@@ -950,10 +917,10 @@ static void pick_instance(int mode, int mr, int bpt, int rows_per_split, int lis
     Q4_PICK(kModeDown)
   }
 #undef Q4_PICK
-  if (bpt == 2) *smem = smem_plan<1, 2, BIG, FMT>(rows_per_split, list_cap, owner_splits).total;
-  else if (mr == 1) *smem = smem_plan<1, 1, BIG, FMT>(rows_per_split, list_cap, owner_splits).total;
-  else if (mr == 2) *smem = smem_plan<2, 1, BIG, FMT>(rows_per_split, list_cap, owner_splits).total;
-  else *smem = smem_plan<4, 1, BIG, FMT>(rows_per_split, list_cap, owner_splits).total;
+  if (bpt == 2) *smem = smem_plan<1, 2, BIG, FMT>(rows_per_split, list_cap, senders).total;
+  else if (mr == 1) *smem = smem_plan<1, 1, BIG, FMT>(rows_per_split, list_cap, senders).total;
+  else if (mr == 2) *smem = smem_plan<2, 1, BIG, FMT>(rows_per_split, list_cap, senders).total;
+  else *smem = smem_plan<4, 1, BIG, FMT>(rows_per_split, list_cap, senders).total;
 }
 
 int max_active_clusters(int mode, int mr, int bpt, bool big, int fmt, int rows_per_split,
@@ -961,13 +928,14 @@ int max_active_clusters(int mode, int mr, int bpt, bool big, int fmt, int rows_p
   // occupancy query for the kernel instance that launch_gemv would pick
   const void* fn = nullptr;
   uint32_t smem = 0;
+  const int senders = static_cast<int>(cluster.y * cluster.z);
   if (fmt == kFmtQ8) {
     if (big || mode != kModeGemv) return 0;
-    pick_instance<false, kFmtQ8>(mode, mr, bpt, rows_per_split, list_cap, cluster.y, &fn, &smem);
+    pick_instance<false, kFmtQ8>(mode, mr, bpt, rows_per_split, list_cap, senders, &fn, &smem);
   } else if (big) {
-    pick_instance<true, kFmtQ4>(mode, mr, bpt, rows_per_split, list_cap, cluster.y, &fn, &smem);
+    pick_instance<true, kFmtQ4>(mode, mr, bpt, rows_per_split, list_cap, senders, &fn, &smem);
   } else {
-    pick_instance<false, kFmtQ4>(mode, mr, bpt, rows_per_split, list_cap, cluster.y, &fn, &smem);
+    pick_instance<false, kFmtQ4>(mode, mr, bpt, rows_per_split, list_cap, senders, &fn, &smem);
   }
   if (!fn) return 0;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
