@@ -182,6 +182,21 @@ def sweep_plan(layers, block_bytes=18):
     return shapes, wbytes
 
 
+def device_weights(torch, q4, dev, K, N, fmt, seed, stream):
+    """(weights on the device, their Q4_LAYOUT_* code) for a seeded K x N
+    matrix: Q4_0 or Q8_0 blocks, or Q4_0 blocks repacked once, on the GPU and
+    before any timing, into the planar layout."""
+    gen = si.q8_weights if fmt == "q8_0" else si.q4_weights
+    B = torch.from_numpy(gen(K, N, seed=seed, stream=stream)).to(dev)
+    if fmt == "q8_0":
+        return B, q4.Q4_LAYOUT_Q8_0
+    if fmt == "q4_0_planar":
+        P = torch.empty(q4.q4_planar_bytes(K, N), dtype=torch.uint8, device=dev)
+        q4.q4_repack(P, B, K, N)
+        return P, q4.Q4_LAYOUT_PLANAR
+    return B, q4.Q4_LAYOUT_BLOCKS
+
+
 def build_sweep(torch, dev, layers, seed=0, fmt="q4_0"):
     """Device weights, one contiguous A buffer and one contiguous C buffer."""
     import quantized_weight_q4_gb300 as q4
@@ -200,15 +215,16 @@ def build_sweep(torch, dev, layers, seed=0, fmt="q4_0"):
     hC = torch.empty(oc, dtype=torch.float32).pin_memory()
     calls = []
     weights = []
+    layout = q4.Q4_LAYOUT_BLOCKS
     for i, (K, N) in enumerate(shapes):
-        gen = si.q8_weights if q8 else si.q4_weights
-        B = torch.from_numpy(gen(K, N, seed=seed, stream=100 + i)).to(dev)
+        B, layout = device_weights(torch, q4, dev, K, N, fmt, seed, 100 + i)
         weights.append(B)
         hA[a_off[i]:a_off[i] + K] = torch.from_numpy(si.activations_f32(1, K, seed, 10000 + i)[0])
         calls.append((dC[c_off[i]:c_off[i] + N].view(1, N), dA[a_off[i]:a_off[i] + K].view(1, K),
                       B, 1, N, K))
     dA.copy_(hA)
-    seq = MatmulSequence(calls, b_layout=q4.Q4_LAYOUT_Q8_0 if q8 else q4.Q4_LAYOUT_BLOCKS)
+    torch.cuda.synchronize()
+    seq = MatmulSequence(calls, b_layout=layout)
     return dict(seq=seq, dA=dA, dC=dC, hA=hA, hC=hC, weights=weights, shapes=shapes,
                 wbytes=wbytes, launches_per_step=len(shapes))
 
@@ -336,7 +352,7 @@ def run_ours(args, ws, rank, local):
         "roofline": {
             "bound": "hbm",
             "kernel": "q4_gemv_kernel (GEMV, one row of A, 2 blocks per thread, 32-row stages"
-                      + (", Q8_0 blocks)" if args.format == "q8_0" else ")"),
+                      + {"q8_0": ", Q8_0 blocks)", "q4_0_planar": ", planar Q4_0)"}.get(args.format, ")"),
             "achieved": round(achieved, 2),
             "peak": hbm_peak,
             "unit": "GB/s",
@@ -404,12 +420,11 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
         N = args.n if args.n else (4096 if args.workload == "gemv" else 12288)
         q8 = args.format == "q8_0"
         wbytes = K * si.nblocks(N) * (34 if q8 else 18)
-        layout = q4.Q4_LAYOUT_Q8_0 if q8 else q4.Q4_LAYOUT_BLOCKS
         copies = max(1, -(-4 * l2 // wbytes))   # >= 4x L2 of distinct weights per pass
         bf16 = args.workload == "batched"
         fns, keep = [], []
         for i in range(copies):
-            B = to_dev((si.q8_weights if q8 else si.q4_weights)(K, N, seed=0, stream=500 + i))
+            B, layout = device_weights(torch, q4, dev, K, N, args.format, 0, 500 + i)
             A = si.activations_bf16(M, K, 0, 600 + i) if bf16 else si.activations_f32(M, K, 0, 600 + i)
             A = to_dev(A.view(np.int16)).view(torch.bfloat16) if bf16 else to_dev(A)
             C = torch.empty((M, N), dtype=torch.float32, device=dev)
@@ -732,8 +747,9 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--slots", type=int, default=4, help="host_stream: device weight slots")
-    ap.add_argument("--format", choices=("q4_0", "q8_0"), default="q4_0",
-                    help="weight format (decode sweep, gemv, batched)")
+    ap.add_argument("--format", choices=("q4_0", "q8_0", "q4_0_planar"), default="q4_0",
+                    help="weight format (decode sweep, gemv, batched); q4_0_planar: the Q4_0 "
+                         "blocks repacked once into the planar layout before timing")
     ap.add_argument("--m", type=int, default=1, help="rows of A (gemv, batched)")
     ap.add_argument("--k", type=int, default=0)
     ap.add_argument("--n", type=int, default=0)

@@ -86,14 +86,16 @@ Q4_API int q4_matmul(float *C, const float *A, const void *B, int64_t M, int64_t
  *              prints no layout; reading: blocks {fp16 d; int8 q[32]} of 34
  *              bytes, 32 output columns of one row each, K rows of
  *              ceil(N/32) blocks, w = q * d), for M <= 64 only (else
- *              Q4_ERR_SHAPE); Q4_LAYOUT_PLANAR is a storage form for
- *              q4_repack/q4_unpack and gives Q4_ERR_SHAPE here
+ *              Q4_ERR_SHAPE); or Q4_LAYOUT_PLANAR (q4_repack's output for
+ *              this K x N), for M <= 64 only (else Q4_ERR_SHAPE): the same
+ *              GEMV on the same values, so C is bit-identical to the
+ *              Q4_LAYOUT_BLOCKS result for the same shape
  *   workspace  unused by this entry point (q4_matmul_workspace_size returns
  *              0); accepted for interface stability, may be NULL.
  *   stream     cudaStream_t (NULL = legacy default stream)
  * Kernel choice:
- *   - M < 8, or fp32 A, or Q8_0 weights, or a shape the GEMM below does not
- *     take: the split-K GEMV on the CUDA cores, in chunks of up to 4 rows of
+ *   - M < 8, or fp32 A, or Q8_0 or planar weights, or a shape the GEMM below
+ *     does not take: the split-K GEMV on the CUDA cores, in chunks of up to 4 rows of
  *     A.  The splits of each column tile run as one thread-block cluster and
  *     are added on chip in fixed order.  Exact fp32 dequantisation.
  *   - M >= 8 with bf16 A, ceil(N/32) % 8 == 0 and K % 8 == 0 (and, for

@@ -167,7 +167,7 @@ void choose_split(int mode, int mr, int fmt, int list_cap, int64_t K, int64_t nb
   // and its residency
   const int bpt = *bpt_out;
   const int64_t big_rows = q4::gemv_stage_rows(bpt, true);
-  if (fmt == q4::kFmtQ4 && *rows_out >= big_min_stages(mr) * big_rows) {
+  if (fmt != q4::kFmtQ8 && *rows_out >= big_min_stages(mr) * big_rows) {
     const int64_t rows = split_rows(K, *nsplit_out, bpt, true);
     const dim3 cl(1, static_cast<unsigned>(*nsplit_out), static_cast<unsigned>(pair));
     if (ceil_div(K, rows) == *nsplit_out &&
@@ -258,10 +258,17 @@ int gemv_run(DeviceState* s, void* C, int c_dtype, const void* A, int a_dtype, c
   p.rows_per_split = g.rows_per_split;
   q4::fill_decode_consts(p, fmt);
   const int64_t block_bytes = (fmt == q4::kFmtQ8) ? 34 : 18;
-  p.use_tma = (p.nb % 8 == 0 &&
-               q4::encode_weight_tmap(&p.tmap[0], B, K, p.nb, 1, K * p.nb * block_bytes, g.bpt,
-                                      g.big, fmt))
-                  ? 1 : 0;
+  if (fmt == q4::kFmtQ4P) {
+    p.qs_offset = static_cast<long long>(q4_planar_qs_offset(K, N));
+    p.use_tma = (p.nb % 8 == 0 &&
+                 q4::encode_planar_tmaps(p.tmap, B, K, p.nb, p.qs_offset, g.bpt, g.big))
+                    ? 1 : 0;
+  } else {
+    p.use_tma = (p.nb % 8 == 0 &&
+                 q4::encode_weight_tmap(&p.tmap[0], B, K, p.nb, 1, K * p.nb * block_bytes, g.bpt,
+                                        g.big, fmt))
+                    ? 1 : 0;
+  }
   p.A = A;
   p.a_dtype = a_dtype;
   p.a_ld = K;
@@ -386,10 +393,12 @@ int q4_matmul_ex(void* C, int c_dtype, const void* A, int a_dtype, const void* B
   if (M > (1LL << 30) || N > (1LL << 30) || K > (1LL << 30)) return Q4_ERR_SHAPE;
   if ((c_dtype != Q4_F32 && c_dtype != Q4_BF16) || (a_dtype != Q4_F32 && a_dtype != Q4_BF16))
     return Q4_ERR_DTYPE;
-  if (b_layout == Q4_LAYOUT_PLANAR) return Q4_ERR_SHAPE;
-  if (b_layout != Q4_LAYOUT_BLOCKS && b_layout != Q4_LAYOUT_Q8_0) return Q4_ERR_ARG;
-  const int fmt = (b_layout == Q4_LAYOUT_Q8_0) ? q4::kFmtQ8 : q4::kFmtQ4;
-  if (fmt == q4::kFmtQ8 && M > 64) return Q4_ERR_SHAPE;   // Q8_0: the GEMV (M <= 64) only
+  if (b_layout != Q4_LAYOUT_BLOCKS && b_layout != Q4_LAYOUT_Q8_0 && b_layout != Q4_LAYOUT_PLANAR)
+    return Q4_ERR_ARG;
+  const int fmt = (b_layout == Q4_LAYOUT_Q8_0)    ? q4::kFmtQ8
+                  : (b_layout == Q4_LAYOUT_PLANAR) ? q4::kFmtQ4P
+                                                   : q4::kFmtQ4;
+  if (fmt != q4::kFmtQ4 && M > 64) return Q4_ERR_SHAPE;   // Q8_0, planar: the GEMV (M <= 64) only
   if (!aligned16(C) || !aligned16(A) || !aligned16(B) || (workspace && !aligned16(workspace)))
     return Q4_ERR_ALIGN;
 

@@ -77,6 +77,7 @@ struct Fmt<kFmtQ4> {
   static constexpr int kBias = 8;          // code offset removed after the loop
   static constexpr int kPairGap = 8;       // second column of an accumulator pair
   static constexpr int kTmaElem = 2;       // tensor-map element size (uint16)
+  static constexpr bool kPlanar = false;
 };
 template <>
 struct Fmt<kFmtQ8> {
@@ -85,6 +86,15 @@ struct Fmt<kFmtQ8> {
   static constexpr int kBias = 128;
   static constexpr int kPairGap = 4;
   static constexpr int kTmaElem = 4;       // uint32: a 2-block-per-thread row segment is 544 B
+  static constexpr bool kPlanar = false;
+};
+// Planar Q4_0: the same blocks and arithmetic, stored as a plane of fp16
+// scales d[K][nb] and a plane of nibbles qs[K][nb][16].  A stage holds its
+// rows' nibbles [rows][tile blocks][16] followed by their scales
+// [rows][tile blocks]: every block's codes are 16-byte aligned.
+template <>
+struct Fmt<kFmtQ4P> : Fmt<kFmtQ4> {
+  static constexpr bool kPlanar = true;
 };
 
 // A stage is one TMA box.  Long slices use 18 KB boxes (BIG): bulk copies of
@@ -98,8 +108,9 @@ struct TileCfg {
   static constexpr int kBlocks = kLanesPerRow * BPT;                // blocks per column tile
   static constexpr int kCols = kBlocks * kBlockCols;                // 256 * BPT
   static constexpr int kRowBytes = kBlocks * Fmt<FMT>::kBytes;      // 144 or 272 per BPT
-  static constexpr int kRows = (BIG && FMT == kFmtQ4) ? 128 / BPT : 32;   // rows of one stage
+  static constexpr int kRows = (BIG && FMT != kFmtQ8) ? 128 / BPT : 32;   // rows of one stage
   static constexpr int kStageBytes = kRows * kRowBytes;
+  static constexpr int kQsBytes = kRows * kBlocks * 16;             // planar: nibbles, then scales
   static constexpr int kStages = (147456 / kStageBytes);            // 8, 16 or 32
   static constexpr int kGroupWarps = BIG ? 8 : 4;                   // warps sharing a stage
   static constexpr int kGroupRows = kGroupWarps * 32 / kLanesPerRow;
@@ -109,6 +120,7 @@ struct TileCfg {
   // word-aligned 20-byte read ends at most at the row's last byte, so rows
   // carry no padding.
   static_assert(kStageBytes % 128 == 0, "TMA destinations must be 128-byte aligned");
+  static_assert(kQsBytes % 128 == 0, "the planar scale box must start 128-byte aligned");
 };
 
 // Reduction buffer of one (warp, row of A): 8 lanes-in-row x BPT blocks x 32
@@ -357,6 +369,30 @@ __device__ __forceinline__ void load_blocks(const uint8_t* row, uint32_t off, bo
   }
 }
 
+// Planar Q4_0: the BPT consecutive blocks a thread owns in one staged row, the
+// codes from the row's nibbles at `qs_row` (16-byte aligned, one 16-byte read
+// per block), the scales from its scale row at `d_row` (2 * BPT bytes,
+// aligned to their size).
+template <int BPT>
+__device__ __forceinline__ void load_planar(const uint8_t* qs_row, const uint8_t* d_row,
+                                            uint32_t (&dbits)[BPT], uint32_t (&qs)[BPT][4]) {
+#pragma unroll
+  for (int bb = 0; bb < BPT; ++bb) {
+    const uint4 v = reinterpret_cast<const uint4*>(qs_row)[bb];
+    qs[bb][0] = v.x;
+    qs[bb][1] = v.y;
+    qs[bb][2] = v.z;
+    qs[bb][3] = v.w;
+  }
+  if constexpr (BPT == 2) {
+    const uint32_t both = *reinterpret_cast<const uint32_t*>(d_row);
+    dbits[0] = both & 0xFFFFu;
+    dbits[1] = both >> 16;
+  } else {
+    dbits[0] = *reinterpret_cast<const uint16_t*>(d_row);
+  }
+}
+
 // Waits on `bar` (bounded_wait: gives up if the CTA failed or after the wait
 // limit, recording the timeout).  Threads never leave their loops early, so
 // every named barrier is still reached.
@@ -371,6 +407,8 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, vol
 struct StreamDesc {
   const uint8_t* B;   // matrix base
   const void* tmap;   // tensor map of the weight stack (TMA path) or null
+  const void* tmap2;  // planar: tensor map of the scale plane
+  long long qs_offset;   // planar: byte offset of the nibble plane from B
   int expert;         // expert index in the stack (0 for a single matrix)
   int nb;             // blocks per row
   int b0, tb;         // first block of the tile, blocks in the tile
@@ -383,6 +421,36 @@ __device__ __forceinline__ void produce_stage(const StreamDesc& sd, int s, uint8
   using T = TileCfg<BPT, BIG, FMT>;
   constexpr int kBB = Fmt<FMT>::kBytes;
   const int r0 = s * T::kRows;
+  if constexpr (Fmt<FMT>::kPlanar) {
+    if (sd.tmap) {
+      // two boxes of kRows rows: the nibbles (uint32, 4 per block) and the
+      // scales (uint16, 1 per block); rows past K read as zero
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full, T::kStageBytes);
+        tma_load_3d(stage, sd.tmap, sd.b0 * 4, sd.k0 + r0, 0, full);
+        tma_load_3d(stage + T::kQsBytes, sd.tmap2, sd.b0, sd.k0 + r0, 0, full);
+      }
+    } else {
+      // 16-byte nibble units and 2-byte scales; rows past the slice and
+      // blocks past the row are written as zeros, as the tensor copies do
+      const int nr = min(T::kRows, sd.rows - r0);
+      const uint4* qsrc = reinterpret_cast<const uint4*>(sd.B + sd.qs_offset);
+      const uint16_t* dsrc = reinterpret_cast<const uint16_t*>(sd.B);
+      uint4* qdst = reinterpret_cast<uint4*>(stage);
+      uint16_t* ddst = reinterpret_cast<uint16_t*>(stage + T::kQsBytes);
+      for (int u = lane; u < T::kRows * T::kBlocks; u += 32) {
+        const int r = u / T::kBlocks;
+        const int b = u - r * T::kBlocks;
+        const bool in = (r < nr && b < sd.tb);
+        const size_t e = static_cast<size_t>(sd.k0 + r0 + r) * sd.nb + sd.b0 + b;
+        qdst[u] = in ? __ldg(qsrc + e) : make_uint4(0u, 0u, 0u, 0u);
+        ddst[u] = in ? __ldg(dsrc + e) : static_cast<uint16_t>(0);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(full);
+    }
+    return;
+  }
   if (sd.tmap) {
     // one box of kRows rows x kRowBytes; rows past K and blocks past the row
     // read as zero (a slice is a whole number of boxes, except the last one,
@@ -627,6 +695,8 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
     // ================= producer warp =================
     StreamDesc sd;
     sd.tmap = p.use_tma ? static_cast<const void*>(&p.tmap[which]) : nullptr;
+    sd.tmap2 = (Fmt<FMT>::kPlanar && p.use_tma) ? static_cast<const void*>(&p.tmap[1]) : nullptr;
+    sd.qs_offset = p.qs_offset;
     sd.expert = expert;
     sd.B = (which ? p.B2 : p.B) + static_cast<size_t>(expert) * p.b_stride;
     sd.nb = p.nb;
@@ -713,9 +783,15 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
 #pragma unroll 2
         for (int rr = 0; rr < T::kRowsPerThread; ++rr) {
           const int rs = rp + rr * T::kGroupRows;   // row within the stage
-          const uint8_t* row = ring + slot * T::kStageBytes + rs * T::kRowBytes;
           uint32_t dbits[BPT], qs[BPT][Fmt<FMT>::kWords];
-          load_blocks<BPT, FMT>(row, boff, odd, dbits, qs);
+          if constexpr (Fmt<FMT>::kPlanar) {
+            const uint8_t* st = ring + slot * T::kStageBytes;
+            load_planar<BPT>(st + (rs * T::kBlocks + pi * BPT) * 16,
+                             st + T::kQsBytes + (rs * T::kBlocks + pi * BPT) * 2, dbits, qs);
+          } else {
+            const uint8_t* row = ring + slot * T::kStageBytes + rs * T::kRowBytes;
+            load_blocks<BPT, FMT>(row, boff, odd, dbits, qs);
+          }
           const float* a = a_s + s * T::kRows + rs;
 #pragma unroll
           for (int bb = 0; bb < BPT; ++bb)
@@ -897,6 +973,11 @@ cudaError_t launch_gemv(const GemvParams& p, int mr, int bpt, bool big, int fmt,
     if (p.mode != kModeGemv || big) return cudaErrorInvalidValue;
     return launch_mode<kModeGemv, false, kFmtQ8>(p, mr, bpt, grid, cluster, st, pdl);
   }
+  if (fmt == kFmtQ4P) {   // the plain GEMV
+    if (p.mode != kModeGemv) return cudaErrorInvalidValue;
+    return big ? launch_mode<kModeGemv, true, kFmtQ4P>(p, mr, bpt, grid, cluster, st, pdl)
+               : launch_mode<kModeGemv, false, kFmtQ4P>(p, mr, bpt, grid, cluster, st, pdl);
+  }
   return big ? launch_big<true>(p, mr, bpt, grid, cluster, st, pdl)
              : launch_big<false>(p, mr, bpt, grid, cluster, st, pdl);
 }
@@ -932,6 +1013,10 @@ int max_active_clusters(int mode, int mr, int bpt, bool big, int fmt, int rows_p
   if (fmt == kFmtQ8) {
     if (big || mode != kModeGemv) return 0;
     pick_instance<false, kFmtQ8>(mode, mr, bpt, rows_per_split, list_cap, senders, &fn, &smem);
+  } else if (fmt == kFmtQ4P) {
+    if (mode != kModeGemv) return 0;
+    if (big) pick_instance<true, kFmtQ4P>(mode, mr, bpt, rows_per_split, list_cap, senders, &fn, &smem);
+    else pick_instance<false, kFmtQ4P>(mode, mr, bpt, rows_per_split, list_cap, senders, &fn, &smem);
   } else if (big) {
     pick_instance<true, kFmtQ4>(mode, mr, bpt, rows_per_split, list_cap, senders, &fn, &smem);
   } else {
@@ -995,8 +1080,8 @@ void fill_decode_consts(GemvParams& p, int fmt) {
   }
 }
 
-bool encode_weight_tmap(CUtensorMap* map, const void* base, int64_t K, int64_t nb,
-                        int64_t experts, int64_t matrix_bytes, int bpt, bool big, int fmt) {
+// cuTensorMapEncodeTiled from the driver (null if unavailable).
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -1004,9 +1089,16 @@ bool encode_weight_tmap(CUtensorMap* map, const void* base, int64_t K, int64_t n
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
                                          &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess || !fn)
-      return false;
+      return nullptr;
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
+  return encode;
+}
+
+bool encode_weight_tmap(CUtensorMap* map, const void* base, int64_t K, int64_t nb,
+                        int64_t experts, int64_t matrix_bytes, int bpt, bool big, int fmt) {
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
+  if (!encode) return false;
   if (nb % kLanesPerRow != 0) return false;
   // Q4_0: uint16 elements, a row is nb*9 of them; Q8_0: uint32 elements, a
   // row is nb*34/4 (nb is a multiple of 8, so the tile starts, 8*bpt blocks
@@ -1027,6 +1119,37 @@ bool encode_weight_tmap(CUtensorMap* map, const void* base, int64_t K, int64_t n
                             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool encode_planar_tmaps(CUtensorMap* maps, const void* base, int64_t K, int64_t nb,
+                         int64_t qs_offset, int bpt, bool big) {
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
+  if (!encode) return false;
+  // nb % 8 == 0 makes the scale rows (nb * 2 bytes) 16-byte multiples and
+  // every tile start (8*bpt blocks apart) a whole, 16-byte aligned element
+  if (nb % kLanesPerRow != 0 || qs_offset % 16 != 0) return false;
+  const cuuint32_t rows = static_cast<cuuint32_t>(gemv_stage_rows(bpt, big));
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  // the nibble plane: uint32 [1][K][nb*4], boxes of 8*bpt blocks (32*bpt words)
+  const cuuint64_t qdims[3] = {static_cast<cuuint64_t>(nb * 4), static_cast<cuuint64_t>(K), 1u};
+  const cuuint64_t qstrides[2] = {static_cast<cuuint64_t>(nb * 16),
+                                  static_cast<cuuint64_t>(K * nb * 16)};
+  const cuuint32_t qbox[3] = {static_cast<cuuint32_t>(kLanesPerRow * bpt * 4), rows, 1u};
+  CUresult r = encode(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT32, 3,
+                      const_cast<uint8_t*>(static_cast<const uint8_t*>(base) + qs_offset), qdims,
+                      qstrides, qbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  // the scale plane: uint16 [1][K][nb], boxes of 8*bpt scales
+  const cuuint64_t ddims[3] = {static_cast<cuuint64_t>(nb), static_cast<cuuint64_t>(K), 1u};
+  const cuuint64_t dstrides[2] = {static_cast<cuuint64_t>(nb * 2),
+                                  static_cast<cuuint64_t>(K * nb * 2)};
+  const cuuint32_t dbox[3] = {static_cast<cuuint32_t>(kLanesPerRow * bpt), rows, 1u};
+  r = encode(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), ddims,
+             dstrides, dbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

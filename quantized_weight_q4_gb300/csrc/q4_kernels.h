@@ -10,15 +10,18 @@ namespace q4 {
 
 enum : int { kModeGemv = 0, kModeGateUp = 1, kModeDown = 2 };
 // Weight formats of the GEMV kernel (values of the public Q4_LAYOUT_* codes
-// are not used here: the host maps Q4_LAYOUT_BLOCKS -> kFmtQ4 and
-// Q4_LAYOUT_Q8_0 -> kFmtQ8).
-enum : int { kFmtQ4 = 0, kFmtQ8 = 1 };
+// are not used here: the host maps Q4_LAYOUT_BLOCKS -> kFmtQ4,
+// Q4_LAYOUT_Q8_0 -> kFmtQ8 and Q4_LAYOUT_PLANAR -> kFmtQ4P, the Q4_0 blocks
+// split into a scale plane and a nibble plane; plain GEMV mode only).
+enum : int { kFmtQ4 = 0, kFmtQ8 = 1, kFmtQ4P = 2 };
 
 // Arguments of q4_gemv_kernel (one struct, passed by value as a __grid_constant__
 // parameter so that the tensor maps inside it are addressable by TMA).
 struct GemvParams {
   // TMA tensor maps of the weights (B and B2) as 3-D uint16 tensors
-  // [experts][K rows][nb*9 halfwords]; valid when use_tma != 0.
+  // [experts][K rows][nb*9 halfwords]; valid when use_tma != 0.  Planar
+  // Q4_0 (kFmtQ4P): tmap[0] maps the nibble plane, tmap[1] the scale plane.
+  // GEMV mode only.
   CUtensorMap tmap[2];
   int use_tma;
   int mode;
@@ -26,6 +29,7 @@ struct GemvParams {
   const uint8_t* B;
   const uint8_t* B2;
   long long b_stride;   // bytes per expert matrix
+  long long qs_offset;  // kFmtQ4P: byte offset of the nibble plane from B
   int K, N, nb;
   // split-K tiling (grid.x = column tiles of 8*BPT blocks, grid.y = splits;
   // the splits of a tile form one thread-block cluster)
@@ -52,7 +56,8 @@ struct GemvParams {
 // big: 18 KB pipeline stages instead of 32-row ones (rows_per_split a multiple of
 // gemv_stage_rows(bpt, big) either way).
 // cluster: (1, nsplit, 1), or (1, nsplit, 2) for the gate/up kernel.
-// fmt: kFmtQ4 (block_q4_0) or kFmtQ8 (Q8_0: plain GEMV mode and big = false only).
+// fmt: kFmtQ4 (block_q4_0), kFmtQ8 (Q8_0: plain GEMV mode and big = false only)
+// or kFmtQ4P (planar Q4_0: plain GEMV mode only).
 cudaError_t launch_gemv(const GemvParams& p, int mr, int bpt, bool big, int fmt, dim3 grid,
                         dim3 cluster, cudaStream_t st, bool pdl);
 constexpr int kMaxCluster = 16;   // non-portable thread-block cluster size limit
@@ -70,6 +75,13 @@ void fill_decode_consts(GemvParams& p, int fmt);
 // stage of rows.  Needs nb % 8 == 0 and a 16-byte aligned base.
 bool encode_weight_tmap(CUtensorMap* map, const void* base, int64_t K, int64_t nb,
                         int64_t experts, int64_t matrix_bytes, int bpt, bool big, int fmt);
+// Planar Q4_0 (Q4_LAYOUT_PLANAR, one K x nb matrix at `base`): maps[0] = the
+// nibble plane at base + qs_offset as uint32 [K][nb*4], maps[1] = the scale
+// plane at base as uint16 [K][nb]; boxes of one tile row segment (8*bpt
+// blocks) by one stage of rows.  Needs nb % 8 == 0, a 16-byte aligned base and
+// qs_offset a multiple of 16.
+bool encode_planar_tmaps(CUtensorMap* maps, const void* base, int64_t K, int64_t nb,
+                         int64_t qs_offset, int bpt, bool big);
 // h[i] = SiLU(g[i]) * u[i] for i < n, fp32 (programmatic dependent launch).
 cudaError_t launch_silu_mul(float* h, const float* g, const float* u, size_t n, cudaStream_t st);
 // out[t] = sum_k w[t,k] * y[t*topk+k] (slot order), plus addend[t] if given.
