@@ -284,7 +284,9 @@ int gemv_run(DeviceState* s, void* C, int c_dtype, const void* A, int a_dtype, c
 
 // The routed-expert kernels (gate/up, down, slot combine) for a validated
 // problem, on a workspace of at least m.total bytes; the combine adds
-// `addend` (fp32 [T, H], or null) after the weighted sum.
+// `addend` (fp32 [T, H], or null) after the weighted sum.  With `out` null the
+// combine is left out and the per-slot down outputs stay in the workspace at
+// m.off_y ([T*topk, H] fp32).
 int moe_run(DeviceState* s, const MoeShape& m, float* out, const void* x, int x_dtype,
             const void* W_gate, const void* W_up, const void* W_down, const int32_t* topk_idx,
             const float* topk_w, int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I,
@@ -352,6 +354,7 @@ int moe_run(DeviceState* s, const MoeShape& m, float* out, const void* x, int x_
                       dim3(1, m.nsplit_d, 1), st, true);
   if (e != cudaSuccess) return Q4_ERR_CUDA;
 
+  if (!out) return Q4_OK;
   e = q4::launch_moe_combine(out, y, topk_idx, topk_w, addend, static_cast<int>(T),
                              static_cast<int>(topk), static_cast<int>(E), static_cast<int>(H), st,
                              true);
@@ -477,10 +480,12 @@ int q4_moe_gate(int32_t* topk_idx, float* topk_w, const float* logits, int64_t T
 }
 
 namespace {
-// Workspace of q4_moe_block: routing, the shared expert's routing and output,
-// then one expert workspace serving the routed and the shared problem in turn.
+// Workspace of q4_moe_block: routing, the shared expert's routing, its output
+// (dense path) or its own expert workspace (one-expert path, whose per-slot
+// down output is the addend of the routed combine), then the routed problem's
+// expert workspace.
 struct BlockLayout {
-  size_t idx, w, sidx, sw, ys, sg, su, sh, moe, total;
+  size_t idx, w, sidx, sw, ys, sg, su, sh, moe_s, moe, total;
 };
 
 // The shared expert runs as one (E = 1) routed expert at T = 1, where gate and
@@ -501,7 +506,7 @@ BlockLayout block_layout(int64_t T, int64_t topk, int64_t E, int64_t H, int64_t 
   b.sw = o;
   o += round_up(static_cast<size_t>(T) * 4, 256);
   b.ys = o;
-  o += (Is > 0) ? round_up(static_cast<size_t>(T * H) * 4, 256) : 0;
+  o += (Is > 0 && shared_dense(T)) ? round_up(static_cast<size_t>(T * H) * 4, 256) : 0;
   const size_t tis = (Is > 0 && shared_dense(T)) ? round_up(static_cast<size_t>(T * Is) * 4, 256) : 0;
   b.sg = o;
   o += tis;
@@ -509,13 +514,10 @@ BlockLayout block_layout(int64_t T, int64_t topk, int64_t E, int64_t H, int64_t 
   o += tis;
   b.sh = o;
   o += tis;
+  b.moe_s = o;
+  o += (Is > 0 && !shared_dense(T)) ? q4_moe_workspace_size(T, 1, 1, H, Is) : 0;
   b.moe = o;
-  size_t need = q4_moe_workspace_size(T, topk, E, H, I);
-  if (Is > 0 && !shared_dense(T)) {
-    const size_t sneed = q4_moe_workspace_size(T, 1, 1, H, Is);
-    if (sneed > need) need = sneed;
-  }
-  b.total = o + need;
+  b.total = o + q4_moe_workspace_size(T, topk, E, H, I);
   return b;
 }
 }  // namespace
@@ -582,11 +584,14 @@ int q4_moe_block(float* out, const void* x, int x_dtype, const float* logits, co
                                       static_cast<int>(topk), Is > 0 ? sidx : nullptr,
                                       Is > 0 ? sw : nullptr, st);
   if (e != cudaSuccess) return Q4_ERR_CUDA;
-  // shared expert: every token, weight 1
+  // shared expert: every token, weight 1.  On the one-expert path its down
+  // output, one slot per token, is already the shared expert's result
+  // ([T, H]): no combine of its own, the routed combine adds it.
   if (Is > 0 && !shared_dense(T)) {
-    rc = moe_run(s, *ms, ys, x, x_dtype, S_gate, S_up, S_down, sidx, sw, T, 1, 1, H, Is,
-                 w8 + b.moe, nullptr, st);
+    rc = moe_run(s, *ms, nullptr, x, x_dtype, S_gate, S_up, S_down, sidx, sw, T, 1, 1, H, Is,
+                 w8 + b.moe_s, nullptr, st);
     if (rc != Q4_OK) return rc;
+    ys = reinterpret_cast<float*>(w8 + b.moe_s + ms->off_y);
   } else if (Is > 0) {
     float* sg = reinterpret_cast<float*>(w8 + b.sg);
     float* su = reinterpret_cast<float*>(w8 + b.su);
