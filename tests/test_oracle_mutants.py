@@ -44,6 +44,9 @@ MUTANTS = {
     "q8 codes read unsigned": ("    if (q >= 128)\n        q -= 256;                          /* two's complement */", "    (void)0;"),
     "q8 codes offset by one byte": ("    int q = (int)blk[2 + j % QO_BLOCK];", "    int q = (int)blk[1 + j % QO_BLOCK];"),
     "q8 blocks 18 bytes apart": ("    const uint8_t *blk = B + (k * nb + j / QO_BLOCK) * QO_Q8_BYTES;", "    const uint8_t *blk = B + (k * nb + j / QO_BLOCK) * QO_BLOCK_BYTES;"),
+    "silu without its g factor": ("double silu = g[i] * sgm;", "double silu = sgm;"),
+    "every token reads row 0 of x": ("xt[i] = act_at(x, x_dtype, t * H + i);", "xt[i] = act_at(x, x_dtype, i);"),
+    "bf16 exponent bias off by one": ("v = ldexp((double)(128 + f), e - 134);", "v = ldexp((double)(128 + f), e - 133);"),
     "q8 activation row stride": ("            double av = act_at(A, a_dtype, i * K + k);", "            double av = act_at(A, a_dtype, i + k);"),
 }
 
@@ -58,6 +61,7 @@ BATTERY = [
     lambda: pins.test_matmul_exact_rational(3, 17, 40),
     pins.test_fused_equals_textbook,
     pins.test_moe_closed_form,
+    pins.test_moe_closed_form_two_tokens,
     lambda: pins.test_silu_closed_forms(oracle),
     pins.test_bf16_tiles_hand_rounded,
     pins.test_bf16_tiles_equal_exact_product_when_representable,

@@ -334,6 +334,31 @@ def test_moe_closed_form():
     assert np.all(out1 == 0)
 
 
+def test_moe_closed_form_two_tokens():
+    """Each token's experts read that token's row of x: token 0 is e_0, token 1
+    is 2 * e_0 (so its g and u double), with different routings."""
+    import oracle
+    E, H, I, T, topk = 3, 32, 32, 2, 2
+    gcodes = [[(l % 16) for l in range(32)], [8] * 32, [(15 - l % 16) for l in range(32)]]
+    ucodes = [[9 + (l % 3) for l in range(32)], [(l % 16) for l in range(32)], [10] * 32]
+    Wg, Wu, Wd = _expert_closed_form(E, gcodes, ucodes)
+    x = np.zeros((T, H), np.float32)
+    x[0, 0] = 1.0
+    x[1, 0] = 2.0
+    idx = np.array([[2, 0], [0, 2]], np.int32)
+    w = np.array([[0.25, 0.75], [0.5, 0.5]], np.float32)
+    out, _, _ = oracle.moe(x, Wg, Wu, Wd, idx, w, T, topk, E, H, I, stages=True)
+    for t in range(T):
+        s = float(x[t, 0])
+        for j in range(H):
+            exp = 0.0
+            for k, e in enumerate(idx[t]):
+                gv = s * (gcodes[e][j] - 8)
+                uv = s * (ucodes[e][j] - 8)
+                exp += float(w[t, k]) * (gv / (1.0 + math.exp(-gv))) * uv
+            assert abs(out[t, j] - exp) <= 1e-15 * (1 + abs(exp)), (t, j)
+
+
 def test_silu_closed_forms(oracle_lib):
     assert oracle_lib.silu(0.0) == 0.0
     assert abs(oracle_lib.silu(1.0) - 1.0 / (1.0 + math.exp(-1.0))) < 1e-16
