@@ -91,7 +91,9 @@ Q4_API int q4_matmul(float *C, const float *A, const void *B, int64_t M, int64_t
  *              GEMV on the same values, so C is bit-identical to the
  *              Q4_LAYOUT_BLOCKS result for the same shape
  *   workspace  unused by this entry point (q4_matmul_workspace_size returns
- *              0); accepted for interface stability, may be NULL.
+ *              0); accepted for interface stability, may be NULL.  (The
+ *              tensor-core GEMM's small-M form keeps its own scratch per
+ *              stream, see below.)
  *   stream     cudaStream_t (NULL = legacy default stream)
  * Kernel choice:
  *   - M < 8, or fp32 A, or Q8_0 or planar weights, or a shape the GEMM below
@@ -104,7 +106,14 @@ Q4_API int q4_matmul(float *C, const float *A, const void *B, int64_t M, int64_t
  *     dequantised to a bf16 tile element bf16_rn((q - 8) * d) and the
  *     products are accumulated in fp32; the result is A . bf16_rn(W), whose
  *     deviation from A . W is bounded by 2^-9 * sum|a*w| plus the fp32
- *     accumulation error.
+ *     accumulation error.  Up to 128 rows each output tile's K range is
+ *     split; up to 32 rows the splits may run as independent CTAs that add
+ *     their partial tiles through library-owned scratch of the calling
+ *     stream (partial tiles and per-tile arrival counters, cudaMalloc'd by
+ *     the first such call on that stream and grown by a larger one; a call
+ *     made while the stream is being captured without that scratch uses the
+ *     on-chip cluster combine instead).  Either way the splits are added in
+ *     a fixed order.
  *   Both are deterministic (no floating-point atomics, fixed orders).
  * Launches use programmatic dependent launch: a kernel may start streaming
  * its weights while the previous kernel on the stream finishes, and reads A

@@ -48,6 +48,13 @@ struct DeviceState {
   // launch shapes already chosen for a problem size (the choice runs occupancy queries)
   std::map<std::tuple<int64_t, int64_t, int64_t, int>, GemvShape> gemv_shapes;
   std::map<std::tuple<int64_t, int64_t, int64_t, int64_t, int64_t>, MoeShape> moe_shapes;
+  // per stream: the small-M GEMM's partial tiles and its zeroed tile tickets
+  struct GemmScratch {
+    float* part = nullptr;
+    size_t part_bytes = 0;
+    unsigned* tickets = nullptr;
+  };
+  std::map<cudaStream_t, GemmScratch> gemm_scratch;
 };
 
 std::mutex g_mu;
@@ -71,6 +78,54 @@ int current_state(DeviceState** out) {
 }
 
 // Library-owned workspace of at least `bytes`, zero-filled when (re)allocated.
+// The small-M GEMM's scratch for stream `st`: partial tiles (at least `bytes`)
+// and a zeroed ticket array.  It allocates only outside stream capture and
+// returns false when it cannot; the caller then takes the cluster form.
+bool gemm_scratch(DeviceState* s, cudaStream_t st, size_t bytes, float** part,
+                  unsigned** tickets) {
+  DeviceState::GemmScratch& g = s->gemm_scratch[st];
+  if (!g.tickets || g.part_bytes < bytes) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return false;
+    if (!g.tickets) {
+      unsigned* t = nullptr;
+      const size_t tb = q4::kMaxGemmTickets * sizeof(unsigned);
+      if (cudaMalloc(&t, tb) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+      }
+      if (cudaMemsetAsync(t, 0, tb, st) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(t);
+        return false;
+      }
+      g.tickets = t;
+    }
+    if (g.part_bytes < bytes) {
+      if (g.part) {   // kernels on this stream may still read the old buffer
+        if (cudaStreamSynchronize(st) != cudaSuccess) return false;
+        cudaFree(g.part);
+        g.part = nullptr;
+        g.part_bytes = 0;
+      }
+      const size_t want = bytes + bytes / 4;
+      if (cudaMalloc(&g.part, want) != cudaSuccess) {
+        cudaGetLastError();
+        g.part = nullptr;
+        return false;
+      }
+      g.part_bytes = want;
+    }
+  }
+  *part = g.part;
+  *tickets = g.tickets;
+  return true;
+}
+
 int owned_workspace(DeviceState* s, size_t bytes, void** ws) {
   if (bytes == 0) {
     *ws = s->ws;
@@ -412,9 +467,18 @@ int q4_matmul_ex(void* C, int c_dtype, const void* A, int a_dtype, const void* B
   int rc = current_state(&s);
   if (rc != Q4_OK) return rc;
   if (fmt == q4::kFmtQ4 && M >= kMinTensorRows && a_dtype == Q4_BF16 &&
-      q4::gemm_supported(M, N, K) && (M > 128 || q4::gemm_small_split(M, N, K) > 0))
-    return launch_status(q4::launch_gemm(C, c_dtype, A, B, M, N, K, s->status, s->sms,
-                                         static_cast<cudaStream_t>(stream)));
+      q4::gemm_supported(M, N, K) && (M > 128 || q4::gemm_small_split(M, N, K) > 0)) {
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float* part = nullptr;
+    unsigned* tickets = nullptr;
+    const int sg = q4::gemm_global_split(M, N, K, s->sms);
+    if (sg > 0 && !gemm_scratch(s, st, q4::gemm_part_bytes(M, N, sg), &part, &tickets)) {
+      part = nullptr;
+      tickets = nullptr;
+    }
+    return launch_status(
+        q4::launch_gemm(C, c_dtype, A, B, M, N, K, s->status, s->sms, st, part, tickets));
+  }
   return gemv_run(s, C, c_dtype, A, a_dtype, B, fmt, M, N, K, static_cast<cudaStream_t>(stream));
 }
 

@@ -565,7 +565,72 @@ __global__ void __launch_bounds__(Cfg<MT, DW, SPLIT>::kThreads, 1)
     }
   }
 
-  if (SPLIT) {
+  if (SPLIT && p.gsplit) {
+    // ---- split-K combine through global memory ----
+    // (1) the accumulator is complete: the MMA thread waited for its MMAs
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const int S = p.nsplit;
+    const int tile = blockIdx.x / S, split = blockIdx.x % S;
+    Work w;
+    const bool have = work_item<MT, SPLIT>(p, 0, w);
+    const int rows = min(p.M - w.m0, 128);   // valid rows of the tile
+    const size_t tile_floats = static_cast<size_t>(rows) * BN;
+    if (warp >= 2 && have && !*s_fail) {
+      // (2) this split's partial tile, rows x 256 fp32, row-major: each lane
+      //     writes its row's 32 columns of a chunk as eight 16-byte stores
+      float* mine = p.part + (static_cast<size_t>(tile) * S + split) * tile_floats;
+      const int wd = warp - 2, q = warp & 3;
+      const int c0 = (wd >> 2) * C::kEpiCols;
+      const int row = q * 32 + lane;
+#pragma unroll 1
+      for (int c = c0; c < c0 + C::kEpiCols; c += 32) {
+        uint32_t acc[32], v[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, acc);
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+          for (int s = 0; s < 8; ++s) v[8 * t + chunk_col(s)] = acc[8 * t + s];
+        if (row < rows) {
+          float4* dst = reinterpret_cast<float4*>(mine + static_cast<size_t>(row) * BN + c);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        }
+      }
+    }
+    // (3) every split takes one ticket after its partial is visible; the one
+    //     that takes the last adds the S partials in split order and stores C
+    __threadfence();
+    __syncthreads();
+    __shared__ int s_last;
+    if (threadIdx.x == 0)
+      s_last = (atomicAdd(&p.tickets[tile], 1u) == static_cast<unsigned>(S - 1)) ? 1 : 0;
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      if (warp >= 2 && have && !*s_fail) {
+        const float* base = p.part + static_cast<size_t>(tile) * S * tile_floats;
+        const int items = rows * (BN / 4);
+        for (int i = threadIdx.x - 64; i < items; i += DW * 32) {
+          const int r = i / (BN / 4), c4 = (i % (BN / 4)) * 4;
+          const float* src = base + static_cast<size_t>(r) * BN + c4;
+          float4 acc = __ldcg(reinterpret_cast<const float4*>(src));
+          for (int s = 1; s < S; ++s) {
+            const float4 t = __ldcg(reinterpret_cast<const float4*>(src + s * tile_floats));
+            acc.x += t.x;
+            acc.y += t.y;
+            acc.z += t.z;
+            acc.w += t.w;
+          }
+          store_group4(p, w.m0 + r, w.n0 + c4, acc);
+        }
+      }
+      if (threadIdx.x == 0) p.tickets[tile] = 0u;   // zero again for the next launch
+    }
+  } else if (SPLIT) {
     // ---- split-K combine over the cluster ----
     // (1) Every CTA of the cluster is past its main loop: its MMAs and copies
     //     are complete (the MMA thread and the producer waited for them), so
@@ -782,9 +847,40 @@ int gemm_small_split(int64_t M, int64_t N, int64_t K) {
   return best;
 }
 
+int gemm_global_split(int64_t M, int64_t N, int64_t K, int sms) {
+  // the partial tiles grow with M: on K = 5120, N = 12288 (48 tiles) the
+  // global form with 3 splits against the cluster form with 2 measured
+  // +26% / +19% / +8% at M = 8 / 16 / 32 and -8% at M = 64 (GB300)
+  if (M > 32 || sms <= 0) return 0;
+  const int64_t tiles = (N + gemm::BN - 1) / gemm::BN;
+  const int64_t ksteps = (K + gemm::BK - 1) / gemm::BK;
+  if (tiles > kMaxGemmTickets) return 0;
+  // one CTA per SM (the shared-memory plan allows no more): every split of
+  // every tile in one wave
+  int64_t S = sms / tiles;
+  if (S > gemm::kMaxSplit) S = gemm::kMaxSplit;
+  if (S > ksteps) S = ksteps;
+  if (S < 2) return 0;
+  // the cluster form combines on chip; the global form pays a write and a
+  // read of the partial tiles, so it runs only where it has more splits
+  const int sc = gemm_small_split(M, N, K);
+  if (sc > 0 && S <= sc) return 0;
+  return static_cast<int>(S);
+}
+
+size_t gemm_part_bytes(int64_t M, int64_t N, int S) {
+  const int64_t tiles = (N + gemm::BN - 1) / gemm::BN;
+  const int64_t rows = M < 128 ? M : 128;
+  return static_cast<size_t>(tiles) * S * rows * gemm::BN * sizeof(float);
+}
+
 cudaError_t launch_gemm(void* C, int c_dtype, const void* A, const void* B, int64_t M, int64_t N,
-                        int64_t K, unsigned* err, int sms, cudaStream_t st) {
+                        int64_t K, unsigned* err, int sms, cudaStream_t st, float* part,
+                        unsigned* tickets) {
   GemmParams p;
+  p.gsplit = 0;
+  p.part = nullptr;
+  p.tickets = nullptr;
   p.C = C;
   p.c_dtype = c_dtype;
   p.M = static_cast<int>(M);
@@ -803,10 +899,24 @@ cudaError_t launch_gemm(void* C, int c_dtype, const void* A, const void* B, int6
     cudaLaunchConfig_t cfg = make_cfg<2, 8, false>(attr, grid, 1, st);
     return cudaLaunchKernelEx(&cfg, gemm::q4_gemm_tc_kernel<2, 8, false>, p);
   }
+  const int a_rows = static_cast<int>(((M + 15) / 16) * 16);   // M <= 128
+  // small-M form through global memory: S independent CTAs per tile
+  const int Sg = (part && tickets) ? gemm_global_split(M, N, K, sms) : 0;
+  if (Sg > 0) {
+    if (!encode_maps(p, A, B, M, N, K, a_rows)) return cudaErrorInvalidValue;
+    p.nsplit = Sg;
+    p.gsplit = 1;
+    p.part = part;
+    p.tickets = tickets;
+    cudaError_t e = prepare<1, kSmallDW, true>();
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = (N + gemm::BN - 1) / gemm::BN;
+    cudaLaunchConfig_t cfg = make_cfg<1, kSmallDW, true>(attr, static_cast<int>(tiles * Sg), 1, st);
+    return cudaLaunchKernelEx(&cfg, gemm::q4_gemm_tc_kernel<1, kSmallDW, true>, p);
+  }
   // small-M form: one 128 x 256 tile per cluster of S CTAs splitting K
   const int S = gemm_small_split(M, N, K);
   if (S <= 0) return cudaErrorInvalidConfiguration;
-  const int a_rows = static_cast<int>(((M + 15) / 16) * 16);   // M <= 128
   if (!encode_maps(p, A, B, M, N, K, a_rows)) return cudaErrorInvalidValue;
   p.nsplit = S;
   cudaError_t e = prepare<1, kSmallDW, true>();

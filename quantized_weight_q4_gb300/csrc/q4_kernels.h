@@ -99,6 +99,14 @@ struct GemmParams {
   int nsplit;           // small-M form: K splits per tile (the cluster size)
   int a_rows;           // rows of one A box (tile rows, or M rounded up to 16)
   unsigned* err;        // device status word
+  // small-M form through global memory (gsplit != 0): the K splits of a tile
+  // are independent CTAs (no cluster); each writes its fp32 partial tile to
+  // part [tile][split][rows][256] and takes a ticket from tickets[tile]; the
+  // CTA with the last ticket adds the partials in split order, stores C and
+  // returns the ticket to zero
+  int gsplit;
+  float* part;
+  unsigned* tickets;
 };
 // Shapes the tensor-core GEMM accepts: nb = ceil(N/32) a multiple of 8 (whole
 // 256-column tiles of blocks, 16-byte row pitch) and K a multiple of 8
@@ -107,10 +115,22 @@ bool gemm_supported(int64_t M, int64_t N, int64_t K);
 // A: bf16, 16-byte aligned; B: blocks layout, 16-byte aligned.  M > 128 runs
 // the persistent prefill form (`sms` bounds its grid), M <= 128 the split-K
 // small-M form.
+// M <= 128 with `part` and `tickets` given and gemm_global_split() > 0 runs
+// the small-M form through global memory (part: gemm_part_bytes() bytes;
+// tickets: at least ceil(N/256) counters, zero, left zero by every launch;
+// both owned by one stream at a time).
 cudaError_t launch_gemm(void* C, int c_dtype, const void* A, const void* B, int64_t M, int64_t N,
-                        int64_t K, unsigned* err, int sms, cudaStream_t st);
+                        int64_t K, unsigned* err, int sms, cudaStream_t st, float* part = nullptr,
+                        unsigned* tickets = nullptr);
 // K splits the small-M form uses for this shape (0: the form cannot take it).
 int gemm_small_split(int64_t M, int64_t N, int64_t K);
+// Tile counters a stream's ticket array holds (N up to 1,048,576 columns).
+constexpr int kMaxGemmTickets = 4096;
+// K splits of the global-memory small-M form (0: the cluster form is chosen:
+// the global form runs for M <= 32, where it fits more CTAs in one wave).
+int gemm_global_split(int64_t M, int64_t N, int64_t K, int sms);
+// Bytes of partial tiles the global-memory form needs for that split.
+size_t gemm_part_bytes(int64_t M, int64_t N, int S);
 
 // q4_misc.cu
 cudaError_t launch_dequant(void* W, int w_dtype, const uint8_t* B, int64_t K, int64_t N,

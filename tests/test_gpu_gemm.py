@@ -218,3 +218,59 @@ def test_small_m_one_hot_rows_give_bf16_tiles():
     C = run(si.f32_to_bf16_bits(A), B, M, N, K).cpu().numpy()
     Wb = oracle.dequant_bf16(B, K, N)
     assert np.array_equal(C, (Wb[ks].astype(np.uint32) << 16).view(np.float32))
+
+
+def _sampled_tile_check(C, A, B, M, N, K, seed, what, nsample=24):
+    """24 seeded block columns of C against the bf16-tile oracle."""
+    nb = si.nblocks(N)
+    cols = np.sort(si.rng(seed, 5).choice(nb, size=min(nsample, nb), replace=False))
+    Bs = B.reshape(K, nb, 18)[:, cols].reshape(K, -1)
+    Cb, Sb = oracle.matmul_bf16_tiles(A, Bs, M, 32 * len(cols), K)
+    got = to_host64(C).reshape(M, nb, 32)[:, cols].reshape(M, -1)
+    assert_tile_tol(got, Cb, Sb, what)
+
+
+@pytest.mark.parametrize("M", [8, 32, 64])
+def test_small_m_batched_decode_shape(M):
+    """K = 5120, N = 12288 (48 column tiles), bf16 A: up to 32 rows the K
+    splits of a tile run as independent CTAs (144 of the 152 SMs in one wave)
+    and are added through global memory, at 64 rows over a cluster; sampled
+    columns against the bf16-tile oracle, and two runs bit-identical."""
+    K, N = 5120, 12288
+    A = si.activations_bf16(M, K, seed=50 + M)
+    B = si.q4_weights(K, N, seed=50)
+    c1 = run(A, B, M, N, K)
+    c2 = run(A, B, M, N, K)
+    assert torch.equal(c1, c2)
+    _sampled_tile_check(c1, A, B, M, N, K, M, f"M={M} 5120x12288")
+
+
+def test_small_m_capture_on_a_fresh_stream():
+    """A stream captured before any eager call has no scratch for the global
+    split: the captured call takes the cluster form.  Both forms match the
+    bf16-tile oracle; eager calls on the same stream afterwards repeat
+    exactly, and leave every tile ticket at zero (a third call agrees)."""
+    M, K, N = 16, 5120, 4096
+    A = si.activations_bf16(M, K, seed=61)
+    B = si.q4_weights(K, N, seed=61)
+    dA, dB = to_dev(A), to_dev(B)
+    s = torch.cuda.Stream()
+    out = torch.empty((M, N), dtype=torch.float32, device=device())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        q4.q4_matmul_ex(out, dA, dB, M, N, K, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert q4.q4_get_device_status() == q4.Q4_OK
+    Cb, Sb = oracle.matmul_bf16_tiles(A, B, M, N, K)
+    assert_tile_tol(to_host64(out), Cb, Sb, "captured (cluster form)")
+    eager = []
+    for _ in range(3):
+        c = torch.empty((M, N), dtype=torch.float32, device=device())
+        with torch.cuda.stream(s):
+            q4.q4_matmul_ex(c, dA, dB, M, N, K, stream=s)
+        s.synchronize()
+        eager.append(c)
+    assert q4.q4_get_device_status() == q4.Q4_OK
+    assert torch.equal(eager[0], eager[1]) and torch.equal(eager[1], eager[2])
+    assert_tile_tol(to_host64(eager[0]), Cb, Sb, "eager (global split)")
