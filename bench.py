@@ -72,7 +72,7 @@ TRAFFIC = {
 # The same for the prefill GEMM kernel (q4_gemm_tc_kernel), one launch of
 # M = 2048, K = 5120, N = 12288 (profiles/q4_gemm_tc_kernel_prefill_2048x5120x12288.md).
 TRAFFIC_GEMM = {
-    "5f2e214e94e09c0b": 67983872,
+    "644fb65072bc35ec": 67818240,
 }
 
 
