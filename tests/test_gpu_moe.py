@@ -118,3 +118,45 @@ def test_moe_after_gemv_shares_library_workspace():
         C = gemv_run(A, B, M, N, K)
         C64, S = oracle.matmul(A, B, M, N, K)
         assert np.all(np.abs(C.cpu().numpy() - C64) <= 1e-3 * S + 1e-6)
+
+
+def test_moe_every_slot_invalid_gives_zeros():
+    """No valid routing entry at all: no expert runs, out is exactly zero (the
+    oracle's value), and the index error is flagged."""
+    T, topk, E, H, I = 2, 3, 4, 256, 64
+    x, Wg, Wu, Wd, idx, w = make(T, topk, E, H, I, seed=6)
+    idx = np.full_like(idx, -1)
+    out = torch.full((T, H), 7.0, dtype=torch.float32, device=device())
+    q4.q4_moe_experts_ex(out, to_dev(x), to_dev(Wg), to_dev(Wu), to_dev(Wd), to_dev(idx),
+                         to_dev(w), T, topk, E, H, I)
+    torch.cuda.synchronize()
+    assert not out.any()
+    assert q4.q4_get_device_status() == q4.Q4_ERR_DEVICE
+    assert q4.q4_last_device_flags() & q4.Q4_DEVERR_INDEX
+
+
+@pytest.mark.parametrize("T", [1, 5])
+def test_moe_captured_on_a_fresh_stream_equals_eager(T):
+    """Captured into a CUDA graph on a stream that has seen no eager call, and
+    then called eagerly on it: bit-identical outputs, within the oracle's
+    tolerance."""
+    topk, E, H, I = 3, 6, 512, 96
+    x, Wg, Wu, Wd, idx, w = make(T, topk, E, H, I, seed=20 + T)
+    d = [to_dev(a) for a in (x, Wg, Wu, Wd, idx, w)]
+    ws = torch.empty(q4.q4_moe_workspace_size(T, topk, E, H, I), dtype=torch.uint8,
+                     device=device())
+    s = torch.cuda.Stream()
+    cap = torch.empty((T, H), dtype=torch.float32, device=device())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        q4.q4_moe_experts_ex(cap, *d, T, topk, E, H, I, workspace=ws, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    eager = torch.empty_like(cap)
+    with torch.cuda.stream(s):
+        q4.q4_moe_experts_ex(eager, *d, T, topk, E, H, I, workspace=ws, stream=s)
+    s.synchronize()
+    assert q4.q4_get_device_status() == q4.Q4_OK
+    assert torch.equal(cap, eager)
+    ref, tol, _ = oracle.moe(x, Wg, Wu, Wd, idx, w, T, topk, E, H, I)
+    check(eager.cpu().numpy().astype(np.float64), ref, tol, f"captured and eager T={T}")
