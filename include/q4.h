@@ -107,7 +107,7 @@ Q4_API int q4_matmul(float *C, const float *A, const void *B, int64_t M, int64_t
  *     products are accumulated in fp32; the result is A . bf16_rn(W), whose
  *     deviation from A . W is bounded by 2^-9 * sum|a*w| plus the fp32
  *     accumulation error.  Up to 128 rows each output tile's K range is
- *     split; up to 32 rows the splits may run as independent CTAs that add
+ *     split; up to 40 rows the splits may run as independent CTAs that add
  *     their partial tiles through library-owned scratch of the calling
  *     stream (partial tiles and per-tile arrival counters, cudaMalloc'd by
  *     the first such call on that stream and grown by a larger one; a call

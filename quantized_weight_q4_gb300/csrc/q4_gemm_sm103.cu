@@ -850,8 +850,9 @@ int gemm_small_split(int64_t M, int64_t N, int64_t K) {
 int gemm_global_split(int64_t M, int64_t N, int64_t K, int sms) {
   // the partial tiles grow with M: on K = 5120, N = 12288 (48 tiles) the
   // global form with 3 splits against the cluster form with 2 measured
-  // +26% / +19% / +8% at M = 8 / 16 / 32 and -8% at M = 64 (GB300)
-  if (M > 32 || sms <= 0) return 0;
+  // +26% / +19% / +8% / +4% at M = 8 / 16 / 32 / 40, even at 48, -4% at 56
+  // and -8% at 64 (GB300)
+  if (M > 40 || sms <= 0) return 0;
   const int64_t tiles = (N + gemm::BN - 1) / gemm::BN;
   const int64_t ksteps = (K + gemm::BK - 1) / gemm::BK;
   if (tiles > kMaxGemmTickets) return 0;

@@ -127,7 +127,7 @@ int gemm_small_split(int64_t M, int64_t N, int64_t K);
 // Tile counters a stream's ticket array holds (N up to 1,048,576 columns).
 constexpr int kMaxGemmTickets = 4096;
 // K splits of the global-memory small-M form (0: the cluster form is chosen:
-// the global form runs for M <= 32, where it fits more CTAs in one wave).
+// the global form runs for M <= 40, where it fits more CTAs in one wave).
 int gemm_global_split(int64_t M, int64_t N, int64_t K, int sms);
 // Bytes of partial tiles the global-memory form needs for that split.
 size_t gemm_part_bytes(int64_t M, int64_t N, int S);
