@@ -73,7 +73,8 @@ extern "C" {
  * q4_matmul -- C = A . W, fp32 A [M, K], fp32 C [M, N], B in Q4_LAYOUT_BLOCKS,
  * on the legacy default stream.
  * [engine page §3.4: matmul_q4_0(A, B, C, M, N, K), C overwritten as in §3.2]
- * Allocates nothing: the split-K partial sums are combined on chip.
+ * Allocates nothing: fp32 activations take the split-K GEMV, whose partial
+ * sums are combined on chip.
  */
 Q4_API int q4_matmul(float *C, const float *A, const void *B, int64_t M, int64_t N, int64_t K);
 
@@ -90,30 +91,38 @@ Q4_API int q4_matmul(float *C, const float *A, const void *B, int64_t M, int64_t
  *              this K x N), for M <= 64 only (else Q4_ERR_SHAPE): the same
  *              GEMV on the same values, so C is bit-identical to the
  *              Q4_LAYOUT_BLOCKS result for the same shape
- *   workspace  unused by this entry point (q4_matmul_workspace_size returns
- *              0); accepted for interface stability, may be NULL.  (The
- *              tensor-core GEMM's small-M form keeps its own scratch per
- *              stream, see below.)
+ *   workspace  may be NULL.  Shapes whose tensor-core GEMM splits K over
+ *              independent CTAs (bf16 A, 8 <= M <= 40) add the splits'
+ *              partial tiles through scratch: q4_matmul_workspace_size(M, N,
+ *              K) bytes of it (0 for every other shape).  A workspace of at
+ *              least that size is used for it; its bytes must be zero before
+ *              the first call that uses them and every completed call leaves
+ *              them zero (zero it again after a Q4_ERR_DEVICE status).  With
+ *              no such workspace an eager call uses scratch the library owns
+ *              per stream (cudaMalloc'd by the first such call on the stream,
+ *              replaced by a larger one when a later call needs more, after
+ *              that stream has drained), and a call made while the stream is
+ *              captured into a CUDA graph combines the splits on chip
+ *              instead, so that no graph holds library-owned scratch.
+ *              Calls that share one workspace must not overlap on the GPU;
+ *              that includes replays of graphs captured with it.
  *   stream     cudaStream_t (NULL = legacy default stream)
  * Kernel choice:
- *   - M < 8, or fp32 A, or Q8_0 or planar weights, or a shape the GEMM below
- *     does not take: the split-K GEMV on the CUDA cores, in chunks of up to 4 rows of
- *     A.  The splits of each column tile run as one thread-block cluster and
- *     are added on chip in fixed order.  Exact fp32 dequantisation.
- *   - M >= 8 with bf16 A, ceil(N/32) % 8 == 0 and K % 8 == 0 (and, for
- *     M <= 128, a shape its split-K form takes): the tensor-core GEMM
- *     (prompt batching, engine page §5.2).  Each weight is
- *     dequantised to a bf16 tile element bf16_rn((q - 8) * d) and the
- *     products are accumulated in fp32; the result is A . bf16_rn(W), whose
- *     deviation from A . W is bounded by 2^-9 * sum|a*w| plus the fp32
- *     accumulation error.  Up to 128 rows each output tile's K range is
- *     split; up to 40 rows the splits may run as independent CTAs that add
- *     their partial tiles through library-owned scratch of the calling
- *     stream (partial tiles and per-tile arrival counters, cudaMalloc'd by
- *     the first such call on that stream and grown by a larger one; a call
- *     made while the stream is being captured without that scratch uses the
- *     on-chip cluster combine instead).  Either way the splits are added in
- *     a fixed order.
+ *   - fp32 A, M < 8, K < 1024, Q8_0 or planar weights, or a shape the GEMM
+ *     below does not take: the split-K GEMV on the CUDA cores, in chunks of
+ *     up to 4 rows of A.  The splits of each column tile run as one
+ *     thread-block cluster and are added on chip in fixed order.  Exact fp32
+ *     dequantisation: |C - A.W| <= 1e-3 * sum|a*w| + 1e-6 for any input.
+ *   - bf16 A with M >= 8, K >= 1024, ceil(N/32) % 8 == 0 and K % 8 == 0 (and,
+ *     for M <= 128, a shape its split-K form takes): the tensor-core GEMM
+ *     (prompt batching, engine page §5.2), as q4_matmul_bf16_tiles below.
+ *     Its result A . bf16_rn(W) deviates from A . W by at most 2^-9 *
+ *     sum|a*w| plus the fp32 accumulation error; the rounding errors of the
+ *     weights have random signs, and from K = 1024 on their sum stays within
+ *     1e-3 * sum|a*w| + 1e-6 on random data.  An input built so that every
+ *     weight's rounding has the sign of its activation can reach 2^-9 *
+ *     sum|a*w|: callers that need the stated bound for any input pass fp32
+ *     activations.
  *   Both are deterministic (no floating-point atomics, fixed orders).
  * Launches use programmatic dependent launch: a kernel may start streaming
  * its weights while the previous kernel on the stream finishes, and reads A
@@ -126,8 +135,37 @@ Q4_API int q4_matmul_ex(void *C, int c_dtype, const void *A, int a_dtype,
                  const void *B, int b_layout, int64_t M, int64_t N, int64_t K,
                  void *workspace, size_t workspace_bytes, void *stream);
 
-/* Bytes of workspace q4_matmul_ex needs for this shape (currently always 0). */
+/* Bytes of workspace q4_matmul_ex and q4_matmul_bf16_tiles use for this shape
+ * (the partial tiles of the small-M tensor-core form, bf16 A; 0 for shapes
+ * that need none).  0 also when no CUDA device can be queried. */
 Q4_API size_t q4_matmul_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/*
+ * q4_matmul_bf16_tiles -- C = A . bf16_rn(W) on the tensor cores (tcgen05),
+ * for any K [engine page §5.2: a prompt's tokens batched into one matmul].
+ * Every weight is dequantised once to the bf16 tile element
+ * bf16_rn((q - 8) * d) (q4_dequant_bf16 gives the same values) and the bf16 x
+ * bf16 products are accumulated in fp32 in tensor memory.  A is bf16 [M, K];
+ * C fp32 or bf16 (RN of the fp32 result) [M, N]; B in Q4_LAYOUT_BLOCKS.
+ * Shapes: M >= 8, ceil(N/32) % 8 == 0, K % 8 == 0 (16-byte row pitches),
+ * else Q4_ERR_SHAPE.  M > 128 runs the persistent prefill form (256 x 256
+ * output tiles); M <= 128 splits K over 2..16 CTAs per 128 x 256 tile,
+ * combined in fixed order over a cluster or, up to 40 rows, through the
+ * workspace described under q4_matmul_ex.  Deterministic.
+ */
+Q4_API int q4_matmul_bf16_tiles(void *C, int c_dtype, const void *A, const void *B,
+                                int64_t M, int64_t N, int64_t K, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
+/*
+ * q4_release_scratch -- waits for the current device to finish all work,
+ * then frees every buffer the library owns on it: the per-stream scratch of
+ * the small-M GEMM and the library-owned workspace of the routed-expert calls
+ * (with the ones larger calls replaced, kept until now because CUDA graphs
+ * captured earlier may use them).  A graph captured with a NULL workspace
+ * must not be replayed after this call.  Returns Q4_OK or Q4_ERR_CUDA.
+ */
+Q4_API int q4_release_scratch(void);
 
 /*
  * q4_moe_experts -- DeepSeek-V2-style routed experts on the legacy default
@@ -153,8 +191,12 @@ Q4_API int q4_moe_experts(float *out, const void *x, const void *W_gate, const v
  * bytes) holds the intermediate SiLU(g)*u rows and the per-slot down outputs;
  * its contents need no initialisation.  NULL selects a library-owned
  * workspace, allocated (cudaMalloc) by the first call that needs more than it
- * has: make one call of the largest shape before capturing a CUDA graph.
- * Calls sharing a workspace must not overlap in time. */
+ * has.  No allocation happens while the stream is being captured: such a
+ * call returns Q4_ERR_WORKSPACE, so make one call of the largest shape before
+ * capturing a CUDA graph.  A workspace that a larger one replaces stays
+ * allocated until q4_release_scratch(), since graphs may still use it.
+ * Calls sharing a workspace must not overlap in time (the library-owned one
+ * is shared by every stream of the device). */
 Q4_API int q4_moe_experts_ex(float *out, const void *x, int x_dtype, const void *W_gate,
                       const void *W_up, const void *W_down, const int32_t *topk_idx,
                       const float *topk_w, int64_t T, int64_t topk, int64_t E,
@@ -162,6 +204,27 @@ Q4_API int q4_moe_experts_ex(float *out, const void *x, int x_dtype, const void 
                       void *stream);
 
 Q4_API size_t q4_moe_workspace_size(int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I);
+
+/*
+ * q4_moe_experts_trace -- q4_moe_experts_ex (same kernels, same results) that
+ * also returns the chain's intermediate values, so that each stage can be
+ * checked on its own [KTransformers page, «优化三»: gate and up, SiLU(g) * u,
+ * down, the weighted sum of the slots; C++ DeepSeek engine page §8.2:
+ * checking a forward pass stage by stage on fixed inputs].
+ * Row s = t * topk + k of each array belongs to slot k of token t:
+ *   g, u  fp32 [T * topk, I]   the gate and up matmul outputs
+ *   h     fp32 [T * topk, I]   SiLU(g) * u, the down projection's input
+ *   y     fp32 [T * topk, H]   the down outputs, before the routing weights
+ * Rows of slots whose index lies outside [0, E) are not written.  The
+ * workspace is required (>= q4_moe_workspace_size bytes).  All pointers are
+ * device pointers, 16-byte aligned.
+ */
+Q4_API int q4_moe_experts_trace(float *out, const void *x, int x_dtype, const void *W_gate,
+                                const void *W_up, const void *W_down,
+                                const int32_t *topk_idx, const float *topk_w, int64_t T,
+                                int64_t topk, int64_t E, int64_t H, int64_t I,
+                                void *workspace, size_t workspace_bytes, float *g, float *u,
+                                float *h, float *y, void *stream);
 
 /*
  * q4_moe_experts_noalloc -- q4_moe_experts_ex without a workspace argument,

@@ -239,6 +239,32 @@ static void row_matmul_abs(const double *a, const uint8_t *B, int64_t N, int64_t
     }
 }
 
+/* c[j] = sum_k |a[k]| * |d_kj| * (q_kj + 8): the magnitudes of the two sums
+ * the GPU's exact-dequant decode accumulates for output j, sum a*d*q and
+ * 8 * sum a*d, whose difference is the product (used by the rounding bound
+ * of the expert chain). */
+static void row_matmul_absq(const double *a, const uint8_t *B, int64_t N, int64_t K,
+                            double *c)
+{
+    int64_t nb = (N + QO_BLOCK - 1) / QO_BLOCK;
+    for (int64_t j = 0; j < N; j++)
+        c[j] = 0.0;
+    for (int64_t k = 0; k < K; k++) {
+        double av = fabs(a[k]);
+        const uint8_t *row = B + k * nb * QO_BLOCK_BYTES;
+        for (int64_t b = 0; b < nb; b++) {
+            const uint8_t *blk = row + b * QO_BLOCK_BYTES;
+            double d = fabs(block_scale(blk));
+            for (int l = 0; l < QO_BLOCK; l++) {
+                int64_t j = b * QO_BLOCK + l;
+                if (j >= N)
+                    break;
+                c[j] += av * d * (double)(block_nibble(blk, l) + 8);
+            }
+        }
+    }
+}
+
 /* C [M, N] = A [M, K] . W, with S [M, N] = sum_k |A[i,k] * W[k,j]| (may be
  * NULL).  A is fp32 (a_dtype 0) or bf16 bits (a_dtype 1), row-major.
  * [Eng §3.4 matmul_q4_0; C is overwritten as in §3.2.] */
@@ -287,14 +313,30 @@ static double sigmoid(double g) { return 1.0 / (1.0 + exp(-g)); }
  * lies outside [0, E) contribute nothing.  [KT «优化三»: routed experts as
  * batched GEMVs, 6 of 160 per token; «规则二»: gate -> top-k -> experts.]
  *
- * tol[t, j] (may be NULL) is the per-element tolerance obtained by carrying
- * the single-matmul tolerance 1e-3*sum|a*w| + 1e-6 through the chain to first
- * order: the gate and up errors through SiLU(g)*u, then through down, then
- * through the weighted sum.
+ * tol[t, j] (may be NULL) bounds the deviation of an fp32 evaluation of the
+ * chain from out, to first order.  The pages state a tolerance for one
+ * matmul only; carried through the chain it exceeds the output itself, so
+ * the chain's bound is taken from the rounding of fp32 arithmetic instead:
+ *   - one matmul output over K rows, evaluated as the sums sum a*d*q and
+ *     8 * sum a*d in fp32 by a summation tree of depth at most
+ *     D(K) = ceil(K/32) + 40, is off by at most gamma(D) * Sq with
+ *     Sq = sum_k |a_k * d_kj| * (q_kj + 8) and gamma(n) = n*u / (1 - n*u),
+ *     u = 2^-24 (the standard bound for floating-point sums);
+ *   - SiLU(g) * u in fp32, with exp from a library routine of a few ulp, is
+ *     off by at most (8 + 2|g|) * u relative;
+ *   - the errors dg, du of gate and up reach h = SiLU(g) * u as
+ *     |SiLU'(g) * u| * dg + |SiLU(g)| * du, and those of h reach the down
+ *     output as sum_i |Wd[i, j]| * dh_i;
+ *   - the weighted sum over topk slots adds gamma(topk) * sum_k |w_k * y_k|;
+ *   - 1e-6 is added once, the absolute term of the pages' tolerance.
  * g, u, h (may be NULL) receive the per-slot stage values [T*topk, I]. */
 /* The chain above with the slot weights in fp64 (w64) or fp32 (w32), and an
  * extra tolerance term wrel * |w_k| * |y_k[j]| for weights known only to a
  * relative error wrel (0 for exact weights). */
+#define QO_U (1.0 / 16777216.0)
+static double qo_gamma(double n) { return n * QO_U / (1.0 - n * QO_U); }
+static double qo_depth(int64_t K) { return (double)((K + 31) / 32) + 40.0; }
+
 static void moe_core(const void *x, int x_dtype,
                      const uint8_t *Wg, const uint8_t *Wu, const uint8_t *Wd,
                      const int32_t *idx, const float *w32, const double *w64, double wrel,
@@ -305,22 +347,28 @@ static void moe_core(const void *x, int x_dtype,
     int64_t nbH = (H + QO_BLOCK - 1) / QO_BLOCK;
     size_t up_bytes = (size_t)(H * nbI * QO_BLOCK_BYTES);
     size_t down_bytes = (size_t)(I * nbH * QO_BLOCK_BYTES);
+    double gam_gu = qo_gamma(qo_depth(H));
+    double gam_d = qo_gamma(qo_depth(I));
+    double gam_sum = qo_gamma((double)topk);
 
     double *xt = (double *)malloc(sizeof(double) * (size_t)H);
     double *g = (double *)malloc(sizeof(double) * (size_t)I);
-    double *sg = (double *)malloc(sizeof(double) * (size_t)I);
+    double *qg = (double *)malloc(sizeof(double) * (size_t)I);
     double *u = (double *)malloc(sizeof(double) * (size_t)I);
-    double *su = (double *)malloc(sizeof(double) * (size_t)I);
+    double *qu = (double *)malloc(sizeof(double) * (size_t)I);
     double *h = (double *)malloc(sizeof(double) * (size_t)I);
     double *dh = (double *)malloc(sizeof(double) * (size_t)I);
     double *y = (double *)malloc(sizeof(double) * (size_t)H);
-    double *sy = (double *)malloc(sizeof(double) * (size_t)H);
+    double *qy = (double *)malloc(sizeof(double) * (size_t)H);
+    double *prop = (double *)malloc(sizeof(double) * (size_t)H);
+    double *wy = (double *)malloc(sizeof(double) * (size_t)H);
 
     for (int64_t t = 0; t < T; t++) {
         for (int64_t i = 0; i < H; i++)
             xt[i] = act_at(x, x_dtype, t * H + i);
         for (int64_t j = 0; j < H; j++) {
             out[t * H + j] = 0.0;
+            wy[j] = 0.0;
             if (tol)
                 tol[t * H + j] = 1e-6;
         }
@@ -337,34 +385,44 @@ static void moe_core(const void *x, int x_dtype,
             const uint8_t *wg = Wg + (size_t)e * up_bytes;
             const uint8_t *wu = Wu + (size_t)e * up_bytes;
             const uint8_t *wd = Wd + (size_t)e * down_bytes;
-            row_matmul(xt, wg, I, H, g, sg);
-            row_matmul(xt, wu, I, H, u, su);
+            row_matmul(xt, wg, I, H, g, NULL);
+            row_matmul(xt, wu, I, H, u, NULL);
+            if (tol) {
+                row_matmul_absq(xt, wg, I, H, qg);
+                row_matmul_absq(xt, wu, I, H, qu);
+            }
             for (int64_t i = 0; i < I; i++) {
                 double sgm = sigmoid(g[i]);
                 double silu = g[i] * sgm;
                 double dsilu = sgm * (1.0 + g[i] * (1.0 - sgm));
                 h[i] = silu * u[i];
-                dh[i] = fabs(dsilu * u[i]) * (1e-3 * sg[i] + 1e-6)
-                      + fabs(silu) * (1e-3 * su[i] + 1e-6);
+                if (tol)
+                    dh[i] = fabs(dsilu * u[i]) * gam_gu * qg[i]
+                          + fabs(silu) * gam_gu * qu[i]
+                          + (8.0 + 2.0 * fabs(g[i])) * QO_U * fabs(h[i]);
                 if (g_out) g_out[slot * I + i] = g[i];
                 if (u_out) u_out[slot * I + i] = u[i];
                 if (h_out) h_out[slot * I + i] = h[i];
             }
-            row_matmul(h, wd, H, I, y, sy);
+            row_matmul(h, wd, H, I, y, NULL);
             for (int64_t j = 0; j < H; j++)
                 out[t * H + j] += wk * y[j];
             if (tol) {
                 /* prop[j] = sum_i dh[i] * |Wd[i, j]| */
-                double *prop = (double *)malloc(sizeof(double) * (size_t)H);
                 row_matmul_abs(dh, wd, H, I, prop);
-                for (int64_t j = 0; j < H; j++)
-                    tol[t * H + j] += fabs(wk) * (1e-3 * sy[j] + 1e-6 + prop[j]
-                                                  + wrel * fabs(y[j]));
-                free(prop);
+                row_matmul_absq(h, wd, H, I, qy);
+                for (int64_t j = 0; j < H; j++) {
+                    tol[t * H + j] += fabs(wk) * (prop[j] + gam_d * qy[j] + wrel * fabs(y[j]));
+                    wy[j] += fabs(wk * y[j]);
+                }
             }
         }
+        if (tol)
+            for (int64_t j = 0; j < H; j++)
+                tol[t * H + j] += gam_sum * wy[j];
     }
-    free(xt); free(g); free(sg); free(u); free(su); free(h); free(dh); free(y); free(sy);
+    free(xt); free(g); free(qg); free(u); free(qu); free(h); free(dh); free(y); free(qy);
+    free(prop); free(wy);
 }
 
 void q4o_moe(const void *x, int x_dtype,
@@ -454,10 +512,11 @@ void q4o_moe_block(const void *x, int x_dtype, const float *logits,
         sw[t] = 1.0;
     moe_core(x, x_dtype, Sg, Su, Sd, sidx, NULL, sw, 0.0, T, 1, 1, H, Is,
              so, st, NULL, NULL, NULL);
+    /* the shared rows are added to the routed sum in fp32: one more rounding */
     for (int64_t i = 0; i < T * H; i++) {
-        out[i] += so[i];
         if (tol)
-            tol[i] += st[i];
+            tol[i] += st[i] + QO_U * (fabs(out[i]) + fabs(so[i]));
+        out[i] += so[i];
     }
     free(sidx); free(sw); free(so); free(st);
 }

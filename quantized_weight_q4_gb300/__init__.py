@@ -54,10 +54,15 @@ SIGNATURES = {
     "q4_matmul": (_int, [_vp, _vp, _vp, _i64, _i64, _i64]),
     "q4_matmul_ex": (_int, [_vp, _int, _vp, _int, _vp, _int, _i64, _i64, _i64, _vp, _sz, _vp]),
     "q4_matmul_workspace_size": (_sz, [_i64, _i64, _i64]),
+    "q4_matmul_bf16_tiles": (_int, [_vp, _int, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _vp]),
+    "q4_release_scratch": (_int, []),
     "q4_moe_experts": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64]),
     "q4_moe_experts_ex": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _vp, _vp,
                                  _i64, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
     "q4_moe_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _i64]),
+    "q4_moe_experts_trace": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _vp, _vp,
+                                    _i64, _i64, _i64, _i64, _i64, _vp, _sz,
+                                    _vp, _vp, _vp, _vp, _vp]),
     "q4_moe_experts_noalloc": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _vp, _vp,
                                       _i64, _i64, _i64, _i64, _i64, _vp]),
     "q4_moe_static_scratch_bytes": (_sz, []),
@@ -168,6 +173,22 @@ def q4_matmul_ex(C, A, B, M: int, N: int, K: int, workspace=None, stream=None,
         M, N, K, _ptr(workspace), ws_bytes, _stream(stream)))
 
 
+def q4_matmul_bf16_tiles(C, A, B, M: int, N: int, K: int, workspace=None, stream=None) -> None:
+    """C = A . bf16_rn(W) on the tensor cores (bf16 A), whatever K."""
+    _require_cuda(C, A, B, workspace)
+    if _dtype_code(A) != Q4_BF16:
+        raise TypeError("q4_matmul_bf16_tiles takes bf16 activations")
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("q4_matmul_bf16_tiles", lib().q4_matmul_bf16_tiles(
+        _ptr(C), _dtype_code(C), _ptr(A), _ptr(B), M, N, K, _ptr(workspace), ws_bytes,
+        _stream(stream)))
+
+
+def q4_release_scratch() -> None:
+    """Frees the library-owned scratch and workspaces of the current device."""
+    _check("q4_release_scratch", lib().q4_release_scratch())
+
+
 def _seq_ops(ops):
     """ops: list of (C, A, B_host, M, N, K): C and A CUDA tensors, B a pinned CPU tensor."""
     arr = (SeqOp * len(ops))()
@@ -212,6 +233,17 @@ def q4_moe_experts_ex(out, x, W_gate, W_up, W_down, topk_idx, topk_w, T: int, to
         _ptr(out), _ptr(x), _dtype_code(x), _ptr(W_gate), _ptr(W_up), _ptr(W_down),
         _ptr(topk_idx), _ptr(topk_w), T, topk, E, H, I, _ptr(workspace), ws_bytes,
         _stream(stream)))
+
+
+def q4_moe_experts_trace(out, x, W_gate, W_up, W_down, topk_idx, topk_w, T: int, topk: int,
+                         E: int, H: int, I: int, workspace, g, u, h, y, stream=None) -> None:
+    """q4_moe_experts_ex that also writes g, u, h [T*topk, I] and y [T*topk, H]."""
+    _require_cuda(out, x, W_gate, W_up, W_down, topk_idx, topk_w, workspace, g, u, h, y)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("q4_moe_experts_trace", lib().q4_moe_experts_trace(
+        _ptr(out), _ptr(x), _dtype_code(x), _ptr(W_gate), _ptr(W_up), _ptr(W_down),
+        _ptr(topk_idx), _ptr(topk_w), T, topk, E, H, I, _ptr(workspace), ws_bytes,
+        _ptr(g), _ptr(u), _ptr(h), _ptr(y), _stream(stream)))
 
 
 def q4_moe_workspace_size(T: int, topk: int, E: int, H: int, I: int) -> int:

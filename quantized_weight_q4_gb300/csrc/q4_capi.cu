@@ -48,13 +48,21 @@ struct DeviceState {
   // launch shapes already chosen for a problem size (the choice runs occupancy queries)
   std::map<std::tuple<int64_t, int64_t, int64_t, int>, GemvShape> gemv_shapes;
   std::map<std::tuple<int64_t, int64_t, int64_t, int64_t, int64_t>, MoeShape> moe_shapes;
-  // per stream: the small-M GEMM's partial tiles and its zeroed tile tickets
+  // per stream (keyed by its cudaStreamGetId, so that one handle naming a
+  // different stream in each host thread, as cudaStreamPerThread does, gets
+  // one entry per stream): the small-M GEMM's partial tiles and its zeroed
+  // tile tickets.  Only eager calls use it; a stream being captured never
+  // does, so no CUDA graph holds these pointers.
   struct GemmScratch {
     float* part = nullptr;
     size_t part_bytes = 0;
     unsigned* tickets = nullptr;
   };
-  std::map<cudaStream_t, GemmScratch> gemm_scratch;
+  std::map<unsigned long long, GemmScratch> gemm_scratch;
+  // library-owned workspaces replaced by larger ones: a CUDA graph captured
+  // while one was current may still use it, so it is kept until
+  // q4_release_scratch()
+  std::vector<void*> retired;
 };
 
 std::mutex g_mu;
@@ -77,70 +85,84 @@ int current_state(DeviceState** out) {
   return Q4_OK;
 }
 
-// Library-owned workspace of at least `bytes`, zero-filled when (re)allocated.
-// The small-M GEMM's scratch for stream `st`: partial tiles (at least `bytes`)
-// and a zeroed ticket array.  It allocates only outside stream capture and
-// returns false when it cannot; the caller then takes the cluster form.
+// True if `st` is being captured into a CUDA graph (or its state cannot be read).
+bool capturing(cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return true;
+  }
+  return cs != cudaStreamCaptureStatusNone;
+}
+
+// The small-M GEMM's library scratch for stream `st`: partial tiles (at least
+// `bytes`) and a zeroed ticket array.  Eager calls only: it returns false for
+// a stream being captured (no graph may hold library scratch, whose buffers a
+// later, larger call replaces) and when it cannot allocate; the caller then
+// takes the cluster form.  A buffer outgrown by a later call is freed after
+// the stream has drained, since only that stream's kernels use it.
 bool gemm_scratch(DeviceState* s, cudaStream_t st, size_t bytes, float** part,
                   unsigned** tickets) {
-  DeviceState::GemmScratch& g = s->gemm_scratch[st];
-  if (!g.tickets || g.part_bytes < bytes) {
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+  if (capturing(st)) return false;
+  unsigned long long id = 0;
+  if (cudaStreamGetId(st, &id) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  DeviceState::GemmScratch& g = s->gemm_scratch[id];
+  if (!g.tickets) {
+    unsigned* t = nullptr;
+    const size_t tb = q4::kMaxGemmTickets * sizeof(unsigned);
+    if (cudaMalloc(&t, tb) != cudaSuccess) {
       cudaGetLastError();
       return false;
     }
-    if (cs != cudaStreamCaptureStatusNone) return false;
-    if (!g.tickets) {
-      unsigned* t = nullptr;
-      const size_t tb = q4::kMaxGemmTickets * sizeof(unsigned);
-      if (cudaMalloc(&t, tb) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-      }
-      if (cudaMemsetAsync(t, 0, tb, st) != cudaSuccess) {
-        cudaGetLastError();
-        cudaFree(t);
-        return false;
-      }
-      g.tickets = t;
+    if (cudaMemsetAsync(t, 0, tb, st) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(t);
+      return false;
     }
-    if (g.part_bytes < bytes) {
-      if (g.part) {   // kernels on this stream may still read the old buffer
-        if (cudaStreamSynchronize(st) != cudaSuccess) return false;
-        cudaFree(g.part);
-        g.part = nullptr;
-        g.part_bytes = 0;
-      }
-      const size_t want = bytes + bytes / 4;
-      if (cudaMalloc(&g.part, want) != cudaSuccess) {
-        cudaGetLastError();
-        g.part = nullptr;
-        return false;
-      }
-      g.part_bytes = want;
+    g.tickets = t;
+  }
+  if (g.part_bytes < bytes) {
+    if (g.part) {   // kernels on this stream may still read the old buffer
+      if (cudaStreamSynchronize(st) != cudaSuccess) return false;
+      cudaFree(g.part);
+      g.part = nullptr;
+      g.part_bytes = 0;
     }
+    const size_t want = bytes + bytes / 4;
+    if (cudaMalloc(&g.part, want) != cudaSuccess) {
+      cudaGetLastError();
+      g.part = nullptr;
+      return false;
+    }
+    g.part_bytes = want;
   }
   *part = g.part;
   *tickets = g.tickets;
   return true;
 }
 
-int owned_workspace(DeviceState* s, size_t bytes, void** ws) {
+// Library-owned workspace of at least `bytes`.  A larger one is allocated
+// only outside stream capture (Q4_ERR_WORKSPACE while `st` is captured); the
+// one it replaces is retired, not freed, because a graph captured earlier may
+// still use it.
+int owned_workspace(DeviceState* s, size_t bytes, cudaStream_t st, void** ws) {
   if (bytes == 0) {
     *ws = s->ws;
     return Q4_OK;
   }
   if (s->ws_bytes < bytes) {
-    if (s->ws) {
-      if (cudaDeviceSynchronize() != cudaSuccess) return Q4_ERR_CUDA;
-      cudaFree(s->ws);
-      s->ws = nullptr;
-      s->ws_bytes = 0;
+    if (capturing(st)) return Q4_ERR_WORKSPACE;
+    const size_t want = bytes + bytes / 4;
+    void* p = nullptr;
+    if (cudaMalloc(&p, want) != cudaSuccess) {
+      cudaGetLastError();
+      return Q4_ERR_CUDA;
     }
-    size_t want = bytes + bytes / 4;
-    if (cudaMalloc(&s->ws, want) != cudaSuccess) return Q4_ERR_CUDA;
-    if (cudaMemset(s->ws, 0, want) != cudaSuccess) return Q4_ERR_CUDA;
+    if (s->ws) s->retired.push_back(s->ws);
+    s->ws = p;
     s->ws_bytes = want;
   }
   *ws = s->ws;
@@ -345,7 +367,8 @@ int gemv_run(DeviceState* s, void* C, int c_dtype, const void* A, int a_dtype, c
 int moe_run(DeviceState* s, const MoeShape& m, float* out, const void* x, int x_dtype,
             const void* W_gate, const void* W_up, const void* W_down, const int32_t* topk_idx,
             const float* topk_w, int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I,
-            void* ws, const float* addend, cudaStream_t st) {
+            void* ws, const float* addend, cudaStream_t st, float* g_trace = nullptr,
+            float* u_trace = nullptr) {
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   const int64_t nbI = ceil_div(I, 32), nbH = ceil_div(H, 32);
   float* h = reinterpret_cast<float*>(w8 + m.off_h);
@@ -360,6 +383,8 @@ int moe_run(DeviceState* s, const MoeShape& m, float* out, const void* x, int x_
   p.list_cap = m.list_cap;
   p.h = h;
   p.y = y;
+  p.g_trace = g_trace;
+  p.u_trace = u_trace;
   p.err = s->status;
   p.c_dtype = 0;
   q4::fill_decode_consts(p, q4::kFmtQ4);
@@ -437,11 +462,62 @@ const char* q4_status_str(int status) {
   }
 }
 
+}  // extern "C"
+
+namespace {
+// Shapes the tensor-core GEMM takes at all (bf16 A).
+bool gemm_shape_ok(int64_t M, int64_t N, int64_t K) {
+  return M >= kMinTensorRows && q4::gemm_supported(M, N, K) &&
+         (M > 128 || q4::gemm_small_split(M, N, K) > 0);
+}
+
+// Shapes whose q4_matmul_ex runs the tensor-core GEMM.  Below kMinTensorK the
+// bf16 tile rounding (up to 2^-9 relative per weight) is not averaged out over
+// enough products to keep |err| <= 1e-3 * sum|a*w| on random data, so short
+// reductions take the exact-dequant GEMV.
+constexpr int64_t kMinTensorK = 1024;
+bool takes_gemm(int fmt, int a_dtype, int64_t M, int64_t N, int64_t K) {
+  return fmt == q4::kFmtQ4 && a_dtype == Q4_BF16 && K >= kMinTensorK && gemm_shape_ok(M, N, K);
+}
+
+// Caller workspace of the small-M GEMM's global-memory form: the tile
+// tickets (zero before first use, left zero by every completed call), then
+// the partial tiles.
+size_t gemm_ticket_bytes(int64_t N) { return round_up(static_cast<size_t>(ceil_div(N, 256)) * 4, 256); }
+
+// The tensor-core GEMM for a validated problem (the caller holds g_mu).
+int gemm_run(DeviceState* s, void* C, int c_dtype, const void* A, const void* B, int64_t M,
+             int64_t N, int64_t K, void* workspace, size_t workspace_bytes, cudaStream_t st) {
+  float* part = nullptr;
+  unsigned* tickets = nullptr;
+  const int sg = q4::gemm_global_split(M, N, K, s->sms);
+  if (sg > 0) {
+    const size_t tb = gemm_ticket_bytes(N);
+    const size_t need = tb + q4::gemm_part_bytes(M, N, sg);
+    if (workspace && workspace_bytes >= need) {
+      tickets = static_cast<unsigned*>(workspace);
+      part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + tb);
+    } else if (!gemm_scratch(s, st, q4::gemm_part_bytes(M, N, sg), &part, &tickets)) {
+      part = nullptr;
+      tickets = nullptr;
+    }
+  }
+  return launch_status(
+      q4::launch_gemm(C, c_dtype, A, B, M, N, K, s->status, s->sms, st, part, tickets));
+}
+}  // namespace
+
+extern "C" {
+
 size_t q4_matmul_workspace_size(int64_t M, int64_t N, int64_t K) {
-  (void)M;
-  (void)N;
-  (void)K;
-  return 0;   // split-K partial sums are combined on chip
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  if (current_state(&s) != Q4_OK) return 0;
+  if (!gemm_shape_ok(M, N, K)) return 0;
+  const int sg = q4::gemm_global_split(M, N, K, s->sms);
+  if (sg <= 0) return 0;
+  return gemm_ticket_bytes(N) + q4::gemm_part_bytes(M, N, sg);
 }
 
 int q4_matmul_ex(void* C, int c_dtype, const void* A, int a_dtype, const void* B, int b_layout,
@@ -460,26 +536,30 @@ int q4_matmul_ex(void* C, int c_dtype, const void* A, int a_dtype, const void* B
   if (!aligned16(C) || !aligned16(A) || !aligned16(B) || (workspace && !aligned16(workspace)))
     return Q4_ERR_ALIGN;
 
-  (void)workspace;
-  (void)workspace_bytes;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* s = nullptr;
   int rc = current_state(&s);
   if (rc != Q4_OK) return rc;
-  if (fmt == q4::kFmtQ4 && M >= kMinTensorRows && a_dtype == Q4_BF16 &&
-      q4::gemm_supported(M, N, K) && (M > 128 || q4::gemm_small_split(M, N, K) > 0)) {
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    float* part = nullptr;
-    unsigned* tickets = nullptr;
-    const int sg = q4::gemm_global_split(M, N, K, s->sms);
-    if (sg > 0 && !gemm_scratch(s, st, q4::gemm_part_bytes(M, N, sg), &part, &tickets)) {
-      part = nullptr;
-      tickets = nullptr;
-    }
-    return launch_status(
-        q4::launch_gemm(C, c_dtype, A, B, M, N, K, s->status, s->sms, st, part, tickets));
-  }
-  return gemv_run(s, C, c_dtype, A, a_dtype, B, fmt, M, N, K, static_cast<cudaStream_t>(stream));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (takes_gemm(fmt, a_dtype, M, N, K))
+    return gemm_run(s, C, c_dtype, A, B, M, N, K, workspace, workspace_bytes, st);
+  return gemv_run(s, C, c_dtype, A, a_dtype, B, fmt, M, N, K, st);
+}
+
+int q4_matmul_bf16_tiles(void* C, int c_dtype, const void* A, const void* B, int64_t M, int64_t N,
+                         int64_t K, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!C || !A || !B || M <= 0 || N <= 0 || K <= 0) return Q4_ERR_ARG;
+  if (M > (1LL << 30) || N > (1LL << 30) || K > (1LL << 30)) return Q4_ERR_SHAPE;
+  if (c_dtype != Q4_F32 && c_dtype != Q4_BF16) return Q4_ERR_DTYPE;
+  if (!aligned16(C) || !aligned16(A) || !aligned16(B) || (workspace && !aligned16(workspace)))
+    return Q4_ERR_ALIGN;
+  if (!gemm_shape_ok(M, N, K)) return Q4_ERR_SHAPE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  int rc = current_state(&s);
+  if (rc != Q4_OK) return rc;
+  return gemm_run(s, C, c_dtype, A, B, M, N, K, workspace, workspace_bytes,
+                  static_cast<cudaStream_t>(stream));
 }
 
 int q4_matmul(float* C, const float* A, const void* B, int64_t M, int64_t N, int64_t K) {
@@ -518,11 +598,49 @@ int q4_moe_experts_ex(float* out, const void* x, int x_dtype, const void* W_gate
   if (ws) {
     if (workspace_bytes < m.total) return Q4_ERR_WORKSPACE;
   } else {
-    rc = owned_workspace(s, m.total, &ws);
+    rc = owned_workspace(s, m.total, static_cast<cudaStream_t>(stream), &ws);
     if (rc != Q4_OK) return rc;
   }
   return moe_run(s, m, out, x, x_dtype, W_gate, W_up, W_down, topk_idx, topk_w, T, topk, E, H, I,
                  ws, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int q4_moe_experts_trace(float* out, const void* x, int x_dtype, const void* W_gate,
+                         const void* W_up, const void* W_down, const int32_t* topk_idx,
+                         const float* topk_w, int64_t T, int64_t topk, int64_t E, int64_t H,
+                         int64_t I, void* workspace, size_t workspace_bytes, float* g, float* u,
+                         float* h, float* y, void* stream) {
+  if (!out || !x || !W_gate || !W_up || !W_down || !topk_idx || !topk_w || !workspace || !g ||
+      !u || !h || !y)
+    return Q4_ERR_ARG;
+  if (T <= 0 || topk <= 0 || E <= 0 || H <= 0 || I <= 0) return Q4_ERR_ARG;
+  if (topk > 16 || T * topk > 8192 || E > (1 << 20) || H > (1 << 24) || I > (1 << 24))
+    return Q4_ERR_SHAPE;
+  if (x_dtype != Q4_F32 && x_dtype != Q4_BF16) return Q4_ERR_DTYPE;
+  if (!aligned16(out) || !aligned16(x) || !aligned16(W_gate) || !aligned16(W_up) ||
+      !aligned16(W_down) || !aligned16(topk_idx) || !aligned16(topk_w) || !aligned16(workspace) ||
+      !aligned16(g) || !aligned16(u) || !aligned16(h) || !aligned16(y))
+    return Q4_ERR_ALIGN;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  int rc = current_state(&s);
+  if (rc != Q4_OK) return rc;
+  const MoeShape& m = cached_moe_shape(s, T, topk, E, H, I);
+  if (4LL * m.mr * m.rows_gu > kMaxASliceBytes || 4LL * m.mr * m.rows_d > kMaxASliceBytes)
+    return Q4_ERR_SHAPE;
+  if (workspace_bytes < m.total) return Q4_ERR_WORKSPACE;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  rc = moe_run(s, m, out, x, x_dtype, W_gate, W_up, W_down, topk_idx, topk_w, T, topk, E, H, I,
+               workspace, nullptr, st, g, u);
+  if (rc != Q4_OK) return rc;
+  // h and y are the workspace rows the kernels used
+  const uint8_t* w8 = static_cast<const uint8_t*>(workspace);
+  const size_t n = static_cast<size_t>(T * topk);
+  if (cudaMemcpyAsync(h, w8 + m.off_h, n * I * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(y, w8 + m.off_y, n * H * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return Q4_ERR_CUDA;
+  return Q4_OK;
 }
 
 int q4_moe_experts(float* out, const void* x, const void* W_gate, const void* W_up,
@@ -632,7 +750,7 @@ int q4_moe_block(float* out, const void* x, int x_dtype, const float* logits, co
   if (ws) {
     if (workspace_bytes < b.total) return Q4_ERR_WORKSPACE;
   } else {
-    rc = owned_workspace(s, b.total, &ws);
+    rc = owned_workspace(s, b.total, static_cast<cudaStream_t>(stream), &ws);
     if (rc != Q4_OK) return rc;
   }
   uint8_t* w8 = static_cast<uint8_t*>(ws);
@@ -750,5 +868,24 @@ int q4_get_device_status(void* stream) {
 }
 
 unsigned int q4_last_device_flags(void) { return g_last_flags; }
+
+int q4_release_scratch(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  int rc = current_state(&s);
+  if (rc != Q4_OK) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) return Q4_ERR_CUDA;
+  for (auto& kv : s->gemm_scratch) {
+    cudaFree(kv.second.part);
+    cudaFree(kv.second.tickets);
+  }
+  s->gemm_scratch.clear();
+  for (void* p : s->retired) cudaFree(p);
+  s->retired.clear();
+  cudaFree(s->ws);
+  s->ws = nullptr;
+  s->ws_bytes = 0;
+  return Q4_OK;
+}
 
 }  // extern "C"

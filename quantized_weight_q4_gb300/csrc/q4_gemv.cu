@@ -842,7 +842,12 @@ __global__ void __launch_bounds__(Crew<MR>::kThreads, 1)
               }
               // SiLU(g) * u, SiLU(g) = g * sigmoid(g)
               const float silu = g / (1.0f + __expf(-g));
-              p.h[static_cast<size_t>(list[m0 + m]) * ncols + col] = silu * u;
+              const size_t o = static_cast<size_t>(list[m0 + m]) * ncols + col;
+              p.h[o] = silu * u;
+              if (p.g_trace) {
+                p.g_trace[o] = g;
+                p.u_trace[o] = u;
+              }
             } else {
               float acc_s = 0.f;
               for (int sp = 0; sp < ns; ++sp) acc_s += v[sp * T::kCols];

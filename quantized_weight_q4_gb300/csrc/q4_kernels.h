@@ -49,6 +49,8 @@ struct GemvParams {
   int list_cap;         // shared-memory list entries (>= nslots, >= ceil(E/32))
   float* h;             // [nslots, I] SiLU(g) * u
   float* y;             // [nslots, H] down outputs
+  float* g_trace;       // gate/up: if not null, g and u [nslots, I] are also
+  float* u_trace;       //   written there (q4_moe_experts_trace)
   unsigned* err;        // device status word
 };
 

@@ -1,5 +1,6 @@
-"""GPU tensor-core GEMM (bf16 A, M >= 8: the split-K small-M form up to 128
-rows, the persistent prefill form above) against the oracle.
+"""GPU tensor-core GEMM (q4_matmul_bf16_tiles: bf16 A, M >= 8, the split-K
+small-M form up to 128 rows, the persistent prefill form above) against the
+oracle, and q4_matmul_ex's choice between it and the exact GEMV.
 
 The path dequantises every weight to a bf16 tile element, bf16_rn((q-8)*d),
 and accumulates bf16 x bf16 products in fp32.  Its own oracle is therefore
@@ -29,8 +30,13 @@ pytestmark = pytest.mark.gpu
 
 
 def run(A, B, M, N, K, c_dtype=torch.float32):
+    """The tensor-core GEMM (q4_matmul_bf16_tiles) for bf16 A; q4_matmul_ex
+    for fp32 A."""
     C = torch.empty((M, N), dtype=c_dtype, device=device())
-    q4.q4_matmul_ex(C, to_dev(A), to_dev(B), M, N, K)
+    if A.dtype == np.uint16:
+        q4.q4_matmul_bf16_tiles(C, to_dev(A), to_dev(B), M, N, K)
+    else:
+        q4.q4_matmul_ex(C, to_dev(A), to_dev(B), M, N, K)
     torch.cuda.synchronize()
     assert q4.q4_get_device_status() == q4.Q4_OK
     return C
@@ -245,9 +251,100 @@ def test_small_m_batched_decode_shape(M):
     _sampled_tile_check(c1, A, B, M, N, K, M, f"M={M} 5120x12288")
 
 
+def test_matmul_ex_short_k_takes_the_exact_gemv():
+    """bf16 A, M >= 8, K < 1024: q4_matmul_ex runs the exact-dequant GEMV, so
+    the stated tolerance holds with no widening; one-hot rows give the exact
+    fp32 weights, not their bf16 roundings."""
+    M, K, N = 16, 520, 1000
+    A = si.activations_bf16(M, K, seed=71)
+    B = si.q4_weights(K, N, seed=71)
+    C = torch.empty((M, N), dtype=torch.float32, device=device())
+    q4.q4_matmul_ex(C, to_dev(A), to_dev(B), M, N, K)
+    torch.cuda.synchronize()
+    C64, S = oracle.matmul(A, B, M, N, K)
+    assert_within_matmul_tol(to_host64(C), C64, S, "M=16 K=520 bf16 A")
+    ks = si.rng(71, 2).choice(K, size=M, replace=False)
+    H = np.zeros((M, K), np.float32)
+    H[np.arange(M), ks] = 1.0
+    q4.q4_matmul_ex(C, to_dev(si.f32_to_bf16_bits(H)), to_dev(B), M, N, K)
+    torch.cuda.synchronize()
+    assert np.array_equal(C.cpu().numpy(), oracle.dequant_f32(B, K, N)[ks])
+    assert q4.q4_get_device_status() == q4.Q4_OK
+
+
+def test_small_m_eager_capture_grow_replay():
+    """Eager M = 8, a graph captured at M = 8, eager M = 40 on the same stream
+    (which may replace that stream's library scratch), then replays of the
+    graph: the captured call holds no library scratch (it combines its splits
+    on chip), so every result matches the bf16-tile oracle and repeats."""
+    K, N = 5120, 4096
+    s = torch.cuda.Stream()
+    ins = {}
+    for M in (8, 40):
+        A = si.activations_bf16(M, K, seed=80 + M)
+        ins[M] = (A, to_dev(A))
+    B = si.q4_weights(K, N, seed=80)
+    dB = to_dev(B)
+    outs = {M: torch.empty((M, N), dtype=torch.float32, device=device()) for M in (8, 40)}
+    with torch.cuda.stream(s):
+        q4.q4_matmul_ex(outs[8], ins[8][1], dB, 8, N, K, stream=s)
+    s.synchronize()
+    first = outs[8].clone()
+    cap = torch.empty((8, N), dtype=torch.float32, device=device())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        q4.q4_matmul_ex(cap, ins[8][1], dB, 8, N, K, stream=s)
+    with torch.cuda.stream(s):
+        q4.q4_matmul_ex(outs[40], ins[40][1], dB, 40, N, K, stream=s)
+    s.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert q4.q4_get_device_status() == q4.Q4_OK
+    for M, got in ((8, first), (8, cap), (40, outs[40])):
+        Cb, Sb = oracle.matmul_bf16_tiles(ins[M][0], B, M, N, K)
+        assert_tile_tol(to_host64(got), Cb, Sb, f"M={M}")
+    with torch.cuda.stream(s):
+        q4.q4_matmul_ex(outs[8], ins[8][1], dB, 8, N, K, stream=s)
+    s.synchronize()
+    assert torch.equal(outs[8], first)
+
+
+@pytest.mark.parametrize("M", [8, 40])
+def test_small_m_caller_workspace_in_a_graph(M):
+    """A zeroed caller workspace of q4_matmul_workspace_size bytes carries the
+    global split's tickets and partial tiles, eagerly and inside a captured
+    graph; replays agree with the eager call and the oracle, and leave the
+    tickets at zero."""
+    K, N = 5120, 12288
+    nbytes = q4.q4_matmul_workspace_size(M, N, K)
+    assert nbytes > 0
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=device())
+    A = si.activations_bf16(M, K, seed=90 + M)
+    B = si.q4_weights(K, N, seed=90)
+    dA, dB = to_dev(A), to_dev(B)
+    s = torch.cuda.Stream()
+    eager = torch.empty((M, N), dtype=torch.float32, device=device())
+    with torch.cuda.stream(s):
+        q4.q4_matmul_ex(eager, dA, dB, M, N, K, workspace=ws, stream=s)
+    s.synchronize()
+    cap = torch.empty_like(eager)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        q4.q4_matmul_ex(cap, dA, dB, M, N, K, workspace=ws, stream=s)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert q4.q4_get_device_status() == q4.Q4_OK
+    assert torch.equal(cap, eager)
+    tickets = ws[:4 * ((N + 255) // 256)].cpu().numpy()
+    assert not tickets.any()
+    _sampled_tile_check(eager, A, B, M, N, K, M, f"workspace M={M}")
+
+
 def test_small_m_capture_on_a_fresh_stream():
-    """A stream captured before any eager call has no scratch for the global
-    split: the captured call takes the cluster form.  Both forms match the
+    """A call captured into a graph never uses library scratch: it takes the
+    cluster form.  Both forms match the
     bf16-tile oracle; eager calls on the same stream afterwards repeat
     exactly, and leave every tile ticket at zero (a third call agrees)."""
     M, K, N = 16, 5120, 4096

@@ -4,8 +4,9 @@ Some callers cannot allocate device memory (a stream being captured into a
 CUDA graph in global mode, loops that must not allocate after start-up, hosts
 whose allocator owns all device memory).  q4_moe_experts_noalloc serves them
 with scratch built into the library.  Here it is called through the C ABI
-twice in a row and checked against q4_moe_experts_ex with a caller workspace,
-within the oracle's per-element tolerance.  This file is collected last.
+twice in a row and checked against q4_moe_experts_ex with a caller workspace
+and against the oracle, within the oracle's per-element tolerance.  This file
+is collected last.
 """
 
 import ctypes
@@ -44,7 +45,8 @@ def test_noalloc_matches_workspace_entry_point():
     q4.q4_moe_experts_ex(ref, dx, dg, du, dd, di, dw, T, topk, E, H, I, workspace=ws)
     torch.cuda.synchronize()
     ref_h = ref.cpu().numpy().astype(np.float64)
-    _, tol, _ = oracle.moe(x, Wg, Wu, Wd, idx, w, T, topk, E, H, I)
+    want, tol, _ = oracle.moe(x, Wg, Wu, Wd, idx, w, T, topk, E, H, I)
+    assert np.all(np.abs(ref_h - want) <= tol)
 
     stream = torch.cuda.current_stream().cuda_stream
     for _ in range(2):   # two calls in a row share the static scratch
@@ -57,7 +59,11 @@ def test_noalloc_matches_workspace_entry_point():
         assert rc == q4.Q4_OK, q4.status_str(rc)
         torch.cuda.synchronize()
         got = out.cpu().numpy().astype(np.float64)
+        # the same kernels on the same inputs: within the tolerance of the
+        # workspace entry point's result (in fact equal to it), and of the oracle
         assert np.all(np.abs(got - ref_h) <= tol)
+        assert np.array_equal(got, ref_h)
+        assert np.all(np.abs(got - want) <= tol)
     assert q4.q4_get_device_status() == q4.Q4_OK
 
 
