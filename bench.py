@@ -4,8 +4,16 @@
 Default workload (``--workload decode_sweep_7b``): one decode token through a
 7B-like model's Q4_0 weights, M = 1, fp32 activations: 32 layers x
 {4 x (K=4096, N=4096), 2 x (4096, 11008), 1 x (11008, 4096)} GEMVs, 224 in all,
-3,642,753,024 bytes of weights, run back to back from one CUDA graph.  One
-step = one pass of the 224 GEMVs.  Metric: weight bytes streamed per second.
+3,642,753,024 bytes of weights, each GEMV with its own fresh input.  One step =
+one pass of the 224 GEMVs, run as one persistent launch (q4_gemv_seq_run)
+captured in a CUDA graph.  Metric: weight bytes streamed per second.  The
+line also carries the same sweep with a decoder layer's ordering and as a
+graph of 224 separate launches (``sweep_variants``), every other configuration
+of the benchmark as a short nested run (``records``: one 4096 x 4096 GEMV, the
+batched 5120 x 12288 decode at M = 1, 4, 8, 64, the routed experts at T = 1
+and 32, the M = 2048 prefill GEMM), and two CPU baselines: the oracle
+(``cpu_baseline``) and the pages' fused fp32 loop with OpenMP on every
+physical core (``cpu_baseline_openmp``).
 
 Other workloads (``--workload``), each printing its own line: ``gemv`` (one
 GEMV, fp32 A, default K = N = 4096, --m/--k/--n), ``batched`` (K = 5120,
@@ -66,6 +74,15 @@ def measured_peaks():
 TRAFFIC = {
     # profiles/q4_gemv_kernel_decode_sweep_7b.md: mean over the sweep's 4:2:1 shape mix
     "d74610c072511ba9": 16312210,
+}
+
+
+# The same for the persistent decode-sequence kernel (q4_gemv_seq_kernel), per
+# launch of the whole 32-layer sweep: captured on the 4-layer sweep (455 MB of
+# weights, above the L2 size) and scaled by 8, the units of work growing with
+# the layers.
+TRAFFIC_SEQ = {
+    "37eb09061c91e201": 3688161280,
 }
 
 
@@ -229,6 +246,61 @@ def build_sweep(torch, dev, layers, seed=0, fmt="q4_0"):
                 wbytes=wbytes, launches_per_step=len(shapes))
 
 
+def sweep_deps(n, kind):
+    """Dependency lists of the sweep's ops (7 per layer: q, k, v, o, gate, up,
+    down).  'none': every op has its own fresh input; 'layer': a decoder
+    layer's ordering (q, k, v after the previous down; o after q, k, v; gate
+    and up after o; down after gate and up); 'chain': each op after the one
+    before it."""
+    out = []
+    for i in range(n):
+        if kind == "none":
+            out.append([])
+        elif kind == "chain":
+            out.append([i - 1] if i else [])
+        else:
+            j, base = i % 7, i - i % 7
+            if j < 3:
+                out.append([base - 1] if base else [])
+            elif j == 3:
+                out.append([base, base + 1, base + 2])
+            elif j < 6:
+                out.append([base + 3])
+            else:
+                out.append([base + 4, base + 5])
+    return out
+
+
+DEPS_TEXT = {
+    "none": "every GEMV has its own fresh input, no ordering",
+    "layer": "a decoder layer's ordering: q, k, v after the previous layer's down; o after "
+             "q, k, v; gate and up after o; down after gate and up",
+    "chain": "every GEMV reads its input only after the previous GEMV has completed",
+}
+
+
+class SeqGraph:
+    """A decode sequence plan (one persistent launch per step), its run
+    captured once into a CUDA graph and replayed."""
+
+    def __init__(self, torch, q4, calls, deps, slice_rows=0):
+        ops = [(C.view(-1), A.view(-1), B, N, K, d) for (C, A, B, M, N, K), d in zip(calls, deps)]
+        self.plan = q4.GemvSequence(ops, slice_rows=slice_rows)
+        self.stream = torch.cuda.Stream()
+        with torch.cuda.stream(self.stream):
+            self.plan.run(stream=self.stream)
+        self.stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            self.plan.run(stream=self.stream)
+
+    def capture(self):
+        return self
+
+    def replay(self):
+        self.graph.replay()
+
+
 def time_graph(torch, seq, steps, warmup):
     seq.capture()
     for _ in range(warmup):
@@ -261,6 +333,60 @@ def cpu_baseline_sweep(layers_sample, seed=0, fmt="q4_0"):
     return total_bytes, total_t
 
 
+def cpu_openmp_sweep(layers_sample, budget_s=6.0, seed=0):
+    """The engine page's fused fp32 loop with OpenMP over column blocks
+    (cpu_baseline/), one thread per physical core, on the first
+    `layers_sample` layers of the sweep, repeated for about `budget_s`."""
+    import cpu_baseline
+    cores = cpu_baseline.physical_cores()
+    shapes, _ = sweep_plan(layers_sample)
+    mats = [(si.activations_f32(1, K, seed, 10000 + i), si.q4_weights(K, N, seed=seed, stream=100 + i),
+             N, K) for i, (K, N) in enumerate(shapes)]
+    for A, B, N, K in mats[:2]:
+        cpu_baseline.matmul(A, B, 1, N, K, cores)   # build and warm up
+    nbytes, t, passes = 0, 0.0, 0
+    while t < budget_s and passes < 50:
+        for A, B, N, K in mats:
+            t0 = time.perf_counter()
+            cpu_baseline.matmul(A, B, 1, N, K, cores)
+            t += time.perf_counter() - t0
+            nbytes += B.nbytes
+        passes += 1
+    return {"value": round(nbytes / t / 1e9, 3), "unit": "GB/s", "cores": cores,
+            "kind": "fused fp32 Q4_0 loop (engine page §3.2-§3.4), OpenMP schedule(static) "
+                    "over column blocks, one thread per physical core",
+            "sample": f"first {layers_sample} of 32 layers ({7 * layers_sample} GEMVs), "
+                      f"{passes} passes, {nbytes} weight bytes in {t:.1f} s"}
+
+
+def summarize(line):
+    """The fields of a bench line that a nested record keeps."""
+    keep = ("value", "unit", "ms_per_step", "steps", "warmup", "config", "roofline", "clocks",
+            "gpu_launches", "launches_per_step")
+    return {k: line[k] for k in keep if k in line}
+
+
+def nested_records(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
+    """Every configuration of the benchmark besides the decode sweep, each a
+    short run of its own workload: one 4096 x 4096 GEMV, the batched
+    5120 x 12288 decode at M = 1, 4, 8, 64, the routed experts at T = 1 and
+    32, and the M = 2048 prefill GEMM."""
+    base = dict(vars(args))
+    recs = {}
+    plan = [("gemv_4096x4096", dict(workload="gemv", m=1, k=4096, n=4096, steps=200)),
+            ("batched_m1", dict(workload="batched", m=1, k=0, n=0, steps=100)),
+            ("batched_m4", dict(workload="batched", m=4, k=0, n=0, steps=100)),
+            ("batched_m8", dict(workload="batched", m=8, k=0, n=0, steps=100)),
+            ("batched_m64", dict(workload="batched", m=64, k=0, n=0, steps=100)),
+            ("moe_t1", dict(workload="moe", tokens=1, steps=50)),
+            ("moe_t32", dict(workload="moe", tokens=32, steps=10)),
+            ("prefill_m2048", dict(workload="prefill", m=2048, k=0, n=0, steps=20))]
+    for name, kw in plan:
+        a = argparse.Namespace(**{**base, "format": "q4_0", "warmup": 5, **kw})
+        recs[name] = summarize(run_other(a, ws, rank, local, torch, q4, dev, hbm_peak, peak_src))
+    return recs
+
+
 def run_ours(args, ws, rank, local):
     import torch
     import __graft_entry__
@@ -274,15 +400,26 @@ def run_ours(args, ws, rank, local):
         return run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src)
 
     # CPU baseline first (rank 0 at N = 1 only), while the GPU is idle
-    cpu = None
+    cpu = cpu_omp = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         nbytes, t = cpu_baseline_sweep(args.cpu_layers, fmt=args.format)
         cpu = {"value": nbytes / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"first {args.cpu_layers} of 32 layers ({7 * args.cpu_layers} GEMVs, "
                          f"{nbytes} weight bytes), fp64 oracle, 1 thread, {t:.1f} s"}
+        if args.format == "q4_0":
+            try:
+                cpu_omp = cpu_openmp_sweep(4)
+            except (OSError, subprocess.CalledProcessError) as e:
+                cpu_omp = {"unavailable": f"the OpenMP baseline did not build or load: {e}"}
 
     w = build_sweep(torch, dev, args.layers, fmt=args.format)
-    seq = w["seq"]
+    use_seq = args.launch == "seq" and args.format == "q4_0"
+    if use_seq:
+        seq = SeqGraph(torch, q4, w["seq"].calls, sweep_deps(len(w["shapes"]), args.deps),
+                       args.slice_rows)
+        w["launches_per_step"] = 1
+    else:
+        seq = w["seq"]
     torch.cuda.synchronize()
 
     # device-resident timing (inputs already in HBM)
@@ -316,13 +453,47 @@ def run_ours(args, ws, rank, local):
     barrier(ws)
     e2e_t = max_over_ranks(ws, e2e_t)
 
+    # the same sweep with other launch structures (same weights and inputs)
+    variants = {}
+    if use_seq and not args.no_records:
+        vsteps = min(args.steps, 100)
+        for name, make in (
+                ("layer_ordered", lambda: SeqGraph(torch, q4, w["seq"].calls,
+                                                   sweep_deps(len(w["shapes"]), "layer"),
+                                                   args.slice_rows)),
+                ("serial_launches", lambda: w["seq"])):
+            g = make()
+            with ClockSampler(local) as vclk:
+                vt = time_graph(torch, g, vsteps, args.warmup)
+            vt = max_over_ranks(ws, vt)
+            variants[name] = {
+                "value": round(ws * w["wbytes"] * vsteps / vt / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(vt / vsteps * 1e3, 5), "steps": vsteps, "warmup": args.warmup,
+                "launch": ("one persistent launch per step, dependencies: " + DEPS_TEXT["layer"]
+                           if name == "layer_ordered" else
+                           "one CUDA graph of 224 GEMV launches (q4_matmul_ex, split-K GEMV) "
+                           "with programmatic dependent launch"),
+                "gpu_launches": vsteps * (1 if name == "layer_ordered" else len(w["shapes"])),
+                "clocks": vclk.summary()}
+        status = q4.q4_get_device_status()
+        if status != q4.Q4_OK:
+            raise SystemExit(f"device status {status} after the sweep variants")
+    records = None
+    if not args.no_records and args.format == "q4_0":
+        records = nested_records(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src)
+
     wbytes = w["wbytes"]
     value = ws * wbytes * args.steps / elapsed / 1e9
     per_launch_bytes = wbytes / w["launches_per_step"]
     avg_launch_s = elapsed / (args.steps * w["launches_per_step"])
     achieved = per_launch_bytes / avg_launch_s / 1e9
-    h = kernel_source_hash()
-    traffic = TRAFFIC.get(h) if args.format == "q4_0" else None
+    if use_seq:
+        h = kernel_source_hash(("q4_gemv_seq.cu", "q4_gemv_core.cuh", "q4_device.cuh",
+                                "q4_kernels.h"))
+        traffic = TRAFFIC_SEQ.get(h)
+    else:
+        h = kernel_source_hash()
+        traffic = TRAFFIC.get(h) if args.format == "q4_0" else None
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -344,15 +515,23 @@ def run_ours(args, ws, rank, local):
             "shapes_per_layer": "4x(K=4096,N=4096) 2x(4096,11008) 1x(11008,4096)",
             "M": 1, "a_dtype": "f32", "c_dtype": "f32",
             "weight_bytes_per_step": wbytes,
-            "launch": "one CUDA graph of 224 GEMV launches with programmatic dependent launch",
+            "launch": (f"one persistent launch per step (q4_gemv_seq_run: counter clear + "
+                       f"{seq.plan.grid} resident CTAs taking 512x512 units in op order), "
+                       f"captured in a CUDA graph" if use_seq else
+                       "one CUDA graph of 224 GEMV launches with programmatic dependent launch"),
+            "deps": (args.deps + ": " + DEPS_TEXT[args.deps]) if use_seq else "serial launches",
+            "slice_rows": (args.slice_rows or "library's choice") if use_seq else None,
             "l2": "no flush: each step streams 3.64 GB of weights, > 28x the 129 MB L2",
             "parallelism": f"replicas x{ws}",
             "pct_of_hbm_peak": round(100.0 * value / ws / hbm_peak, 2),
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "q4_gemv_kernel (GEMV, one row of A, 2 blocks per thread, 32-row stages"
-                      + {"q8_0": ", Q8_0 blocks)", "q4_0_planar": ", planar Q4_0)"}.get(args.format, ")"),
+            "kernel": ("q4_gemv_seq_kernel (persistent: 18 KB TMA stages, 8 consumer warps, "
+                       "2 CTAs per SM; all 224 GEMVs in one launch)" if use_seq else
+                       "q4_gemv_kernel (GEMV, one row of A, 2 blocks per thread, 32-row stages"
+                       + {"q8_0": ", Q8_0 blocks)", "q4_0_planar": ", planar Q4_0)"}.get(args.format, ")")),
+            "kernel_source_hash": h,
             "achieved": round(achieved, 2),
             "peak": hbm_peak,
             "unit": "GB/s",
@@ -372,6 +551,9 @@ def run_ours(args, ws, rank, local):
         },
         "gpu_launches": args.steps * w["launches_per_step"],
         "clocks": clk.summary(),
+        "cpu_baseline_openmp": cpu_omp,
+        "sweep_variants": variants or None,
+        "records": records,
     }
     return line
 
@@ -411,6 +593,23 @@ class GraphOf:
         return s.elapsed_time(e) / 1e3
 
 
+_MOE = {}
+
+
+def moe_device_weights(to_dev, E, H, I):
+    """The seeded expert stacks on the device, generated once per process."""
+    key = (E, H, I)
+    if key not in _MOE:
+        _MOE[key] = tuple(to_dev(a) for a in si.moe_weights(E, H, I, seed=0))
+    return _MOE[key]
+
+
+# kernels one call of a workload launches (routed experts: gate/up, down and the
+# slot combine; MoE block: router, shared expert, routed experts)
+KERNELS_PER_CALL = {"gemv": 1, "batched": 1, "moe": 3, "quantize": 1, "prefill": 1,
+                    "moe_block": 6}
+
+
 def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
     to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
@@ -447,9 +646,7 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
         units = copies
     elif args.workload == "moe":
         T, E, H, I, topk = args.tokens, 160, 5120, 1536, 6
-        Wg, Wu, Wd = si.moe_weights(E, H, I, seed=0)
-        dWg, dWu, dWd = to_dev(Wg), to_dev(Wu), to_dev(Wd)
-        del Wg, Wu, Wd
+        dWg, dWu, dWd = moe_device_weights(to_dev, E, H, I)
         R = args.routings
         fns, keep, uniq = [], [], 0
         per_expert = (2 * H * si.nblocks(I) + I * si.nblocks(H)) * 18
@@ -609,7 +806,9 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
         "roofline": {"bound": "hbm", "achieved": round(value / ws, 2), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(value / ws / hbm_peak, 4),
                      "peak_source": peak_src, "traffic": None},
-        "gpu_launches": None, "clocks": clk.summary(), "launches_per_step": units,
+        "gpu_launches": args.steps * units * (8 if args.workload == "moe_block" and args.tokens > 1
+                                              else KERNELS_PER_CALL.get(args.workload, 1)),
+        "clocks": clk.summary(), "launches_per_step": units,
     }
 
 
@@ -743,9 +942,19 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_sweep_7b")
     ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--launch", choices=("seq", "graph"), default="seq",
+                    help="decode sweep: one persistent launch per step (seq) or a graph of "
+                         "one launch per GEMV (graph)")
+    ap.add_argument("--deps", choices=("none", "layer", "chain"), default="none",
+                    help="decode sweep with --launch seq: the ops' dependency structure")
+    ap.add_argument("--slice-rows", type=int, default=0,
+                    help="decode sweep with --launch seq: rows per unit of work (0: the "
+                         "library's choice)")
     ap.add_argument("--cpu-layers", type=int, default=24)
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-records", action="store_true",
+                    help="decode sweep: skip the nested records of the other configurations")
     ap.add_argument("--slots", type=int, default=4, help="host_stream: device weight slots")
     ap.add_argument("--format", choices=("q4_0", "q8_0", "q4_0_planar"), default="q4_0",
                     help="weight format (decode sweep, gemv, batched); q4_0_planar: the Q4_0 "

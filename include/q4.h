@@ -313,6 +313,79 @@ Q4_API size_t q4_host_stream_slot_bytes(const q4_seq_op *ops, int n);
 Q4_API int q4_matmul_host_stream(const q4_seq_op *ops, int n, void *staging, size_t staging_bytes,
                                  int slots, void *stream, void *copy_stream);
 
+/*
+ * Decode sequence -- a list of M = 1 GEMVs (C_i = A_i . W_i) run by ONE
+ * persistent launch [engine page §2.1: decoding a token streams every weight
+ * matrix of the model once, one matrix-vector product each; §3.4 the fused
+ * Q4_0 loop].  One launch keeps the HBM busy across the matrices instead of
+ * filling and draining a pipeline per matrix.
+ *
+ * q4_gemv_op -- one GEMV of the sequence:
+ *   C       device [N], c_dtype Q4_F32 or Q4_BF16 (RN of the fp32 result)
+ *   A       device [K], a_dtype Q4_F32 or Q4_BF16
+ *   B       device, K rows of ceil(N/32) block_q4_0 (Q4_LAYOUT_BLOCKS);
+ *           ceil(N/32) must be a multiple of 8 (else Q4_ERR_SHAPE)
+ *   deps    indices of up to 4 EARLIER ops of the same sequence whose C must
+ *           be complete before this op reads A (e.g. when A is, or is
+ *           computed from, their output); ndeps = 0 for none.  Weights are
+ *           streamed regardless; only the reads of A wait.
+ *   slice_rows  rows of K per unit of work: 0 for the library's choice
+ *           (512), else a multiple of 64 up to 512 (else Q4_ERR_ARG).  Every
+ *           unit ends in a reduction over its CTA and adds one partial row to
+ *           its tile's combine, so shorter units cost more.
+ * Every C is overwritten.  Results are deterministic (each output is summed
+ * in a fixed order) and equal A . W within 1e-3 * sum|a*w| + 1e-6, like
+ * q4_matmul_ex (the same exact dequantisation; other summation splits).
+ */
+typedef struct q4_gemv_op {
+  void *C;
+  const void *A;
+  const void *B;
+  int64_t N, K;
+  int a_dtype, c_dtype;
+  int ndeps;
+  int deps[4];
+  int slice_rows;
+} q4_gemv_op;
+
+/* Opaque plan of a decode sequence (host object). */
+typedef struct q4_gemv_seq q4_gemv_seq;
+
+/* Bytes of device buffer a plan for `ops` needs (0 if the ops are invalid):
+ * the ops' descriptors, counters, and 2 KB of partial sums per unit of work
+ * (a unit: 512 output columns x slice_rows rows of one op). */
+Q4_API size_t q4_gemv_seq_bytes(const q4_gemv_op *ops, int n);
+
+/*
+ * q4_gemv_seq_create -- checks the ops and writes their descriptors into
+ * `buf` (a device buffer of >= q4_gemv_seq_bytes bytes, 256-byte aligned,
+ * owned by the caller, which must keep it, the weights and the A and C
+ * buffers alive while the plan is used).  Synchronous; not for use while a
+ * stream is being captured.  The pointers of every op are fixed in the plan:
+ * new inputs are written into the same A buffers.  Errors: Q4_ERR_ARG (null
+ * pointer, size <= 0, a dependency that is not an earlier op), Q4_ERR_DTYPE,
+ * Q4_ERR_ALIGN (a pointer not 16-byte aligned, buf not 256-byte aligned),
+ * Q4_ERR_SHAPE, Q4_ERR_WORKSPACE (buf too small), Q4_ERR_CUDA.
+ */
+Q4_API int q4_gemv_seq_create(const q4_gemv_op *ops, int n, void *buf, size_t buf_bytes,
+                              q4_gemv_seq **plan);
+
+/*
+ * q4_gemv_seq_run -- runs the whole sequence on `stream`: one small clear of
+ * the plan's counters, then one launch of a resident grid (two CTAs per SM)
+ * that takes units of work in op order from a shared counter.  Asynchronous;
+ * can be captured into a CUDA graph.  Runs of one plan must not overlap on the
+ * GPU.  The current device must be the plan's.  A wait that runs out (1 s)
+ * records Q4_DEVERR_TIMEOUT (q4_get_device_status).
+ */
+Q4_API int q4_gemv_seq_run(const q4_gemv_seq *plan, void *stream);
+
+/* Frees the host object of a plan (the caller's device buffer is untouched). */
+Q4_API void q4_gemv_seq_destroy(q4_gemv_seq *plan);
+
+/* CTAs of the plan's launch (for measurement). */
+Q4_API int q4_gemv_seq_grid(const q4_gemv_seq *plan);
+
 /* Synchronises `stream`, then reads and clears the device status word of the
  * current device: Q4_OK, Q4_ERR_DEVICE (bits in q4_last_device_flags()) or
  * Q4_ERR_CUDA. */

@@ -49,6 +49,14 @@ class SeqOp(ctypes.Structure):
                 ("a_dtype", ctypes.c_int), ("c_dtype", ctypes.c_int)]
 
 
+class GemvOp(ctypes.Structure):
+    """q4_gemv_op of include/q4.h: one M = 1 GEMV of a decode sequence."""
+    _fields_ = [("C", ctypes.c_void_p), ("A", ctypes.c_void_p), ("B", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("a_dtype", ctypes.c_int), ("c_dtype", ctypes.c_int),
+                ("ndeps", ctypes.c_int), ("deps", ctypes.c_int * 4), ("slice_rows", ctypes.c_int)]
+
+
 # name -> (restype, argtypes), as declared in include/q4.h
 SIGNATURES = {
     "q4_matmul": (_int, [_vp, _vp, _vp, _i64, _i64, _i64]),
@@ -80,6 +88,12 @@ SIGNATURES = {
     "q4_selftest_wait": (_int, [_i64, _int, _vp]),
     "q4_host_stream_slot_bytes": (_sz, [ctypes.POINTER(SeqOp), _int]),
     "q4_matmul_host_stream": (_int, [ctypes.POINTER(SeqOp), _int, _vp, _sz, _int, _vp, _vp]),
+    "q4_gemv_seq_bytes": (_sz, [ctypes.POINTER(GemvOp), _int]),
+    "q4_gemv_seq_create": (_int, [ctypes.POINTER(GemvOp), _int, _vp, _sz,
+                                  ctypes.POINTER(ctypes.c_void_p)]),
+    "q4_gemv_seq_run": (_int, [_vp, _vp]),
+    "q4_gemv_seq_destroy": (None, [_vp]),
+    "q4_gemv_seq_grid": (_int, [_vp]),
     "q4_get_device_status": (_int, [_vp]),
     "q4_last_device_flags": (ctypes.c_uint, []),
     "q4_status_str": (ctypes.c_char_p, [_int]),
@@ -211,6 +225,56 @@ def q4_matmul_host_stream(ops, staging, slots: int, stream=None, copy_stream=Non
     nbytes = staging.numel() * staging.element_size()
     _check("q4_matmul_host_stream", lib().q4_matmul_host_stream(
         arr, len(ops), _ptr(staging), nbytes, slots, _stream(stream), _stream(copy_stream)))
+
+
+def _gemv_ops(ops, slice_rows=0):
+    arr = (GemvOp * len(ops))()
+    for i, op in enumerate(ops):
+        C, A, B, N, K = op[:5]
+        deps = list(op[5]) if len(op) > 5 else []
+        _require_cuda(C, A, B)
+        if len(deps) > 4:
+            raise ValueError("at most 4 dependencies per op")
+        d = (ctypes.c_int * 4)(*(deps + [0] * (4 - len(deps))))
+        arr[i] = GemvOp(_ptr(C), _ptr(A), _ptr(B), N, K, _dtype_code(A), _dtype_code(C),
+                        len(deps), d, slice_rows)
+    return arr
+
+
+class GemvSequence:
+    """A decode sequence of M = 1 GEMVs run by one persistent launch
+    (q4_gemv_seq_*).  ops: list of (C, A, B, N, K) or (C, A, B, N, K, deps),
+    CUDA tensors, deps a list of indices of earlier ops whose C must be
+    complete before this op reads A.  slice_rows: rows per unit of work for
+    every op (0: the library's choice).  The tensors are referenced by the
+    plan and kept alive with it."""
+
+    def __init__(self, ops, slice_rows: int = 0):
+        import torch
+        self.ops = list(ops)
+        arr = _gemv_ops(self.ops, slice_rows)
+        L = lib()
+        nbytes = L.q4_gemv_seq_bytes(arr, len(self.ops))
+        if nbytes == 0:
+            raise Q4Error("q4_gemv_seq_bytes", Q4_ERR_ARG)
+        self.buf = torch.empty(nbytes, dtype=torch.uint8, device=self.ops[0][0].device)
+        plan = ctypes.c_void_p()
+        _check("q4_gemv_seq_create", L.q4_gemv_seq_create(arr, len(self.ops), _ptr(self.buf),
+                                                          nbytes, ctypes.byref(plan)))
+        self.plan = plan
+
+    def run(self, stream=None) -> None:
+        _check("q4_gemv_seq_run", lib().q4_gemv_seq_run(self.plan, _stream(stream)))
+
+    @property
+    def grid(self) -> int:
+        return lib().q4_gemv_seq_grid(self.plan)
+
+    def __del__(self):
+        plan = getattr(self, "plan", None)
+        if plan is not None and _lib is not None:
+            _lib.q4_gemv_seq_destroy(plan)
+            self.plan = None
 
 
 def q4_matmul_workspace_size(M: int, N: int, K: int) -> int:

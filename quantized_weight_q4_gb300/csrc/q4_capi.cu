@@ -3,6 +3,7 @@
 #include <cstdint>
 #include <cstring>
 #include <map>
+#include <new>
 #include <mutex>
 #include <tuple>
 #include <vector>
@@ -790,6 +791,179 @@ int q4_moe_block(float* out, const void* x, int x_dtype, const float* logits, co
   return moe_run(s, m, out, x, x_dtype, W_gate, W_up, W_down, idx, w, T, topk, E, H, I,
                  w8 + b.moe, Is > 0 ? ys : nullptr, st);
 }
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode sequence: many M = 1 GEMVs in one persistent launch
+// ---------------------------------------------------------------------------
+struct q4_gemv_seq {
+  int device;
+  uint8_t* buf;
+  int nops, total_units, grid, stages;
+  size_t counters_off, counters_bytes, part_off;
+  unsigned* status;
+};
+
+namespace {
+struct SeqLayout {
+  size_t descs, counters, counters_bytes, part, total;
+  int units, tiles;
+};
+
+// Checks the ops and lays out the plan buffer: op descriptors, the counters
+// cleared before every run (unit queue, done tiles per op, tile tickets),
+// then one 512-float partial row per unit.
+// Rows per unit of op i: the caller's choice, else 512.  Shorter units were
+// measured slower on GB300 with and without dependencies: each unit pays a
+// reduction over the CTA and its tile's combine a load per unit.
+int64_t seq_slice_rows(const q4_gemv_op* ops, int n, int i) {
+  (void)n;
+  return ops[i].slice_rows > 0 ? ops[i].slice_rows : q4::seq_max_slice_rows();
+}
+
+int seq_layout(const q4_gemv_op* ops, int n, SeqLayout* L) {
+  if (!ops || n <= 0 || n > (1 << 20)) return Q4_ERR_ARG;
+  const int64_t tc = q4::seq_tile_cols();
+  int64_t units = 0, tiles = 0;
+  for (int i = 0; i < n; ++i) {
+    const q4_gemv_op& o = ops[i];
+    if (!o.C || !o.A || !o.B || o.N <= 0 || o.K <= 0) return Q4_ERR_ARG;
+    if (o.N > (1LL << 30) || o.K > (1LL << 30)) return Q4_ERR_SHAPE;
+    if ((o.a_dtype != Q4_F32 && o.a_dtype != Q4_BF16) ||
+        (o.c_dtype != Q4_F32 && o.c_dtype != Q4_BF16))
+      return Q4_ERR_DTYPE;
+    if (o.ndeps < 0 || o.ndeps > 4) return Q4_ERR_ARG;
+    for (int j = 0; j < o.ndeps; ++j)
+      if (o.deps[j] < 0 || o.deps[j] >= i) return Q4_ERR_ARG;
+    if (!aligned16(o.C) || !aligned16(o.A) || !aligned16(o.B)) return Q4_ERR_ALIGN;
+    if (ceil_div(o.N, 32) % 8 != 0) return Q4_ERR_SHAPE;   // 16-byte row pitch for TMA
+    if (o.slice_rows < 0 || o.slice_rows > q4::seq_max_slice_rows() ||
+        o.slice_rows % q4::seq_stage_rows() != 0)
+      return Q4_ERR_ARG;
+  }
+  for (int i = 0; i < n; ++i) {
+    const q4_gemv_op& o = ops[i];
+    const int64_t nt = ceil_div(o.N, tc), ns = ceil_div(o.K, seq_slice_rows(ops, n, i));
+    units += nt * ns;
+    tiles += nt;
+  }
+  if (units > (1LL << 30)) return Q4_ERR_SHAPE;
+  L->units = static_cast<int>(units);
+  L->tiles = static_cast<int>(tiles);
+  L->descs = 0;
+  L->counters = round_up(sizeof(q4::SeqOpDesc) * n, 256);
+  L->counters_bytes = round_up(static_cast<size_t>(1 + n + tiles) * 4, 256);
+  L->part = L->counters + L->counters_bytes;
+  L->total = L->part + static_cast<size_t>(units) * tc * 4;
+  return Q4_OK;
+}
+}  // namespace
+
+extern "C" {
+
+size_t q4_gemv_seq_bytes(const q4_gemv_op* ops, int n) {
+  SeqLayout L;
+  return seq_layout(ops, n, &L) == Q4_OK ? L.total : 0;
+}
+
+int q4_gemv_seq_create(const q4_gemv_op* ops, int n, void* buf, size_t buf_bytes,
+                       q4_gemv_seq** plan) {
+  if (!plan) return Q4_ERR_ARG;
+  *plan = nullptr;
+  SeqLayout L;
+  int rc = seq_layout(ops, n, &L);
+  if (rc != Q4_OK) return rc;
+  if (!buf) return Q4_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(buf) & 255u) != 0) return Q4_ERR_ALIGN;
+  if (buf_bytes < L.total) return Q4_ERR_WORKSPACE;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  rc = current_state(&s);
+  if (rc != Q4_OK) return rc;
+  int stages = 5;
+  int per_sm = q4::seq_ctas_per_sm(stages);
+  if (per_sm < 2) {
+    stages = 4;
+    per_sm = q4::seq_ctas_per_sm(stages);
+  }
+  if (per_sm < 1) return Q4_ERR_CUDA;
+
+  std::vector<q4::SeqOpDesc> d(static_cast<size_t>(n));
+  std::memset(d.data(), 0, sizeof(q4::SeqOpDesc) * n);
+  const int64_t tc = q4::seq_tile_cols();
+  int unit_base = 0, ticket_base = 0;
+  for (int i = 0; i < n; ++i) {
+    const q4_gemv_op& o = ops[i];
+    q4::SeqOpDesc& e = d[i];
+    const int64_t nb = ceil_div(o.N, 32);
+    if (!q4::encode_weight_tmap(&e.tmap, o.B, o.K, nb, 1, o.K * nb * 18, 2, true, q4::kFmtQ4))
+      return Q4_ERR_CUDA;
+    e.A = o.A;
+    e.C = o.C;
+    e.K = static_cast<int>(o.K);
+    e.N = static_cast<int>(o.N);
+    e.nb = static_cast<int>(nb);
+    e.ntiles = static_cast<int>(ceil_div(o.N, tc));
+    const int64_t sr = seq_slice_rows(ops, n, i);
+    e.slice_rows = static_cast<int>(sr);
+    e.nslices = static_cast<int>(ceil_div(o.K, sr));
+    e.unit_base = unit_base;
+    e.ticket_base = ticket_base;
+    e.a_dtype = o.a_dtype;
+    e.c_dtype = o.c_dtype;
+    e.ndeps = o.ndeps;
+    for (int j = 0; j < o.ndeps; ++j) e.deps[j] = o.deps[j];
+    unit_base += e.ntiles * e.nslices;
+    ticket_base += e.ntiles;
+  }
+  uint8_t* b8 = static_cast<uint8_t*>(buf);
+  if (cudaMemcpy(b8 + L.descs, d.data(), sizeof(q4::SeqOpDesc) * n, cudaMemcpyHostToDevice) !=
+          cudaSuccess ||
+      cudaMemset(b8 + L.counters, 0, L.counters_bytes) != cudaSuccess)
+    return Q4_ERR_CUDA;
+  q4_gemv_seq* h = new (std::nothrow) q4_gemv_seq;
+  if (!h) return Q4_ERR_ARG;
+  cudaGetDevice(&h->device);
+  h->buf = b8;
+  h->nops = n;
+  h->total_units = L.units;
+  h->stages = stages;
+  h->grid = per_sm * s->sms;
+  h->counters_off = L.counters;
+  h->counters_bytes = L.counters_bytes;
+  h->part_off = L.part;
+  h->status = s->status;
+  *plan = h;
+  return Q4_OK;
+}
+
+int q4_gemv_seq_run(const q4_gemv_seq* plan, void* stream) {
+  if (!plan) return Q4_ERR_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device) return Q4_ERR_ARG;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(plan->buf + plan->counters_off, 0, plan->counters_bytes, st) != cudaSuccess)
+    return Q4_ERR_CUDA;
+  q4::SeqParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.ops = reinterpret_cast<const q4::SeqOpDesc*>(plan->buf);
+  p.nops = plan->nops;
+  p.total_units = plan->total_units;
+  unsigned* c = reinterpret_cast<unsigned*>(plan->buf + plan->counters_off);
+  p.queue = c;
+  p.done = c + 1;
+  p.tickets = c + 1 + plan->nops;
+  p.part = reinterpret_cast<float*>(plan->buf + plan->part_off);
+  p.err = plan->status;
+  for (int i = 0; i < 4; ++i) p.kmask[i] = 0xFu << (4 * i);
+  return launch_status(q4::launch_gemv_seq(p, plan->grid, plan->stages, st));
+}
+
+void q4_gemv_seq_destroy(q4_gemv_seq* plan) { delete plan; }
+
+int q4_gemv_seq_grid(const q4_gemv_seq* plan) { return plan ? plan->grid : 0; }
 
 int q4_quantize(void* B, const void* W, int w_dtype, int64_t K, int64_t N, void* stream) {
   if (!B || !W || K <= 0 || N <= 0) return Q4_ERR_ARG;

@@ -91,6 +91,39 @@ cudaError_t launch_moe_combine(float* out, const float* y, const int32_t* idx, c
                                const float* addend, int T, int topk, int E, int H,
                                cudaStream_t st, bool pdl);
 
+// q4_gemv_seq.cu: a sequence of M = 1 GEMVs in one persistent launch.
+// One op of the sequence, as the kernel reads it from global memory.
+struct SeqOpDesc {      // 64-byte aligned through its tensor map
+  CUtensorMap tmap;     // weights: uint16 [1][K][nb*9], boxes of 144 x 64
+  const void* A;        // [K], fp32 (a_dtype 0) or bf16 (1)
+  void* C;              // [N], fp32 (c_dtype 0) or bf16 (1)
+  int K, N, nb;
+  int ntiles, nslices;  // column tiles of 512 columns, K slices of slice_rows rows
+  int slice_rows;       // a multiple of 64, at most 512
+  int unit_base;        // first unit of the op (units: tile-major, slice-minor)
+  int ticket_base;      // first tile counter of the op
+  int a_dtype, c_dtype;
+  int ndeps;
+  int deps[4];          // earlier ops whose outputs must be complete before A is read
+};
+struct SeqParams {
+  const SeqOpDesc* ops;
+  int nops, total_units;
+  unsigned* queue;      // unit counter (zero at launch)
+  unsigned* done;       // [nops] completed tiles per op (zero at launch)
+  unsigned* tickets;    // [total tiles] slices added per tile (zero at launch)
+  float* part;          // [total_units][512] partial sums
+  unsigned* err;        // device status word
+  uint32_t kmask[4];    // nibble masks (fill as for the GEMV)
+};
+// CTAs per SM that the persistent kernel with `stages` ring slots (4 or 5)
+// can keep resident (0 if it cannot launch).
+int seq_ctas_per_sm(int stages);
+int seq_tile_cols();       // columns of a unit (512)
+int seq_stage_rows();      // rows of one pipeline stage (64)
+int seq_max_slice_rows();  // rows of the longest unit (512)
+cudaError_t launch_gemv_seq(const SeqParams& p, int grid, int stages, cudaStream_t st);
+
 // q4_gemm_sm103.cu: the prefill GEMM on the tensor cores.
 struct GemmParams {
   CUtensorMap tmap_a;   // A: bf16 [M][K], boxes of 64 K x 256 rows, 128-byte swizzle

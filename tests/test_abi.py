@@ -114,3 +114,47 @@ def test_host_stream_checks_on_host(L):
     assert L.q4_matmul_host_stream(ops, 2, vp(good), 1 << 20, 2, s1, s2) == q4.Q4_ERR_DTYPE
     ops[1].a_dtype, ops[1].C = 1, bad
     assert L.q4_matmul_host_stream(ops, 2, vp(good), 1 << 20, 2, s1, s2) == q4.Q4_ERR_ALIGN
+
+
+def test_gemv_seq_checks_on_host(L):
+    """The decode sequence checks every op, and the plan buffer, before any
+    CUDA call; its buffer holds 2 KB of partial sums per unit of 512 columns
+    x 512 rows."""
+    vp = ctypes.c_void_p
+    good = 0x10000
+
+    def op(N, K, deps=(), a=0, c=0, C=good, rows=512):
+        d = (ctypes.c_int * 4)(*(list(deps) + [0] * (4 - len(deps))))
+        return q4.GemvOp(C, good, good, N, K, a, c, len(deps), d, rows)
+
+    ops = (q4.GemvOp * 3)(op(4096, 4096), op(11008, 4096, [0]), op(4096, 11008, [0, 1]))
+    units = 8 * 8 + 22 * 8 + 8 * 22
+    nbytes = L.q4_gemv_seq_bytes(ops, 3)
+    assert units * 2048 < nbytes < units * 2048 + 65536
+    # the library's choice is 512 rows; 128-row units: 32, 32 and 86 slices
+    auto = (q4.GemvOp * 3)(op(4096, 4096, rows=0), op(11008, 4096, [0], rows=0),
+                           op(4096, 11008, [0, 1], rows=0))
+    assert L.q4_gemv_seq_bytes(auto, 3) == nbytes
+    short = (q4.GemvOp * 3)(op(4096, 4096, rows=128), op(11008, 4096, [0], rows=128),
+                            op(4096, 11008, [0, 1], rows=128))
+    units_short = 8 * 32 + 22 * 32 + 8 * 86
+    assert units_short * 2048 < L.q4_gemv_seq_bytes(short, 3) < units_short * 2048 + 65536
+    plan = vp()
+    create = lambda o, n, buf, size: L.q4_gemv_seq_create(o, n, vp(buf), size, ctypes.byref(plan))
+    assert create(ops, 3, good + 16, nbytes) == q4.Q4_ERR_ALIGN
+    assert create(ops, 3, good, nbytes - 1) == q4.Q4_ERR_WORKSPACE
+    assert create(ops, 0, good, nbytes) == q4.Q4_ERR_ARG
+    assert L.q4_gemv_seq_bytes(ops, 0) == 0
+    cases = [((op(4096, 4096), op(4096, 4096, [1])), q4.Q4_ERR_ARG),     # not an earlier op
+             ((op(4096, 4096, [-1]),), q4.Q4_ERR_ARG),
+             ((op(100, 64),), q4.Q4_ERR_SHAPE),                          # 4 blocks per row
+             ((op(256, 64, a=3),), q4.Q4_ERR_DTYPE),
+             ((op(256, 0),), q4.Q4_ERR_ARG),
+             ((op(256, 64, C=good + 4),), q4.Q4_ERR_ALIGN),
+             ((op(256, 64, rows=100),), q4.Q4_ERR_ARG),                  # not a multiple of 64
+             ((op(256, 64, rows=1024),), q4.Q4_ERR_ARG)]
+    for bad, code in cases:
+        arr = (q4.GemvOp * len(bad))(*bad)
+        assert L.q4_gemv_seq_bytes(arr, len(bad)) == 0
+        assert create(arr, len(bad), good, 1 << 30) == code
+    assert plan.value is None

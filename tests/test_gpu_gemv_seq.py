@@ -1,0 +1,225 @@
+"""The decode sequence (q4_gemv_seq_*): many M = 1 GEMVs in one persistent
+launch (C++ DeepSeek engine page §2.1: a decoded token streams every weight
+matrix once; §3.4 the fused Q4_0 loop), against the fp64 oracle.
+
+Every op's C is compared with oracle.matmul at the stated tolerance
+1e-3 * sum|a*w| + 1e-6.  Dependencies are checked by chains in which an op's
+A is the C of an earlier op, pre-filled with NaN before each run: an op that
+read its A before its dependency completed would produce NaN or a value off
+the oracle's, which takes the GPU's own earlier output as its input.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+from gpu_util import assert_within_matmul_tol, device, to_dev, to_host64, torch
+
+import quantized_weight_q4_gb300 as q4
+
+pytestmark = pytest.mark.gpu
+
+
+def act(K, seed, dt):
+    return si.activations_bf16(1, K, seed) if dt == "bf16" else si.activations_f32(1, K, seed)
+
+
+def run_plan(seq):
+    seq.run()
+    torch.cuda.synchronize()
+    assert q4.q4_get_device_status() == q4.Q4_OK
+
+
+# (K, N, a_dtype, c_dtype): K tails of the 64-row stage and the 512-row unit
+# (K = 1, 3, 63, 65, 513), N tails of the 512-column tile and of the block
+SHAPES = [(300, 256, "f32", "f32"), (1, 512, "f32", "f32"), (3, 1000, "bf16", "f32"),
+          (63, 250, "f32", "bf16"), (65, 2040, "bf16", "bf16"), (513, 4096, "f32", "f32"),
+          (1025, 1000, "bf16", "f32"), (4096, 760, "f32", "f32"), (2048, 12288, "bf16", "f32")]
+
+
+@pytest.mark.parametrize("slice_rows", [0, 64, 192])
+def test_seq_ragged_shapes(slice_rows):
+    ops, host = [], []
+    for i, (K, N, adt, cdt) in enumerate(SHAPES):
+        A = act(K, 100 + i, adt)
+        B = si.q4_weights(K, N, seed=200 + i)
+        C = torch.full((N,), float("nan"), device=device(),
+                       dtype=torch.float32 if cdt == "f32" else torch.bfloat16)
+        ops.append((C, to_dev(A)[0], to_dev(B), N, K))
+        host.append((A, B, K, N, cdt))
+    seq = q4.GemvSequence(ops, slice_rows=slice_rows)
+    run_plan(seq)
+    for (C, *_), (A, B, K, N, cdt) in zip(ops, host):
+        C64, S = oracle.matmul(A, B, 1, N, K)
+        got = to_host64(C).reshape(1, N)
+        if cdt == "f32":
+            assert_within_matmul_tol(got, C64, S, f"K={K} N={N}")
+        else:
+            assert (np.abs(got - C64) <= 1e-3 * S + 1e-6 + 2.0 ** -8 * np.abs(C64)).all()
+
+
+def chain(n, K0, N, seed, multi=False):
+    """op 0: A0 . W0 (K0 x N); op i > 0: C_{i-1} . W_i (N x N), deps [i-1]
+    (with `multi`, op i also waits on every earlier op, up to 4)."""
+    A0 = si.activations_f32(1, K0, seed)
+    Ws = [si.q4_weights(K0 if i == 0 else N, N, seed, 10 + i) for i in range(n)]
+    Cs = [torch.full((N,), float("nan"), dtype=torch.float32, device=device()) for _ in range(n)]
+    dA0 = to_dev(A0)[0]
+    ops = []
+    for i in range(n):
+        deps = [] if i == 0 else ([i - 1] + list(range(max(0, i - 4), i - 1)))[:4] if multi else [i - 1]
+        ops.append((Cs[i], dA0 if i == 0 else Cs[i - 1], to_dev(Ws[i]), N, K0 if i == 0 else N, deps))
+    return A0, Ws, Cs, ops
+
+
+@pytest.mark.parametrize("multi", [False, True])
+def test_seq_dependency_chain(multi):
+    n, K0, N = 8, 2048, 1024
+    A0, Ws, Cs, ops = chain(n, K0, N, seed=5, multi=multi)
+    seq = q4.GemvSequence(ops)
+    results = []
+    for _ in range(2):
+        for C in Cs:
+            C.fill_(float("nan"))
+        run_plan(seq)
+        results.append([C.cpu().numpy() for C in Cs])
+        prev = A0
+        for i in range(n):
+            K = K0 if i == 0 else N
+            C64, S = oracle.matmul(prev, Ws[i], 1, N, K)
+            got = results[-1][i].astype(np.float64).reshape(1, N)
+            assert_within_matmul_tol(got, C64, S, f"chain op {i}")
+            # the GPU's own output is the next op's input
+            prev = results[-1][i].reshape(1, N).astype(np.float32)
+    for a, b in zip(*results):
+        assert np.array_equal(a, b)   # deterministic
+
+
+def test_seq_graph_capture_equals_eager():
+    n, K0, N = 5, 4096, 2048
+    A0, Ws, Cs, ops = chain(n, K0, N, seed=9)
+    seq = q4.GemvSequence(ops)
+    run_plan(seq)
+    eager = [C.clone() for C in Cs]
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        seq.run(stream=s)
+    for _ in range(3):
+        for C in Cs:
+            C.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert q4.q4_get_device_status() == q4.Q4_OK
+        for a, b in zip(eager, Cs):
+            assert torch.equal(a, b)
+
+
+@pytest.fixture(scope="module")
+def sweep():
+    """The 7B-like decode sweep: 32 layers x {4 x (4096, 4096), 2 x (4096, 11008),
+    1 x (11008, 4096)}, fp32 A, one fresh A per matrix (3.64 GB of weights)."""
+    shapes = si.sweep_shapes()
+    ops, host = [], []
+    for i, (K, N) in enumerate(shapes):
+        B = si.q4_weights(K, N, seed=0, stream=100 + i)
+        A = si.activations_f32(1, K, 0, 10000 + i)
+        C = torch.empty((N,), dtype=torch.float32, device=device())
+        ops.append((C, to_dev(A)[0], to_dev(B), N, K))
+        host.append((A, B, K, N))
+    return ops, host
+
+
+def test_seq_decode_sweep_sampled(sweep):
+    """All 224 GEMVs of the sweep in one launch; seven of them (each shape,
+    first and last layer) against the oracle on 24 seeded block columns, and
+    two runs bit-identical."""
+    ops, host = sweep
+    seq = q4.GemvSequence(ops)
+    run_plan(seq)
+    first = [op[0].clone() for op in ops]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    seq.run()
+    e1.record()
+    run_plan(seq)
+    assert all(torch.equal(a, op[0]) for a, op in zip(first, ops))
+    # a coarse guard against a stall (a wait running to a limit): 3.64 GB of
+    # weights take well under 20 ms
+    assert e0.elapsed_time(e1) < 20.0
+    for i in (0, 3, 4, 6, 100, 219, 223):
+        A, B, K, N = host[i]
+        nb = si.nblocks(N)
+        cols = np.sort(si.rng(i, 3).choice(nb, size=24, replace=False))
+        Bs = B.reshape(K, nb, 18)[:, cols].reshape(K, -1)
+        C64, S = oracle.matmul(A, Bs, 1, 32 * len(cols), K)
+        got = to_host64(ops[i][0]).reshape(nb, 32)[cols].reshape(1, -1)
+        assert_within_matmul_tol(got, C64, S, f"sweep op {i} (K={K} N={N})")
+
+
+def test_seq_layer_dependencies_sweep(sweep):
+    """The same sweep with a decoder layer's ordering: q, k, v after the
+    previous layer's down; o after q, k, v; gate and up after o; down after
+    gate and up.  The results do not depend on the ordering (fresh inputs):
+    with the same units (256 rows) bit-identical to the run without
+    dependencies; with the library's choice of units, sampled ops against the
+    oracle."""
+    ops, host = sweep
+    plain = q4.GemvSequence(ops, slice_rows=256)
+    run_plan(plain)
+    want = [op[0].clone() for op in ops]
+    dep_ops = []
+    for i, op in enumerate(ops):
+        j = i % 7
+        base = i - j
+        if j < 3:
+            deps = [base - 1] if base > 0 else []
+        elif j == 3:
+            deps = [base, base + 1, base + 2]
+        elif j < 6:
+            deps = [base + 3]
+        else:
+            deps = [base + 4, base + 5]
+        dep_ops.append(tuple(op[:5]) + (deps,))
+    seq = q4.GemvSequence(dep_ops, slice_rows=256)
+    for op in ops:
+        op[0].fill_(float("nan"))
+    run_plan(seq)
+    assert all(torch.equal(a, op[0]) for a, op in zip(want, ops))
+    auto = q4.GemvSequence(dep_ops)
+    for op in ops:
+        op[0].fill_(float("nan"))
+    run_plan(auto)
+    for i in (2, 3, 5, 6, 118, 223):
+        A, B, K, N = host[i]
+        nb = si.nblocks(N)
+        cols = np.sort(si.rng(i, 4).choice(nb, size=16, replace=False))
+        Bs = B.reshape(K, nb, 18)[:, cols].reshape(K, -1)
+        C64, S = oracle.matmul(A, Bs, 1, 32 * len(cols), K)
+        got = to_host64(ops[i][0]).reshape(nb, 32)[cols].reshape(1, -1)
+        assert_within_matmul_tol(got, C64, S, f"layer-ordered op {i} (K={K} N={N})")
+
+
+def test_seq_bf16_output_is_rounded_fp32():
+    K, N = 3000, 4096
+    A = si.activations_f32(1, K, 3)
+    B = to_dev(si.q4_weights(K, N, seed=3))
+    dA = to_dev(A)[0]
+    c32 = torch.empty((N,), dtype=torch.float32, device=device())
+    c16 = torch.empty((N,), dtype=torch.bfloat16, device=device())
+    run_plan(q4.GemvSequence([(c32, dA, B, N, K)]))
+    run_plan(q4.GemvSequence([(c16, dA, B, N, K)]))
+    assert torch.equal(c32.to(torch.bfloat16).view(torch.int16), c16.view(torch.int16))
+
+
+def test_seq_invalid_plans():
+    K, N = 64, 256
+    B = to_dev(si.q4_weights(K, N, seed=1))
+    A = torch.zeros((K,), dtype=torch.float32, device=device())
+    C = torch.zeros((N,), dtype=torch.float32, device=device())
+    with pytest.raises(q4.Q4Error):   # a dependency on a later op
+        q4.GemvSequence([(C, A, B, N, K, [1]), (C, A, B, N, K)])
+    Bo = to_dev(si.q4_weights(K, 100, seed=1))   # ceil(100/32) = 4 blocks per row
+    with pytest.raises(q4.Q4Error):
+        q4.GemvSequence([(C, A, Bo, 100, K)])
