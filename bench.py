@@ -622,13 +622,19 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
         copies = max(1, -(-4 * l2 // wbytes))   # >= 4x L2 of distinct weights per pass
         bf16 = args.workload == "batched"
         fns, keep = [], []
+        # one zeroed workspace for the calls' K-slice partials (the calls run
+        # one after another on one stream), so that the captured calls take
+        # the same kernels as eager ones
+        wsb = q4.q4_matmul_workspace_size(M, N, K) if bf16 else 0
+        wspace = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev) if wsb else None
         for i in range(copies):
             B, layout = device_weights(torch, q4, dev, K, N, args.format, 0, 500 + i)
             A = si.activations_bf16(M, K, 0, 600 + i) if bf16 else si.activations_f32(M, K, 0, 600 + i)
             A = to_dev(A.view(np.int16)).view(torch.bfloat16) if bf16 else to_dev(A)
             C = torch.empty((M, N), dtype=torch.float32, device=dev)
             keep += [A, B, C]
-            fns.append(lambda C=C, A=A, B=B: q4.q4_matmul_ex(C, A, B, M, N, K, b_layout=layout))
+            fns.append(lambda C=C, A=A, B=B: q4.q4_matmul_ex(C, A, B, M, N, K, workspace=wspace,
+                                                             b_layout=layout))
         g = GraphOf(torch, fns)
         barrier(ws)
         with ClockSampler(local) as clk:

@@ -108,19 +108,23 @@ Q4_API int q4_matmul(float *C, const float *A, const void *B, int64_t M, int64_t
  *              that includes replays of graphs captured with it.
  *   stream     cudaStream_t (NULL = legacy default stream)
  * Kernel choice:
- *   - fp32 A, M < 8, K < 1024, Q8_0 or planar weights, or a shape the GEMM
- *     below does not take: the split-K GEMV on the CUDA cores, in chunks of
+ *   - fp32 A, M < 4, K < 1024, Q8_0 or planar weights, or a shape the GEMMs
+ *     below do not take: the split-K GEMV on the CUDA cores, in chunks of
  *     up to 4 rows of A.  The splits of each column tile run as one
  *     thread-block cluster and are added on chip in fixed order.  Exact fp32
  *     dequantisation: |C - A.W| <= 1e-3 * sum|a*w| + 1e-6 for any input.
- *   - bf16 A with M >= 8, K >= 1024, ceil(N/32) % 8 == 0 and K % 8 == 0 (and,
- *     for M <= 128, a shape its split-K form takes): the tensor-core GEMM
- *     (prompt batching, engine page §5.2), as q4_matmul_bf16_tiles below.
- *     Its result A . bf16_rn(W) deviates from A . W by at most 2^-9 *
+ *   - bf16 A with 4 <= M, K >= 1024, ceil(N/32) % 8 == 0 and K % 8 == 0:
+ *     the tensor-core GEMM (prompt batching, engine page §5.2), as
+ *     q4_matmul_bf16_tiles below: up to 32 rows the few-row form (the
+ *     weights as the MMA's 128-row operand, the tokens as its N), which needs
+ *     the workspace described above when captured into a graph (without one
+ *     a captured call takes the split-K GEMV below 8 rows, the cluster form
+ *     from 8), above 32 rows the split-K and persistent forms.
+ *     Its result A . bf16_rn(W) deviates from A . W by at most 2^-8 *
  *     sum|a*w| plus the fp32 accumulation error; the rounding errors of the
  *     weights have random signs, and from K = 1024 on their sum stays within
  *     1e-3 * sum|a*w| + 1e-6 on random data.  An input built so that every
- *     weight's rounding has the sign of its activation can reach 2^-9 *
+ *     weight's rounding has the sign of its activation can reach 2^-8 *
  *     sum|a*w|: callers that need the stated bound for any input pass fp32
  *     activations.
  *   Both are deterministic (no floating-point atomics, fixed orders).
@@ -147,11 +151,16 @@ Q4_API size_t q4_matmul_workspace_size(int64_t M, int64_t N, int64_t K);
  * bf16_rn((q - 8) * d) (q4_dequant_bf16 gives the same values) and the bf16 x
  * bf16 products are accumulated in fp32 in tensor memory.  A is bf16 [M, K];
  * C fp32 or bf16 (RN of the fp32 result) [M, N]; B in Q4_LAYOUT_BLOCKS.
- * Shapes: M >= 8, ceil(N/32) % 8 == 0, K % 8 == 0 (16-byte row pitches),
- * else Q4_ERR_SHAPE.  M > 128 runs the persistent prefill form (256 x 256
- * output tiles); M <= 128 splits K over 2..16 CTAs per 128 x 256 tile,
- * combined in fixed order over a cluster or, up to 40 rows, through the
- * workspace described under q4_matmul_ex.  Deterministic.
+ * Shapes: ceil(N/32) % 8 == 0, K % 8 == 0 (16-byte row pitches), else
+ * Q4_ERR_SHAPE.  M <= 32 runs the few-row form: CTAs of 256 output columns
+ * and a K slice, the dequantised weights as the MMA's A operand (M = 128)
+ * and the tokens as N = 16, 32 or 64, the slices added through the
+ * workspace described under q4_matmul_ex; a call captured without that
+ * workspace returns Q4_ERR_SHAPE below 8 rows and takes the split form from
+ * 8.  32 < M <= 128 splits K over 2..16 CTAs per 128 x 256 tile, combined in
+ * fixed order over a cluster or, up to 40 rows, through the workspace;
+ * M > 128 runs the persistent prefill form (256 x 256 output tiles).
+ * Deterministic.
  */
 Q4_API int q4_matmul_bf16_tiles(void *C, int c_dtype, const void *A, const void *B,
                                 int64_t M, int64_t N, int64_t K, void *workspace,

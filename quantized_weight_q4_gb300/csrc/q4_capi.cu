@@ -473,7 +473,7 @@ bool gemm_shape_ok(int64_t M, int64_t N, int64_t K) {
 }
 
 // Shapes whose q4_matmul_ex runs the tensor-core GEMM.  Below kMinTensorK the
-// bf16 tile rounding (up to 2^-9 relative per weight) is not averaged out over
+// bf16 tile rounding (up to 2^-8 relative per weight) is not averaged out over
 // enough products to keep |err| <= 1e-3 * sum|a*w| on random data, so short
 // reductions take the exact-dequant GEMV.
 constexpr int64_t kMinTensorK = 1024;
@@ -481,10 +481,44 @@ bool takes_gemm(int fmt, int a_dtype, int64_t M, int64_t N, int64_t K) {
   return fmt == q4::kFmtQ4 && a_dtype == Q4_BF16 && K >= kMinTensorK && gemm_shape_ok(M, N, K);
 }
 
-// Caller workspace of the small-M GEMM's global-memory form: the tile
-// tickets (zero before first use, left zero by every completed call), then
-// the partial tiles.
+// Caller workspace of the tensor-core forms that add K slices through global
+// memory: the tile tickets (zero before first use, left zero by every
+// completed call), then the partial tiles.
 size_t gemm_ticket_bytes(int64_t N) { return round_up(static_cast<size_t>(ceil_div(N, 256)) * 4, 256); }
+
+// The few-row form (weights as the MMA's A operand) takes bf16 A with up to
+// 32 rows.  Measured on 5120 x 12288 (GB/s of weights): 1425 / 1360 / 1253 /
+// 1107 at M = 4 / 8 / 16 / 32 against 1396 (split-K GEMV) / 1085 / 1094 /
+// 1152 (the GEMM's split forms); at M = 2 the GEMV (2110) and at M = 64 the
+// cluster form (989 against 830) are faster.
+constexpr int64_t kMaxSkinnyRows = 32;
+constexpr int64_t kMinSkinnyRows = 4;
+bool takes_skinny(int64_t M, int64_t N, int64_t K) {
+  return M <= kMaxSkinnyRows && q4::skinny_supported(M, N, K);
+}
+
+// The few-row form for a validated problem (the caller holds g_mu).  Its K
+// slices meet in the caller's workspace, else in the stream's library scratch
+// (eager calls only); a call captured without a workspace returns
+// Q4_ERR_SHAPE so that the caller takes another form.
+int skinny_run(DeviceState* s, void* C, int c_dtype, const void* A, const void* B, int64_t M,
+               int64_t N, int64_t K, void* workspace, size_t workspace_bytes, cudaStream_t st) {
+  const int S = q4::skinny_split(N, K, s->sms);
+  float* part = nullptr;
+  unsigned* tickets = nullptr;
+  if (S > 1) {
+    const size_t tb = gemm_ticket_bytes(N);
+    const size_t pb = q4::skinny_part_bytes(M, N, S);
+    if (workspace && workspace_bytes >= tb + pb) {
+      tickets = static_cast<unsigned*>(workspace);
+      part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + tb);
+    } else if (!gemm_scratch(s, st, pb, &part, &tickets)) {
+      return Q4_ERR_SHAPE;
+    }
+  }
+  return launch_status(
+      q4::launch_skinny(C, c_dtype, A, B, M, N, K, s->status, S, part, tickets, st));
+}
 
 // The tensor-core GEMM for a validated problem (the caller holds g_mu).
 int gemm_run(DeviceState* s, void* C, int c_dtype, const void* A, const void* B, int64_t M,
@@ -515,6 +549,10 @@ size_t q4_matmul_workspace_size(int64_t M, int64_t N, int64_t K) {
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* s = nullptr;
   if (current_state(&s) != Q4_OK) return 0;
+  if (takes_skinny(M, N, K)) {
+    const int S = q4::skinny_split(N, K, s->sms);
+    return S > 1 ? gemm_ticket_bytes(N) + q4::skinny_part_bytes(M, N, S) : 0;
+  }
   if (!gemm_shape_ok(M, N, K)) return 0;
   const int sg = q4::gemm_global_split(M, N, K, s->sms);
   if (sg <= 0) return 0;
@@ -542,6 +580,11 @@ int q4_matmul_ex(void* C, int c_dtype, const void* A, int a_dtype, const void* B
   int rc = current_state(&s);
   if (rc != Q4_OK) return rc;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (fmt == q4::kFmtQ4 && a_dtype == Q4_BF16 && M >= kMinSkinnyRows && K >= kMinTensorK &&
+      takes_skinny(M, N, K)) {
+    rc = skinny_run(s, C, c_dtype, A, B, M, N, K, workspace, workspace_bytes, st);
+    if (rc != Q4_ERR_SHAPE) return rc;   // else: captured without a workspace
+  }
   if (takes_gemm(fmt, a_dtype, M, N, K))
     return gemm_run(s, C, c_dtype, A, B, M, N, K, workspace, workspace_bytes, st);
   return gemv_run(s, C, c_dtype, A, a_dtype, B, fmt, M, N, K, st);
@@ -554,13 +597,17 @@ int q4_matmul_bf16_tiles(void* C, int c_dtype, const void* A, const void* B, int
   if (c_dtype != Q4_F32 && c_dtype != Q4_BF16) return Q4_ERR_DTYPE;
   if (!aligned16(C) || !aligned16(A) || !aligned16(B) || (workspace && !aligned16(workspace)))
     return Q4_ERR_ALIGN;
-  if (!gemm_shape_ok(M, N, K)) return Q4_ERR_SHAPE;
+  if (!takes_skinny(M, N, K) && !gemm_shape_ok(M, N, K)) return Q4_ERR_SHAPE;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* s = nullptr;
   int rc = current_state(&s);
   if (rc != Q4_OK) return rc;
-  return gemm_run(s, C, c_dtype, A, B, M, N, K, workspace, workspace_bytes,
-                  static_cast<cudaStream_t>(stream));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (takes_skinny(M, N, K)) {
+    rc = skinny_run(s, C, c_dtype, A, B, M, N, K, workspace, workspace_bytes, st);
+    if (rc != Q4_ERR_SHAPE || !gemm_shape_ok(M, N, K)) return rc;
+  }
+  return gemm_run(s, C, c_dtype, A, B, M, N, K, workspace, workspace_bytes, st);
 }
 
 int q4_matmul(float* C, const float* A, const void* B, int64_t M, int64_t N, int64_t K) {

@@ -167,6 +167,28 @@ int gemm_global_split(int64_t M, int64_t N, int64_t K, int sms);
 // Bytes of partial tiles the global-memory form needs for that split.
 size_t gemm_part_bytes(int64_t M, int64_t N, int S);
 
+// q4_gemm_skinny.cu: the few-row GEMM (1 <= M <= 32, bf16 A) with the weights
+// as the MMA's A operand and the tokens as its N.
+struct SkinnyParams {
+  CUtensorMap tmap_a;   // activations: bf16 [M][K], boxes of 64 K x NT rows, 128-byte swizzle
+  CUtensorMap tmap_w;   // weights: uint16 [K][nb*9], boxes of 72 halfwords x 128 rows
+  void* C;              // [M][N] fp32 (c_dtype 0) or bf16 (1)
+  int c_dtype;
+  int M, N, K;
+  int nsplit;           // K slices per 256-column tile (CTAs per tile)
+  float* part;          // nsplit > 1: [tiles][nsplit][M][256] partial sums
+  unsigned* tickets;    // nsplit > 1: [tiles] counters, zero at launch, left zero
+  unsigned* err;        // device status word
+};
+constexpr int kMaxSkinnyTickets = 4096;
+bool skinny_supported(int64_t M, int64_t N, int64_t K);
+// K slices per column tile: one CTA per SM over all tiles and slices.
+int skinny_split(int64_t N, int64_t K, int sms);
+size_t skinny_part_bytes(int64_t M, int64_t N, int S);
+cudaError_t launch_skinny(void* C, int c_dtype, const void* A, const void* B, int64_t M, int64_t N,
+                          int64_t K, unsigned* err, int S, float* part, unsigned* tickets,
+                          cudaStream_t st);
+
 // q4_misc.cu
 cudaError_t launch_dequant(void* W, int w_dtype, const uint8_t* B, int64_t K, int64_t N,
                            cudaStream_t st);

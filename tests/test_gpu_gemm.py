@@ -8,9 +8,9 @@ A . bf16_rn(W) in fp64 (oracle.matmul_bf16_tiles), and parity is checked
 against it element by element within 1e-4 * sum|a*bf16(w)| + 1e-6, ten times
 tighter than the matmul tolerance (only the fp32 accumulation differs).
 
-Against the exact product A.W each weight carries up to 2^-9 relative
+Against the exact product A.W each weight carries up to 2^-8 relative
 rounding, so the bound that holds at every K is
-|gpu - A.W| <= 2^-9 * S + 1e-4 * S + 1e-6 (S = sum|a*w|); at the prefill
+|gpu - A.W| <= 2^-8 * S + 1e-4 * S + 1e-6 (S = sum|a*w|); at the prefill
 size (K = 5120) the matmul tolerance 1e-3 * S + 1e-6 holds as well, because
 the rounding errors have random signs and average out over K terms.
 Exact cases: one-hot rows reproduce the bf16 tile values bit for bit; the
@@ -43,10 +43,10 @@ def run(A, B, M, N, K, c_dtype=torch.float32):
 
 
 def assert_exact_bound(got, C64, S, what):
-    """|gpu - A.W| <= 2^-9 * S + 1e-4 * S + 1e-6: bf16 tile rounding plus fp32
+    """|gpu - A.W| <= 2^-8 * S + 1e-4 * S + 1e-6: bf16 tile rounding plus fp32
     accumulation.  Returns max |err| / S."""
     err = np.abs(got - C64)
-    tol = (2.0 ** -9 + 1e-4) * S + 1e-6
+    tol = (2.0 ** -8 + 1e-4) * S + 1e-6
     bad = ~(err <= tol)
     if bad.any():
         i = tuple(np.argwhere(bad)[0])

@@ -122,10 +122,10 @@ def test_batched_decode_5120x12288(M):
 
 
 def test_gemv_needs_no_workspace():
-    """Split-K partial sums are combined on chip: no workspace is needed, and
-    a caller-provided one is ignored."""
+    """The GEMV combines its split-K partial sums on chip: a caller-provided
+    workspace is ignored (q4_matmul_workspace_size reports what the
+    tensor-core forms of the same shape may use)."""
     M, K, N = 1, 4096, 4096
-    assert q4.q4_matmul_workspace_size(M, N, K) == 0
     A = si.activations_f32(M, K, seed=1)
     B = si.q4_weights(K, N, seed=1)
     ws = torch.zeros(256, dtype=torch.uint8, device=device())
