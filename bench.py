@@ -72,7 +72,7 @@ def measured_peaks():
 # from an ncu capture, keyed by the hash of the kernel sources it was taken on.
 # A changed source hash makes the figure stale and the bench reports null.
 TRAFFIC = {
-    # profiles/q4_gemv_kernel_decode_sweep_7b.md: mean over the sweep's 4:2:1 shape mix
+    # mean per launch over the sweep's 4:2:1 shape mix
     "d74610c072511ba9": 16312210,
 }
 
@@ -87,7 +87,7 @@ TRAFFIC_SEQ = {
 
 
 # The same for the prefill GEMM kernel (q4_gemm_tc_kernel), one launch of
-# M = 2048, K = 5120, N = 12288 (profiles/q4_gemm_tc_kernel_prefill_2048x5120x12288.md).
+# M = 2048, K = 5120, N = 12288.
 TRAFFIC_GEMM = {
     "30b9eed67c09283f": 67344640,
 }
