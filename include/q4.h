@@ -339,9 +339,11 @@ Q4_API int q4_matmul_host_stream(const q4_seq_op *ops, int n, void *staging, siz
  *           computed from, their output); ndeps = 0 for none.  Weights are
  *           streamed regardless; only the reads of A wait.
  *   slice_rows  rows of K per unit of work: 0 for the library's choice
- *           (512), else a multiple of 64 up to 512 (else Q4_ERR_ARG).  Every
- *           unit ends in a reduction over its CTA and adds one partial row to
- *           its tile's combine, so shorter units cost more.
+ *           (2048, or 512 for an op that a later op depends on, so that it
+ *           completes soon after its last unit starts), else a multiple of 64
+ *           up to 2048 (else Q4_ERR_ARG).  Every unit ends in a reduction over
+ *           its CTA and adds one partial row to its tile's combine, so
+ *           shorter units cost more.
  * Every C is overwritten.  Results are deterministic (each output is summed
  * in a fixed order) and equal A . W within 1e-3 * sum|a*w| + 1e-6, like
  * q4_matmul_ex (the same exact dequantisation; other summation splits).

@@ -861,12 +861,18 @@ struct SeqLayout {
 // Checks the ops and lays out the plan buffer: op descriptors, the counters
 // cleared before every run (unit queue, done tiles per op, tile tickets),
 // then one 512-float partial row per unit.
-// Rows per unit of op i: the caller's choice, else 512.  Shorter units were
-// measured slower on GB300 with and without dependencies: each unit pays a
-// reduction over the CTA and its tile's combine a load per unit.
+// Rows per unit of op i: the caller's choice; else 512 for an op that a later
+// op waits for, 2048 for the others.  Each unit ends in a reduction over its
+// CTA and a ticket of its tile, which its consumers wait for: long units
+// spread that cost (independent sweep on GB300: 4421 GB/s at 512 rows, 5316
+// at 2048), while an op that others wait for must finish soon after its last
+// unit is handed out (layer-ordered sweep: 1745 GB/s at 512, 817 at 2048).
 int64_t seq_slice_rows(const q4_gemv_op* ops, int n, int i) {
-  (void)n;
-  return ops[i].slice_rows > 0 ? ops[i].slice_rows : q4::seq_max_slice_rows();
+  if (ops[i].slice_rows > 0) return ops[i].slice_rows;
+  for (int j = i + 1; j < n; ++j)
+    for (int k = 0; k < ops[j].ndeps; ++k)
+      if (ops[j].deps[k] == i) return q4::seq_default_slice_rows();
+  return q4::seq_max_slice_rows();
 }
 
 int seq_layout(const q4_gemv_op* ops, int n, SeqLayout* L) {

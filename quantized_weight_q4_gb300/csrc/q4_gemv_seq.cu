@@ -47,7 +47,8 @@ constexpr int kTileCols = kTileBlocks * kBlockCols;      // 512 columns
 constexpr int kRowBytes = kTileBlocks * kBlockBytes;     // 288 bytes of a tile row
 constexpr int kStageRows = 64;
 constexpr int kStageBytes = kStageRows * kRowBytes;      // 18432 bytes
-constexpr int kMaxSliceStages = 8;                       // stages of the longest unit
+constexpr int kDefaultSliceStages = 8;                   // stages of a unit by default
+constexpr int kMaxSliceStages = 32;                      // stages of the longest unit
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 64;                // + producer warp + A warp
@@ -90,6 +91,20 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+// ticket = *p; *p += 1, with release semantics for this thread's earlier
+// writes and those ordered before them (cumulative), and acquire semantics
+// for its later reads, at GPU scope: one round trip, no full fences.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+// *p += 1 with release semantics at GPU scope; nothing is returned, so the
+// thread does not wait for the round trip.
+__device__ __forceinline__ void red_add_release_gpu(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 // Orders this thread's earlier generic-proxy view of global memory before its
 // later async-proxy (bulk copy) reads.
@@ -443,9 +458,8 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const SeqParam
       for (int i = 0; i < kBPT; ++i) __stcg(part + tid + 256 * i, colv[i]);
       if (!consumers_meet(csync, cphase, s_fail, p.err)) break;
       if (tid == 0) {
-        __threadfence();
-        const unsigned t = atomicAdd(&p.tickets[d.ticket_base + tile], 1u);
-        __threadfence();
+        // every consumer's partial store is ordered before this by the meet
+        const unsigned t = atom_add_acq_rel_gpu(&p.tickets[d.ticket_base + tile], 1u);
         *s_last = (t == static_cast<unsigned>(nslices - 1)) ? 1 : 0;
       }
       if (!consumers_meet(csync, cphase, s_fail, p.err)) break;
@@ -487,10 +501,7 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const SeqParam
     }
     // the tile's C is stored: count it for the op (after every thread's stores)
     if (!consumers_meet(csync, cphase, s_fail, p.err)) break;
-    if (tid == 0) {
-      __threadfence();
-      atomicAdd(&p.done[op], 1u);
-    }
+    if (tid == 0) red_add_release_gpu(&p.done[op], 1u);
   }
 }
 
@@ -517,6 +528,7 @@ int seq_ctas_per_sm(int stages) {
 int seq_tile_cols() { return seq::kTileCols; }
 int seq_stage_rows() { return seq::kStageRows; }
 int seq_max_slice_rows() { return seq::kMaxSliceStages * seq::kStageRows; }
+int seq_default_slice_rows() { return seq::kDefaultSliceStages * seq::kStageRows; }
 
 cudaError_t launch_gemv_seq(const SeqParams& p, int grid, int stages, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
