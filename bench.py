@@ -78,13 +78,13 @@ TRAFFIC = {
 
 
 # The same for the persistent decode-sequence kernel (q4_gemv_seq_kernel), per
-# launch of the whole 32-layer sweep: captured on the 4-layer sweep (455 MB of
-# weights, above the L2 size) and scaled by 8, the units of work growing with
-# the layers.
-# (the hash covers the kernel's own sources)
+# launch of the whole 32-layer sweep, keyed by the hash of the kernel's own
+# sources and the plan's buffer size (which counts its units of work: the
+# partial sums they write and read back are the traffic beyond the weights).
 SEQ_SOURCES = ("q4_gemv_seq.cu", "q4_gemv_core.cuh", "q4_device.cuh")
 TRAFFIC_SEQ = {
-    "8d3aa2b1ca856f08": 3707478016,
+    # captured on the 32-layer launch itself (one pass per launch)
+    "a23a3f326b9a0b01/7396864": 3972904960,
 }
 
 
@@ -490,7 +490,7 @@ def run_ours(args, ws, rank, local):
     avg_launch_s = elapsed / (args.steps * w["launches_per_step"])
     achieved = per_launch_bytes / avg_launch_s / 1e9
     if use_seq:
-        h = kernel_source_hash(SEQ_SOURCES)
+        h = f"{kernel_source_hash(SEQ_SOURCES)}/{seq.plan.buf.numel()}"
         traffic = TRAFFIC_SEQ.get(h)
     else:
         h = kernel_source_hash()
@@ -517,7 +517,8 @@ def run_ours(args, ws, rank, local):
             "M": 1, "a_dtype": "f32", "c_dtype": "f32",
             "weight_bytes_per_step": wbytes,
             "launch": (f"one persistent launch per step (q4_gemv_seq_run: counter clear + "
-                       f"{seq.plan.grid} resident CTAs taking 512x512 units in op order), "
+                       f"{seq.plan.grid} resident CTAs taking units of 512 columns x 512..4096 "
+                       f"rows in op order), "
                        f"captured in a CUDA graph" if use_seq else
                        "one CUDA graph of 224 GEMV launches with programmatic dependent launch"),
             "deps": (args.deps + ": " + DEPS_TEXT[args.deps]) if use_seq else "serial launches",

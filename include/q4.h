@@ -338,12 +338,17 @@ Q4_API int q4_matmul_host_stream(const q4_seq_op *ops, int n, void *staging, siz
  *           be complete before this op reads A (e.g. when A is, or is
  *           computed from, their output); ndeps = 0 for none.  Weights are
  *           streamed regardless; only the reads of A wait.
- *   slice_rows  rows of K per unit of work: 0 for the library's choice
- *           (2048, or 512 for an op that a later op depends on, so that it
- *           completes soon after its last unit starts), else a multiple of 64
- *           up to 2048 (else Q4_ERR_ARG).  Every unit ends in a reduction over
- *           its CTA and adds one partial row to its tile's combine, so
- *           shorter units cost more.
+ *   slice_rows  rows of K per unit of work: 0 for the library's choice,
+ *           else a multiple of 64 up to 4096 (else Q4_ERR_ARG).  Every unit
+ *           ends in a reduction over its CTA and adds one partial row to its
+ *           tile's combine, so shorter units cost more, while long units near
+ *           the end of the sequence leave CTAs idle.  The library's choice:
+ *           512 for an op that a later op depends on (so that it completes
+ *           soon after its last unit starts); otherwise the longest of 4096,
+ *           2048, 1024 and 512 rows such that the weights from this op to the
+ *           end of the sequence hold at least half a unit for each of 304
+ *           CTAs (152 SMs x 2), i.e. 4096 rows while 179.3 MB or more remain,
+ *           2048 from 89.7 MB, 1024 from 44.8 MB, 512 below.
  * Every C is overwritten.  Results are deterministic (each output is summed
  * in a fixed order) and equal A . W within 1e-3 * sum|a*w| + 1e-6, like
  * q4_matmul_ex (the same exact dequantisation; other summation splits).

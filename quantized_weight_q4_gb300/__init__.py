@@ -246,7 +246,9 @@ class GemvSequence:
     (q4_gemv_seq_*).  ops: list of (C, A, B, N, K) or (C, A, B, N, K, deps),
     CUDA tensors, deps a list of indices of earlier ops whose C must be
     complete before this op reads A.  slice_rows: rows per unit of work for
-    every op (0: the library's choice).  The tensors are referenced by the
+    every op, a multiple of 64 up to 4096 (0: the library's choice, which
+    shortens the units of ops that others wait for and of the sequence's
+    last weights).  The tensors are referenced by the
     plan and kept alive with it."""
 
     def __init__(self, ops, slice_rows: int = 0):

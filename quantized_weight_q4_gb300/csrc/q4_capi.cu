@@ -861,18 +861,43 @@ struct SeqLayout {
 // Checks the ops and lays out the plan buffer: op descriptors, the counters
 // cleared before every run (unit queue, done tiles per op, tile tickets),
 // then one 512-float partial row per unit.
-// Rows per unit of op i: the caller's choice; else 512 for an op that a later
-// op waits for, 2048 for the others.  Each unit ends in a reduction over its
-// CTA and a ticket of its tile, which its consumers wait for: long units
-// spread that cost (independent sweep on GB300: 4421 GB/s at 512 rows, 5316
-// at 2048), while an op that others wait for must finish soon after its last
-// unit is handed out (layer-ordered sweep: 1745 GB/s at 512, 817 at 2048).
-int64_t seq_slice_rows(const q4_gemv_op* ops, int n, int i) {
-  if (ops[i].slice_rows > 0) return ops[i].slice_rows;
-  for (int j = i + 1; j < n; ++j)
-    for (int k = 0; k < ops[j].ndeps; ++k)
-      if (ops[j].deps[k] == i) return q4::seq_default_slice_rows();
-  return q4::seq_max_slice_rows();
+// Rows per unit of each op: the caller's choice; else 512 for an op that a
+// later op waits for (it must finish soon after its last unit is handed out);
+// else the longest of 4096, 2048, 1024 and 512 rows whose units, kSeqTailRounds
+// per CTA of a full grid (kSeqNominalCtas), still fit in the weights from this
+// op to the end of the sequence, so that units shorten as the sweep nears its
+// end and the CTAs finish together.  Each unit ends in a reduction over its
+// CTA and, with more than one slice per tile, a ticket of its tile, which its
+// consumers wait for: long units spread that cost (independent sweep on
+// GB300: 4421 GB/s at 512 rows, 5413 at 2048, 5552 at 4096, 5698 at 4096 with
+// the last 192 MB in 512-row units), while ops that others wait for run best
+// with short ones (layer-ordered sweep: 1745 GB/s at 512 rows, 817 at 2048).
+constexpr double kSeqTailRounds = 0.5;
+constexpr int64_t kSeqNominalCtas = 304;   // 152 SMs x 2 CTAs
+
+int64_t op_weight_bytes(const q4_gemv_op& o) { return o.K * ceil_div(o.N, 32) * 18; }
+
+// rows[i] = rows per unit of op i (ops already checked).
+void seq_plan_rows(const q4_gemv_op* ops, int n, std::vector<int64_t>* rows) {
+  rows->assign(static_cast<size_t>(n), 0);
+  std::vector<char> waited(static_cast<size_t>(n), 0);
+  for (int j = 0; j < n; ++j)
+    for (int k = 0; k < ops[j].ndeps; ++k) waited[ops[j].deps[k]] = 1;
+  int64_t remaining = 0;
+  for (int i = n - 1; i >= 0; --i) {
+    remaining += op_weight_bytes(ops[i]);
+    int64_t r = ops[i].slice_rows;
+    if (r == 0 && waited[i]) r = q4::seq_default_slice_rows();
+    if (r == 0) {
+      r = q4::seq_max_slice_rows();
+      const int64_t unit_bytes_per_row = q4::seq_tile_cols() / 32 * 18;
+      while (r > q4::seq_default_slice_rows() &&
+             static_cast<double>(remaining) <
+                 kSeqTailRounds * kSeqNominalCtas * unit_bytes_per_row * r)
+        r /= 2;
+    }
+    (*rows)[i] = r;
+  }
 }
 
 int seq_layout(const q4_gemv_op* ops, int n, SeqLayout* L) {
@@ -895,9 +920,11 @@ int seq_layout(const q4_gemv_op* ops, int n, SeqLayout* L) {
         o.slice_rows % q4::seq_stage_rows() != 0)
       return Q4_ERR_ARG;
   }
+  std::vector<int64_t> rows;
+  seq_plan_rows(ops, n, &rows);
   for (int i = 0; i < n; ++i) {
     const q4_gemv_op& o = ops[i];
-    const int64_t nt = ceil_div(o.N, tc), ns = ceil_div(o.K, seq_slice_rows(ops, n, i));
+    const int64_t nt = ceil_div(o.N, tc), ns = ceil_div(o.K, rows[i]);
     units += nt * ns;
     tiles += nt;
   }
@@ -946,6 +973,8 @@ int q4_gemv_seq_create(const q4_gemv_op* ops, int n, void* buf, size_t buf_bytes
   std::vector<q4::SeqOpDesc> d(static_cast<size_t>(n));
   std::memset(d.data(), 0, sizeof(q4::SeqOpDesc) * n);
   const int64_t tc = q4::seq_tile_cols();
+  std::vector<int64_t> rows;
+  seq_plan_rows(ops, n, &rows);
   int unit_base = 0, ticket_base = 0;
   for (int i = 0; i < n; ++i) {
     const q4_gemv_op& o = ops[i];
@@ -959,7 +988,7 @@ int q4_gemv_seq_create(const q4_gemv_op* ops, int n, void* buf, size_t buf_bytes
     e.N = static_cast<int>(o.N);
     e.nb = static_cast<int>(nb);
     e.ntiles = static_cast<int>(ceil_div(o.N, tc));
-    const int64_t sr = seq_slice_rows(ops, n, i);
+    const int64_t sr = rows[i];
     e.slice_rows = static_cast<int>(sr);
     e.nslices = static_cast<int>(ceil_div(o.K, sr));
     e.unit_base = unit_base;

@@ -9,7 +9,7 @@
 // reduction and drain leave the HBM idle for microseconds each time, one
 // resident grid (two CTAs per SM) streams all of the sequence's weights.
 //  * The work is cut into units of (op, column tile of 16 blocks = 512
-//    columns, K slice of 64 to 512 rows, chosen per op).  Units are numbered op by op, and within
+//    columns, K slice of 64 to 4096 rows, chosen per op).  Units are numbered op by op, and within
 //    an op tile by tile; a global counter hands them out in that order.
 //  * In each CTA a producer warp issues one TMA tensor copy per 64-row stage
 //    (18 KB) into a ring, and a second warp copies the stage's 64 entries of A
@@ -48,7 +48,7 @@ constexpr int kRowBytes = kTileBlocks * kBlockBytes;     // 288 bytes of a tile 
 constexpr int kStageRows = 64;
 constexpr int kStageBytes = kStageRows * kRowBytes;      // 18432 bytes
 constexpr int kDefaultSliceStages = 8;                   // stages of a unit by default
-constexpr int kMaxSliceStages = 32;                      // stages of the longest unit
+constexpr int kMaxSliceStages = 64;                      // stages of the longest unit
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 64;                // + producer warp + A warp

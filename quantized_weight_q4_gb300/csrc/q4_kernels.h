@@ -99,7 +99,7 @@ struct SeqOpDesc {      // 64-byte aligned through its tensor map
   void* C;              // [N], fp32 (c_dtype 0) or bf16 (1)
   int K, N, nb;
   int ntiles, nslices;  // column tiles of 512 columns, K slices of slice_rows rows
-  int slice_rows;       // a multiple of 64, at most 2048
+  int slice_rows;       // a multiple of 64, at most 4096
   int unit_base;        // first unit of the op (units: tile-major, slice-minor)
   int ticket_base;      // first tile counter of the op
   int a_dtype, c_dtype;
@@ -121,7 +121,7 @@ struct SeqParams {
 int seq_ctas_per_sm(int stages);
 int seq_tile_cols();       // columns of a unit (512)
 int seq_stage_rows();      // rows of one pipeline stage (64)
-int seq_max_slice_rows();      // rows of the longest unit (2048)
+int seq_max_slice_rows();      // rows of the longest unit (4096)
 int seq_default_slice_rows();  // rows of a unit by default (512)
 cudaError_t launch_gemv_seq(const SeqParams& p, int grid, int stages, cudaStream_t st);
 

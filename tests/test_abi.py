@@ -118,8 +118,8 @@ def test_host_stream_checks_on_host(L):
 
 def test_gemv_seq_checks_on_host(L):
     """The decode sequence checks every op, and the plan buffer, before any
-    CUDA call; its buffer holds 2 KB of partial sums per unit of 512 columns
-    x 512 rows."""
+    CUDA call; its buffer holds 2 KB of partial sums per unit (512 columns
+    of 64 to 4096 rows), which shows how many units the plan has."""
     vp = ctypes.c_void_p
     good = 0x10000
 
@@ -132,11 +132,18 @@ def test_gemv_seq_checks_on_host(L):
     nbytes = L.q4_gemv_seq_bytes(ops, 3)
     assert units * 2048 < nbytes < units * 2048 + 65536
     # the library's choice: 512 rows for ops 0 and 1, which op 2 waits for,
-    # 2048 for op 2 (6 slices of its 11008 rows)
+    # and for op 2, the whole sequence being under one half-round of 1024-row
+    # units (0.5 x 304 CTAs x 1024 rows x 288 bytes = 44.8 MB)
     auto = (q4.GemvOp * 3)(op(4096, 4096, rows=0), op(11008, 4096, [0], rows=0),
                            op(4096, 11008, [0, 1], rows=0))
-    units_auto = 8 * 8 + 22 * 8 + 8 * 6
+    units_auto = 8 * 8 + 22 * 8 + 8 * 22
     assert units_auto * 2048 < L.q4_gemv_seq_bytes(auto, 3) < units_auto * 2048 + 65536
+    # ten independent (K = 11008, N = 4096) ops of 25,362,432 weight bytes:
+    # counted from the end, units of 512 rows while under 44.8 MB remain
+    # (1 op), 1024 under 89.7 MB (2), 2048 under 179.3 MB (4), then 4096 (3)
+    graded = (q4.GemvOp * 10)(*[op(4096, 11008, rows=0) for _ in range(10)])
+    units_graded = 8 * (3 * 3 + 4 * 6 + 2 * 11 + 1 * 22)
+    assert units_graded * 2048 < L.q4_gemv_seq_bytes(graded, 10) < units_graded * 2048 + 65536
     short = (q4.GemvOp * 3)(op(4096, 4096, rows=128), op(11008, 4096, [0], rows=128),
                             op(4096, 11008, [0, 1], rows=128))
     units_short = 8 * 32 + 22 * 32 + 8 * 86
@@ -154,7 +161,7 @@ def test_gemv_seq_checks_on_host(L):
              ((op(256, 0),), q4.Q4_ERR_ARG),
              ((op(256, 64, C=good + 4),), q4.Q4_ERR_ALIGN),
              ((op(256, 64, rows=100),), q4.Q4_ERR_ARG),                  # not a multiple of 64
-             ((op(256, 64, rows=2112),), q4.Q4_ERR_ARG)]
+             ((op(256, 64, rows=4160),), q4.Q4_ERR_ARG)]     # over 4096
     for bad, code in cases:
         arr = (q4.GemvOp * len(bad))(*bad)
         assert L.q4_gemv_seq_bytes(arr, len(bad)) == 0
