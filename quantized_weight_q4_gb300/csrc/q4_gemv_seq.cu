@@ -214,6 +214,13 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const SeqParam
     int posted = 0;   // ring phases posted: stages, then the end marker
     bool failed = false;
     while (!failed) {
+      // take a unit only once the ring has room for its first stage, so that
+      // no CTA holds a unit that it cannot start loading while others idle
+      if (gs >= STAGES &&
+          !bounded_wait(&empty[gs % STAGES], ((gs / STAGES) - 1) & 1, s_fail, p.err)) {
+        failed = true;
+        break;
+      }
       const int u = static_cast<int>(atomicAdd(p.queue, 1u));
       const bool end = (u >= p.total_units);
       int op = 0, tile = 0, slice = 0, nst = 1, K = 0, srows = 0;
@@ -230,7 +237,8 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const SeqParam
       }
       for (int st = 0; st < nst; ++st, ++gs) {
         const int slot = gs % STAGES;
-        if (gs >= STAGES && !bounded_wait(&empty[slot], ((gs / STAGES) - 1) & 1, s_fail, p.err)) {
+        if (st > 0 && gs >= STAGES &&
+            !bounded_wait(&empty[slot], ((gs / STAGES) - 1) & 1, s_fail, p.err)) {
           failed = true;
           break;
         }
