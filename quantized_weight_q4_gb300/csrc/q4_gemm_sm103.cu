@@ -356,18 +356,86 @@ __global__ void __launch_bounds__(Cfg<MT, DW, SPLIT>::kThreads, 1)
         // accumulator c / BN; the warps of one lane quarter split them
         const int c0 = (wd >> 2) * C::kEpiCols;
         const int mt = c0 / BN;
-        const int row = w.m0 + mt * 128 + q * 32 + lane;
+        const int row0 = w.m0 + mt * 128 + q * 32;   // the warp's 32 rows
+        const int row = row0 + lane;
+        if (p.use_tma_c) {
+          // Through shared memory and TMA tensor stores: boxes of 32 rows x
+          // 128 bytes (32 fp32 or 64 bf16 columns), 128-byte swizzled (each
+          // lane writes its row's 16-byte chunks at chunk ^ (row % 8): no bank
+          // conflicts), two in flight per warp.  The staging boxes sit in the
+          // B ring, which no MMA reads and no dequant writes between tiles.
+          uint8_t* stg = sB + wd * 8192;
+          const int box_cols = p.c_dtype == 0 ? 32 : 64;
+          int nbox = 0;
 #pragma unroll 1
-        for (int c = c0; c < c0 + C::kEpiCols; c += 32) {
-          uint32_t acc[32];
-          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, acc);
-          const int col0 = w.n0 + (c - mt * BN);
-          if (row < p.M && col0 < p.N) store_row32(p, row, col0, acc);
+          for (int c = c0; c < c0 + C::kEpiCols; c += box_cols, ++nbox) {
+            uint8_t* box = stg + (nbox & 1) * 4096;
+            if (nbox >= 2) {   // the store issued from this box two boxes ago has read it
+              if (lane == 0) bulk_wait_read<1>();
+              __syncwarp();
+            }
+#pragma unroll 1
+            for (int h = 0; h < box_cols / 32; ++h) {
+              uint32_t acc[32], v[32];
+              tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c + 32 * h, acc);
+              // tensor-memory column 8t + s holds output column 8t + chunk_col(s)
+#pragma unroll
+              for (int t = 0; t < 4; ++t)
+#pragma unroll
+                for (int s8 = 0; s8 < 8; ++s8) v[8 * t + chunk_col(s8)] = acc[8 * t + s8];
+              uint8_t* rowp = box + lane * 128;
+              if (p.c_dtype == 0) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
+                      make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  uint4 o;
+                  o.x = bf16_bits(__uint_as_float(v[8 * j])) |
+                        (bf16_bits(__uint_as_float(v[8 * j + 1])) << 16);
+                  o.y = bf16_bits(__uint_as_float(v[8 * j + 2])) |
+                        (bf16_bits(__uint_as_float(v[8 * j + 3])) << 16);
+                  o.z = bf16_bits(__uint_as_float(v[8 * j + 4])) |
+                        (bf16_bits(__uint_as_float(v[8 * j + 5])) << 16);
+                  o.w = bf16_bits(__uint_as_float(v[8 * j + 6])) |
+                        (bf16_bits(__uint_as_float(v[8 * j + 7])) << 16);
+                  *reinterpret_cast<uint4*>(rowp + (((4 * h + j) ^ (lane & 7)) << 4)) = o;
+                }
+              }
+            }
+            fence_async_smem();   // the TMA store reads the box through the async proxy
+            __syncwarp();
+            const int col = w.n0 + (c - mt * BN);
+            if (lane == 0) {
+              if (row0 < p.M && col < p.N) tma_store_2d(&p.tmap_c, box, col, row0);
+              bulk_commit();
+            }
+          }
+          // the boxes are read before the B ring takes the next tile's stages
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+        } else {
+#pragma unroll 1
+          for (int c = c0; c < c0 + C::kEpiCols; c += 32) {
+            uint32_t acc[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, acc);
+            const int col0 = w.n0 + (c - mt * BN);
+            if (row < p.M && col0 < p.N) store_row32(p, row, col0, acc);
+          }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tmem_empty);
+      if (p.use_tma_c) {
+        // every warp's staging boxes (in the B ring) have been read before
+        // any warp writes the next tile's B stages over them
+        int v2 = 1;
+        if (lane == 0) v2 = gwait(tmem_empty, it & 1, s_fail, p.err) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, v2, 0) != 0;
+      }
     }
   }
 
@@ -502,6 +570,8 @@ __global__ void __launch_bounds__(Cfg<MT, DW, SPLIT>::kThreads, 1)
     }
   }
 
+  // the epilogue's TMA stores are complete before the CTA ends
+  if (!SPLIT && warp >= 2 && lane == 0) bulk_wait<0>();
   // everyone (the MMA thread after its drain) meets here before the tensor
   // memory is released
   tc_fence_before();
@@ -621,6 +691,24 @@ bool encode_maps(GemmParams& p, const void* A, const void* B, int64_t M, int64_t
   return true;
 }
 
+// C for the prefill form's TMA stores: [M][N] fp32 or bf16, boxes of 128 bytes
+// x 32 rows, 128-byte swizzle.  False (the epilogue then stores row by row)
+// when the row pitch is not a multiple of 16 bytes.
+bool encode_c_map(GemmParams& p, void* C, int c_dtype, int64_t M, int64_t N) {
+  auto encode = get_encode();
+  const int64_t es = c_dtype == 0 ? 4 : 2;
+  if (!encode || (N * es) % 16 != 0) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N * es)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / es), 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(&p.tmap_c,
+                c_dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool gemm_supported(int64_t M, int64_t N, int64_t K) {
@@ -685,6 +773,7 @@ cudaError_t launch_gemm(void* C, int c_dtype, const void* A, const void* B, int6
                         int64_t K, unsigned* err, int sms, cudaStream_t st, float* part,
                         unsigned* tickets) {
   GemmParams p;
+  p.use_tma_c = 0;
   p.gsplit = 0;
   p.part = nullptr;
   p.tickets = nullptr;
@@ -698,6 +787,7 @@ cudaError_t launch_gemm(void* C, int c_dtype, const void* A, const void* B, int6
   if (M > 128) {
     // prefill form: persistent, one CTA per SM at most
     if (!encode_maps(p, A, B, M, N, K, PrefillCfg::kBM)) return cudaErrorInvalidValue;
+    p.use_tma_c = encode_c_map(p, C, c_dtype, M, N) ? 1 : 0;
     p.nsplit = 1;
     cudaError_t e = prepare<2, 8, false>();
     if (e != cudaSuccess) return e;

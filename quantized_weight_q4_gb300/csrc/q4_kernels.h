@@ -129,6 +129,9 @@ cudaError_t launch_gemv_seq(const SeqParams& p, int grid, int stages, cudaStream
 struct GemmParams {
   CUtensorMap tmap_a;   // A: bf16 [M][K], boxes of 64 K x 256 rows, 128-byte swizzle
   CUtensorMap tmap_b;   // weights: uint16 [K][nb*9], boxes of 72 halfwords x 64 rows
+  CUtensorMap tmap_c;   // prefill form, use_tma_c: C [M][N], boxes of 128 bytes x 32 rows,
+                        // 128-byte swizzle (written with TMA stores)
+  int use_tma_c;
   void* C;              // [M][N] fp32 (c_dtype 0) or bf16 (1)
   int c_dtype;
   int M, N, K;

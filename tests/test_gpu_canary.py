@@ -53,7 +53,8 @@ def check_guard(raw, n, dtype, what):
 
 
 # (M, K, N, a_dtype, c_dtype, entry): GEMV tails, tensor-core small-M (global
-# form up to 40 rows, cluster form above), prefill with M and N tails
+# form up to 40 rows, cluster form above), prefill with M and N tails (its
+# TMA-store epilogue: boxes of 32 rows clipped at M and N)
 CASES = [
     (1, 300, 250, "f32", "f32", "ex"), (3, 517, 1000, "f32", "f32", "ex"),
     (5, 64, 33, "bf16", "bf16", "ex"), (7, 2049, 4000, "bf16", "f32", "ex"),
@@ -61,6 +62,7 @@ CASES = [
     (9, 1024, 250, "bf16", "f32", "tiles"), (33, 5120, 1000, "bf16", "bf16", "tiles"),
     (40, 2048, 4096, "bf16", "f32", "tiles"), (100, 1000, 250, "bf16", "f32", "tiles"),
     (129, 520, 1000, "bf16", "bf16", "tiles"), (300, 2048, 2040, "bf16", "f32", "tiles"),
+    (333, 640, 1000, "bf16", "bf16", "ex"),
 ]
 
 

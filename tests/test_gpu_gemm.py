@@ -371,3 +371,25 @@ def test_small_m_capture_on_a_fresh_stream():
     assert q4.q4_get_device_status() == q4.Q4_OK
     assert torch.equal(eager[0], eager[1]) and torch.equal(eager[1], eager[2])
     assert_tile_tol(to_host64(eager[0]), Cb, Sb, "eager (global split)")
+
+
+# Prefill with more 256 x 256 tiles than SMs and an uneven last round (2048 x
+# 5888 = 8 x 23 = 184 tiles; K = 520: nine K steps, the last one short): CTAs
+# take several tiles, and each tile's epilogue stages C in shared memory that
+# the next tile's B stages reuse (the TMA-store epilogue).
+def test_prefill_several_tiles_per_cta():
+    M, K, N = 2048, 520, 5888
+    A = si.activations_bf16(M, K, seed=21)
+    B = si.q4_weights(K, N, seed=21)
+    C = run(A, B, M, N, K)
+    C2 = run(A, B, M, N, K)
+    assert torch.equal(C, C2)
+    Ch = to_host64(C)
+    rows = np.unique(np.concatenate([si.rng(21, 1).choice(M, 10, replace=False),
+                                     [0, 255, 256, 1023, 1024, M - 1]]))
+    Cb, Sb = oracle.matmul_bf16_tiles(A[rows], B, len(rows), N, K)
+    assert_tile_tol(Ch[rows], Cb, Sb, "several tiles per CTA")
+    C64, S = oracle.matmul(A[rows], B, len(rows), N, K)
+    assert_exact_bound(Ch[rows], C64, S, "several tiles per CTA")
+    C16 = run(A, B, M, N, K, c_dtype=torch.bfloat16)
+    assert torch.equal(C.to(torch.bfloat16).view(torch.int16), C16.view(torch.int16))
