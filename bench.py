@@ -436,12 +436,17 @@ def run_ours(args, ws, rank, local):
     if status != q4.Q4_OK:
         raise SystemExit(f"device status {status} after the timed region")
 
-    # end to end: pinned host A -> device, graph, device C -> pinned host
+    # end to end: pinned host A -> device, the public call (through the C
+    # ABI: host-side checks and launches on the clock, no graph), device C ->
+    # pinned host
     stream = seq.stream
     def e2e_step():
         with torch.cuda.stream(stream):
             w["dA"].copy_(w["hA"], non_blocking=True)
-            seq.graph.replay()
+            if use_seq:
+                seq.plan.run(stream=stream)                 # q4_gemv_seq_run
+            else:
+                w["seq"].run_eager(stream=stream)           # one q4_matmul_ex per GEMV
             w["hC"].copy_(w["dC"], non_blocking=True)
         stream.synchronize()
     for _ in range(max(3, args.warmup)):
@@ -549,7 +554,9 @@ def run_ours(args, ws, rank, local):
             "h2d_bytes_per_step": int(w["hA"].numel() * 4),
             "d2h_bytes_per_step": int(w["hC"].numel() * 4),
             "steps": e2e_steps,
-            "note": "per step: pinned A -> device, graph replay, C -> pinned host, stream sync",
+            "note": ("per step: pinned A -> device, the C-ABI call (" +
+                     ("q4_gemv_seq_run" if use_seq else "224 x q4_matmul_ex") +
+                     "), C -> pinned host, stream sync"),
         },
         "gpu_launches": args.steps * w["launches_per_step"],
         "clocks": clk.summary(),
