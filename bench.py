@@ -84,7 +84,7 @@ TRAFFIC = {
 SEQ_SOURCES = ("q4_gemv_seq.cu", "q4_gemv_core.cuh", "q4_device.cuh")
 TRAFFIC_SEQ = {
     # captured on the 32-layer launch itself (one pass per launch)
-    "0077d00f27368ff4/7396864": 3918930432,
+    "f5772ec32b66d5e1/7454208": 3935703040,
 }
 
 
@@ -666,7 +666,7 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
         fns, keep, uniq = [], [], 0
         per_expert = (2 * H * si.nblocks(I) + I * si.nblocks(H)) * 18
         wsz = q4.q4_moe_workspace_size(T, topk, E, H, I)
-        wspace = torch.empty(wsz, dtype=torch.uint8, device=dev)
+        wspace = torch.zeros(wsz, dtype=torch.uint8, device=dev)
         for r in range(R):
             idx, w = si.routing(T, E, topk, seed=r)
             x = si.activations_bf16(T, H, seed=r)
@@ -729,7 +729,7 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
         per_expert = (2 * H * si.nblocks(I) + I * si.nblocks(H)) * 18
         shared_bytes = (2 * H * si.nblocks(Is) + Is * si.nblocks(H)) * 18
         wsz = q4.q4_moe_block_workspace_size(T, topk, E, H, I, Is)
-        wspace = torch.empty(wsz, dtype=torch.uint8, device=dev)
+        wspace = torch.zeros(wsz, dtype=torch.uint8, device=dev)
         for r in range(R):
             logits = si.router_logits(T, E, seed=r)
             order = np.argsort(-logits, axis=1, kind="stable")[:, :topk]

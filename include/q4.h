@@ -196,11 +196,23 @@ Q4_API int q4_moe_experts(float *out, const void *x, const void *W_gate, const v
                    int64_t T, int64_t E, int64_t H, int64_t I);
 
 /* q4_moe_experts with x_dtype (Q4_F32 / Q4_BF16), any topk in [1, 16],
- * an explicit workspace and a stream.  The workspace (>= q4_moe_workspace_size
- * bytes) holds the intermediate SiLU(g)*u rows and the per-slot down outputs;
- * its contents need no initialisation.  NULL selects a library-owned
- * workspace, allocated (cudaMalloc) by the first call that needs more than it
- * has.  No allocation happens while the stream is being captured: such a
+ * an explicit workspace and a stream.
+ * From 4 tokens up (and at most 512 slots T * topk, with ceil(I/32) and
+ * ceil(H/32) multiples of 8, H * sizeof(x) and I * 4 multiples of 16 bytes)
+ * the slots run in one launch of the persistent decode kernel: every slot's
+ * gate and up (the last K slice of a column tile forms SiLU(g) * u there),
+ * then every slot's down, each slot waiting only for its own SiLU(g) * u,
+ * then the slot combine.  Fewer tokens, other shapes, or a workspace below
+ * q4_moe_workspace_size run three launches (gate/up, down, slot combine).
+ * The results satisfy the same bound either way.
+ * The workspace (>= q4_moe_workspace_size bytes for the persistent form; the
+ * three-launch form needs less) begins with 64 KB of counters that must be
+ * zero before its first use (e.g. cudaMemset once); every call leaves them
+ * zero unless one of its waits times out (Q4_DEVERR_TIMEOUT), after which
+ * they must be cleared again.  The rest holds the intermediate rows and
+ * partial sums and needs no initialisation.  NULL selects a library-owned
+ * workspace (zeroed when allocated), allocated (cudaMalloc) by the first call
+ * that needs more than it has.  No allocation happens while the stream is being captured: such a
  * call returns Q4_ERR_WORKSPACE, so make one call of the largest shape before
  * capturing a CUDA graph.  A workspace that a larger one replaces stays
  * allocated until q4_release_scratch(), since graphs may still use it.
@@ -245,12 +257,16 @@ Q4_API int q4_moe_experts_trace(float *out, const void *x, int x_dtype, const vo
  *   The scratch is a fixed device array built into the library, of
  *   q4_moe_static_scratch_bytes() bytes (8 MiB) on every GPU that loads the
  *   library, held until the process exits.  Calls whose
- *   q4_moe_workspace_size(T, topk, E, H, I) exceeds it return
- *   Q4_ERR_WORKSPACE.  No call allocates or frees device memory.
+ *   three-launch form's workspace (see q4_moe_experts_ex) exceeds it return
+ *   Q4_ERR_WORKSPACE; a call runs the persistent form only when that form's
+ *   workspace fits too.  No call allocates or frees device memory.
  *   The first call on a device looks up the array's device address; make it
  *   before capturing a stream into a CUDA graph.
  *   All calls on a device share the one array and leave their intermediate
- *   rows in it; nothing needs to start at zero.  Calls that overlap on the
+ *   rows in it.  The array starts zeroed, so its counter header (see
+ *   q4_moe_experts_ex) is zero before the first call; after a call whose
+ *   wait timed out (Q4_DEVERR_TIMEOUT) it is not restored and later calls on
+ *   the persistent form time out too.  Calls that overlap on the
  *   GPU (different streams without ordering) race on the array.
  */
 Q4_API int q4_moe_experts_noalloc(float *out, const void *x, int x_dtype, const void *W_gate,
@@ -449,7 +465,8 @@ Q4_API int q4_moe_gate(int32_t *topk_idx, float *topk_w, const float *logits,
  * ceil(H/32) blocks).  Is = 0 means no shared expert (S_* may be NULL).  The
  * routed sum is taken in slot order and the shared term added last.
  *   out  fp32 [T, H]; x  [T, H] fp32 or bf16 (x_dtype); logits fp32 [T, E]
- * Workspace: q4_moe_block_workspace_size bytes (no initialisation needed),
+ * Workspace: q4_moe_block_workspace_size bytes whose first 64 KB are zero
+ * before its first use (as for q4_moe_experts_ex),
  * or NULL for the library-owned workspace shared with q4_moe_experts_ex.
  * Limits as for q4_moe_gate and q4_moe_experts_ex.
  */

@@ -1,6 +1,7 @@
 // C ABI of the Q4_0 dequant-matmul library: argument checks, launch shapes,
 // workspace management and the device status word.  See include/q4.h.
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
 #include <map>
 #include <new>
@@ -21,6 +22,10 @@ __device__ unsigned int g_q4_status = 0u;
 constexpr int kMaxDevices = 64;
 // The rows of A a CTA uses are copied to shared memory: MR * rows * 4 bytes.
 constexpr int64_t kMaxASliceBytes = 64 * 1024;
+// Every routed-expert workspace starts with this many bytes of counters for
+// the persistent form (zero before the first call, left zero by every call
+// whose waits do not time out); nothing else is stored there.
+constexpr size_t kMoeHeaderBytes = 64 * 1024;
 // From this many rows of bf16 A on, a matmul runs on the tensor cores (the
 // split-K small-M form up to 128 rows, the persistent prefill form above);
 // below it, and for fp32 A, as split-K GEMVs on the CUDA cores.
@@ -64,6 +69,9 @@ struct DeviceState {
   // while one was current may still use it, so it is kept until
   // q4_release_scratch()
   std::vector<void*> retired;
+  // the persistent sequence kernel's ring depth and resident CTAs per SM
+  // (0 until first needed)
+  int seq_stages = 0, seq_per_sm = 0;
 };
 
 std::mutex g_mu;
@@ -160,6 +168,11 @@ int owned_workspace(DeviceState* s, size_t bytes, cudaStream_t st, void** ws) {
     void* p = nullptr;
     if (cudaMalloc(&p, want) != cudaSuccess) {
       cudaGetLastError();
+      return Q4_ERR_CUDA;
+    }
+    // zero (the routed-expert counters in its header start at zero)
+    if (cudaMemset(p, 0, want) != cudaSuccess) {
+      cudaFree(p);
       return Q4_ERR_CUDA;
     }
     if (s->ws) s->retired.push_back(s->ws);
@@ -314,6 +327,23 @@ const MoeShape& cached_moe_shape(DeviceState* s, int64_t T, int64_t topk, int64_
 
 int launch_status(cudaError_t e) { return e == cudaSuccess ? Q4_OK : Q4_ERR_CUDA; }
 
+// The persistent sequence kernel's ring depth (5 stages where two CTAs fit on
+// an SM, else 4) and resident CTAs per SM; Q4_ERR_CUDA if it cannot launch.
+int seq_residency(DeviceState* s) {
+  if (s->seq_per_sm == 0) {
+    int stages = 5;
+    int per_sm = q4::seq_ctas_per_sm(stages, true);
+    if (per_sm < 2) {
+      stages = 4;
+      per_sm = q4::seq_ctas_per_sm(stages, true);
+    }
+    if (per_sm < 1) return Q4_ERR_CUDA;
+    s->seq_stages = stages;
+    s->seq_per_sm = per_sm;
+  }
+  return Q4_OK;
+}
+
 }  // namespace
 
 namespace {
@@ -360,16 +390,235 @@ int gemv_run(DeviceState* s, void* C, int c_dtype, const void* A, int a_dtype, c
                                        st, true));
 }
 
-// The routed-expert kernels (gate/up, down, slot combine) for a validated
-// problem, on a workspace of at least m.total bytes; the combine adds
-// `addend` (fp32 [T, H], or null) after the weighted sum.  With `out` null the
-// combine is left out and the per-slot down outputs stay in the workspace at
-// m.off_y ([T*topk, H] fp32).
+// ---------------------------------------------------------------------------
+// Routed experts of several tokens on the persistent sequence kernel: one
+// launch for every slot's gate, up and down, then the slot combine.  Op 0
+// pairs gate and up of each slot (s = t * topk + k, expert topk_idx[s], A =
+// x[t]); the last K slice of a slot's column tile adds both products and
+// forms h = SiLU(g) * u there, then counts the tile for the slot.  Op 1, down,
+// is segmented over the slots along its output (y[s] = h[s] . W_down[e]);
+// each slot's units wait only for that slot's h.  The launch takes its
+// counters from the workspace header and leaves them zero.  Below
+// kMoeSeqMinTokens tokens the three-launch form measured faster (DeepSeek-V2
+// experts, GB/s of distinct expert weights: one token 1974 against 2796, two
+// tokens 2464 against 2623; four tokens 3537 against 2641).
+// ---------------------------------------------------------------------------
+constexpr int64_t kMoeSeqMinTokens = 4;
+constexpr int64_t kMoeSeqMaxSlots = 512;
+// Most K rows per gate/up unit (DeepSeek-V2 experts, GB/s at 4 / 8 / 32
+// tokens: slices of 2560 rows 3562 / 4163 / 3138; 2048 + 2048 + 1024 rows
+// 3101 / 3930 / 3086; 1024 rows 3537 / 3850 / 2996).
+constexpr int kMoeGuRows = 2560;
+
+struct MoeSeqPlan {
+  bool ok = false;
+  int rows_gu = 0, rows_d = 0;        // K rows per unit of gate/up and of down
+  int seg_tiles = 0, slices_gu = 0;   // gate/up: column tiles per slot, K slices
+  int tiles_d = 0, slices_d = 0;      // down: column tiles per slot, K slices
+  int units_gu = 0, units = 0, ntickets = 0;
+  size_t off_g = 0, off_u = 0, off_h = 0, off_y = 0, off_part = 0, total = 0;   // data layout
+};
+
+MoeSeqPlan moe_seq_plan(int64_t T, int64_t topk, int64_t H, int64_t I, int x_dtype) {
+  MoeSeqPlan q;
+  const int64_t S = T * topk;
+  const int64_t es = x_dtype == Q4_F32 ? 4 : 2;
+  // whole 16-byte tensor-map rows; rows of x and of h start 16-byte aligned
+  if (T < kMoeSeqMinTokens || S > kMoeSeqMaxSlots || ceil_div(I, 32) % 8 != 0 ||
+      ceil_div(H, 32) % 8 != 0 || (H * es) % 16 != 0 || I % 4 != 0)
+    return q;
+  const int64_t tc = q4::seq_tile_cols(), stage = q4::seq_stage_rows();
+  q.seg_tiles = static_cast<int>(ceil_div(I, tc));
+  q.tiles_d = static_cast<int>(ceil_div(H, tc));
+  // K slices of equal length (whole stages): an uneven last slice leaves its
+  // units short of the others at the end of the sweep
+  auto even_rows = [stage](int64_t K, int64_t most) {
+    return static_cast<int>(round_up(ceil_div(K, ceil_div(K, most)), stage));
+  };
+  q.rows_gu = even_rows(H, kMoeGuRows);
+  q.rows_d = even_rows(I, q4::seq_max_slice_rows());
+  q.slices_gu = static_cast<int>(ceil_div(H, q.rows_gu));
+  q.slices_d = static_cast<int>(ceil_div(I, q.rows_d));
+  const int64_t units_gu = 2 * S * q.seg_tiles * q.slices_gu;
+  const int64_t units = units_gu + S * q.tiles_d * q.slices_d;
+  const int64_t tickets = S * q.seg_tiles + (q.slices_d > 1 ? S * q.tiles_d : 0);
+  if (units > (1 << 24) || 4 * (2 + 2 + S + tickets) > static_cast<int64_t>(kMoeHeaderBytes))
+    return q;
+  q.units_gu = static_cast<int>(units_gu);
+  q.units = static_cast<int>(units);
+  q.ntickets = static_cast<int>(tickets);
+  size_t o = 0;
+  for (size_t* off : {&q.off_g, &q.off_u, &q.off_h}) {
+    *off = o;
+    o += round_up(static_cast<size_t>(S * I) * 4, 256);
+  }
+  q.off_y = o;
+  o += round_up(static_cast<size_t>(S * H) * 4, 256);
+  q.off_part = o;
+  o += static_cast<size_t>(q.slices_d > 1 ? units : units_gu) * tc * 4;
+  q.total = o;
+  q.ok = true;
+  return q;
+}
+
+// Bytes after the header of a routed-expert workspace for the three-launch
+// form (the least any call needs), and for the form the call prefers.
+size_t moe_old_data_bytes(int64_t T, int64_t topk, int64_t H, int64_t I) {
+  const size_t nslots = static_cast<size_t>(T * topk);
+  return round_up(nslots * I * 4, 256) + round_up(nslots * H * 4, 256);
+}
+size_t moe_data_bytes(int64_t T, int64_t topk, int64_t H, int64_t I) {
+  const MoeSeqPlan q = moe_seq_plan(T, topk, H, I, Q4_BF16);
+  const MoeSeqPlan q32 = moe_seq_plan(T, topk, H, I, Q4_F32);
+  size_t b = moe_old_data_bytes(T, topk, H, I);
+  if (q.ok) b = std::max(b, q.total);
+  if (q32.ok) b = std::max(b, q32.total);
+  return b;
+}
+
+}  // namespace
+
+namespace q4 {
+size_t moe_min_workspace_bytes(int64_t T, int64_t topk, int64_t H, int64_t I) {
+  return kMoeHeaderBytes + moe_old_data_bytes(T, topk, H, I);
+}
+}  // namespace q4
+
+namespace {
+
+int moe_seq_run(DeviceState* s, const MoeSeqPlan& q, void* counters, void* data, float* out,
+                const void* x, int x_dtype, const void* W_gate, const void* W_up,
+                const void* W_down, const int32_t* topk_idx, const float* topk_w, int64_t T,
+                int64_t topk, int64_t E, int64_t H, int64_t I, const float* addend,
+                cudaStream_t st, float* g_trace, float* u_trace, float* h_trace,
+                float* y_trace) {
+  int rc = seq_residency(s);
+  if (rc != Q4_OK) return rc;
+  const int64_t S = T * topk;
+  uint8_t* d8 = static_cast<uint8_t*>(data);
+  float* g = g_trace ? g_trace : reinterpret_cast<float*>(d8 + q.off_g);
+  float* u = u_trace ? u_trace : reinterpret_cast<float*>(d8 + q.off_u);
+  float* h = h_trace ? h_trace : reinterpret_cast<float*>(d8 + q.off_h);
+  float* y = y_trace ? y_trace : reinterpret_cast<float*>(d8 + q.off_y);
+  const int64_t nbI = ceil_div(I, 32), nbH = ceil_div(H, 32);
+
+  q4::SeqParams p;
+  std::memset(&p, 0, sizeof(p));
+  q4::SeqOpDesc& gu = p.inl[0];
+  if (!q4::encode_weight_tmap(&gu.tmap, W_gate, H, nbI, E, H * nbI * 18, 2, true, q4::kFmtQ4) ||
+      !q4::encode_weight_tmap(&gu.tmap2, W_up, H, nbI, E, H * nbI * 18, 2, true, q4::kFmtQ4))
+    return Q4_ERR_CUDA;
+  gu.A = x;
+  gu.C = g;
+  gu.C2 = u;
+  gu.h = h;
+  gu.eidx = topk_idx;
+  gu.K = static_cast<int>(H);
+  gu.N = static_cast<int>(2 * S * I);
+  gu.nb = static_cast<int>(nbI);
+  gu.ntiles = static_cast<int>(2 * S) * q.seg_tiles;
+  gu.nslices = q.slices_gu;
+  gu.slice_rows = q.rows_gu;
+  gu.unit_base = 0;
+  gu.ticket_base = 0;
+  gu.a_dtype = x_dtype;
+  gu.c_dtype = Q4_F32;
+  gu.seg_mode = 1;
+  gu.nseg = static_cast<int>(2 * S);
+  gu.seg_len = static_cast<int>(I);
+  gu.seg_tiles = q.seg_tiles;
+  gu.a_seg_div = static_cast<int>(2 * topk);   // segments 2s, 2s + 1: token s / topk
+  gu.a_seg_stride = static_cast<int>(H);
+  gu.pair = 1;
+  gu.seg_done_base = 0;
+  gu.seg_need = 0;   // no per-slot dependency
+  gu.E = static_cast<int>(E);
+
+  q4::SeqOpDesc& d = p.inl[1];
+  if (!q4::encode_weight_tmap(&d.tmap, W_down, I, nbH, E, I * nbH * 18, 2, true, q4::kFmtQ4))
+    return Q4_ERR_CUDA;
+  d.A = h;
+  d.C = y;
+  d.eidx = topk_idx;
+  d.K = static_cast<int>(I);
+  d.N = static_cast<int>(S * H);
+  d.nb = static_cast<int>(nbH);
+  d.ntiles = static_cast<int>(S) * q.tiles_d;
+  d.nslices = q.slices_d;
+  d.slice_rows = q.rows_d;
+  d.unit_base = q.units_gu;
+  d.ticket_base = static_cast<int>(S) * q.seg_tiles;
+  d.a_dtype = Q4_F32;
+  d.c_dtype = Q4_F32;
+  d.seg_mode = 1;
+  d.nseg = static_cast<int>(S);
+  d.seg_len = static_cast<int>(H);
+  d.seg_tiles = q.tiles_d;
+  d.a_seg_div = 1;
+  d.a_seg_stride = static_cast<int>(I);
+  d.seg_dep = 0;
+  d.seg_need = q.seg_tiles;
+  d.E = static_cast<int>(E);
+
+  unsigned* c = static_cast<unsigned*>(counters);
+  p.ops = nullptr;
+  p.nops = 2;
+  p.total_units = q.units;
+  p.queue = c;
+  p.exits = c + 1;
+  p.done = c + 2;
+  p.seg_done = c + 4;
+  p.nseg_done = static_cast<int>(S);
+  p.tickets = c + 4 + S;
+  p.ntickets = q.ntickets;
+  p.reset = 1;
+  p.part = reinterpret_cast<float*>(d8 + q.off_part);
+  p.err = s->status;
+  for (int i = 0; i < 4; ++i) p.kmask[i] = 0xFu << (4 * i);
+  const int grid = std::min(s->seq_per_sm * s->sms, q.units);
+  cudaError_t e = q4::launch_gemv_seq(p, grid, s->seq_stages, st, true, true);
+  if (e != cudaSuccess) return Q4_ERR_CUDA;
+  if (!out) return Q4_OK;
+  return launch_status(q4::launch_moe_combine(out, y, topk_idx, topk_w, addend,
+                                              static_cast<int>(T), static_cast<int>(topk),
+                                              static_cast<int>(E), static_cast<int>(H), st, true));
+}
+
+// Where moe_run with `out` null leaves the per-slot down outputs y [T*topk,
+// H] in the data part `ws`.
+float* moe_y_rows(void* ws, const MoeShape& m, bool seq_form, int64_t T, int64_t topk, int64_t H,
+                  int64_t I, int x_dtype) {
+  const size_t off = seq_form ? moe_seq_plan(T, topk, H, I, x_dtype).off_y : m.off_y;
+  return reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + off);
+}
+
+// Whether the call runs the persistent form: its shape and a data part of
+// `data_bytes` (the rest of the workspace after the header) large enough.
+bool moe_takes_seq(int64_t T, int64_t topk, int64_t H, int64_t I, int x_dtype, size_t data_bytes) {
+  const MoeSeqPlan q = moe_seq_plan(T, topk, H, I, x_dtype);
+  return q.ok && data_bytes >= q.total;
+}
+
+// The routed experts for a validated problem: the persistent form
+// (moe_seq_run) where moe_takes_seq, else the gate/up, down and slot combine
+// kernels.  `counters` is the workspace header (kMoeHeaderBytes, zero), `ws`
+// the rest (`data_bytes` of it, at least moe_old_data_bytes).  The combine
+// adds `addend` (fp32 [T, H], or null) after the weighted sum.  With `out`
+// null the combine is left out and the per-slot down outputs stay in the
+// workspace (moe_y_rows).  The trace pointers, when given, receive g, u, h
+// and y.
 int moe_run(DeviceState* s, const MoeShape& m, float* out, const void* x, int x_dtype,
             const void* W_gate, const void* W_up, const void* W_down, const int32_t* topk_idx,
             const float* topk_w, int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I,
-            void* ws, const float* addend, cudaStream_t st, float* g_trace = nullptr,
-            float* u_trace = nullptr) {
+            void* counters, void* ws, size_t data_bytes, const float* addend, cudaStream_t st,
+            float* g_trace = nullptr, float* u_trace = nullptr, float* h_trace = nullptr,
+            float* y_trace = nullptr) {
+  if (moe_takes_seq(T, topk, H, I, x_dtype, data_bytes))
+    return moe_seq_run(s, moe_seq_plan(T, topk, H, I, x_dtype), counters, ws, out, x, x_dtype,
+                       W_gate, W_up, W_down, topk_idx, topk_w, T, topk, E, H, I, addend, st,
+                       g_trace, u_trace, h_trace, y_trace);
+  if (4LL * m.mr * m.rows_gu > kMaxASliceBytes || 4LL * m.mr * m.rows_d > kMaxASliceBytes)
+    return Q4_ERR_SHAPE;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   const int64_t nbI = ceil_div(I, 32), nbH = ceil_div(H, 32);
   float* h = reinterpret_cast<float*>(w8 + m.off_h);
@@ -435,6 +684,12 @@ int moe_run(DeviceState* s, const MoeShape& m, float* out, const void* x, int x_
                       dim3(1, m.nsplit_d, 1), st, true);
   if (e != cudaSuccess) return Q4_ERR_CUDA;
 
+  if (h_trace && cudaMemcpyAsync(h_trace, h, static_cast<size_t>(m.nslots) * I * 4,
+                                 cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return Q4_ERR_CUDA;
+  if (y_trace && cudaMemcpyAsync(y_trace, y, static_cast<size_t>(m.nslots) * H * 4,
+                                 cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return Q4_ERR_CUDA;
   if (!out) return Q4_OK;
   e = q4::launch_moe_combine(out, y, topk_idx, topk_w, addend, static_cast<int>(T),
                              static_cast<int>(topk), static_cast<int>(E), static_cast<int>(H), st,
@@ -616,9 +871,8 @@ int q4_matmul(float* C, const float* A, const void* B, int64_t M, int64_t N, int
 
 size_t q4_moe_workspace_size(int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I) {
   if (T <= 0 || topk <= 0 || E <= 0 || H <= 0 || I <= 0) return 0;
-  // h [T*topk, I] and y [T*topk, H] in fp32, each rounded up to 256 bytes
-  const size_t nslots = static_cast<size_t>(T * topk);
-  return round_up(nslots * I * 4, 256) + round_up(nslots * H * 4, 256);
+  // the counter header, then the preferred form's rows and partial sums
+  return kMoeHeaderBytes + moe_data_bytes(T, topk, H, I);
 }
 
 int q4_moe_experts_ex(float* out, const void* x, int x_dtype, const void* W_gate, const void* W_up,
@@ -640,17 +894,18 @@ int q4_moe_experts_ex(float* out, const void* x, int x_dtype, const void* W_gate
   int rc = current_state(&s);
   if (rc != Q4_OK) return rc;
   const MoeShape& m = cached_moe_shape(s, T, topk, E, H, I);
-  if (4LL * m.mr * m.rows_gu > kMaxASliceBytes || 4LL * m.mr * m.rows_d > kMaxASliceBytes)
-    return Q4_ERR_SHAPE;
   void* ws = workspace;
+  size_t bytes = workspace_bytes;
   if (ws) {
-    if (workspace_bytes < m.total) return Q4_ERR_WORKSPACE;
+    if (bytes < kMoeHeaderBytes + moe_old_data_bytes(T, topk, H, I)) return Q4_ERR_WORKSPACE;
   } else {
-    rc = owned_workspace(s, m.total, static_cast<cudaStream_t>(stream), &ws);
+    bytes = kMoeHeaderBytes + moe_data_bytes(T, topk, H, I);
+    rc = owned_workspace(s, bytes, static_cast<cudaStream_t>(stream), &ws);
     if (rc != Q4_OK) return rc;
   }
   return moe_run(s, m, out, x, x_dtype, W_gate, W_up, W_down, topk_idx, topk_w, T, topk, E, H, I,
-                 ws, nullptr, static_cast<cudaStream_t>(stream));
+                 ws, static_cast<uint8_t*>(ws) + kMoeHeaderBytes, bytes - kMoeHeaderBytes,
+                 nullptr, static_cast<cudaStream_t>(stream));
 }
 
 int q4_moe_experts_trace(float* out, const void* x, int x_dtype, const void* W_gate,
@@ -675,20 +930,12 @@ int q4_moe_experts_trace(float* out, const void* x, int x_dtype, const void* W_g
   int rc = current_state(&s);
   if (rc != Q4_OK) return rc;
   const MoeShape& m = cached_moe_shape(s, T, topk, E, H, I);
-  if (4LL * m.mr * m.rows_gu > kMaxASliceBytes || 4LL * m.mr * m.rows_d > kMaxASliceBytes)
-    return Q4_ERR_SHAPE;
-  if (workspace_bytes < m.total) return Q4_ERR_WORKSPACE;
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  rc = moe_run(s, m, out, x, x_dtype, W_gate, W_up, W_down, topk_idx, topk_w, T, topk, E, H, I,
-               workspace, nullptr, st, g, u);
-  if (rc != Q4_OK) return rc;
-  // h and y are the workspace rows the kernels used
-  const uint8_t* w8 = static_cast<const uint8_t*>(workspace);
-  const size_t n = static_cast<size_t>(T * topk);
-  if (cudaMemcpyAsync(h, w8 + m.off_h, n * I * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(y, w8 + m.off_y, n * H * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-    return Q4_ERR_CUDA;
-  return Q4_OK;
+  if (workspace_bytes < kMoeHeaderBytes + moe_old_data_bytes(T, topk, H, I))
+    return Q4_ERR_WORKSPACE;
+  return moe_run(s, m, out, x, x_dtype, W_gate, W_up, W_down, topk_idx, topk_w, T, topk, E, H, I,
+                 workspace, static_cast<uint8_t*>(workspace) + kMoeHeaderBytes,
+                 workspace_bytes - kMoeHeaderBytes, nullptr, static_cast<cudaStream_t>(stream), g,
+                 u, h, y);
 }
 
 int q4_moe_experts(float* out, const void* x, const void* W_gate, const void* W_up,
@@ -726,7 +973,7 @@ struct BlockLayout {
 bool shared_dense(int64_t T) { return T > 1; }
 BlockLayout block_layout(int64_t T, int64_t topk, int64_t E, int64_t H, int64_t I, int64_t Is) {
   BlockLayout b;
-  size_t o = 0;
+  size_t o = kMoeHeaderBytes;   // the routed-expert counters (both expert calls)
   b.idx = o;
   o += round_up(static_cast<size_t>(T * topk) * 4, 256);
   b.w = o;
@@ -745,9 +992,9 @@ BlockLayout block_layout(int64_t T, int64_t topk, int64_t E, int64_t H, int64_t 
   b.sh = o;
   o += tis;
   b.moe_s = o;
-  o += (Is > 0 && !shared_dense(T)) ? q4_moe_workspace_size(T, 1, 1, H, Is) : 0;
+  o += (Is > 0 && !shared_dense(T)) ? round_up(moe_data_bytes(T, 1, H, Is), 256) : 0;
   b.moe = o;
-  b.total = o + q4_moe_workspace_size(T, topk, E, H, I);
+  b.total = o + moe_data_bytes(T, topk, H, I);
   return b;
 }
 }  // namespace
@@ -779,7 +1026,8 @@ int q4_moe_block(float* out, const void* x, int x_dtype, const float* logits, co
   int rc = current_state(&s);
   if (rc != Q4_OK) return rc;
   const MoeShape& m = cached_moe_shape(s, T, topk, E, H, I);
-  if (4LL * m.mr * m.rows_gu > kMaxASliceBytes || 4LL * m.mr * m.rows_d > kMaxASliceBytes)
+  if (!moe_seq_plan(T, topk, H, I, x_dtype).ok &&
+      (4LL * m.mr * m.rows_gu > kMaxASliceBytes || 4LL * m.mr * m.rows_d > kMaxASliceBytes))
     return Q4_ERR_SHAPE;
   const MoeShape* ms = nullptr;
   if (Is > 0 && !shared_dense(T)) {
@@ -818,10 +1066,12 @@ int q4_moe_block(float* out, const void* x, int x_dtype, const float* logits, co
   // output, one slot per token, is already the shared expert's result
   // ([T, H]): no combine of its own, the routed combine adds it.
   if (Is > 0 && !shared_dense(T)) {
+    const size_t sbytes = moe_data_bytes(T, 1, H, Is);
     rc = moe_run(s, *ms, nullptr, x, x_dtype, S_gate, S_up, S_down, sidx, sw, T, 1, 1, H, Is,
-                 w8 + b.moe_s, nullptr, st);
+                 w8, w8 + b.moe_s, sbytes, nullptr, st);
     if (rc != Q4_OK) return rc;
-    ys = reinterpret_cast<float*>(w8 + b.moe_s + ms->off_y);
+    ys = moe_y_rows(w8 + b.moe_s, *ms, moe_takes_seq(T, 1, H, Is, x_dtype, sbytes), T, 1, H, Is,
+                    x_dtype);
   } else if (Is > 0) {
     float* sg = reinterpret_cast<float*>(w8 + b.sg);
     float* su = reinterpret_cast<float*>(w8 + b.su);
@@ -836,7 +1086,7 @@ int q4_moe_block(float* out, const void* x, int x_dtype, const float* logits, co
   }
   // routed experts; the shared expert's rows are added after the weighted sum
   return moe_run(s, m, out, x, x_dtype, W_gate, W_up, W_down, idx, w, T, topk, E, H, I,
-                 w8 + b.moe, Is > 0 ? ys : nullptr, st);
+                 w8, w8 + b.moe, moe_data_bytes(T, topk, H, I), Is > 0 ? ys : nullptr, st);
 }
 
 }  // extern "C"
@@ -963,10 +1213,10 @@ int q4_gemv_seq_create(const q4_gemv_op* ops, int n, void* buf, size_t buf_bytes
   rc = current_state(&s);
   if (rc != Q4_OK) return rc;
   int stages = 5;
-  int per_sm = q4::seq_ctas_per_sm(stages);
+  int per_sm = q4::seq_ctas_per_sm(stages, false);
   if (per_sm < 2) {
     stages = 4;
-    per_sm = q4::seq_ctas_per_sm(stages);
+    per_sm = q4::seq_ctas_per_sm(stages, false);
   }
   if (per_sm < 1) return Q4_ERR_CUDA;
 

@@ -713,10 +713,14 @@ int max_active_clusters(int mode, int mr, int bpt, bool big, int fmt, int rows_p
     pick_instance<false, kFmtQ4>(mode, mr, bpt, rows_per_split, list_cap, senders, &fn, &smem);
   }
   if (!fn) return 0;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  // a failed query leaves no error pending for the caller's next launch
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    cudaGetLastError();
     return 0;
-  cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  }
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess ||
+      cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    cudaGetLastError();   // tolerated: the query below then counts what fits
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster.x, cluster.y, cluster.z);
   cfg.blockDim = dim3(mr == 1 ? Crew<1>::kThreads : mr == 2 ? Crew<2>::kThreads : Crew<4>::kThreads);

@@ -63,10 +63,12 @@ struct SlotMeta {
   int unit;    // global unit index, -1: end of the sequence
   int op;
   int tile;
-  int flags;   // bit 0: the unit's last stage; bit 1: A is bf16; bit 2: end
-  int k0;      // first row of the stage
+  int flags;   // bit 0: the unit's last stage; bit 1: A is bf16; bit 2: end;
+               // bit 3: the unit's expert index is invalid
+  int k0;      // first row of A of the stage
   int rows;    // rows of the stage below K (1..64)
-  int pad[2];
+  int slice;   // the unit's K slice
+  int seg;     // the unit's segment (0 for unsegmented ops)
 };
 
 struct Smem {
@@ -160,19 +162,72 @@ __device__ __forceinline__ uint32_t a_bulk_bytes(int rows, int a_dtype) {
   return (static_cast<uint32_t>(rows) * es) & ~15u;
 }
 
-// Index of the op holding unit u: the last op whose unit_base <= u.
+// Index of the op holding unit u: the last op whose unit_base <= u.  (With
+// SEG the ops may sit in the kernel's parameters: generic loads.)
+template <bool SEG>
 __device__ __forceinline__ int op_of_unit(const SeqOpDesc* ops, int nops, int u) {
   int lo = 0, hi = nops - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(&ops[mid].unit_base) <= u) lo = mid;
+    if ((SEG ? ops[mid].unit_base : __ldg(&ops[mid].unit_base)) <= u) lo = mid;
     else hi = mid - 1;
   }
   return lo;
 }
 
-template <int STAGES>
-__global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const SeqParams p) {
+// Expert of segment `seg` of op d (0 without an index list; a pair op's
+// segments 2s and 2s + 1 both belong to slot s), and whether it lies in
+// [0, E).
+template <bool SEG>
+__device__ __forceinline__ int seg_expert(const SeqOpDesc& d, int seg, bool& valid) {
+  if (!SEG || !d.eidx) {
+    valid = true;
+    return 0;
+  }
+  const int e = __ldcg(d.eidx + (d.pair ? (seg >> 1) : seg));
+  valid = (e >= 0 && e < d.E);
+  return e;
+}
+
+// Tile and K slice of unit `local` (0-based within op d): tile-major.
+__device__ __forceinline__ void unit_coords(const SeqOpDesc& d, int local, int& tile, int& slice) {
+  tile = local / d.nslices;
+  slice = local - tile * d.nslices;
+}
+
+// Output columns of tile `tile` of op d: the segment it belongs to, its first
+// column within the segment, the segment's width, and where the segment's
+// row of C starts (a pair op's odd segments go to C2).
+struct TileCols {
+  int seg, c0, width;
+  size_t row;   // element offset of the segment's row in `out`
+  void* out;
+};
+template <bool SEG>
+__device__ __forceinline__ TileCols tile_cols(const SeqOpDesc& d, int tile) {
+  TileCols t;
+  if (SEG && d.seg_mode == 1) {
+    t.seg = tile / d.seg_tiles;
+    t.c0 = (tile - t.seg * d.seg_tiles) * kTileCols;
+    t.width = d.seg_len;
+    const int row = d.pair ? (t.seg >> 1) : t.seg;
+    t.row = static_cast<size_t>(row) * d.seg_len;
+    t.out = (d.pair && (t.seg & 1)) ? d.C2 : d.C;
+  } else {
+    t.seg = 0;
+    t.c0 = tile * kTileCols;
+    t.width = d.N;
+    t.row = 0;
+    t.out = d.C;
+  }
+  return t;
+}
+
+// SEG: the ops may be segmented, paired or in the parameters, and the launch
+// may reset its counters; without it, every op is a plain GEMV read from
+// global memory and none of that code is compiled in.
+template <int STAGES, bool SEG>
+__global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const __grid_constant__ SeqParams p) {
   constexpr Smem L = smem_layout<STAGES>();
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem + L.ring;
@@ -204,8 +259,11 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const SeqParam
   }
   __syncthreads();
   // The counters this launch uses were cleared by the stream operation just
-  // before it, and A may come from the kernel before: wait for both.
+  // before it (or by the launch before, `reset`), and A and the expert
+  // indices may come from the kernel before: wait for all of them.
   pdl_wait();
+  pdl_launch_dependents();
+  const SeqOpDesc* ops = (SEG && !p.ops) ? p.inl : p.ops;
 
   if (warp == kConsumerWarps) {
     // ===================== producer: weights =====================
@@ -223,17 +281,31 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const SeqParam
       }
       const int u = static_cast<int>(atomicAdd(p.queue, 1u));
       const bool end = (u >= p.total_units);
-      int op = 0, tile = 0, slice = 0, nst = 1, K = 0, srows = 0;
+      // the unit's weight rows [w0, w0 + urows) of matrix `expert`, columns
+      // from cx (uint16 elements), and its first row of A
+      int op = 0, tile = 0, nst = 1, urows = 0, w0 = 0, a0 = 0, cx = 0, expert = 0;
+      int uslice = 0, useg = 0;
+      bool valid = true, second = false;
       if (!end) {
-        op = op_of_unit(p.ops, p.nops, u);
-        const SeqOpDesc& d = p.ops[op];
-        const int local = u - d.unit_base;
-        tile = local / d.nslices;
-        slice = local - tile * d.nslices;
-        K = d.K;
-        srows = d.slice_rows;
-        const int rows = min(srows, K - slice * srows);
-        nst = (rows + kStageRows - 1) / kStageRows;
+        op = op_of_unit<SEG>(ops, p.nops, u);
+        const SeqOpDesc& d = ops[op];
+        int slice;
+        unit_coords(d, u - d.unit_base, tile, slice);
+        uslice = slice;
+        int seg = 0;
+        const int sl = slice, klen = d.K;
+        const TileCols tc = tile_cols<SEG>(d, tile);
+        if (SEG && d.seg_mode == 1) seg = tc.seg;
+        useg = seg;
+        second = SEG && d.pair && (seg & 1);
+        cx = (tc.c0 / kTileCols) * kTileBlocks * 9;
+        w0 = sl * d.slice_rows;
+        urows = min(d.slice_rows, klen - w0);
+        // the segment's row of A (routed tokens: one row per token)
+        a0 = ((SEG && d.a_seg_div) ? (seg / d.a_seg_div) * d.a_seg_stride : 0) + w0;
+        expert = seg_expert<SEG>(d, seg, valid);
+        if (!valid) atomicOr(p.err, kDevErrIndex);
+        nst = (urows + kStageRows - 1) / kStageRows;
       }
       for (int st = 0; st < nst; ++st, ++gs) {
         const int slot = gs % STAGES;
@@ -251,18 +323,24 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const SeqParam
           posted = gs + 1;
           break;
         }
-        const int k0 = slice * srows + st * kStageRows;
-        const int rows = min(kStageRows, K - k0);
-        const SeqOpDesc& d = p.ops[op];
+        const int rows = min(kStageRows, urows - st * kStageRows);
+        const SeqOpDesc& d = ops[op];
         m.unit = u;
         m.op = op;
         m.tile = tile;
-        m.flags = ((st == nst - 1) ? 1 : 0) | (d.a_dtype == 0 ? 0 : 2);
-        m.k0 = k0;
+        m.flags = ((st == nst - 1) ? 1 : 0) | (d.a_dtype != 0 ? 2 : 0) | (valid ? 0 : 8);
+        m.k0 = a0 + st * kStageRows;
         m.rows = rows;
-        mbar_arrive_expect_tx(&full[slot], kStageBytes + a_bulk_bytes(rows, d.a_dtype));
-        tma_load_3d(ring + slot * kStageBytes, &d.tmap, tile * kTileBlocks * 9, k0, 0,
-                    &full[slot]);
+        m.slice = uslice;
+        m.seg = useg;
+        // a segment with an expert index outside [0, E) reads no weights: its
+        // stages hold stale data and its outputs are not written
+        const uint32_t tx = (valid ? kStageBytes : 0u) + a_bulk_bytes(rows, d.a_dtype);
+        if (tx) mbar_arrive_expect_tx(&full[slot], tx);
+        else mbar_arrive(&full[slot]);
+        if (valid)
+          tma_load_3d(ring + slot * kStageBytes, second ? &d.tmap2 : &d.tmap, cx,
+                      w0 + st * kStageRows, expert, &full[slot]);
         mbar_arrive(&claimed[slot]);
         posted = gs + 1;
       }
@@ -281,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const SeqParam
     fence_proxy_async();
     int gs = 0;
     int verified = -1;   // ops up to this one have their dependencies done
+    int vseg_op = -1, vseg = -1;   // segments up to vseg of op vseg_op have theirs
     bool failed = false; // after a failure: serve the remaining slots unchecked
     while (true) {
       const int slot = gs % STAGES;
@@ -297,14 +376,42 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const SeqParam
         if (lane == 0) mbar_arrive(&full[slot]);
         break;
       }
-      const SeqOpDesc& d = p.ops[m.op];
+      const SeqOpDesc& d = ops[m.op];
+      // a segment waits for its own slot's inputs
+      if (SEG && !failed && d.seg_need > 0 && (m.op != vseg_op || m.seg > vseg)) {
+        int ok = 1;
+        if (lane == 0) {
+          const unsigned long long t0 = globaltimer();
+          const unsigned* c = p.seg_done + ops[d.seg_dep].seg_done_base + m.seg;
+          while (ld_acquire_gpu(c) < static_cast<unsigned>(d.seg_need)) {
+            if (*s_fail || globaltimer() - t0 > kWaitLimitNs) {
+              if (!*s_fail) {
+                *s_fail = 1;
+                atomicOr(p.err, kDevErrTimeout);
+              }
+              ok = 0;
+              break;
+            }
+            __nanosleep(200);
+          }
+          fence_proxy_async();
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();
+        if (ok) {
+          vseg_op = m.op;
+          vseg = m.seg;
+        } else {
+          failed = true;
+        }
+      }
       if (!failed && m.op > verified) {
         int ok = 1;
         if (lane == 0) {
           const unsigned long long t0 = globaltimer();
           for (int i = 0; i < d.ndeps && ok; ++i) {
             const int dep = d.deps[i];
-            const unsigned need = static_cast<unsigned>(p.ops[dep].ntiles);
+            const unsigned need = static_cast<unsigned>(ops[dep].ntiles);
             while (ld_acquire_gpu(&p.done[dep]) < need) {
               if (*s_fail || globaltimer() - t0 > kWaitLimitNs) {
                 if (!*s_fail) {
@@ -324,9 +431,9 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const SeqParam
         if (ok) verified = m.op;
         else failed = true;
       }
+      uint8_t* dst = aring + slot * (kStageRows * kARowBytes);
       const uint32_t es = d.a_dtype == 0 ? 4u : 2u;
       const uint32_t bulk = a_bulk_bytes(m.rows, d.a_dtype);
-      uint8_t* dst = aring + slot * (kStageRows * kARowBytes);
       const uint8_t* src = static_cast<const uint8_t*>(d.A) + static_cast<size_t>(m.k0) * es;
       if (lane == 0 && bulk) bulk_load(dst, src, bulk, &full[slot]);
       // the last few entries below K, then zeros up to the stage's 64 rows
@@ -371,7 +478,23 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const SeqParam
     const int slot = gs % STAGES;
     if (!bounded_wait(&full[slot], (gs / STAGES) & 1, s_fail, p.err)) break;
     const int flags = vmeta[slot].flags;
-    if (flags & 4) break;
+    if (flags & 4) {
+      // the end of the sequence for this CTA: with `reset`, the last CTA to
+      // get here zeroes the counters for the next launch (every producer has
+      // stopped taking units and every tile is complete by then)
+      if (SEG && p.reset && consumers_meet(csync, cphase, s_fail, p.err) && tid == 0) {
+        const unsigned n = atom_add_acq_rel_gpu(p.exits, 1u);
+        if (n == gridDim.x - 1) {
+          *p.queue = 0u;
+          for (int i = 0; i < p.nops; ++i) p.done[i] = 0u;
+          for (int i = 0; i < p.ntickets; ++i) p.tickets[i] = 0u;
+          for (int i = 0; i < p.nseg_done; ++i) p.seg_done[i] = 0u;
+          __threadfence();
+          *p.exits = 0u;
+        }
+      }
+      break;
+    }
     const uint8_t* stage = ring + slot * kStageBytes;
     const uint8_t* as = aring + slot * (kStageRows * kARowBytes);
 #pragma unroll
@@ -393,12 +516,12 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const SeqParam
     }
     // the unit's last stage: its slot is released only once the unit's
     // identity has been read from it
-    const int unit = vmeta[slot].unit;
     const int op = vmeta[slot].op;
     const int tile = vmeta[slot].tile;
+    const int uslice = vmeta[slot].slice;
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
-    const SeqOpDesc& d = p.ops[op];
+    const SeqOpDesc& d = ops[op];
 
     // ---- the unit is complete: reduce over the CTA ----
     finish_acc<1, kBPT, kFmtQ4>(acc, sad);
@@ -449,63 +572,102 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const SeqParam
       colv[i] = s;
     }
     const int nslices = d.nslices;
-    if (nslices == 1) {
+    const TileCols tc = tile_cols<SEG>(d, tile);
+    const bool unit_valid = !SEG || !(flags & 8);
+    const bool pair = SEG && d.pair;
+    // a pair op's tile shares one ticket with its partner (the slot's other
+    // product on the same columns): the last of their slices combines both
+    const int pslot = tc.seg >> 1;
+    const int ptile = pslot * d.seg_tiles + tc.c0 / kTileCols;
+    if (nslices == 1 && !pair) {
       // the unit is the whole tile: store C directly
 #pragma unroll
       for (int i = 0; i < kBPT; ++i) {
-        const int col = tile * kTileCols + tid + 256 * i;
-        if (col < d.N) {
-          if (d.c_dtype == 0) reinterpret_cast<float*>(d.C)[col] = colv[i];
-          else reinterpret_cast<__nv_bfloat16*>(d.C)[col] = __float2bfloat16_rn(colv[i]);
+        const int c = tc.c0 + tid + 256 * i;
+        if (unit_valid && c < tc.width) {
+          const size_t col = tc.row + c;
+          if (d.c_dtype == 0) reinterpret_cast<float*>(tc.out)[col] = colv[i];
+          else reinterpret_cast<__nv_bfloat16*>(tc.out)[col] = __float2bfloat16_rn(colv[i]);
         }
       }
     } else {
       // ---- partial sums of the unit -> global scratch, then the tile's ticket ----
-      float* part = p.part + static_cast<size_t>(unit) * kTileCols;
+      // (partial rows are kept tile by tile, slice by slice, whatever the
+      // order in which the units are handed out)
+      const float* base =
+          p.part + static_cast<size_t>(d.unit_base + tile * nslices) * kTileCols;
+      float* part = const_cast<float*>(base) + static_cast<size_t>(uslice) * kTileCols;
 #pragma unroll
       for (int i = 0; i < kBPT; ++i) __stcg(part + tid + 256 * i, colv[i]);
       if (!consumers_meet(csync, cphase, s_fail, p.err)) break;
       if (tid == 0) {
         // every consumer's partial store is ordered before this by the meet
-        const unsigned t = atom_add_acq_rel_gpu(&p.tickets[d.ticket_base + tile], 1u);
-        *s_last = (t == static_cast<unsigned>(nslices - 1)) ? 1 : 0;
+        const int ti = pair ? ptile : tile;
+        const unsigned need = static_cast<unsigned>(pair ? 2 * nslices : nslices);
+        const unsigned t = atom_add_acq_rel_gpu(&p.tickets[d.ticket_base + ti], 1u);
+        *s_last = (t == need - 1u) ? 1 : 0;
       }
       if (!consumers_meet(csync, cphase, s_fail, p.err)) break;
       if (!*s_last) continue;
-      // every slice of the tile has written its partial: add them in slice order
-      const float* base =
-          p.part + static_cast<size_t>(d.unit_base + tile * nslices) * kTileCols;
-      float sums[kBPT];
+      // every slice has written its partial: add them in slice order
+      {
+        // the tile's sum (a pair: both products' sums, then h = SiLU(g) * u)
+        const int t0 = pair ? (2 * pslot) * d.seg_tiles + tc.c0 / kTileCols : tile;
+        const float* b0 = p.part + static_cast<size_t>(d.unit_base + t0 * nslices) * kTileCols;
+        const float* b1 = b0 + static_cast<size_t>(d.seg_tiles) * nslices * kTileCols;
+        const int nsum = pair ? 2 : 1;
+        float sums[2][kBPT];
 #pragma unroll
-      for (int i = 0; i < kBPT; ++i) sums[i] = 0.f;
-      // the loads of a batch are independent, so their L2 latencies overlap;
-      // the additions keep slice order
-      constexpr int kBatch = 8;
-      for (int sl0 = 0; sl0 < nslices; sl0 += kBatch) {
-        float v[kBPT][kBatch];
+        for (int i = 0; i < kBPT; ++i) sums[0][i] = sums[1][i] = 0.f;
+        constexpr int kBatch = 8;
+        for (int sl0 = 0; sl0 < nslices; sl0 += kBatch) {
+          float v[2][kBPT][kBatch];
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b)
+          for (int q = 0; q < 2; ++q)
 #pragma unroll
-          for (int i = 0; i < kBPT; ++i)
-            v[i][b] = (sl0 + b < nslices)
-                          ? __ldcg(base + static_cast<size_t>(sl0 + b) * kTileCols + tid + 256 * i)
-                          : 0.f;
+            for (int b = 0; b < kBatch; ++b)
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b)
+              for (int i = 0; i < kBPT; ++i)
+                v[q][i][b] = (q < nsum && sl0 + b < nslices)
+                                 ? __ldcg((q ? b1 : b0) + static_cast<size_t>(sl0 + b) * kTileCols +
+                                          tid + 256 * i)
+                                 : 0.f;
 #pragma unroll
-          for (int i = 0; i < kBPT; ++i)
-            if (sl0 + b < nslices) sums[i] = (sl0 + b == 0) ? v[i][b] : sums[i] + v[i][b];
-      }
+          for (int q = 0; q < 2; ++q)
 #pragma unroll
-      for (int i = 0; i < kBPT; ++i) {
-        const int c = tid + 256 * i;
-        const int col = tile * kTileCols + c;
-        const float sum = sums[i];
-        if (col < d.N) {
-          if (d.c_dtype == 0) reinterpret_cast<float*>(d.C)[col] = sum;
-          else reinterpret_cast<__nv_bfloat16*>(d.C)[col] = __float2bfloat16_rn(sum);
+            for (int b = 0; b < kBatch; ++b)
+#pragma unroll
+              for (int i = 0; i < kBPT; ++i)
+                if (sl0 + b < nslices)
+                  sums[q][i] = (sl0 + b == 0) ? v[q][i][b] : sums[q][i] + v[q][i][b];
+        }
+#pragma unroll
+        for (int i = 0; i < kBPT; ++i) {
+          const int c = tc.c0 + tid + 256 * i;
+          if (unit_valid && c < tc.width) {
+            const size_t col = tc.row + c;
+            if (pair) {
+              const float g = sums[0][i], u = sums[1][i];
+              reinterpret_cast<float*>(d.C)[col] = g;
+              reinterpret_cast<float*>(d.C2)[col] = u;
+              d.h[col] = g / (1.0f + __expf(-g)) * u;
+            } else if (d.c_dtype == 0) {
+              reinterpret_cast<float*>(tc.out)[col] = sums[0][i];
+            } else {
+              reinterpret_cast<__nv_bfloat16*>(tc.out)[col] = __float2bfloat16_rn(sums[0][i]);
+            }
+          }
         }
       }
+    }
+    if (pair) {
+      // the slot's h is stored on these columns: count them for the slot
+      if (!consumers_meet(csync, cphase, s_fail, p.err)) break;
+      if (tid == 0) {
+        red_add_release_gpu(&p.seg_done[d.seg_done_base + pslot], 1u);
+        red_add_release_gpu(&p.done[op], 2u);
+      }
+      continue;
     }
     // the tile's C is stored: count it for the op (after every thread's stores)
     if (!consumers_meet(csync, cphase, s_fail, p.err)) break;
@@ -518,13 +680,19 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const SeqParam
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-int seq_ctas_per_sm(int stages) {
-  const void* fn = stages == 4 ? (const void*)seq::q4_gemv_seq_kernel<4>
-                               : (const void*)seq::q4_gemv_seq_kernel<5>;
+int seq_ctas_per_sm(int stages, bool seg) {
+  const void* fn = stages == 4 ? (seg ? (const void*)seq::q4_gemv_seq_kernel<4, true>
+                                      : (const void*)seq::q4_gemv_seq_kernel<4, false>)
+                               : (seg ? (const void*)seq::q4_gemv_seq_kernel<5, true>
+                                      : (const void*)seq::q4_gemv_seq_kernel<5, false>);
   const uint32_t smem = stages == 4 ? seq::smem_layout<4>().total : seq::smem_layout<5>().total;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  // a failed call leaves no error pending for the caller's next launch
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    cudaGetLastError();
     return 0;
-  cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  }
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+    cudaGetLastError();   // tolerated: the occupancy query below counts what fits
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, seq::kThreads, smem) != cudaSuccess) {
     cudaGetLastError();
@@ -538,17 +706,27 @@ int seq_stage_rows() { return seq::kStageRows; }
 int seq_max_slice_rows() { return seq::kMaxSliceStages * seq::kStageRows; }
 int seq_default_slice_rows() { return seq::kDefaultSliceStages * seq::kStageRows; }
 
-cudaError_t launch_gemv_seq(const SeqParams& p, int grid, int stages, cudaStream_t st) {
+cudaError_t launch_gemv_seq(const SeqParams& p, int grid, int stages, cudaStream_t st,
+                            bool pdl, bool seg) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(seq::kThreads);
   cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
   if (stages == 4) {
     cfg.dynamicSmemBytes = seq::smem_layout<4>().total;
-    return cudaLaunchKernelEx(&cfg, seq::q4_gemv_seq_kernel<4>, p);
+    return seg ? cudaLaunchKernelEx(&cfg, seq::q4_gemv_seq_kernel<4, true>, p)
+               : cudaLaunchKernelEx(&cfg, seq::q4_gemv_seq_kernel<4, false>, p);
   }
   cfg.dynamicSmemBytes = seq::smem_layout<5>().total;
-  return cudaLaunchKernelEx(&cfg, seq::q4_gemv_seq_kernel<5>, p);
+  return seg ? cudaLaunchKernelEx(&cfg, seq::q4_gemv_seq_kernel<5, true>, p)
+             : cudaLaunchKernelEx(&cfg, seq::q4_gemv_seq_kernel<5, false>, p);
 }
 
 }  // namespace q4

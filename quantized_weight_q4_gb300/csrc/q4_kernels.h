@@ -92,38 +92,80 @@ cudaError_t launch_moe_combine(float* out, const float* y, const int32_t* idx, c
                                cudaStream_t st, bool pdl);
 
 // q4_gemv_seq.cu: a sequence of M = 1 GEMVs in one persistent launch.
-// One op of the sequence, as the kernel reads it from global memory.
-struct SeqOpDesc {      // 64-byte aligned through its tensor map
-  CUtensorMap tmap;     // weights: uint16 [1][K][nb*9], boxes of 144 x 64
-  const void* A;        // [K], fp32 (a_dtype 0) or bf16 (1)
+// One op of the sequence, as the kernel reads it from global memory (a plan)
+// or from its parameters (inline ops).
+//
+// An op may be segmented over the slots of routed tokens (segmented along
+// its output columns): segment s holds the product A_s . W[eidx[s]] in
+// C[s] (seg_len columns, seg_tiles column tiles), the expert eidx[s] picking
+// the matrix of a tensor map over E experts, and A_s = A + (s / a_seg_div) *
+// a_seg_stride.  With `pair`, segments 2s and 2s + 1 are slot s's products
+// with the matrices of tmap (into C[s]) and tmap2 (into C2[s]); one ticket
+// serves both tiles of a column, and the last of their K slices adds both
+// products, stores them and h[s] = SiLU(C[s]) * C2[s] on those columns, and
+// counts the column tile in seg_done[seg_done_base + s].  With seg_need > 0,
+// segment s reads A only once op seg_dep's seg_done[.. + s] has reached
+// seg_need (a zeroed descriptor has no such dependency).  Segments whose index lies outside [0, E) read no weights and
+// write nothing.
+struct SeqOpDesc {      // 64-byte aligned through its tensor maps
+  CUtensorMap tmap;     // weights: uint16 [E][K][nb*9], boxes of 144 x 64
+  CUtensorMap tmap2;    // pair: the second matrices
+  const void* A;        // [K] (or per segment, see a_seg_div), fp32 (a_dtype 0) or bf16 (1)
   void* C;              // [N], fp32 (c_dtype 0) or bf16 (1)
-  int K, N, nb;
+  void* C2;             // pair: the second products, fp32 [nseg / 2][seg_len]
+  float* h;             // pair: SiLU(C) * C2, fp32 [nseg / 2][seg_len]
+  const int32_t* eidx;  // expert of each slot, or null (matrix 0)
+  int K, N, nb;         // the op's K and N (segmented: N = nseg x seg_len)
   int ntiles, nslices;  // column tiles of 512 columns, K slices of slice_rows rows
   int slice_rows;       // a multiple of 64, at most 4096
   int unit_base;        // first unit of the op (units: tile-major, slice-minor)
   int ticket_base;      // first tile counter of the op
   int a_dtype, c_dtype;
+  int seg_mode;         // 0: none; 1: segmented along N
+  int nseg, seg_len;    // segments, and columns of each
+  int seg_tiles;        // column tiles per segment
+  int a_seg_div;        // segments per row of A (0: one A for all segments)
+  int a_seg_stride;     // elements between rows of A
+  int pair;             // segments form (tmap, tmap2) pairs of one slot
+  int seg_done_base;    // pair: first per-slot counter in seg_done
+  int seg_dep, seg_need;// per-segment dependency on op seg_dep (seg_need 0: none)
+  int E;                // experts of the tensor maps (valid eidx values: [0, E))
   int ndeps;
   int deps[4];          // earlier ops whose outputs must be complete before A is read
 };
+constexpr int kSeqInlineOps = 2;
 struct SeqParams {
-  const SeqOpDesc* ops;
+  const SeqOpDesc* ops; // the ops in global memory, or null: the inline ops below
   int nops, total_units;
   unsigned* queue;      // unit counter (zero at launch)
   unsigned* done;       // [nops] completed tiles per op (zero at launch)
-  unsigned* tickets;    // [total tiles] slices added per tile (zero at launch)
+  unsigned* tickets;    // [ntickets] slices added per tile (pairs: per tile pair) (zero at launch)
+  unsigned* seg_done;   // [nseg_done] completed column tiles per slot of pair ops (zero at launch)
+  unsigned* exits;      // reset != 0: CTAs finished (zero at launch)
+  int ntickets, nseg_done;
+  int reset;            // nonzero: the last CTA to finish zeroes the counters
   float* part;          // [total_units][512] partial sums
   unsigned* err;        // device status word
   uint32_t kmask[4];    // nibble masks (fill as for the GEMV)
+  SeqOpDesc inl[kSeqInlineOps];
 };
+// q4_capi.cu: the least workspace a routed-expert call of this shape takes
+// (the counter header and the three-launch form's rows); calls with more may
+// run the persistent form.
+size_t moe_min_workspace_bytes(int64_t T, int64_t topk, int64_t H, int64_t I);
 // CTAs per SM that the persistent kernel with `stages` ring slots (4 or 5)
 // can keep resident (0 if it cannot launch).
-int seq_ctas_per_sm(int stages);
+int seq_ctas_per_sm(int stages, bool seg);   // seg: the segmented instance
 int seq_tile_cols();       // columns of a unit (512)
 int seq_stage_rows();      // rows of one pipeline stage (64)
 int seq_max_slice_rows();      // rows of the longest unit (4096)
 int seq_default_slice_rows();  // rows of a unit by default (512)
-cudaError_t launch_gemv_seq(const SeqParams& p, int grid, int stages, cudaStream_t st);
+// `pdl`: launched with programmatic stream serialization (the kernel waits
+// for the previous grid before touching memory).
+// seg: the instance for segmented or inline ops and counter resets; without
+// it, the ops must be plain GEMVs in global memory and `reset` zero.
+cudaError_t launch_gemv_seq(const SeqParams& p, int grid, int stages, cudaStream_t st,
+                            bool pdl = false, bool seg = false);
 
 // q4_gemm_sm103.cu: the prefill GEMM on the tensor cores.
 struct GemmParams {

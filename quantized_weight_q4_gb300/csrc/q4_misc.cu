@@ -84,6 +84,7 @@ cudaError_t launch_dequant(void* W, int w_dtype, const uint8_t* B, int64_t K, in
                            cudaStream_t st) {
   const int64_t nb = (N + kBlockCols - 1) / kBlockCols;
   const unsigned g = grid_for(K * nb);
+  (void)cudaGetLastError();   // report this launch's error, not an earlier one's
   if (w_dtype == 0)
     q4_dequant_kernel<false><<<g, 256, 0, st>>>(W, B, K, N, nb);
   else
@@ -97,6 +98,7 @@ cudaError_t launch_repack(uint8_t* dst, const uint8_t* src, int64_t K, int64_t N
   const int64_t nblk = K * nb;
   const int64_t qs_off = (nblk * 2 + 15) / 16 * 16;
   const unsigned g = grid_for(nblk);
+  (void)cudaGetLastError();   // report this launch's error, not an earlier one's
   if (to_planar)
     q4_repack_kernel<true><<<g, 256, 0, st>>>(dst, src, nblk, qs_off);
   else
@@ -177,6 +179,7 @@ cudaError_t launch_quantize(uint8_t* B, const void* W, int w_dtype, int64_t K, i
   const int64_t nblk = K * nb;
   int64_t grid = (nblk + 255) / 256;
   if (grid > 65536) grid = 65536;
+  (void)cudaGetLastError();   // report this launch's error, not an earlier one's
   if (w_dtype == 1)
     q4_quantize_kernel<true><<<static_cast<unsigned>(grid), 256, 0, st>>>(B, W, K, N, nb);
   else
@@ -207,6 +210,7 @@ __global__ void __launch_bounds__(32) q4_wait_selftest_kernel(unsigned* err,
 
 cudaError_t launch_wait_selftest(unsigned* err, unsigned long long limit_ns, bool arrive,
                                  cudaStream_t st) {
+  (void)cudaGetLastError();   // report this launch's error, not an earlier one's
   q4_wait_selftest_kernel<<<1, 32, 0, st>>>(err, limit_ns, arrive ? 1 : 0);
   return cudaGetLastError();
 }

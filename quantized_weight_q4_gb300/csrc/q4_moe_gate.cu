@@ -91,6 +91,7 @@ cudaError_t launch_moe_gate(int32_t* topk_idx, float* topk_w, const float* logit
                             int topk, int32_t* shared_idx, float* shared_w, cudaStream_t st) {
   const int warps = 4;
   const int grid = (T + warps - 1) / warps;
+  (void)cudaGetLastError();   // report this launch's error, not an earlier one's
   q4_moe_gate_kernel<<<grid, warps * 32, 0, st>>>(topk_idx, topk_w, logits, T, E, topk,
                                                   shared_idx, shared_w);
   return cudaGetLastError();

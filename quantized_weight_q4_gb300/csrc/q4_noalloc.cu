@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include "q4.h"
+#include "q4_kernels.h"
 
 namespace {
 
@@ -54,7 +55,8 @@ int q4_moe_experts_noalloc(float* out, const void* x, int x_dtype, const void* W
                            const float* topk_w, int64_t T, int64_t topk, int64_t E, int64_t H,
                            int64_t I, void* stream) {
   if (T <= 0 || topk <= 0 || E <= 0 || H <= 0 || I <= 0) return Q4_ERR_ARG;
-  const size_t need = q4_moe_workspace_size(T, topk, E, H, I);
+  // the least the call takes; with the 8 MiB it may not take the persistent form
+  const size_t need = q4::moe_min_workspace_bytes(T, topk, H, I);
   if (need > kStaticScratchBytes) return Q4_ERR_WORKSPACE;
   void* scratch = nullptr;
   const int rc = static_scratch(&scratch);

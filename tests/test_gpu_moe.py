@@ -143,7 +143,7 @@ def test_moe_captured_on_a_fresh_stream_equals_eager(T):
     topk, E, H, I = 3, 6, 512, 96
     x, Wg, Wu, Wd, idx, w = make(T, topk, E, H, I, seed=20 + T)
     d = [to_dev(a) for a in (x, Wg, Wu, Wd, idx, w)]
-    ws = torch.empty(q4.q4_moe_workspace_size(T, topk, E, H, I), dtype=torch.uint8,
+    ws = torch.zeros(q4.q4_moe_workspace_size(T, topk, E, H, I), dtype=torch.uint8,
                      device=device())
     s = torch.cuda.Stream()
     cap = torch.empty((T, H), dtype=torch.float32, device=device())

@@ -36,7 +36,7 @@ U = 2.0 ** -24
 def trace(x, dW, idx, w, T, topk, E, H, I):
     f = lambda *s: torch.full(s, float("nan"), dtype=torch.float32, device=device())
     out, g, u, h, y = f(T, H), f(T * topk, I), f(T * topk, I), f(T * topk, I), f(T * topk, H)
-    ws = torch.empty(q4.q4_moe_workspace_size(T, topk, E, H, I), dtype=torch.uint8,
+    ws = torch.zeros(q4.q4_moe_workspace_size(T, topk, E, H, I), dtype=torch.uint8,
                      device=device())
     q4.q4_moe_experts_trace(out, to_dev(x), *dW, to_dev(idx), to_dev(w), T, topk, E, H, I,
                             ws, g, u, h, y)

@@ -40,7 +40,7 @@ def test_noalloc_matches_workspace_entry_point():
     assert q4.q4_moe_workspace_size(T, topk, E, H, I) <= L.q4_moe_static_scratch_bytes()
 
     ref = torch.empty((T, H), dtype=torch.float32, device=device())
-    ws = torch.empty(q4.q4_moe_workspace_size(T, topk, E, H, I), dtype=torch.uint8,
+    ws = torch.zeros(q4.q4_moe_workspace_size(T, topk, E, H, I), dtype=torch.uint8,
                      device=device())
     q4.q4_moe_experts_ex(ref, dx, dg, du, dd, di, dw, T, topk, E, H, I, workspace=ws)
     torch.cuda.synchronize()
