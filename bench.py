@@ -767,12 +767,16 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
         per_copy = wbytes + M * K * 2 + M * N * 2
         copies = max(1, -(-4 * l2 // per_copy))   # >= 4x L2 of distinct A, B and C per pass
         fns, keep = [], []
+        # the workspace carries the last round's shared-K partial tiles (one
+        # workspace serves the calls in turn: each leaves its tickets zero)
+        wsz = q4.q4_matmul_workspace_size(M, N, K)
+        wspace = torch.zeros(max(wsz, 1), dtype=torch.uint8, device=dev)
         for i in range(copies):
             B = to_dev(si.q4_weights(K, N, seed=0, stream=700 + i))
             A = to_dev(si.activations_bf16(M, K, 0, 800 + i).view(np.int16)).view(torch.bfloat16)
             C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             keep += [A, B, C]
-            fns.append(lambda C=C, A=A, B=B: q4.q4_matmul_ex(C, A, B, M, N, K))
+            fns.append(lambda C=C, A=A, B=B: q4.q4_matmul_ex(C, A, B, M, N, K, workspace=wspace))
         g = GraphOf(torch, fns)
         barrier(ws)
         with ClockSampler(local) as clk:

@@ -92,9 +92,13 @@ Q4_API int q4_matmul(float *C, const float *A, const void *B, int64_t M, int64_t
  *              GEMV on the same values, so C is bit-identical to the
  *              Q4_LAYOUT_BLOCKS result for the same shape
  *   workspace  may be NULL.  Shapes whose tensor-core GEMM splits K over
- *              independent CTAs (bf16 A, 8 <= M <= 40) add the splits'
- *              partial tiles through scratch: q4_matmul_workspace_size(M, N,
- *              K) bytes of it (0 for every other shape).  A workspace of at
+ *              independent CTAs (bf16 A, 8 <= M <= 40; and M > 128 when the
+ *              256 x 256 tiles leave a last round that does not fill the
+ *              SMs: its tiles' K steps are then shared by up to four CTAs
+ *              per tile) add the splits' partial tiles through scratch:
+ *              q4_matmul_workspace_size(M, N, K) bytes of it (0 for every
+ *              other shape; about 38 MB for M = 2048, K = 5120, N = 12288
+ *              on 152 SMs).  A workspace of at
  *              least that size is used for it; its bytes must be zero before
  *              the first call that uses them and every completed call leaves
  *              them zero (zero it again after a Q4_ERR_DEVICE status).  With
@@ -103,7 +107,8 @@ Q4_API int q4_matmul(float *C, const float *A, const void *B, int64_t M, int64_t
  *              replaced by a larger one when a later call needs more, after
  *              that stream has drained), and a call made while the stream is
  *              captured into a CUDA graph combines the splits on chip
- *              instead, so that no graph holds library-owned scratch.
+ *              (M > 128: runs every tile over all of K) instead, so that no
+ *              graph holds library-owned scratch.
  *              Calls that share one workspace must not overlap on the GPU;
  *              that includes replays of graphs captured with it.
  *   stream     cudaStream_t (NULL = legacy default stream)
@@ -140,8 +145,9 @@ Q4_API int q4_matmul_ex(void *C, int c_dtype, const void *A, int a_dtype,
                  void *workspace, size_t workspace_bytes, void *stream);
 
 /* Bytes of workspace q4_matmul_ex and q4_matmul_bf16_tiles use for this shape
- * (the partial tiles of the small-M tensor-core form, bf16 A; 0 for shapes
- * that need none).  0 also when no CUDA device can be queried. */
+ * (the partial tiles of the small-M tensor-core form and of the prefill
+ * form's shared last round, bf16 A; 0 for shapes that need none).  0 also
+ * when no CUDA device can be queried. */
 Q4_API size_t q4_matmul_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*
@@ -159,8 +165,12 @@ Q4_API size_t q4_matmul_workspace_size(int64_t M, int64_t N, int64_t K);
  * workspace returns Q4_ERR_SHAPE below 8 rows and takes the split form from
  * 8.  32 < M <= 128 splits K over 2..16 CTAs per 128 x 256 tile, combined in
  * fixed order over a cluster or, up to 40 rows, through the workspace;
- * M > 128 runs the persistent prefill form (256 x 256 output tiles).
- * Deterministic.
+ * M > 128 runs the persistent prefill form (256 x 256 output tiles, one
+ * CTA per SM taking tiles round-robin; the tiles of an incomplete last round
+ * share their K steps over the grid through the workspace, the part holding
+ * a tile's first K step adding the others' partial tiles in K order).
+ * Deterministic: the parts and their order depend only on the shape and the
+ * SM count.
  */
 Q4_API int q4_matmul_bf16_tiles(void *C, int c_dtype, const void *A, const void *B,
                                 int64_t M, int64_t N, int64_t K, void *workspace,

@@ -780,6 +780,25 @@ int gemm_run(DeviceState* s, void* C, int c_dtype, const void* A, const void* B,
              int64_t N, int64_t K, void* workspace, size_t workspace_bytes, cudaStream_t st) {
   float* part = nullptr;
   unsigned* tickets = nullptr;
+  if (M > 128) {
+    // prefill form: the last round's tiles share K over the grid when the
+    // tail's tickets and partial tiles are at hand (the caller's workspace,
+    // else the stream's library scratch for an eager call)
+    const q4::PrefillPlan pl = q4::prefill_plan(M, N, K, s->sms);
+    const size_t need = q4::prefill_tail_bytes(pl);
+    if (need > 0) {
+      const size_t tb = q4::prefill_tail_ticket_bytes(pl);
+      if (workspace && workspace_bytes >= need) {
+        tickets = static_cast<unsigned*>(workspace);
+        part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + tb);
+      } else if (!gemm_scratch(s, st, need - tb, &part, &tickets)) {
+        part = nullptr;
+        tickets = nullptr;
+      }
+    }
+    return launch_status(
+        q4::launch_gemm(C, c_dtype, A, B, M, N, K, s->status, s->sms, st, part, tickets));
+  }
   const int sg = q4::gemm_global_split(M, N, K, s->sms);
   if (sg > 0) {
     const size_t tb = gemm_ticket_bytes(N);
@@ -809,6 +828,7 @@ size_t q4_matmul_workspace_size(int64_t M, int64_t N, int64_t K) {
     return S > 1 ? gemm_ticket_bytes(N) + q4::skinny_part_bytes(M, N, S) : 0;
   }
   if (!gemm_shape_ok(M, N, K)) return 0;
+  if (M > 128) return q4::prefill_tail_bytes(q4::prefill_plan(M, N, K, s->sms));
   const int sg = q4::gemm_global_split(M, N, K, s->sms);
   if (sg <= 0) return 0;
   return gemm_ticket_bytes(N) + q4::gemm_part_bytes(M, N, sg);

@@ -30,6 +30,27 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   return t;
 }
 
+// ---- GPU-scope acquire / release between CTAs ----------------------------
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// ticket = *p; *p += 1, with release semantics for this thread's earlier
+// writes and those ordered before them (cumulative), and acquire semantics
+// for its later reads, at GPU scope: one round trip, no full fences.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+// *p += 1 with release semantics at GPU scope; nothing is returned, so the
+// thread does not wait for the round trip.
+__device__ __forceinline__ void red_add_release_gpu(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // ---- mbarrier -------------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -154,13 +154,25 @@ __device__ __forceinline__ void store_group4(const GemmParams& p, int row, int c
 }
 
 // A unit of work: one output tile (rows m0.., columns n0..) over K steps
-// [kb, ke) of BK rows.
+// [kb, ke) of BK rows.  Prefill form: `role` 0 stores the tile; in the tail,
+// 1 is the part holding the tile's first K step (it adds the later parts,
+// those of CTAs [c1, c1 + nc), and stores), 2 a later part (it writes its
+// partial tile for that one).
 struct Work {
   int m0, n0, kb, ke;
+  int role, c1, nc;
 };
 
+// Start of the tail's part c: the tail's K steps [0, T) cut into `parts`
+// equal ranges.
+__device__ __forceinline__ int64_t tail_start(int64_t T, int parts, int c) {
+  return static_cast<int64_t>(c) * T / parts;
+}
+
 // The it-th unit of this CTA (false when there is none).  Prefill: tiles
-// blockIdx.x, blockIdx.x + gridDim.x, ... over all K.  Split: the one tile of
+// blockIdx.x, blockIdx.x + gridDim.x, ... below full_tiles over all K, then
+// the pieces of this CTA's range of the tail, one per tile it crosses (at
+// most two: a range is never longer than a tile).  Split: the one tile of
 // the cluster, this CTA's share of K (cluster rank = blockIdx.x % S).
 template <int MT, bool SPLIT>
 __device__ __forceinline__ bool work_item(const GemmParams& p, int it, Work& w) {
@@ -169,6 +181,9 @@ __device__ __forceinline__ bool work_item(const GemmParams& p, int it, Work& w) 
   const int tiles_n = (p.N + BN - 1) / BN;
   const int ksteps = (p.K + BK - 1) / BK;
   int tile;
+  w.role = 0;
+  w.c1 = 0;
+  w.nc = 0;
   if (SPLIT) {
     if (it > 0) return false;
     tile = blockIdx.x / p.nsplit;
@@ -176,15 +191,143 @@ __device__ __forceinline__ bool work_item(const GemmParams& p, int it, Work& w) 
     w.kb = s * ksteps / p.nsplit;
     w.ke = (s + 1) * ksteps / p.nsplit;
   } else {
-    tile = blockIdx.x + it * gridDim.x;
-    w.kb = 0;
-    w.ke = ksteps;
+    const int c = blockIdx.x, G = gridDim.x;
+    const int mine = p.full_tiles > c ? (p.full_tiles - c + G - 1) / G : 0;
+    if (it < mine) {
+      tile = c + it * G;
+      w.kb = 0;
+      w.ke = ksteps;
+    } else {
+      if (c >= p.tail_ctas) return false;
+      const int64_t T = static_cast<int64_t>(tiles_m * tiles_n - p.full_tiles) * ksteps;
+      const int64_t lo = tail_start(T, p.tail_ctas, c), hi = tail_start(T, p.tail_ctas, c + 1);
+      const int64_t t = lo / ksteps + (it - mine);   // tile of the tail
+      const int64_t t0 = t * ksteps;
+      if (lo >= hi || t0 >= hi) return false;
+      w.kb = static_cast<int>(max(lo, t0) - t0);
+      w.ke = static_cast<int>(min(hi, t0 + ksteps) - t0);
+      tile = p.full_tiles + static_cast<int>(t);
+      if (w.kb > 0) {
+        w.role = 2;
+      } else if (w.ke < ksteps) {
+        // the parts of CTAs c + 1 .. that start inside this tile
+        w.role = 1;
+        w.c1 = c + 1;
+        int e = c + 1;
+        while (e < p.tail_ctas && tail_start(T, p.tail_ctas, e) < t0 + ksteps) ++e;
+        w.nc = e - w.c1;
+      }
+    }
   }
   if (tile >= tiles_m * tiles_n) return false;
   w.m0 = (tile % tiles_m) * kBM;
   w.n0 = (tile / tiles_m) * BN;
   return true;
 }
+
+// Prefill tail: the partial tile of CTA c's part, the tensor-memory image of
+// 128 lanes x cols fp32 stored as float4 [cols / 32][8][128]: element (lane
+// r, column c + 4j + i) of 32-column chunk c at float4 (c / 32 * 8 + j) * 128
+// + r, component i, so that a warp's 32 lanes (consecutive rows) move 512
+// contiguous bytes per access.
+__device__ __forceinline__ float4* tail_slot(const GemmParams& p, int c, int cols) {
+  return reinterpret_cast<float4*>(p.part + static_cast<size_t>(c) * 128 * cols);
+}
+
+// Waits (bounded, one thread) until the parts of CTAs [c1, c1 + nc) have
+// released their partial tiles.  On a timeout it marks the CTA failed and
+// records Q4_DEVERR_TIMEOUT.
+__device__ __forceinline__ bool wait_parts(const GemmParams& p, int c1, int nc,
+                                           volatile int* fail) {
+  const unsigned long long t0 = globaltimer();
+  for (int i = 0; i < nc; ++i) {
+    while (ld_acquire_gpu(&p.tickets[c1 + i]) == 0u) {
+      if (*fail || globaltimer() - t0 > kWaitLimitNs) {
+        if (!*fail) {
+          *fail = 1;
+          atomicOr(p.err, kDevErrTimeout);
+        }
+        return false;
+      }
+      __nanosleep(256);
+    }
+  }
+  return true;
+}
+
+// acc (32 accumulators of lane `r`, tensor-memory columns c .. c+31, fp32
+// bits) += the partials of CTAs c1, c1 + 1, ... in that order (K order).
+template <int COLS>
+__device__ __forceinline__ void add_parts(const GemmParams& p, int c1, int nc, int r, int c,
+                                          uint32_t (&acc)[32]) {
+  for (int i = 0; i < nc; ++i) {
+    const float4* src = tail_slot(p, c1 + i, COLS) + (c / 32) * 8 * 128 + r;
+    float4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + j * 128);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      acc[4 * j] = __float_as_uint(__uint_as_float(acc[4 * j]) + v[j].x);
+      acc[4 * j + 1] = __float_as_uint(__uint_as_float(acc[4 * j + 1]) + v[j].y);
+      acc[4 * j + 2] = __float_as_uint(__uint_as_float(acc[4 * j + 2]) + v[j].z);
+      acc[4 * j + 3] = __float_as_uint(__uint_as_float(acc[4 * j + 3]) + v[j].w);
+    }
+  }
+}
+
+// 16 bytes global -> shared, asynchronous, through L2 only (cp.async.cg).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// The first part of a tail tile, TMA epilogue: one lane's rows of the later
+// parts' partial tiles, staged in shared memory two (chunk, part) pairs ahead
+// of their use, so that the L2 round trips overlap.  Pair k = chunk k / nc of
+// the warp's columns, part k % nc, lands in slot k % 3 of the warp's 12 KB
+// (float4 [3][8][32]); each lane copies and later reads only its own row, so
+// no lane waits for another.  The buffer is the A ring, idle by then: a first
+// part is always its CTA's last unit.
+template <int COLS>
+struct PartPrefetch {
+  const GemmParams& p;
+  float4* buf;
+  int c1, nc, r, lane, chunk0, npairs;
+  __device__ __forceinline__ void issue(int k) {
+    if (k < npairs) {
+      const int ch = k / nc, i = k - ch * nc;
+      const float4* src = tail_slot(p, c1 + i, COLS) + (chunk0 + ch) * 8 * 128 + r;
+      float4* dst = buf + (k % 3) * 256 + lane;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) cp_async16(dst + j * 32, src + j * 128);
+    }
+    cp_async_commit();   // empty groups keep the count of groups uniform
+  }
+  // acc += the later parts' rows of chunk `ch`, in part (K) order
+  __device__ __forceinline__ void add(int ch, uint32_t (&acc)[32]) {
+    for (int i = 0; i < nc; ++i) {
+      const int k = ch * nc + i;
+      issue(k + 2);
+      cp_async_wait<2>();   // pair k has landed
+      const float4* src = buf + (k % 3) * 256 + lane;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 v = src[j * 32];
+        acc[4 * j] = __float_as_uint(__uint_as_float(acc[4 * j]) + v.x);
+        acc[4 * j + 1] = __float_as_uint(__uint_as_float(acc[4 * j + 1]) + v.y);
+        acc[4 * j + 2] = __float_as_uint(__uint_as_float(acc[4 * j + 2]) + v.z);
+        acc[4 * j + 3] = __float_as_uint(__uint_as_float(acc[4 * j + 3]) + v.w);
+      }
+    }
+  }
+};
 
 // ---------------------------------------------------------------------------
 template <int MT, int DW, bool SPLIT>
@@ -350,6 +493,31 @@ __global__ void __launch_bounds__(Cfg<MT, DW, SPLIT>::kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       if (SPLIT) break;   // the split form's epilogue follows below
+      if (w.role == 2) {
+        // ---- a later part of a tail tile: its partial tile, released once
+        //      every warp's stores are done (after the meet below) ----
+        float4* slot = tail_slot(p, blockIdx.x, C::kTmemCols);
+        const int c0 = (wd >> 2) * C::kEpiCols;
+        const int r = q * 32 + lane;
+#pragma unroll 1
+        for (int c = c0; c < c0 + C::kEpiCols; c += 32) {
+          uint32_t acc[32];
+          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, acc);
+          float4* dst = slot + (c / 32) * 8 * 128 + r;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            __stcg(dst + j * 128, make_float4(__uint_as_float(acc[4 * j]), __uint_as_float(acc[4 * j + 1]),
+                                        __uint_as_float(acc[4 * j + 2]),
+                                        __uint_as_float(acc[4 * j + 3])));
+        }
+      } else {
+      // the first part of a tail tile adds the later parts' partial tiles
+      bool add = false;
+      if (w.role == 1) {
+        int v = 1;
+        if (lane == 0) v = wait_parts(p, w.c1, w.nc, s_fail) ? 1 : 0;
+        add = __shfl_sync(0xffffffffu, v, 0) != 0;
+      }
       // ---- epilogue: accumulators -> C ----
       {
         // column c of the MT x BN accumulator columns is column c % BN of
@@ -366,6 +534,14 @@ __global__ void __launch_bounds__(Cfg<MT, DW, SPLIT>::kThreads, 1)
           // B ring, which no MMA reads and no dequant writes between tiles.
           uint8_t* stg = sB + wd * 8192;
           const int box_cols = p.c_dtype == 0 ? 32 : 64;
+          static_assert(SPLIT || kStagesA * C::kABytes >= DW * 12288, "partial staging in the A ring");
+          PartPrefetch<C::kTmemCols> pf{p, reinterpret_cast<float4*>(sA + wd * 12288), w.c1,
+                                        w.nc, q * 32 + lane, lane, c0 / 32,
+                                        add ? (C::kEpiCols / 32) * w.nc : 0};
+          if (add) {
+            pf.issue(0);
+            pf.issue(1);
+          }
           int nbox = 0;
 #pragma unroll 1
           for (int c = c0; c < c0 + C::kEpiCols; c += box_cols, ++nbox) {
@@ -378,6 +554,7 @@ __global__ void __launch_bounds__(Cfg<MT, DW, SPLIT>::kThreads, 1)
             for (int h = 0; h < box_cols / 32; ++h) {
               uint32_t acc[32], v[32];
               tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c + 32 * h, acc);
+              if (add) pf.add((c - c0) / 32 + h, acc);
               // tensor-memory column 8t + s holds output column 8t + chunk_col(s)
 #pragma unroll
               for (int t = 0; t < 4; ++t)
@@ -415,26 +592,40 @@ __global__ void __launch_bounds__(Cfg<MT, DW, SPLIT>::kThreads, 1)
           }
           // the boxes are read before the B ring takes the next tile's stages
           if (lane == 0) bulk_wait_read<0>();
+          if (add) cp_async_wait<0>();   // no copy into the A ring outlives the unit
           __syncwarp();
         } else {
 #pragma unroll 1
           for (int c = c0; c < c0 + C::kEpiCols; c += 32) {
             uint32_t acc[32];
             tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, acc);
+            if (add) add_parts<C::kTmemCols>(p, w.c1, w.nc, row - w.m0 - mt * 128, c, acc);
             const int col0 = w.n0 + (c - mt * BN);
             if (row < p.M && col0 < p.N) store_row32(p, row, col0, acc);
           }
         }
       }
+      }   // role 0 or 1
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tmem_empty);
-      if (p.use_tma_c) {
-        // every warp's staging boxes (in the B ring) have been read before
-        // any warp writes the next tile's B stages over them
+      if (p.use_tma_c || w.role != 0) {
+        // all warps meet: every warp's staging boxes (in the B ring) have
+        // been read before any warp writes the next tile's B stages over
+        // them, and in the tail every warp's partial stores or partial reads
+        // are done
         int v2 = 1;
         if (lane == 0) v2 = gwait(tmem_empty, it & 1, s_fail, p.err) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, v2, 0) != 0;
+        if (ok && wd == 0 && lane == 0) {
+          if (w.role == 2) {
+            // the stores the meet ordered before this thread, then the ticket
+            __threadfence();
+            red_add_release_gpu(&p.tickets[blockIdx.x], 1u);
+          } else if (w.role == 1) {
+            for (int i = 0; i < w.nc; ++i) p.tickets[w.c1 + i] = 0u;   // zero for the next launch
+          }
+        }
       }
     }
   }
@@ -763,6 +954,43 @@ int gemm_global_split(int64_t M, int64_t N, int64_t K, int sms) {
   return static_cast<int>(S);
 }
 
+PrefillPlan prefill_plan(int64_t M, int64_t N, int64_t K, int sms) {
+  PrefillPlan pl;
+  const int64_t tiles = ((M + PrefillCfg::kBM - 1) / PrefillCfg::kBM) * ((N + gemm::BN - 1) / gemm::BN);
+  const int64_t ksteps = (K + gemm::BK - 1) / gemm::BK;
+  pl.grid = static_cast<int>(tiles < sms ? tiles : sms);
+  pl.full_tiles = static_cast<int>(tiles);
+  pl.tail_ctas = 0;
+  if (sms <= 0 || tiles <= 0) return pl;
+  const int64_t rem = tiles % sms;
+  if (rem == 0) return pl;
+  // the last round's tiles: their K steps shared by up to kTailParts CTAs per
+  // tile, each CTA's range no longer than a tile; worth it when a range plus
+  // the partial tile's write and read (about kTailCostSteps K steps) is
+  // shorter than a whole tile
+  constexpr int64_t kTailParts = 4, kTailCostSteps = 6;
+  const int64_t T = rem * ksteps;
+  int64_t ctas = std::min<int64_t>(sms, rem * kTailParts);
+  ctas = std::min<int64_t>(ctas, T);
+  if ((T + ctas - 1) / ctas + kTailCostSteps > ksteps) return pl;
+  // every CTA of the grid has work: whole tiles (then the grid fills the
+  // SMs) or a part of the tail
+  pl.grid = tiles >= sms ? sms : static_cast<int>(ctas);
+  pl.full_tiles = static_cast<int>(tiles - rem);
+  pl.tail_ctas = static_cast<int>(ctas);
+  return pl;
+}
+
+size_t prefill_tail_ticket_bytes(const PrefillPlan& pl) {
+  return (static_cast<size_t>(pl.tail_ctas) * sizeof(unsigned) + 255) / 256 * 256;
+}
+
+size_t prefill_tail_bytes(const PrefillPlan& pl) {
+  if (pl.tail_ctas <= 0) return 0;
+  return prefill_tail_ticket_bytes(pl) +
+         static_cast<size_t>(pl.tail_ctas) * 128 * PrefillCfg::kTmemCols * sizeof(float);
+}
+
 size_t gemm_part_bytes(int64_t M, int64_t N, int S) {
   const int64_t tiles = (N + gemm::BN - 1) / gemm::BN;
   const int64_t rows = M < 128 ? M : 128;
@@ -777,6 +1005,8 @@ cudaError_t launch_gemm(void* C, int c_dtype, const void* A, const void* B, int6
   p.gsplit = 0;
   p.part = nullptr;
   p.tickets = nullptr;
+  p.full_tiles = 0;
+  p.tail_ctas = 0;
   p.C = C;
   p.c_dtype = c_dtype;
   p.M = static_cast<int>(M);
@@ -791,8 +1021,16 @@ cudaError_t launch_gemm(void* C, int c_dtype, const void* A, const void* B, int6
     p.nsplit = 1;
     cudaError_t e = prepare<2, 8, false>();
     if (e != cudaSuccess) return e;
+    // the last round's K steps shared over the grid when the caller gives
+    // the tail's tickets and partial tiles (prefill_tail_bytes)
+    const PrefillPlan pl = prefill_plan(M, N, K, sms);
+    const bool tail = pl.tail_ctas > 0 && part && tickets;
     const int64_t tiles = ((M + PrefillCfg::kBM - 1) / PrefillCfg::kBM) * ((N + gemm::BN - 1) / gemm::BN);
-    const int grid = static_cast<int>(tiles < sms ? tiles : sms);
+    p.full_tiles = tail ? pl.full_tiles : static_cast<int>(tiles);
+    p.tail_ctas = tail ? pl.tail_ctas : 0;
+    p.part = tail ? part : nullptr;
+    p.tickets = tail ? tickets : nullptr;
+    const int grid = tail ? pl.grid : static_cast<int>(tiles < sms ? tiles : sms);
     cudaLaunchConfig_t cfg = make_cfg<2, 8, false>(attr, grid, 1, st);
     return cudaLaunchKernelEx(&cfg, gemm::q4_gemm_tc_kernel<2, 8, false>, p);
   }

@@ -188,14 +188,23 @@ struct GemmParams {
   int gsplit;
   float* part;
   unsigned* tickets;
+  // prefill form: tiles [0, full_tiles) run whole, round-robin over the grid;
+  // with tail_ctas > 0 the K steps of the remaining tiles, taken in tile
+  // order as one range, are cut into tail_ctas equal parts, CTA c taking
+  // part c.  The part of a tile that holds its first K step adds the other
+  // parts' fp32 partial tiles (part [tail_ctas][128][MT*256], each written
+  // by the CTA whose part it is, ready once tickets[c] is nonzero) in K
+  // order and stores C; it returns those tickets to zero.
+  int full_tiles, tail_ctas;
 };
 // Shapes the tensor-core GEMM accepts: nb = ceil(N/32) a multiple of 8 (whole
 // 256-column tiles of blocks, 16-byte row pitch) and K a multiple of 8
 // (16-byte row pitch of A).
 bool gemm_supported(int64_t M, int64_t N, int64_t K);
 // A: bf16, 16-byte aligned; B: blocks layout, 16-byte aligned.  M > 128 runs
-// the persistent prefill form (`sms` bounds its grid), M <= 128 the split-K
-// small-M form.
+// the persistent prefill form (`sms` bounds its grid; with `part` and
+// `tickets` laid out as prefill_plan() asks, its last round shares K), M <=
+// 128 the split-K small-M form.
 // M <= 128 with `part` and `tickets` given and gemm_global_split() > 0 runs
 // the small-M form through global memory (part: gemm_part_bytes() bytes;
 // tickets: at least ceil(N/256) counters, zero, left zero by every launch;
@@ -205,6 +214,17 @@ cudaError_t launch_gemm(void* C, int c_dtype, const void* A, const void* B, int6
                         unsigned* tickets = nullptr);
 // K splits the small-M form uses for this shape (0: the form cannot take it).
 int gemm_small_split(int64_t M, int64_t N, int64_t K);
+// The prefill form (M > 128) on `sms` SMs: its grid, the tiles run whole and
+// the CTAs sharing the K steps of the last round's tiles (0: no tail, every
+// tile whole).  The tail needs prefill_tail_bytes() of caller memory: the
+// tickets (prefill_tail_ticket_bytes(), zero, left zero by every launch) and
+// then the partial tiles; launch_gemm takes them as `tickets` and `part`.
+struct PrefillPlan {
+  int grid, full_tiles, tail_ctas;
+};
+PrefillPlan prefill_plan(int64_t M, int64_t N, int64_t K, int sms);
+size_t prefill_tail_ticket_bytes(const PrefillPlan& pl);
+size_t prefill_tail_bytes(const PrefillPlan& pl);
 // Tile counters a stream's ticket array holds (N up to 1,048,576 columns).
 constexpr int kMaxGemmTickets = 4096;
 // K splits of the global-memory small-M form (0: the cluster form is chosen:
