@@ -86,11 +86,12 @@ Q4_API int q4_matmul(float *C, const float *A, const void *B, int64_t M, int64_t
  *              second format (the engine page, §2.1-§2.2, names Q8_0 but
  *              prints no layout; reading: blocks {fp16 d; int8 q[32]} of 34
  *              bytes, 32 output columns of one row each, K rows of
- *              ceil(N/32) blocks, w = q * d), for M <= 64 only (else
- *              Q4_ERR_SHAPE); or Q4_LAYOUT_PLANAR (q4_repack's output for
- *              this K x N), for M <= 64 only (else Q4_ERR_SHAPE): the same
- *              GEMV on the same values, so C is bit-identical to the
- *              Q4_LAYOUT_BLOCKS result for the same shape
+ *              ceil(N/32) blocks, w = q * d); or Q4_LAYOUT_PLANAR
+ *              (q4_repack's output for this K x N).  Both run the split-K
+ *              GEMV below for every M (more than 4 rows in chunks of up to
+ *              4, each chunk streaming the weights again); planar weights
+ *              give C bit-identical to the Q4_LAYOUT_BLOCKS GEMV result for
+ *              the same shape
  *   workspace  may be NULL.  Shapes whose tensor-core GEMM splits K over
  *              independent CTAs (bf16 A, 8 <= M <= 40; and M > 128 when the
  *              256 x 256 tiles leave a last round that does not fill the

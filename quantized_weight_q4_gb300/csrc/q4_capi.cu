@@ -846,7 +846,6 @@ int q4_matmul_ex(void* C, int c_dtype, const void* A, int a_dtype, const void* B
   const int fmt = (b_layout == Q4_LAYOUT_Q8_0)    ? q4::kFmtQ8
                   : (b_layout == Q4_LAYOUT_PLANAR) ? q4::kFmtQ4P
                                                    : q4::kFmtQ4;
-  if (fmt != q4::kFmtQ4 && M > 64) return Q4_ERR_SHAPE;   // Q8_0, planar: the GEMV (M <= 64) only
   if (!aligned16(C) || !aligned16(A) || !aligned16(B) || (workspace && !aligned16(workspace)))
     return Q4_ERR_ALIGN;
 

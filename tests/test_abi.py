@@ -69,10 +69,10 @@ def test_argument_errors_on_host(L):
     # bad dtype and layout codes
     assert L.q4_matmul_ex(good, 7, good, 0, good, 0, 1, 32, 32, None, 0, None) == q4.Q4_ERR_DTYPE
     assert L.q4_matmul_ex(good, 0, good, 0, good, 9, 1, 32, 32, None, 0, None) == q4.Q4_ERR_ARG
-    # Q8_0 and planar weights go through the GEMV only: more than 64 rows is a
-    # shape error (checked before any CUDA call)
-    for layout in (q4.Q4_LAYOUT_Q8_0, q4.Q4_LAYOUT_PLANAR):
-        assert L.q4_matmul_ex(good, 0, good, 0, good, layout, 65, 32, 32, None, 0,
+    # sizes beyond 2^30 are shape errors for every layout (checked before any
+    # CUDA call)
+    for layout in (q4.Q4_LAYOUT_BLOCKS, q4.Q4_LAYOUT_Q8_0, q4.Q4_LAYOUT_PLANAR):
+        assert L.q4_matmul_ex(good, 0, good, 0, good, layout, (1 << 30) + 1, 32, 32, None, 0,
                               None) == q4.Q4_ERR_SHAPE
     # misaligned pointers
     bad = vp(0x10004)

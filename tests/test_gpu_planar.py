@@ -137,11 +137,13 @@ def test_planar_large_equals_blocks(M):
         assert torch.equal(cb, cp), (M, K, N)
 
 
-def test_planar_large_m_rejected():
-    K, N = 64, 256
-    C = torch.empty((65, N), dtype=torch.float32, device=device())
-    A = torch.zeros((65, K), dtype=torch.float32, device=device())
-    P = to_dev(planar_bytes(si.q4_weights(K, N, seed=1), K, N))
-    with pytest.raises(q4.Q4Error) as e:
-        q4.q4_matmul_ex(C, A, P, 65, N, K, b_layout=q4.Q4_LAYOUT_PLANAR)
-    assert e.value.status == q4.Q4_ERR_SHAPE
+@pytest.mark.parametrize("M,K,N", [(65, 300, 520), (130, 1024, 4352)])
+def test_planar_many_rows(M, K, N):
+    """More than 64 rows (fp32 A): the GEMV in chunks of 4 rows, bit-identical
+    to the block layout and within the oracle's tolerance."""
+    A = si.activations_f32(M, K, seed=M)
+    B = si.q4_weights(K, N, seed=M)
+    cb, cp = both_layouts(A, B, M, N, K)
+    assert torch.equal(cb, cp), (M, K, N)
+    C64, S = oracle.matmul(A, B, M, N, K)
+    assert_within_matmul_tol(to_host64(cp), C64, S, f"planar M={M}")

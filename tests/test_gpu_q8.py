@@ -108,11 +108,13 @@ def test_q8_deterministic_and_large_sampled():
         assert_within_matmul_tol(got, C64, S, f"Q8_0 5120x12288 M={M} sampled")
 
 
-def test_q8_large_m_rejected():
-    K, N = 64, 256
-    C = torch.empty((65, N), dtype=torch.float32, device=device())
-    A = torch.zeros((65, K), dtype=torch.float32, device=device())
-    B = to_dev(si.q8_weights(K, N, seed=1))
-    with pytest.raises(q4.Q4Error) as e:
-        q4.q4_matmul_ex(C, A, B, 65, N, K, b_layout=q4.Q4_LAYOUT_Q8_0)
-    assert e.value.status == q4.Q4_ERR_SHAPE
+@pytest.mark.parametrize("M,K,N,adt", [(65, 300, 520, "f32"), (130, 1000, 256, "bf16"),
+                                       (300, 129, 1056, "f32")])
+def test_q8_many_rows(M, K, N, adt):
+    """More than 64 rows: the GEMV in chunks of 4 rows (the last chunk
+    ragged), every output against the oracle."""
+    A = si.activations_f32(M, K, seed=M) if adt == "f32" else si.activations_bf16(M, K, seed=M)
+    B = si.q8_weights(K, N, seed=M + 1)
+    C = to_host64(run(A, B, M, N, K))
+    C64, S = oracle.q8_matmul(A, B, M, N, K)
+    assert_within_matmul_tol(C, C64, S, f"Q8_0 M={M} K={K} N={N} {adt}")
