@@ -84,14 +84,15 @@ TRAFFIC = {
 SEQ_SOURCES = ("q4_gemv_seq.cu", "q4_gemv_core.cuh", "q4_device.cuh")
 TRAFFIC_SEQ = {
     # captured on the 32-layer launch itself (one pass per launch)
-    "f5772ec32b66d5e1/7454208": 3935703040,
+    "8495c733d72dd94e/7454208": 3917498112,
 }
 
 
 # The same for the prefill GEMM kernel (q4_gemm_tc_kernel), one launch of
 # M = 2048, K = 5120, N = 12288.
 TRAFFIC_GEMM = {
-    "f8b3c97b81980056": 73111808,
+    # the last round's K steps shared over the grid (fp32 partial tiles)
+    "abec28abb1733123": 101719296,
 }
 
 
