@@ -169,7 +169,8 @@ Q4_API size_t q4_matmul_workspace_size(int64_t M, int64_t N, int64_t K);
  * M > 128 runs the persistent prefill form (256 x 256 output tiles, one
  * CTA per SM taking tiles round-robin; the tiles of an incomplete last round
  * share their K steps over the grid through the workspace, the part holding
- * a tile's first K step adding the others' partial tiles in K order).
+ * a tile's last K step adding the earlier parts' partial tiles in K order to
+ * its own sums).
  * Deterministic: the parts and their order depend only on the shape and the
  * SM count.
  */

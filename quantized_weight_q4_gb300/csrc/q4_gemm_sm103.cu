@@ -155,8 +155,8 @@ __device__ __forceinline__ void store_group4(const GemmParams& p, int row, int c
 
 // A unit of work: one output tile (rows m0.., columns n0..) over K steps
 // [kb, ke) of BK rows.  Prefill form: `role` 0 stores the tile; in the tail,
-// 1 is the part holding the tile's first K step (it adds the later parts,
-// those of CTAs [c1, c1 + nc), and stores), 2 a later part (it writes its
+// 1 is the part holding the tile's last K step (it adds the earlier parts,
+// those of CTAs [c1, c1 + nc), and stores), 2 an earlier part (it writes its
 // partial tile for that one).
 struct Work {
   int m0, n0, kb, ke;
@@ -172,8 +172,12 @@ __device__ __forceinline__ int64_t tail_start(int64_t T, int parts, int c) {
 // The it-th unit of this CTA (false when there is none).  Prefill: tiles
 // blockIdx.x, blockIdx.x + gridDim.x, ... below full_tiles over all K, then
 // the pieces of this CTA's range of the tail, one per tile it crosses (at
-// most two: a range is never longer than a tile).  Split: the one tile of
-// the cluster, this CTA's share of K (cluster rank = blockIdx.x % S).
+// most two: a range is never longer than a tile), the later tile's first.
+// So a CTA's earlier part (role 2, which never waits) comes before its
+// last-step part (role 1), and a last-step part waits only for CTAs of
+// lower index, which start no later than it does: no chain of waits, and no
+// wait on a CTA that cannot start.  Split: the one tile of the cluster, this
+// CTA's share of K (cluster rank = blockIdx.x % S).
 template <int MT, bool SPLIT>
 __device__ __forceinline__ bool work_item(const GemmParams& p, int it, Work& w) {
   constexpr int kBM = 128 * MT;
@@ -201,21 +205,22 @@ __device__ __forceinline__ bool work_item(const GemmParams& p, int it, Work& w) 
       if (c >= p.tail_ctas) return false;
       const int64_t T = static_cast<int64_t>(tiles_m * tiles_n - p.full_tiles) * ksteps;
       const int64_t lo = tail_start(T, p.tail_ctas, c), hi = tail_start(T, p.tail_ctas, c + 1);
-      const int64_t t = lo / ksteps + (it - mine);   // tile of the tail
+      if (lo >= hi) return false;
+      const int64_t t = (hi - 1) / ksteps - (it - mine);   // tile of the tail, later first
       const int64_t t0 = t * ksteps;
-      if (lo >= hi || t0 >= hi) return false;
+      if (t0 + ksteps <= lo) return false;
       w.kb = static_cast<int>(max(lo, t0) - t0);
       w.ke = static_cast<int>(min(hi, t0 + ksteps) - t0);
       tile = p.full_tiles + static_cast<int>(t);
-      if (w.kb > 0) {
-        w.role = 2;
-      } else if (w.ke < ksteps) {
-        // the parts of CTAs c + 1 .. that start inside this tile
+      if (w.kb > 0 && w.ke == ksteps) {
+        // the parts of CTAs c1 .. c - 1 hold this tile's earlier K steps
         w.role = 1;
-        w.c1 = c + 1;
-        int e = c + 1;
-        while (e < p.tail_ctas && tail_start(T, p.tail_ctas, e) < t0 + ksteps) ++e;
-        w.nc = e - w.c1;
+        int e = c - 1;
+        while (e > 0 && tail_start(T, p.tail_ctas, e) > t0) --e;
+        w.c1 = e;
+        w.nc = c - e;
+      } else if (w.ke < ksteps) {
+        w.role = 2;
       }
     }
   }
@@ -288,13 +293,13 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// The first part of a tail tile, TMA epilogue: one lane's rows of the later
-// parts' partial tiles, staged in shared memory two (chunk, part) pairs ahead
+// The last-step part of a tail tile, TMA epilogue: one lane's rows of the
+// earlier parts' partial tiles, staged in shared memory two (chunk, part) pairs ahead
 // of their use, so that the L2 round trips overlap.  Pair k = chunk k / nc of
 // the warp's columns, part k % nc, lands in slot k % 3 of the warp's 12 KB
 // (float4 [3][8][32]); each lane copies and later reads only its own row, so
-// no lane waits for another.  The buffer is the A ring, idle by then: a first
-// part is always its CTA's last unit.
+// no lane waits for another.  The buffer is the A ring, idle by then: a
+// last-step part is always its CTA's last unit.
 template <int COLS>
 struct PartPrefetch {
   const GemmParams& p;
@@ -511,7 +516,7 @@ __global__ void __launch_bounds__(Cfg<MT, DW, SPLIT>::kThreads, 1)
                                         __uint_as_float(acc[4 * j + 3])));
         }
       } else {
-      // the first part of a tail tile adds the later parts' partial tiles
+      // the last-step part of a tail tile adds the earlier parts' partial tiles
       bool add = false;
       if (w.role == 1) {
         int v = 1;

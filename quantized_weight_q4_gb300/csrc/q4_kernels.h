@@ -191,10 +191,10 @@ struct GemmParams {
   // prefill form: tiles [0, full_tiles) run whole, round-robin over the grid;
   // with tail_ctas > 0 the K steps of the remaining tiles, taken in tile
   // order as one range, are cut into tail_ctas equal parts, CTA c taking
-  // part c.  The part of a tile that holds its first K step adds the other
+  // part c.  The part of a tile that holds its last K step adds the earlier
   // parts' fp32 partial tiles (part [tail_ctas][128][MT*256], each written
   // by the CTA whose part it is, ready once tickets[c] is nonzero) in K
-  // order and stores C; it returns those tickets to zero.
+  // order to its own sums and stores C; it returns those tickets to zero.
   int full_tiles, tail_ctas;
 };
 // Shapes the tensor-core GEMM accepts: nb = ceil(N/32) a multiple of 8 (whole

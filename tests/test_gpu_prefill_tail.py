@@ -4,9 +4,9 @@ page §5.2, a prompt's tokens as one batched matmul).
 
 The 256 x 256 output tiles that do not fill a whole round over the SMs have
 their K steps, taken tile after tile as one range, cut into equal parts over
-up to four CTAs per tile.  The part holding a tile's first K step adds the
-later parts' fp32 partial tiles in K order to its own accumulator and stores
-C.  Only the summation order differs from one accumulator per tile, so the
+up to four CTAs per tile.  The part holding a tile's last K step adds the
+earlier parts' fp32 partial tiles in K order to its own accumulator and
+stores C.  Only the summation order differs from one accumulator per tile, so the
 bf16-tile oracle's tolerance (1e-4 * sum|a*bf16(w)| + 1e-6) still holds, and
 the bound against the exact product (2^-8 + 1e-4) * S + 1e-6.  The tail runs
 when the call has the tail's tickets and partial tiles: the caller's
