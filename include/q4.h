@@ -504,6 +504,23 @@ Q4_API size_t q4_moe_block_workspace_size(int64_t T, int64_t topk, int64_t E, in
  */
 Q4_API int q4_selftest_wait(int64_t limit_ns, int arrive, void *stream);
 
+/*
+ * q4_prefill_units -- test hook; no counterpart on the pages.  Lists, on
+ * the host (no CUDA call), the units of work the persistent prefill form
+ * (q4_matmul_bf16_tiles with M > 128 and its tail workspace) gives each of
+ * its CTAs for this shape on `sms` SMs, computed by the function the kernel
+ * itself runs.  Row i of out[cap][9] (int32): CTA, unit index within the
+ * CTA, first row m0, first column n0, first and end K step (of 64 rows),
+ * role (0: a whole tile; 1: the part holding the tile's last K step, which
+ * adds the earlier parts; 2: an earlier part, which writes its partial
+ * tile), and for role 1 the first CTA and the number of CTAs whose parts it
+ * adds.  Returns the number of units (rows beyond cap are counted, not
+ * written), or Q4_ERR_ARG (M <= 128, non-positive sizes or sms, out NULL
+ * with cap > 0) or Q4_ERR_SHAPE (a size above 2^30).
+ */
+Q4_API int64_t q4_prefill_units(int64_t M, int64_t N, int64_t K, int sms, int32_t *out,
+                                int64_t cap);
+
 /* Human-readable text of a status code (static storage). */
 Q4_API const char *q4_status_str(int status);
 

@@ -86,6 +86,7 @@ SIGNATURES = {
                             _vp, _vp, _vp, _i64, _vp, _sz, _vp]),
     "q4_moe_block_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _i64, _i64]),
     "q4_selftest_wait": (_int, [_i64, _int, _vp]),
+    "q4_prefill_units": (_i64, [_i64, _i64, _i64, _int, _vp, _i64]),
     "q4_host_stream_slot_bytes": (_sz, [ctypes.POINTER(SeqOp), _int]),
     "q4_matmul_host_stream": (_int, [ctypes.POINTER(SeqOp), _int, _vp, _sz, _int, _vp, _vp]),
     "q4_gemv_seq_bytes": (_sz, [ctypes.POINTER(GemvOp), _int]),
@@ -391,6 +392,22 @@ def q4_selftest_wait(limit_ns: int, arrive: bool, stream=None) -> None:
     """One bounded pipeline wait run to its limit (arrive=False) or completed."""
     _check("q4_selftest_wait", lib().q4_selftest_wait(int(limit_ns), 1 if arrive else 0,
                                                       _stream(stream)))
+
+
+def q4_prefill_units(M: int, N: int, K: int, sms: int):
+    """The prefill form's units per CTA for this shape on `sms` SMs (host
+    only): an int32 array [units, 9] of (CTA, unit, m0, n0, first K step,
+    end K step, role, first helper CTA, helper count)."""
+    import numpy as np
+    L = lib()
+    n = L.q4_prefill_units(M, N, K, sms, None, 0)
+    if n < 0:
+        raise Q4Error("q4_prefill_units", int(n))
+    out = np.zeros((max(n, 1), 9), dtype=np.int32)
+    got = L.q4_prefill_units(M, N, K, sms, out.ctypes.data, n)
+    if got != n:
+        raise Q4Error("q4_prefill_units", int(got))
+    return out[:n]
 
 
 def q4_get_device_status(stream=None) -> int:

@@ -1365,6 +1365,13 @@ int q4_dequant_bf16(uint16_t* W, const void* B, int64_t K, int64_t N, void* stre
                                           static_cast<cudaStream_t>(stream)));
 }
 
+int64_t q4_prefill_units(int64_t M, int64_t N, int64_t K, int sms, int32_t* out, int64_t cap) {
+  if (M <= 128 || N <= 0 || K <= 0 || sms <= 0 || cap < 0 || (cap > 0 && !out))
+    return Q4_ERR_ARG;
+  if (M > (1LL << 30) || N > (1LL << 30) || K > (1LL << 30)) return Q4_ERR_SHAPE;
+  return q4::prefill_units(M, N, K, sms, out, cap);
+}
+
 int q4_selftest_wait(int64_t limit_ns, int arrive, void* stream) {
   if (limit_ns <= 0 || limit_ns > 1000000000LL || (arrive != 0 && arrive != 1)) return Q4_ERR_ARG;
   std::lock_guard<std::mutex> lock(g_mu);

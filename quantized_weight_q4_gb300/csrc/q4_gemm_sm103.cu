@@ -165,65 +165,84 @@ struct Work {
 
 // Start of the tail's part c: the tail's K steps [0, T) cut into `parts`
 // equal ranges.
-__device__ __forceinline__ int64_t tail_start(int64_t T, int parts, int c) {
+__host__ __device__ __forceinline__ int64_t tail_start(int64_t T, int parts, int c) {
   return static_cast<int64_t>(c) * T / parts;
 }
 
-// The it-th unit of this CTA (false when there is none).  Prefill: tiles
-// blockIdx.x, blockIdx.x + gridDim.x, ... below full_tiles over all K, then
-// the pieces of this CTA's range of the tail, one per tile it crosses (at
-// most two: a range is never longer than a tile), the later tile's first.
-// So a CTA's earlier part (role 2, which never waits) comes before its
-// last-step part (role 1), and a last-step part waits only for CTAs of
-// lower index, which start no later than it does: no chain of waits, and no
-// wait on a CTA that cannot start.  Split: the one tile of the cluster, this
-// CTA's share of K (cluster rank = blockIdx.x % S).
-template <int MT, bool SPLIT>
-__device__ __forceinline__ bool work_item(const GemmParams& p, int it, Work& w) {
+// Prefill form: the it-th unit of CTA c of a grid of G (false when there is
+// none).  Tiles c, c + G, ... below full_tiles over all K, then the pieces
+// of CTA c's range of the tail, one per tile it crosses (at most two: a
+// range is never longer than a tile), the later tile's first.  So a CTA's
+// earlier part (role 2, which never waits) comes before its last-step part
+// (role 1), and a last-step part waits only for CTAs of lower index, which
+// start no later than it does: no chain of waits, and no wait on a CTA that
+// cannot start.  Host and device share this function (the host lists the
+// units for tests).
+template <int MT>
+__host__ __device__ __forceinline__ bool prefill_unit(int M, int N, int K, int full_tiles,
+                                                      int tail_ctas, int c, int G, int it,
+                                                      Work& w) {
   constexpr int kBM = 128 * MT;
-  const int tiles_m = (p.M + kBM - 1) / kBM;
-  const int tiles_n = (p.N + BN - 1) / BN;
-  const int ksteps = (p.K + BK - 1) / BK;
+  const int tiles_m = (M + kBM - 1) / kBM;
+  const int tiles_n = (N + BN - 1) / BN;
+  const int ksteps = (K + BK - 1) / BK;
   int tile;
   w.role = 0;
   w.c1 = 0;
   w.nc = 0;
-  if (SPLIT) {
-    if (it > 0) return false;
-    tile = blockIdx.x / p.nsplit;
-    const int s = blockIdx.x % p.nsplit;
-    w.kb = s * ksteps / p.nsplit;
-    w.ke = (s + 1) * ksteps / p.nsplit;
+  const int mine = full_tiles > c ? (full_tiles - c + G - 1) / G : 0;
+  if (it < mine) {
+    tile = c + it * G;
+    w.kb = 0;
+    w.ke = ksteps;
   } else {
-    const int c = blockIdx.x, G = gridDim.x;
-    const int mine = p.full_tiles > c ? (p.full_tiles - c + G - 1) / G : 0;
-    if (it < mine) {
-      tile = c + it * G;
-      w.kb = 0;
-      w.ke = ksteps;
-    } else {
-      if (c >= p.tail_ctas) return false;
-      const int64_t T = static_cast<int64_t>(tiles_m * tiles_n - p.full_tiles) * ksteps;
-      const int64_t lo = tail_start(T, p.tail_ctas, c), hi = tail_start(T, p.tail_ctas, c + 1);
-      if (lo >= hi) return false;
-      const int64_t t = (hi - 1) / ksteps - (it - mine);   // tile of the tail, later first
-      const int64_t t0 = t * ksteps;
-      if (t0 + ksteps <= lo) return false;
-      w.kb = static_cast<int>(max(lo, t0) - t0);
-      w.ke = static_cast<int>(min(hi, t0 + ksteps) - t0);
-      tile = p.full_tiles + static_cast<int>(t);
-      if (w.kb > 0 && w.ke == ksteps) {
-        // the parts of CTAs c1 .. c - 1 hold this tile's earlier K steps
-        w.role = 1;
-        int e = c - 1;
-        while (e > 0 && tail_start(T, p.tail_ctas, e) > t0) --e;
-        w.c1 = e;
-        w.nc = c - e;
-      } else if (w.ke < ksteps) {
-        w.role = 2;
-      }
+    if (c >= tail_ctas) return false;
+    const int64_t T = static_cast<int64_t>(tiles_m * tiles_n - full_tiles) * ksteps;
+    const int64_t lo = tail_start(T, tail_ctas, c), hi = tail_start(T, tail_ctas, c + 1);
+    if (lo >= hi) return false;
+    const int64_t t = (hi - 1) / ksteps - (it - mine);   // tile of the tail, later first
+    const int64_t t0 = t * ksteps;
+    if (t0 + ksteps <= lo) return false;
+    w.kb = static_cast<int>((lo > t0 ? lo : t0) - t0);
+    w.ke = static_cast<int>((hi < t0 + ksteps ? hi : t0 + ksteps) - t0);
+    tile = full_tiles + static_cast<int>(t);
+    if (w.kb > 0 && w.ke == ksteps) {
+      // the parts of CTAs c1 .. c - 1 hold this tile's earlier K steps
+      w.role = 1;
+      int e = c - 1;
+      while (e > 0 && tail_start(T, tail_ctas, e) > t0) --e;
+      w.c1 = e;
+      w.nc = c - e;
+    } else if (w.ke < ksteps) {
+      w.role = 2;
     }
   }
+  if (tile >= tiles_m * tiles_n) return false;
+  w.m0 = (tile % tiles_m) * kBM;
+  w.n0 = (tile / tiles_m) * BN;
+  return true;
+}
+
+// The it-th unit of this CTA (false when there is none): the prefill form's
+// (above), or for the split form the one tile of the cluster, this CTA's
+// share of K (cluster rank = blockIdx.x % S).
+template <int MT, bool SPLIT>
+__device__ __forceinline__ bool work_item(const GemmParams& p, int it, Work& w) {
+  if (!SPLIT)
+    return prefill_unit<MT>(p.M, p.N, p.K, p.full_tiles, p.tail_ctas, blockIdx.x, gridDim.x, it,
+                            w);
+  constexpr int kBM = 128 * MT;
+  const int tiles_m = (p.M + kBM - 1) / kBM;
+  const int tiles_n = (p.N + BN - 1) / BN;
+  const int ksteps = (p.K + BK - 1) / BK;
+  w.role = 0;
+  w.c1 = 0;
+  w.nc = 0;
+  if (it > 0) return false;
+  const int tile = blockIdx.x / p.nsplit;
+  const int s = blockIdx.x % p.nsplit;
+  w.kb = s * ksteps / p.nsplit;
+  w.ke = (s + 1) * ksteps / p.nsplit;
   if (tile >= tiles_m * tiles_n) return false;
   w.m0 = (tile % tiles_m) * kBM;
   w.n0 = (tile / tiles_m) * BN;
@@ -984,6 +1003,36 @@ PrefillPlan prefill_plan(int64_t M, int64_t N, int64_t K, int sms) {
   pl.full_tiles = static_cast<int>(tiles - rem);
   pl.tail_ctas = static_cast<int>(ctas);
   return pl;
+}
+
+int64_t prefill_units(int64_t M, int64_t N, int64_t K, int sms, int32_t* out, int64_t cap) {
+  const PrefillPlan pl = prefill_plan(M, N, K, sms);
+  const int64_t tiles =
+      ((M + PrefillCfg::kBM - 1) / PrefillCfg::kBM) * ((N + gemm::BN - 1) / gemm::BN);
+  const bool tail = pl.tail_ctas > 0;
+  const int G = tail ? pl.grid : static_cast<int>(tiles < sms ? tiles : sms);
+  const int full = tail ? pl.full_tiles : static_cast<int>(tiles);
+  int64_t n = 0;
+  for (int c = 0; c < G; ++c) {
+    gemm::Work w;
+    for (int it = 0; gemm::prefill_unit<2>(static_cast<int>(M), static_cast<int>(N),
+                                            static_cast<int>(K), full, pl.tail_ctas, c, G, it, w);
+         ++it, ++n) {
+      if (n < cap) {
+        int32_t* r = out + n * 9;
+        r[0] = c;
+        r[1] = it;
+        r[2] = w.m0;
+        r[3] = w.n0;
+        r[4] = w.kb;
+        r[5] = w.ke;
+        r[6] = w.role;
+        r[7] = w.c1;
+        r[8] = w.nc;
+      }
+    }
+  }
+  return n;
 }
 
 size_t prefill_tail_ticket_bytes(const PrefillPlan& pl) {

@@ -225,6 +225,11 @@ struct PrefillPlan {
 PrefillPlan prefill_plan(int64_t M, int64_t N, int64_t K, int sms);
 size_t prefill_tail_ticket_bytes(const PrefillPlan& pl);
 size_t prefill_tail_bytes(const PrefillPlan& pl);
+// The units the prefill form's CTAs run for this shape on `sms` SMs, in
+// each CTA's order: rows of 9 ints (CTA, unit, m0, n0, first and end K
+// step, role, first helper CTA, helper count) into out[cap][9]; returns the
+// number of units (host only, no CUDA call).
+int64_t prefill_units(int64_t M, int64_t N, int64_t K, int sms, int32_t* out, int64_t cap);
 // Tile counters a stream's ticket array holds (N up to 1,048,576 columns).
 constexpr int kMaxGemmTickets = 4096;
 // K splits of the global-memory small-M form (0: the cluster form is chosen:
