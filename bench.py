@@ -59,6 +59,20 @@ import seeded_inputs as si  # noqa: E402
 METRIC = "Q4_0 dequant-matmul weight GB/s (% HBM peak) at M=1; TFLOP/s at M=2048"
 
 
+# Nominal figures beside the measured ones: HBM3e 8.0 TB/s (the workload's
+# stated target denominator) and the sustained bf16 rate.
+NOMINAL_HBM_GBS = 8000.0
+
+
+def sustained_bf16_tflops():
+    """MEASURED_PEAKS.json's seconds-long bf16 rate under the power cap, or None."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        return json.load(f).get("bf16_tflops_sustained")
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -350,20 +364,54 @@ def pipelined_e2e(torch, q4, w, seq, deps, slice_rows):
     return run
 
 
+# Per-step times (ms) of the last timed region: an event after every replay,
+# on the replaying stream, so that the median and the minimum step can be
+# reported beside the aggregate.
+_STEP_MS = []
+
+
+def _timed_replays(torch, stream, replay, steps):
+    """The timed region: `steps` replays between two events (the value).  A
+    second, separate pass of up to 100 replays with an event after each
+    gives the per-step median and minimum, so that the extra events do not
+    touch the reported aggregate."""
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        s.record()
+        for _ in range(steps):
+            replay()
+        e.record()
+    e.synchronize()
+    total = s.elapsed_time(e) / 1e3
+    n = min(steps, 100)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    with torch.cuda.stream(stream):
+        evs[0].record()
+        for i in range(n):
+            replay()
+            evs[i + 1].record()
+    evs[-1].synchronize()
+    _STEP_MS[:] = [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
+    return total
+
+
+def step_summary():
+    """Median and minimum step (ms) of the per-step pass after the last timed region."""
+    if not _STEP_MS:
+        return None
+    v = sorted(_STEP_MS)
+    n = len(v)
+    med = v[n // 2] if n % 2 else 0.5 * (v[n // 2 - 1] + v[n // 2])
+    return {"median_ms": round(med, 5), "min_ms": round(v[0], 5), "steps": n}
+
+
 def time_graph(torch, seq, steps, warmup):
     seq.capture()
     for _ in range(warmup):
         seq.replay()
     torch.cuda.synchronize()
-    s = torch.cuda.Event(enable_timing=True)
-    e = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(seq.stream):
-        s.record()
-        for _ in range(steps):
-            seq.graph.replay()
-        e.record()
-    e.synchronize()
-    return s.elapsed_time(e) / 1e3
+    return _timed_replays(torch, seq.stream, seq.graph.replay, steps)
 
 
 def cpu_baseline_sweep(layers_sample, seed=0, fmt="q4_0"):
@@ -410,8 +458,8 @@ def cpu_openmp_sweep(layers_sample, budget_s=6.0, seed=0):
 
 def summarize(line):
     """The fields of a bench line that a nested record keeps."""
-    keep = ("value", "unit", "ms_per_step", "steps", "warmup", "config", "roofline", "clocks",
-            "gpu_launches", "launches_per_step")
+    keep = ("value", "unit", "ms_per_step", "step_ms", "steps", "warmup", "config", "roofline",
+            "clocks", "gpu_launches", "launches_per_step")
     return {k: line[k] for k in keep if k in line}
 
 
@@ -476,6 +524,7 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         elapsed = time_graph(torch, seq, args.steps, args.warmup)
+        steps_main = step_summary()
     torch.cuda.synchronize()
     barrier(ws)
     elapsed = max_over_ranks(ws, elapsed)
@@ -558,6 +607,7 @@ def run_ours(args, ws, rank, local):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(elapsed / args.steps * 1e3, 5),
+        "step_ms": steps_main,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -593,6 +643,7 @@ def run_ours(args, ws, rank, local):
             "peak": hbm_peak,
             "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4),
+            "frac_of_nominal_8000": round(achieved / NOMINAL_HBM_GBS, 4),
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
             "algorithmic_bytes_per_launch": round(per_launch_bytes),
             "traffic": traffic,
@@ -644,15 +695,7 @@ class GraphOf:
             for _ in range(warmup):
                 self.graph.replay()
         torch.cuda.synchronize()
-        s = torch.cuda.Event(enable_timing=True)
-        e = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(self.stream):
-            s.record()
-            for _ in range(steps):
-                self.graph.replay()
-            e.record()
-        e.synchronize()
-        return s.elapsed_time(e) / 1e3
+        return _timed_replays(torch, self.stream, self.graph.replay, steps)
 
 
 _MOE = {}
@@ -843,11 +886,13 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
         if status != q4.Q4_OK:
             raise SystemExit(f"device status {status} after the timed region")
         tf_peak = measured_peaks()[1]
+        tf_sustained = sustained_bf16_tflops()
         ghash = kernel_source_hash(("q4_gemm_sm103.cu", "q4_tc_core.cuh", "q4_device.cuh", "q4_kernels.h"))
         return {
             "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(t / args.steps * 1e3, 5), "higher_is_better": True,
+            "ms_per_step": round(t / args.steps * 1e3, 5), "step_ms": step_summary(),
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded)",
             "config": {"workload": "prefill", "M": M, "K": K, "N": N, "a_dtype": "bf16",
@@ -858,6 +903,8 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
                        "weight_gbs": round(wbytes / per_launch / 1e9, 2)},
             "roofline": {"bound": "tensor", "achieved": round(value / ws, 2), "peak": tf_peak,
                          "unit": "TFLOP/s", "frac": round(value / ws / tf_peak, 4),
+                         "frac_of_sustained": (round(value / ws / tf_sustained, 4)
+                                               if tf_sustained else None),
                          "peak_source": peak_src + " (bf16 burst)",
                          "kernel": "q4_gemm_tc_kernel", "kernel_source_hash": ghash,
                          "traffic": TRAFFIC_GEMM.get(ghash)},
@@ -872,11 +919,13 @@ def run_other(args, ws, rank, local, torch, q4, dev, hbm_peak, peak_src):
     return {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(t / args.steps * 1e3, 5), "higher_is_better": True,
+        "ms_per_step": round(t / args.steps * 1e3, 5), "step_ms": step_summary(),
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded)", "config": cfg,
         "roofline": {"bound": "hbm", "achieved": round(value / ws, 2), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(value / ws / hbm_peak, 4),
+                     "frac_of_nominal_8000": round(value / ws / NOMINAL_HBM_GBS, 4),
                      "peak_source": peak_src, "traffic": None},
         "gpu_launches": args.steps * units * (8 if args.workload == "moe_block" and args.tokens > 1
                                               else KERNELS_PER_CALL.get(args.workload, 1)),
