@@ -99,12 +99,14 @@ constexpr int kRedStride = kLanesPerRow * BPT * 33;
 // p = 0..2, and the sign flips 0x80808080.
 struct DecodeConsts {
   uint32_t mask[4];
+  uint32_t hi16;   // 2^16, from a parameter (see accumulate_block's HI_MUL)
 };
 
 __device__ __forceinline__ DecodeConsts load_consts(const GemvParams& p) {
   DecodeConsts c;
 #pragma unroll
   for (int i = 0; i < 4; ++i) c.mask[i] = p.kmask[i];
+  c.hi16 = (c.mask[0] & 0x1u) << 16;
   return c;
 }
 
@@ -164,8 +166,12 @@ __device__ __forceinline__ int acc_col_pair(int j) {   // first column of pair j
 
 // Adds block bb of a staged row (scale bits dbits, codes qs) for MR rows of A
 // (a[m * a_ld], already times 2^64): acc[m][16bb + j] += a'_m * codes of pair
-// j, sad[m][bb] += a'_m.
-template <int MR, int BPT, int FMT>
+// j, sad[m][bb] += a'_m.  HI_MUL: a word's upper half comes down as
+// mul.hi(w, 2^16), which the FMA pipe executes, instead of a shift on the
+// integer pipe (the same value); k.hi16 holds 2^16 read from a parameter, so
+// that the compiler keeps the multiply.  The decode-sequence kernel, whose
+// integer pipe is its busiest unit, takes it.
+template <int MR, int BPT, int FMT, bool HI_MUL = false>
 __device__ __forceinline__ void accumulate_block(f32x2 (&acc)[MR][16 * BPT],
                                                  float (&sad)[MR][BPT], int bb, uint32_t dbits,
                                                  const uint32_t (&qs)[Fmt<FMT>::kWords],
@@ -200,7 +206,8 @@ __device__ __forceinline__ void accumulate_block(f32x2 (&acc)[MR][16 * BPT],
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const uint32_t w0 = qs[2 * h], w1 = qs[2 * h + 1];
-    const uint32_t y0 = w0 >> 16, y1 = w1 >> 16;
+    const uint32_t y0 = HI_MUL ? __umulhi(w0, k.hi16) : w0 >> 16;
+    const uint32_t y1 = HI_MUL ? __umulhi(w1, k.hi16) : w1 >> 16;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
       const f32x2 lo = code_pair(w0, w1, k.mask[p]);

@@ -442,6 +442,7 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const __grid_c
   DecodeConsts kc;
 #pragma unroll
   for (int i = 0; i < 4; ++i) kc.mask[i] = p.kmask[i];
+  kc.hi16 = (kc.mask[0] & 0x1u) << 16;   // 2^16 (mask[0] = 0xF)
   const int pi = lane & 7;
   const int rp = warp * 4 + (lane >> 3);              // row phase within a stage
   const uint32_t boff = static_cast<uint32_t>(pi * kBPT * kBlockBytes);
@@ -488,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const __grid_c
       a *= kAScale;
 #pragma unroll
       for (int bb = 0; bb < kBPT; ++bb)
-        accumulate_block<1, kBPT, kFmtQ4>(acc, sad, bb, dbits[bb], qs[bb], &a, 0, kc);
+        accumulate_block<1, kBPT, kFmtQ4, true>(acc, sad, bb, dbits[bb], qs[bb], &a, 0, kc);
     }
     __syncwarp();
     if (!(flags & 1)) {
