@@ -98,7 +98,7 @@ TRAFFIC = {
 SEQ_SOURCES = ("q4_gemv_seq.cu", "q4_gemv_core.cuh", "q4_device.cuh")
 TRAFFIC_SEQ = {
     # captured on the 32-layer launch itself (one pass per launch)
-    "2b26f959a8e5029d/7454208": 3906809344,
+    "7d1a784ef69b6a66/7454208": 3783943680,
 }
 
 
@@ -634,7 +634,7 @@ def run_ours(args, ws, rank, local):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": ("q4_gemv_seq_kernel (persistent: 18 KB TMA stages, 8 consumer warps, "
+            "kernel": ("q4_gemv_seq_kernel (persistent: 36 KB TMA stages, 8 consumer warps, "
                        "2 CTAs per SM; all 224 GEMVs in one launch)" if use_seq else
                        "q4_gemv_kernel (GEMV, one row of A, 2 blocks per thread, 32-row stages"
                        + {"q8_0": ", Q8_0 blocks)", "q4_0_planar": ", planar Q4_0)"}.get(args.format, ")")),

@@ -327,14 +327,15 @@ const MoeShape& cached_moe_shape(DeviceState* s, int64_t T, int64_t topk, int64_
 
 int launch_status(cudaError_t e) { return e == cudaSuccess ? Q4_OK : Q4_ERR_CUDA; }
 
-// The persistent sequence kernel's ring depth (5 stages where two CTAs fit on
-// an SM, else 4) and resident CTAs per SM; Q4_ERR_CUDA if it cannot launch.
+// The persistent sequence kernel's ring depth (3 stages of 36 KB where two
+// CTAs fit on an SM, else 2) and resident CTAs per SM; Q4_ERR_CUDA if it
+// cannot launch.
 int seq_residency(DeviceState* s) {
   if (s->seq_per_sm == 0) {
-    int stages = 5;
+    int stages = 3;
     int per_sm = q4::seq_ctas_per_sm(stages, true);
     if (per_sm < 2) {
-      stages = 4;
+      stages = 2;
       per_sm = q4::seq_ctas_per_sm(stages, true);
     }
     if (per_sm < 1) return Q4_ERR_CUDA;
@@ -1186,7 +1187,7 @@ int seq_layout(const q4_gemv_op* ops, int n, SeqLayout* L) {
     if (!aligned16(o.C) || !aligned16(o.A) || !aligned16(o.B)) return Q4_ERR_ALIGN;
     if (ceil_div(o.N, 32) % 8 != 0) return Q4_ERR_SHAPE;   // 16-byte row pitch for TMA
     if (o.slice_rows < 0 || o.slice_rows > q4::seq_max_slice_rows() ||
-        o.slice_rows % q4::seq_stage_rows() != 0)
+        o.slice_rows % q4::seq_slice_rows_unit() != 0)
       return Q4_ERR_ARG;
   }
   std::vector<int64_t> rows;
@@ -1231,10 +1232,10 @@ int q4_gemv_seq_create(const q4_gemv_op* ops, int n, void* buf, size_t buf_bytes
   DeviceState* s = nullptr;
   rc = current_state(&s);
   if (rc != Q4_OK) return rc;
-  int stages = 5;
+  int stages = 3;
   int per_sm = q4::seq_ctas_per_sm(stages, false);
   if (per_sm < 2) {
-    stages = 4;
+    stages = 2;
     per_sm = q4::seq_ctas_per_sm(stages, false);
   }
   if (per_sm < 1) return Q4_ERR_CUDA;

@@ -9,11 +9,14 @@
 // reduction and drain leave the HBM idle for microseconds each time, one
 // resident grid (two CTAs per SM) streams all of the sequence's weights.
 //  * The work is cut into units of (op, column tile of 16 blocks = 512
-//    columns, K slice of 64 to 4096 rows, chosen per op).  Units are numbered op by op, and within
-//    an op tile by tile; a global counter hands them out in that order.
-//  * In each CTA a producer warp issues one TMA tensor copy per 64-row stage
-//    (18 KB) into a ring, and a second warp copies the stage's 64 entries of A
-//    (cp.async.bulk) onto the same mbarrier once the op's dependencies have
+//    columns, K slice of 64 to 4096 rows, chosen per op).  Units are
+//    numbered op by op, and within an op tile by tile; a global counter hands
+//    them out in that order.
+//  * In each CTA a producer warp issues two TMA tensor copies (64-row boxes)
+//    per 128-row stage (36 KB) into a three-stage ring, and a second warp
+//    copies the stage's 128 entries of A (cp.async.bulk; zeros past the
+//    unit's rows, so that a half stage adds nothing) onto the same mbarrier
+//    once the op's dependencies have
 //    completed, so that weights keep streaming while an op waits for its
 //    input.  Eight consumer warps decode and accumulate with the same exact
 //    arithmetic as the split-K GEMV (q4_gemv_core.cuh).
@@ -45,10 +48,10 @@ constexpr int kBPT = 2;                                  // blocks per consumer 
 constexpr int kTileBlocks = kLanesPerRow * kBPT;         // 16 blocks per column tile
 constexpr int kTileCols = kTileBlocks * kBlockCols;      // 512 columns
 constexpr int kRowBytes = kTileBlocks * kBlockBytes;     // 288 bytes of a tile row
-constexpr int kStageRows = 64;
-constexpr int kStageBytes = kStageRows * kRowBytes;      // 18432 bytes
-constexpr int kDefaultSliceStages = 8;                   // stages of a unit by default
-constexpr int kMaxSliceStages = 64;                      // stages of the longest unit
+constexpr int kStageRows = 128;                          // two 64-row TMA boxes
+constexpr int kStageBytes = kStageRows * kRowBytes;      // 36864 bytes
+constexpr int kDefaultSliceStages = 4;                   // stages of a unit by default
+constexpr int kMaxSliceStages = 32;                      // stages of the longest unit
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 64;                // + producer warp + A warp
@@ -66,7 +69,7 @@ struct SlotMeta {
   int flags;   // bit 0: the unit's last stage; bit 1: A is bf16; bit 2: end;
                // bit 3: the unit's expert index is invalid
   int k0;      // first row of A of the stage
-  int rows;    // rows of the stage below K (1..64)
+  int rows;    // rows of the stage inside the unit and below K (1..128)
   int slice;   // the unit's K slice
   int seg;     // the unit's segment (0 for unsegmented ops)
 };
@@ -319,9 +322,15 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const __grid_c
         const uint32_t tx = (valid ? kStageBytes : 0u) + a_bulk_bytes(rows, d.a_dtype);
         if (tx) mbar_arrive_expect_tx(&full[slot], tx);
         else mbar_arrive(&full[slot]);
-        if (valid)
-          tma_load_3d(ring + slot * kStageBytes, second ? &d.tmap2 : &d.tmap, cx,
-                      w0 + st * kStageRows, expert, &full[slot]);
+        if (valid) {
+          // two 64-row boxes (the weight maps' box); rows past the unit's
+          // end meet zeros in A, and rows past K read as zeros
+          const CUtensorMap* tm = second ? &d.tmap2 : &d.tmap;
+          const int r0 = w0 + st * kStageRows;
+          tma_load_3d(ring + slot * kStageBytes, tm, cx, r0, expert, &full[slot]);
+          tma_load_3d(ring + slot * kStageBytes + kStageBytes / 2, tm, cx, r0 + kStageRows / 2,
+                      expert, &full[slot]);
+        }
         mbar_arrive(&claimed[slot]);
         posted = gs + 1;
       }
@@ -417,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const __grid_c
       const uint32_t bulk = a_bulk_bytes(m.rows, d.a_dtype);
       const uint8_t* src = static_cast<const uint8_t*>(d.A) + static_cast<size_t>(m.k0) * es;
       if (lane == 0 && bulk) bulk_load(dst, src, bulk, &full[slot]);
-      // the last few entries below K, then zeros up to the stage's 64 rows
+      // the last few entries below K, then zeros up to the stage's rows
       for (uint32_t b = bulk + lane * es; b < kStageRows * es; b += 32 * es) {
         const uint32_t r = b / es;
         if (es == 4) {
@@ -663,11 +672,11 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_seq_kernel(const __grid_c
 // Host side
 // ---------------------------------------------------------------------------
 int seq_ctas_per_sm(int stages, bool seg) {
-  const void* fn = stages == 4 ? (seg ? (const void*)seq::q4_gemv_seq_kernel<4, true>
-                                      : (const void*)seq::q4_gemv_seq_kernel<4, false>)
-                               : (seg ? (const void*)seq::q4_gemv_seq_kernel<5, true>
-                                      : (const void*)seq::q4_gemv_seq_kernel<5, false>);
-  const uint32_t smem = stages == 4 ? seq::smem_layout<4>().total : seq::smem_layout<5>().total;
+  const void* fn = stages == 2 ? (seg ? (const void*)seq::q4_gemv_seq_kernel<2, true>
+                                      : (const void*)seq::q4_gemv_seq_kernel<2, false>)
+                               : (seg ? (const void*)seq::q4_gemv_seq_kernel<3, true>
+                                      : (const void*)seq::q4_gemv_seq_kernel<3, false>);
+  const uint32_t smem = stages == 2 ? seq::smem_layout<2>().total : seq::smem_layout<3>().total;
   // a failed call leaves no error pending for the caller's next launch
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
     cudaGetLastError();
@@ -685,6 +694,7 @@ int seq_ctas_per_sm(int stages, bool seg) {
 
 int seq_tile_cols() { return seq::kTileCols; }
 int seq_stage_rows() { return seq::kStageRows; }
+int seq_slice_rows_unit() { return seq::kStageRows / 2; }
 int seq_max_slice_rows() { return seq::kMaxSliceStages * seq::kStageRows; }
 int seq_default_slice_rows() { return seq::kDefaultSliceStages * seq::kStageRows; }
 
@@ -701,14 +711,14 @@ cudaError_t launch_gemv_seq(const SeqParams& p, int grid, int stages, cudaStream
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  if (stages == 4) {
-    cfg.dynamicSmemBytes = seq::smem_layout<4>().total;
-    return seg ? cudaLaunchKernelEx(&cfg, seq::q4_gemv_seq_kernel<4, true>, p)
-               : cudaLaunchKernelEx(&cfg, seq::q4_gemv_seq_kernel<4, false>, p);
+  if (stages == 2) {
+    cfg.dynamicSmemBytes = seq::smem_layout<2>().total;
+    return seg ? cudaLaunchKernelEx(&cfg, seq::q4_gemv_seq_kernel<2, true>, p)
+               : cudaLaunchKernelEx(&cfg, seq::q4_gemv_seq_kernel<2, false>, p);
   }
-  cfg.dynamicSmemBytes = seq::smem_layout<5>().total;
-  return seg ? cudaLaunchKernelEx(&cfg, seq::q4_gemv_seq_kernel<5, true>, p)
-             : cudaLaunchKernelEx(&cfg, seq::q4_gemv_seq_kernel<5, false>, p);
+  cfg.dynamicSmemBytes = seq::smem_layout<3>().total;
+  return seg ? cudaLaunchKernelEx(&cfg, seq::q4_gemv_seq_kernel<3, true>, p)
+             : cudaLaunchKernelEx(&cfg, seq::q4_gemv_seq_kernel<3, false>, p);
 }
 
 }  // namespace q4

@@ -157,7 +157,8 @@ size_t moe_min_workspace_bytes(int64_t T, int64_t topk, int64_t H, int64_t I);
 // can keep resident (0 if it cannot launch).
 int seq_ctas_per_sm(int stages, bool seg);   // seg: the segmented instance
 int seq_tile_cols();       // columns of a unit (512)
-int seq_stage_rows();      // rows of one pipeline stage (64)
+int seq_stage_rows();      // rows of one pipeline stage (128: two 64-row TMA boxes)
+int seq_slice_rows_unit(); // units are multiples of this many rows (64; a last stage may be half)
 int seq_max_slice_rows();      // rows of the longest unit (4096)
 int seq_default_slice_rows();  // rows of a unit by default (512)
 // `pdl`: launched with programmatic stream serialization (the kernel waits
