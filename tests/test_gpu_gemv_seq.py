@@ -31,9 +31,9 @@ def run_plan(seq):
     assert q4.q4_get_device_status() == q4.Q4_OK
 
 
-# (K, N, a_dtype, c_dtype): K tails of the 64-row stage and of the units
-# (K = 1, 3, 63, 65, 513, 1025; 4096 fills one 4096-row unit), N tails of the
-# 512-column tile and of the block
+# (K, N, a_dtype, c_dtype): K tails of the 128-row stage, of its 64-row TMA
+# boxes and of the units (K = 1, 3, 63, 65, 513, 1025; 4096 fills one
+# 4096-row unit), N tails of the 512-column tile and of the block
 SHAPES = [(300, 256, "f32", "f32"), (1, 512, "f32", "f32"), (3, 1000, "bf16", "f32"),
           (63, 250, "f32", "bf16"), (65, 2040, "bf16", "bf16"), (513, 4096, "f32", "f32"),
           (1025, 1000, "bf16", "f32"), (4096, 760, "f32", "f32"), (2048, 12288, "bf16", "f32")]
