@@ -148,6 +148,11 @@ def test_gemv_seq_checks_on_host(L):
                             op(4096, 11008, [0, 1], rows=128))
     units_short = 8 * 32 + 22 * 32 + 8 * 86
     assert units_short * 2048 < L.q4_gemv_seq_bytes(short, 3) < units_short * 2048 + 65536
+    # a unit may end on half of a 128-row stage: 64 and 192 rows stay valid
+    for r in (64, 192):
+        half = (q4.GemvOp * 1)(op(4096, 4096, rows=r))
+        units_half = 8 * -(-4096 // r)
+        assert units_half * 2048 < L.q4_gemv_seq_bytes(half, 1) < units_half * 2048 + 65536
     plan = vp()
     create = lambda o, n, buf, size: L.q4_gemv_seq_create(o, n, vp(buf), size, ctypes.byref(plan))
     assert create(ops, 3, good + 16, nbytes) == q4.Q4_ERR_ALIGN
