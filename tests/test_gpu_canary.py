@@ -7,7 +7,8 @@ changed, and every element inside it must have been written.  The cases
 cover the tails of each kernel form: N not a multiple of 32 or of the column
 tile, M not a multiple of the rows per pass or per MMA tile, K not a multiple
 of the stage, for the split-K GEMV, the tensor-core GEMM (both small-M forms
-and the prefill form), bf16 and fp32 outputs, and the routed experts' out.
+and the prefill form, its shared last round included), bf16 and fp32
+outputs, and the routed experts' out in both forms.
 (The compute sanitizer is closed on this machine; this is its stand-in for
 out-of-bounds stores.)
 """
@@ -80,7 +81,11 @@ def test_matmul_writes_exactly_its_output(M, K, N, adt, cdt, entry):
     check_guard(raw, M * N, ct, f"M={M} K={K} N={N} {adt}->{cdt} {entry}")
 
 
-@pytest.mark.parametrize("T,topk,E,H,I", [(1, 2, 3, 250, 96), (5, 6, 8, 520, 100)])
+# three launches (T = 1; I = 100 and H = 520 not whole groups of 8 blocks),
+# and the persistent form from 4 tokens with H = 504 and I = 252 ragged
+# inside their 512-column tiles, and a DeepSeek-like slot count
+@pytest.mark.parametrize("T,topk,E,H,I", [(1, 2, 3, 250, 96), (5, 6, 8, 520, 100),
+                                         (5, 3, 6, 504, 252), (4, 6, 16, 1024, 512)])
 def test_moe_writes_exactly_its_output(T, topk, E, H, I):
     Wg, Wu, Wd = si.moe_weights(E, H, I, seed=T)
     x = si.activations_bf16(T, H, seed=T)
